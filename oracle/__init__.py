@@ -1,0 +1,154 @@
+"""CPU fp64 oracle -- test infrastructure only.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package; the product library never does. It wraps
+``oracle.c`` (plain C, double precision) with numpy marshalling and builds
+it with gcc on first use. See ``oracle.c`` for the definitions and the
+passages of the pages each one follows.
+
+Every function here is pinned by ``tests/test_oracle.py`` against closed
+forms, invariants, brute force on tiny inputs, library routines and the
+hand-worked cases under ``tests/golden/``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+
+ERR_ARG, ERR_PAGE_OOB, ERR_NOMEM = 1, 3, 7
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into _build/liboracle.so (gcc, OpenMP, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
+    if force or not fresh:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+                        "-shared", "-fPIC", "-std=c11", "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P, I, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f64.restype = D
+        lib.oracle_kv_append.argtypes = [I] * 6 + [P] * 7
+        lib.oracle_kv_append.restype = I
+        lib.oracle_attention_rows.argtypes = [I] * 7 + [P] * 6 + [D, P, P, I64, P, I]
+        lib.oracle_attention_rows.restype = I
+        lib.oracle_paged_attention.argtypes = [I] * 7 + [P] * 6 + [D, P, I]
+        lib.oracle_paged_attention.restype = I
+        lib.oracle_argmax.argtypes = [P, I64]
+        lib.oracle_argmax.restype = I64
+        lib.oracle_verify_greedy.argtypes = [P, P, P, I, I, I64, P, P, P]
+        lib.oracle_verify_greedy.restype = I
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = I
+        _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise OracleError(f"{what}: oracle error code {rc}")
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def bf16_to_f64(bits: int) -> float:
+    return float(_load().oracle_bf16_to_f64(ctypes.c_uint16(bits)))
+
+
+def kv_append(k_pages, v_pages, k_new, v_new, block_table, pos_start, new_lens, page_size=256):
+    """Return copies of k_pages/v_pages with the new tokens' rows written."""
+    kp, vp = _c(k_pages, np.uint16).copy(), _c(v_pages, np.uint16).copy()
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    bt, ps, nl = _c(block_table, np.int32), _c(pos_start, np.int32), _c(new_lens, np.int32)
+    num_pages, hkv, P, d = kp.shape
+    rc = _load().oracle_kv_append(len(nl), hkv, d, P, num_pages, bt.shape[1], _ptr(kn), _ptr(vn),
+                                  _ptr(kp), _ptr(vp), _ptr(bt), _ptr(ps), _ptr(nl))
+    _check(rc, "kv_append")
+    return kp, vp
+
+
+def _attn_common(q, k_pages, v_pages, block_table, seq_lens, q_lens):
+    q, kp, vp = _c(q, np.uint16), _c(k_pages, np.uint16), _c(v_pages, np.uint16)
+    bt, sl, ql = _c(block_table, np.int32), _c(seq_lens, np.int32), _c(q_lens, np.int32)
+    num_pages, hkv, P, d = kp.shape
+    hq = q.shape[1]
+    dims = (len(sl), hq, hkv, d, P, num_pages, bt.shape[1])
+    return dims, (q, kp, vp, bt, sl, ql)
+
+
+def paged_attention(q, k_pages, v_pages, block_table, seq_lens, q_lens, scale,
+                    n_threads: int = 0) -> np.ndarray:
+    """fp64 attention output [total_q, Hq, d] for every new query token."""
+    dims, arrs = _attn_common(q, k_pages, v_pages, block_table, seq_lens, q_lens)
+    out = np.empty((arrs[0].shape[0], dims[1], dims[3]), dtype=np.float64)
+    rc = _load().oracle_paged_attention(*dims, *[_ptr(a) for a in arrs], float(scale),
+                                        _ptr(out), int(n_threads))
+    _check(rc, "paged_attention")
+    return out
+
+
+def attention_rows(q, k_pages, v_pages, block_table, seq_lens, q_lens, scale,
+                   tokens: Sequence[int], heads: Sequence[int], n_threads: int = 0) -> np.ndarray:
+    """fp64 attention output for selected (packed query token, q head) rows: [n, d]."""
+    dims, arrs = _attn_common(q, k_pages, v_pages, block_table, seq_lens, q_lens)
+    tok, hd = _c(tokens, np.int64), _c(heads, np.int32)
+    out = np.empty((len(tok), dims[3]), dtype=np.float64)
+    rc = _load().oracle_attention_rows(*dims, *[_ptr(a) for a in arrs], float(scale), _ptr(tok),
+                                       _ptr(hd), len(tok), _ptr(out), int(n_threads))
+    _check(rc, "attention_rows")
+    return out
+
+
+def argmax(row) -> int:
+    r = _c(row, np.float32)
+    return int(_load().oracle_argmax(_ptr(r), r.shape[-1]))
+
+
+def verify_greedy(logits, candidates, n_cand, window=None):
+    """Return (accepted, next_tok, window_out or None) for every sequence."""
+    lg = _c(logits, np.float32)
+    B, k1, V = lg.shape
+    k_max = k1 - 1
+    cand = _c(candidates, np.int32).reshape(B, k_max) if k_max > 0 else np.zeros((B, 0), np.int32)
+    nc = _c(n_cand, np.int32)
+    acc = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    win = None if window is None else _c(window, np.int32).copy()
+    rc = _load().oracle_verify_greedy(_ptr(lg), _ptr(cand), _ptr(nc), B, k_max, V, _ptr(acc),
+                                      _ptr(nxt), _ptr(win))
+    _check(rc, "verify_greedy")
+    return acc, nxt, win
+

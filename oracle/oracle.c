@@ -1,0 +1,304 @@
+/*
+ * oracle.c -- CPU fp64 oracle for paged attention and greedy verification.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product library links, includes
+ * or calls this file; only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg use it. It shares no code with the CUDA path.
+ *
+ * It states the plain definitions, slowly and in double precision:
+ *
+ *  - kv_append: the K/V rows of a sequence's new tokens are written into
+ *    the page that the sequence's block table names for their position,
+ *    at slot (position mod page size).  ExLlamaV2 "Dynamic Generator" page,
+ *    section "Continuous batching": the cache is indexed through a block
+ *    table of fixed 256-token pages, and adding or removing sequences only
+ *    touches block indices.
+ *
+ *  - attention: for every new query token of every sequence, gather the
+ *    sequence's keys and values page by page into contiguous arrays, take
+ *    softmax(scale * q.K^T) over the keys the token may see, and weight the
+ *    values with it.  Same page and section for the block-table gather; the
+ *    "Deduplication" section for pages shared between sequences (nothing
+ *    special is done: a shared page is simply read by each sequence that
+ *    names it).  Query token i of a sequence with q_len new tokens and
+ *    seq_len cached tokens sits at position seq_len - q_len + i and sees
+ *    keys 0 .. seq_len - q_len + i (causal inside the new tokens): the
+ *    Hugging Face "Assisted Generation" page, section "How Assisted
+ *    Generation works", says one forward pass over a token sequence yields
+ *    logits at every position, which is what this masking gives.
+ *    Query head h uses KV head h / (Hq / Hkv) (contiguous grouping; the
+ *    pages are silent on grouped heads, this is the plain reading).
+ *
+ *  - greedy verification: per verifier row take the lowest index of the
+ *    largest logit; compare the draft candidates with these left to right;
+ *    the accepted count is the length of the matching prefix and the
+ *    correction token is the verifier's token at the first mismatch (at the
+ *    bonus row when every candidate matched); the draft window grows by 2
+ *    when every candidate matched and shrinks by 1 otherwise.  Hugging Face
+ *    "Assisted Generation" page, section "Assisted Generation loop", steps
+ *    3 (comparison), 4 (correction) and 5 (adjustment); step 1 gives the
+ *    initial window of 5.  Readings where the page is silent: the window
+ *    never drops below 1; with zero candidates nothing can mismatch, so the
+ *    window grows; NaN never wins an argmax and an all-NaN row gives 0;
+ *    -0.0 and +0.0 compare equal (a tie).
+ *
+ * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (no fast-math, so
+ * the arithmetic is the order written here on every machine).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_OK = 0, ORACLE_ERR_ARG = 1, ORACLE_ERR_PAGE_OOB = 3, ORACLE_ERR_NOMEM = 7 };
+
+/* bf16 bit pattern -> double, exact: bf16 is the top half of an IEEE binary32. */
+double oracle_bf16_to_f64(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Physical page holding position `pos` of sequence `b`, or -1 if the block
+ * table entry is out of range. */
+static int64_t page_of(const int32_t *block_table, int max_pages_per_seq, int num_pages,
+                       int page_size, int b, int64_t pos) {
+    int64_t j = pos / page_size;
+    if (j >= max_pages_per_seq) return -1;
+    int32_t id = block_table[(int64_t)b * max_pages_per_seq + j];
+    if (id < 0 || id >= num_pages) return -1;
+    return id;
+}
+
+/* ---------------------------------------------------------------- kv_append */
+
+int oracle_kv_append(int num_seqs, int num_kv_heads, int head_dim, int page_size,
+                     int num_pages, int max_pages_per_seq,
+                     const uint16_t *k_new, const uint16_t *v_new,
+                     uint16_t *k_pages, uint16_t *v_pages,
+                     const int32_t *block_table, const int32_t *pos_start,
+                     const int32_t *new_lens) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0) return ORACLE_ERR_ARG;
+    int64_t row = 0; /* new tokens are packed sequence after sequence */
+    for (int b = 0; b < num_seqs; ++b) {
+        for (int i = 0; i < new_lens[b]; ++i, ++row) {
+            int64_t pos = (int64_t)pos_start[b] + i;
+            int64_t pg = page_of(block_table, max_pages_per_seq, num_pages, page_size, b, pos);
+            if (pg < 0) return ORACLE_ERR_PAGE_OOB;
+            int64_t slot = pos % page_size;
+            for (int g = 0; g < num_kv_heads; ++g) {
+                int64_t dst = ((pg * num_kv_heads + g) * page_size + slot) * head_dim;
+                int64_t src = (row * num_kv_heads + g) * head_dim;
+                for (int c = 0; c < head_dim; ++c) {
+                    k_pages[dst + c] = k_new[src + c];
+                    v_pages[dst + c] = v_new[src + c];
+                }
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------- attention */
+
+typedef struct {
+    int num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, max_pages_per_seq;
+    const uint16_t *q, *k_pages, *v_pages;
+    const int32_t *block_table, *seq_lens, *q_lens;
+    double scale;
+} attn_args;
+
+/* One output row: new token i of sequence b, query head h. `kbuf`/`vbuf`
+ * hold at least seq_len*head_dim doubles, `s` at least seq_len. */
+static int attention_row(const attn_args *a, const int64_t *q_row_of_seq, int b, int i, int h,
+                         double *kbuf, double *vbuf, double *s, double *o) {
+    const int d = a->head_dim;
+    const int group = a->num_q_heads / a->num_kv_heads;
+    const int g = h / group;
+    const int64_t T = a->seq_lens[b];
+    const int64_t n = a->q_lens[b];
+    const int64_t p = T - n + i; /* absolute position of this query token */
+    const int64_t nkeys = p + 1;
+
+    /* 1. gather keys/values 0..p through the block table into contiguous arrays */
+    for (int64_t t = 0; t < nkeys; ++t) {
+        int64_t pg = page_of(a->block_table, a->max_pages_per_seq, a->num_pages, a->page_size, b, t);
+        if (pg < 0) return ORACLE_ERR_PAGE_OOB;
+        int64_t base = ((pg * a->num_kv_heads + g) * a->page_size + t % a->page_size) * d;
+        for (int c = 0; c < d; ++c) {
+            kbuf[t * d + c] = oracle_bf16_to_f64(a->k_pages[base + c]);
+            vbuf[t * d + c] = oracle_bf16_to_f64(a->v_pages[base + c]);
+        }
+    }
+    /* 2. scores s_t = scale * q . k_t */
+    const uint16_t *qr = a->q + ((q_row_of_seq[b] + i) * a->num_q_heads + h) * (int64_t)d;
+    for (int64_t t = 0; t < nkeys; ++t) {
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += oracle_bf16_to_f64(qr[c]) * kbuf[t * d + c];
+        s[t] = a->scale * dot;
+    }
+    /* 3. softmax weights w_t = exp(s_t - max) / sum exp(s - max) */
+    double mx = -INFINITY;
+    for (int64_t t = 0; t < nkeys; ++t) mx = s[t] > mx ? s[t] : mx;
+    double sum = 0.0;
+    for (int64_t t = 0; t < nkeys; ++t) {
+        s[t] = exp(s[t] - mx);
+        sum += s[t];
+    }
+    /* 4. o = sum_t w_t v_t */
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int64_t t = 0; t < nkeys; ++t) {
+        double w = s[t] / sum;
+        for (int c = 0; c < d; ++c) o[c] += w * vbuf[t * d + c];
+    }
+    return ORACLE_OK;
+}
+
+static int check_attn_args(const attn_args *a) {
+    if (a->num_seqs < 0 || a->num_q_heads <= 0 || a->num_kv_heads <= 0 || a->head_dim <= 0 ||
+        a->page_size <= 0 || a->num_q_heads % a->num_kv_heads != 0)
+        return ORACLE_ERR_ARG;
+    for (int b = 0; b < a->num_seqs; ++b)
+        if (a->q_lens[b] < 0 || a->q_lens[b] > a->seq_lens[b]) return ORACLE_ERR_ARG;
+    return ORACLE_OK;
+}
+
+static int64_t *q_row_offsets(const attn_args *a) {
+    int64_t *off = (int64_t *)malloc(sizeof(int64_t) * (a->num_seqs + 1));
+    if (!off) return NULL;
+    off[0] = 0;
+    for (int b = 0; b < a->num_seqs; ++b) off[b + 1] = off[b] + a->q_lens[b];
+    return off;
+}
+
+/* Rows to compute are given as (packed query token, head) pairs; out is
+ * [n_rows, head_dim]. n_threads <= 0 uses the OpenMP default. */
+int oracle_attention_rows(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int page_size, int num_pages, int max_pages_per_seq,
+                          const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                          const int32_t *block_table, const int32_t *seq_lens,
+                          const int32_t *q_lens, double scale,
+                          const int64_t *row_token, const int32_t *row_head, int64_t n_rows,
+                          double *out, int n_threads) {
+    attn_args a = {num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                   max_pages_per_seq, q, k_pages, v_pages, block_table, seq_lens, q_lens, scale};
+    int rc = check_attn_args(&a);
+    if (rc) return rc;
+    int64_t *off = q_row_offsets(&a);
+    if (!off) return ORACLE_ERR_NOMEM;
+    int64_t max_T = 1;
+    for (int b = 0; b < num_seqs; ++b) max_T = seq_lens[b] > max_T ? seq_lens[b] : max_T;
+    int status = ORACLE_OK;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel
+    {
+        double *kbuf = (double *)malloc(sizeof(double) * max_T * head_dim);
+        double *vbuf = (double *)malloc(sizeof(double) * max_T * head_dim);
+        double *s = (double *)malloc(sizeof(double) * max_T);
+        int local = (kbuf && vbuf && s) ? ORACLE_OK : ORACLE_ERR_NOMEM;
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            if (local) continue;
+            int64_t tok = row_token[r];
+            int b = 0; /* which sequence owns packed token `tok` */
+            while (b < num_seqs && off[b + 1] <= tok) ++b;
+            if (b >= num_seqs || row_head[r] < 0 || row_head[r] >= num_q_heads) {
+                local = ORACLE_ERR_ARG;
+                continue;
+            }
+            int e = attention_row(&a, off, b, (int)(tok - off[b]), row_head[r], kbuf, vbuf, s,
+                                  out + r * head_dim);
+            if (e) local = e;
+        }
+        if (local) {
+#pragma omp critical
+            status = status ? status : local;
+        }
+        free(kbuf);
+        free(vbuf);
+        free(s);
+    }
+    free(off);
+    return status;
+}
+
+/* Every row: out is [total_q, num_q_heads, head_dim]. */
+int oracle_paged_attention(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                           int page_size, int num_pages, int max_pages_per_seq,
+                           const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           const int32_t *q_lens, double scale, double *out, int n_threads) {
+    int64_t total_q = 0;
+    for (int b = 0; b < num_seqs; ++b) total_q += q_lens[b] > 0 ? q_lens[b] : 0;
+    int64_t n_rows = total_q * num_q_heads;
+    int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (n_rows ? n_rows : 1));
+    int32_t *head = (int32_t *)malloc(sizeof(int32_t) * (n_rows ? n_rows : 1));
+    if (!tok || !head) {
+        free(tok);
+        free(head);
+        return ORACLE_ERR_NOMEM;
+    }
+    for (int64_t r = 0; r < n_rows; ++r) {
+        tok[r] = r / num_q_heads;
+        head[r] = (int32_t)(r % num_q_heads);
+    }
+    int rc = oracle_attention_rows(num_seqs, num_q_heads, num_kv_heads, head_dim, page_size,
+                                   num_pages, max_pages_per_seq, q, k_pages, v_pages, block_table,
+                                   seq_lens, q_lens, scale, tok, head, n_rows, out, n_threads);
+    free(tok);
+    free(head);
+    return rc;
+}
+
+/* ------------------------------------------------------- greedy verification */
+
+/* Lowest index of the largest value; NaN never wins; all-NaN gives 0. The
+ * comparison is the float comparison itself, so -0.0 == +0.0 is a tie. */
+int64_t oracle_argmax(const float *row, int64_t V) {
+    int64_t best = -1;
+    for (int64_t v = 0; v < V; ++v) {
+        if (isnan(row[v])) continue;
+        if (best < 0 || row[v] > row[best]) best = v;
+    }
+    return best < 0 ? 0 : best;
+}
+
+/* logits [B, k_max+1, V]; candidates [B, k_max]; n_cand [B] in 0..k_max.
+ * window may be NULL; when given it is updated in place. */
+int oracle_verify_greedy(const float *logits, const int32_t *candidates, const int32_t *n_cand,
+                         int B, int k_max, int64_t V, int32_t *accepted, int32_t *next_tok,
+                         int32_t *window) {
+    if (B < 0 || k_max < 0 || V <= 0) return ORACLE_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        int n = n_cand[b];
+        if (n < 0 || n > k_max) return ORACLE_ERR_ARG;
+        const float *rows = logits + (int64_t)b * (k_max + 1) * V;
+        /* step 3: compare left to right */
+        int a = 0;
+        while (a < n && candidates[(int64_t)b * k_max + a] == (int32_t)oracle_argmax(rows + a * V, V))
+            ++a;
+        accepted[b] = a;
+        /* step 4: the verifier's own token where the candidates stopped */
+        next_tok[b] = (int32_t)oracle_argmax(rows + (int64_t)a * V, V);
+        /* step 5: +2 when everything matched, -1 otherwise (never below 1) */
+        if (window) window[b] = (a == n) ? window[b] + 2 : (window[b] - 1 > 1 ? window[b] - 1 : 1);
+    }
+    return ORACLE_OK;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
