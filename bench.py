@@ -1,0 +1,460 @@
+"""Benchmark: paged-attention KV GB/s (fraction of HBM peak) and verified tokens/s.
+
+One step = one pass of the decode hot path over the Llama3-8B-shaped batch
+(64 sequences, 32 q / 8 KV heads, head_dim 128, contexts U[512,1024] in a
+64k-token pool of 256-token pages): kv_append of the 64 new tokens' K/V
+through the block tables, then paged_attn (split-K page streaming + combine).
+`value` counts the algorithmic bytes of paged_attn (each distinct cached
+K/V token once, plus q, out, tables and lengths) over its device time; inputs
+are resident in HBM and L2 is flushed between steps. A second block reports
+the speculative-verification step (16 sequences, q_len 6 causal, then greedy
+accept over [16, 6, 128256] fp32 logits) as verified tokens/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own independently seeded batch on
+its own GPU (no collective on the data path; weak scaling) and rank 0 prints
+one JSON line with the max-over-ranks time. `--impl reference` times the CPU
+fp64 oracle on a bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "paged-attn KV GB/s (frac of HBM peak); verified tokens/s at 1 GB300"
+DECODE_CFG = 1   # Llama3-8B-shaped decode batch
+VERIFY_CFG = 3   # speculative verification batch
+FALLBACK_HBM_GBS = 6800.0
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def counted_bytes(w: wl.Workload, with_logits=False) -> int:
+    """Algorithmic bytes of one paged_attn call: distinct K/V tokens once,
+    q and out (bf16), block table, seq_lens and q_lens (+ logits)."""
+    n = w.unique_kv_bytes() + 2 * w.q.nbytes + w.block_table.nbytes + w.seq_lens.nbytes \
+        + w.q_lens.nbytes
+    if with_logits and w.logits is not None:
+        n += w.logits.nbytes
+    return int(n)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.2)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i] == "Active"})
+        loaded = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- our arm
+class GpuBatch:
+    """A workload resident on the GPU plus everything one step needs."""
+
+    def __init__(self, w: wl.Workload, device):
+        import torch
+
+        import speculative_decode_gb300 as sa
+        self.w, self.sa, self.torch = w, sa, torch
+
+        def T(a):
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                a = a.view(np.int16)
+            return torch.from_numpy(a).to(device)
+
+        self.T = T
+        self.dims = sa.dims_for(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.num_pages,
+                                w.max_pages_per_seq, w.total_q, int(w.q_lens.max()))
+        self.kp, self.vp = T(w.k_pages), T(w.v_pages)
+        self.bt, self.sl, self.ql = T(w.block_table), T(w.seq_lens), T(w.q_lens)
+        self.q, self.k_new, self.v_new = T(w.q), T(w.k_new), T(w.v_new)
+        self.out = torch.zeros_like(self.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws = torch.zeros(sa.paged_attn_workspace_size(self.dims), dtype=torch.uint8,
+                              device=device)
+        self.kernels_attn = sa.paged_attn_kernel_count(self.dims)
+        self.verify = w.logits is not None
+        if self.verify:
+            B, k1, V = w.logits.shape
+            self.logits, self.cand, self.ncand = T(w.logits), T(w.candidates), T(w.n_cand)
+            self.window0 = T(w.window)
+            self.window = self.window0.clone()
+            self.acc = torch.zeros(B, dtype=torch.int32, device=device)
+            self.nxt = torch.zeros_like(self.acc)
+            self.vws = torch.zeros(sa.spec_verify_workspace_size(B, k1 - 1, V),
+                                   dtype=torch.uint8, device=device)
+
+    def append(self):
+        self.sa.kv_append(self.dims, self.k_new, self.v_new, self.kp, self.vp, self.bt, self.sl,
+                          self.ql, err_flag=self.err)
+
+    def attend(self):
+        self.sa.paged_attn(self.dims, self.q, self.kp, self.vp, self.bt, self.sl, self.ql,
+                           self.w.scale, self.out, self.ws, err_flag=self.err)
+
+    def accept(self):
+        self.sa.spec_verify_greedy(self.logits, self.cand, self.ncand, self.acc, self.nxt,
+                                   self.vws, window=self.window, err_flag=self.err)
+
+    def launches_per_step(self):
+        return 1 + self.kernels_attn + (1 if self.verify else 0)
+
+
+def timed_steps(batch: GpuBatch, steps: int, warmup: int, flush, parts):
+    """Run warmup + steps; per step record device time of each named part with
+    CUDA events on the launching stream, flushing L2 before every step."""
+    torch = batch.torch
+    stream = torch.cuda.current_stream()
+    fns = {"append": batch.append, "attend": batch.attend, "accept": batch.accept}
+    for _ in range(warmup):
+        flush()
+        for p in parts:
+            fns[p]()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in parts] for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(steps):
+        flush()
+        for i, p in enumerate(parts):
+            ev[s][i][0].record(stream)
+            fns[p]()
+            ev[s][i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - t0
+    per_part = {p: [ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(steps)]
+                for i, p in enumerate(parts)}
+    return per_part, wall
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def e2e_steps(batch: GpuBatch, steps: int, warmup: int):
+    """The same decode step through the public API with host buffers: every
+    step copies its inputs host->device from pinned memory and reads the
+    attention output back device->host; timed with events around all of it."""
+    torch = batch.torch
+    stream = torch.cuda.current_stream()
+    host_in = [batch.q, batch.k_new, batch.v_new, batch.bt, batch.sl, batch.ql]
+    pinned = [t.cpu().pin_memory() for t in host_in]
+    out_host = torch.empty(batch.out.shape, dtype=batch.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for dst, src in zip(host_in, pinned):
+            dst.copy_(src, non_blocking=True)
+        batch.append()
+        batch.attend()
+        out_host.copy_(batch.out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def run_ours(args):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    barrier()
+    dev = torch.device("cuda", local)
+
+    # L2 flush buffer: twice the L2 size, rewritten before every timed step
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 1 << 20), dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    # ---- headline: decode step on the Llama3-8B-shaped batch
+    w = wl.config(DECODE_CFG, seed=1000 + DECODE_CFG + 1 + 7919 * rank)
+    batch = GpuBatch(w, dev)
+    cbytes = counted_bytes(w)
+    with ClockSampler(local) as clk:
+        parts, wall = timed_steps(batch, args.steps, args.warmup, flush, ["append", "attend"])
+    clocks = clk.summary()
+    t_attn = statistics.mean(parts["attend"])      # ms
+    t_step = statistics.mean([a + b for a, b in zip(parts["append"], parts["attend"])])
+    t_attn_max = max_over_ranks(t_attn)
+    t_step_max = max_over_ranks(t_step)
+    assert int(batch.err.item()) == 0, "device error flag set"
+
+    e2e_ms, h2d, d2h = e2e_steps(batch, max(10, args.steps // 10), args.warmup)
+    e2e_ms = max_over_ranks(e2e_ms)
+
+    # ---- second block: speculative verification step
+    wv = wl.config(VERIFY_CFG, seed=1000 + VERIFY_CFG + 1 + 7919 * rank)
+    vb = GpuBatch(wv, dev)
+    vsteps = max(3, args.steps // 4)
+    vparts, _ = timed_steps(vb, vsteps, args.warmup, flush, ["append", "attend", "accept"])
+    tv_attn = max_over_ranks(statistics.mean(vparts["attend"]))
+    tv_acc = max_over_ranks(statistics.mean(vparts["accept"]))
+    tv_step = max_over_ranks(statistics.mean(
+        [a + b + c for a, b, c in zip(vparts["append"], vparts["attend"], vparts["accept"])]))
+    torch.cuda.synchronize()
+    emitted = int((vb.acc.cpu().numpy() + 1).sum())
+    vq = int(wv.q_lens.sum())
+    vbytes = counted_bytes(wv)
+
+    peak, peak_kind = hbm_peak()
+    achieved = cbytes / (t_attn_max * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(world * cbytes / (t_attn_max * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "accumulate": "f32",
+        "data": "synthetic (seeded bf16 N(0,1) q/k/v, random non-contiguous block tables)",
+        "config": {
+            "workload": w.name,
+            "seqs": w.num_seqs, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+            "head_dim": 128, "page_size": 256, "pool_pages": w.num_pages,
+            "ctx": "uniform[512,1024]", "q_len": 1,
+            "step": "kv_append + paged_attn",
+            "value_counts": "paged_attn algorithmic bytes / paged_attn device time",
+            "l2": "flushed (2x L2 write) before every step",
+            "parallelism": f"replicas x{world} (independent batches, no collective)",
+        },
+        "counted_bytes_per_step": cbytes,
+        "paged_attn_ms": round(t_attn_max, 5),
+        "frac_of_hbm_peak": round(achieved / peak, 4),
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "kernel": "paged_attn call (split_attn_kernel + combine_kernel)",
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s",
+        },
+        "verify": {
+            "workload": wv.name,
+            "query_tokens_per_s": round(world * vq / (tv_attn * 1e-3), 1),
+            "emitted_tokens_per_s": round(world * emitted / ((tv_attn + tv_acc) * 1e-3), 1),
+            "emitted_per_step": emitted,
+            "paged_attn_ms": round(tv_attn, 5),
+            "paged_attn_GBps": round(vbytes / (tv_attn * 1e-3) / 1e9, 1),
+            "spec_verify_ms": round(tv_acc, 5),
+            "spec_verify_GBps": round(wv.logits.nbytes / (tv_acc * 1e-3) / 1e9, 1),
+            "step_ms": round(tv_step, 5),
+            "note": "per attention layer: one layer's attention + one greedy accept",
+        },
+        "e2e": {"value": round(world * cbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": int(args.steps * batch.launches_per_step()),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(w) if (world == 1 and not args.no_cpu_baseline) else None
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------ oracle timing
+def oracle_sample(w: wl.Workload, seqs):
+    """Counted bytes of the attention of the listed sequences (all heads)."""
+    sub = {}
+    P = w.page_size
+    for b in seqs:
+        T = int(w.seq_lens[b])
+        for j in range(-(-T // P)):
+            pid = int(w.block_table[b, j])
+            sub[pid] = max(sub.get(pid, 0), min(P, T - j * P))
+    kv = sum(sub.values()) * w.num_kv_heads * w.head_dim * 4
+    qrows = int(sum(w.q_lens[b] for b in seqs))
+    return kv + 2 * qrows * w.num_q_heads * w.head_dim * 2
+
+
+def time_oracle_sequences(w: wl.Workload, seqs, n_threads=0):
+    import oracle
+    qstart = np.concatenate([[0], np.cumsum(w.q_lens)])
+    toks, heads = [], []
+    for b in seqs:
+        for i in range(int(w.q_lens[b])):
+            for h in range(w.num_q_heads):
+                toks.append(int(qstart[b]) + i)
+                heads.append(h)
+    t0 = time.perf_counter()
+    oracle.attention_rows(w.q, w.k_pages, w.v_pages, w.block_table, w.seq_lens, w.q_lens, w.scale,
+                          toks, heads, n_threads=n_threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w: wl.Workload):
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    seqs = list(range(w.num_seqs))
+    time_oracle_sequences(w, seqs[:2])                      # warm (library load, caches)
+    reps, t = 0, 0.0
+    while reps < 3 and t < 15.0:
+        t += time_oracle_sequences(w, seqs)
+        reps += 1
+    nbytes = oracle_sample(w, seqs) * reps
+    one = time_oracle_sequences(w, seqs[:4], n_threads=1)
+    return {"value": round(nbytes / t / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"full decode batch ({w.num_seqs} seqs x {w.num_q_heads} heads) x {reps}, "
+                      "attention only, fp64",
+            "value_1core": round(oracle_sample(w, seqs[:4]) / one / 1e9, 5)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+    w = wl.config(DECODE_CFG)
+    # bounded sample per step: one sequence of the decode batch (all its heads)
+    for s in range(args.warmup):
+        time_oracle_sequences(w, [s % w.num_seqs])
+    times, nbytes = [], 0
+    t_start = time.perf_counter()
+    for s in range(args.steps):
+        b = s % w.num_seqs
+        times.append(time_oracle_sequences(w, [b]))
+        nbytes += oracle_sample(w, [b])
+        if time.perf_counter() - t_start > 120.0:        # keep the run within minutes
+            break
+    t = sum(times)
+    value = nbytes / t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": len(times),
+        "warmup": args.warmup, "ms_per_step": round(1e3 * t / len(times), 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded decode batch)",
+        "config": {"workload": w.name, "step": "oracle attention of one sequence (all heads)"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": "one sequence of the decode batch per step"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * specattn.h -- C ABI of the GB300 paged-attention + greedy-verification library.
+ *
+ * One GPU (sm_103a), one CUDA stream per call. All buffers, all device memory
+ * and the stream belong to the caller; the library allocates no device memory
+ * inside any call below except sa_plan_create (whose buffer lives until
+ * sa_plan_destroy). Calls are asynchronous on `stream` and never synchronise
+ * (unless the environment variable SA_DEBUG=1 is set, in which case each call
+ * synchronises the stream and folds the device error flag into its status).
+ *
+ * Common conventions
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *     stream.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - Host-detectable argument errors are returned synchronously and nothing
+ *     is launched.
+ *   - Device-detectable errors (a block-table entry outside [0, num_pages), a
+ *     candidate count outside [0, k_max], q_len above the declared maximum)
+ *     are OR-ed into *err_flag (an int32 in device memory, bit (1 << status)),
+ *     and the affected work unit is skipped; its outputs are unspecified. The
+ *     caller clears the flag and reads it when it chooses. err_flag may be
+ *     NULL, in which case such errors are dropped silently.
+ *   - Workspaces are caller-owned device buffers of at least the size the
+ *     matching *_workspace_size call returns, 256-byte aligned, ZERO-FILLED
+ *     BEFORE THEIR FIRST USE. Every call leaves the workspace's counters at
+ *     zero again, so a workspace can be reused call after call on one stream;
+ *     two calls in flight at once need two workspaces.
+ */
+#ifndef SPECATTN_H
+#define SPECATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SA_API __attribute__((visibility("default")))
+#else
+#define SA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SA_OK = 0,
+    SA_ERR_ARG = 1,          /* bad pointer, size or shape (host check) */
+    SA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim != 128) */
+    SA_ERR_PAGE_OOB = 3,     /* block-table entry outside [0, num_pages) (device flag) */
+    SA_ERR_CUDA = 4,         /* a CUDA runtime call failed */
+    SA_ERR_TIMEOUT = 5,      /* a bounded wait inside a kernel gave up (device flag) */
+    SA_ERR_WORKSPACE = 6,    /* workspace missing or too small (host check) */
+    SA_ERR_QLEN = 7          /* q_lens[b] > seq_lens[b] or > max_q_len, n_cand out of range (device flag) */
+} sa_status;
+
+/* Shapes of one batch. The paged K/V layout is [num_pages, num_kv_heads,
+ * page_size, head_dim]: each (page, KV head) is one contiguous
+ * page_size*head_dim block (64 KiB at 256 x 128 bf16), so a page is streamed
+ * with whole-block bulk copies. */
+typedef struct {
+    int32_t num_seqs;          /* B */
+    int32_t num_q_heads;       /* Hq, a multiple of num_kv_heads */
+    int32_t num_kv_heads;      /* Hkv */
+    int32_t head_dim;          /* must be 128 */
+    int32_t page_size;         /* must be 256 */
+    int32_t num_pages;         /* physical pages in the pool */
+    int32_t max_pages_per_seq; /* row stride of block_table */
+    int32_t total_q;           /* sum of q_lens: rows of q and out */
+    int32_t max_q_len;         /* upper bound on every q_lens[b] (1 for decode, k+1 to verify), <= 16 */
+} sa_dims;
+
+typedef struct sa_plan sa_plan;
+
+/* Human-readable name of a status code (static storage). */
+SA_API const char *sa_status_string(int status);
+
+/* Number of SMs of the current device (0 without a usable device). */
+SA_API int sa_device_sm_count(void);
+
+/*
+ * sa_kv_append -- write the K/V rows of the new tokens into their pages.
+ *
+ * ExLlamaV2 "Dynamic Generator" page, section "Continuous batching": the
+ * cache is a pool of fixed 256-token pages indexed through per-sequence block
+ * tables, so a sequence grows by writing through its block table.
+ *
+ * New token i of sequence b (0 <= i < q_lens[b]) sits at absolute position
+ * p = seq_lens[b] - q_lens[b] + i; its row for KV head g goes to
+ * k_pages[block_table[b][p / 256]][g][p % 256][:] (and likewise V).
+ *   k_new, v_new  device bf16 [total_q, num_kv_heads, head_dim], packed
+ *                 sequence after sequence in q_lens order
+ *   k_pages, v_pages  device bf16 [num_pages, num_kv_heads, 256, 128]
+ *   block_table   device int32 [num_seqs, max_pages_per_seq]
+ *   seq_lens, q_lens  device int32 [num_seqs]; seq_lens include the new tokens
+ * Writing into a page that another sequence also indexes is the caller's
+ * responsibility (copy-on-write is the scheduler's job); it is not checked.
+ */
+SA_API int sa_kv_append(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_new,
+                 uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,
+                 const int32_t *seq_lens, const int32_t *q_lens, int32_t *err_flag,
+                 void *stream);
+
+/*
+ * sa_plan_create -- find the page runs that several sequences share.
+ *
+ * ExLlamaV2 "Dynamic Generator" page, section "Deduplication": several
+ * sequences may index the same pages (a common prefix stored once). From host
+ * copies of the block tables and lengths, the plan groups sequences whose
+ * tables start with the same physical pages; paged_attn then streams each such
+ * page from HBM once for the whole group, as one dense contraction on the
+ * tensor cores, and attends the rest of each sequence page by page.
+ *   block_table_host  host int32 [num_seqs, max_pages_per_seq]
+ *   seq_lens_host, q_lens_host  host int32 [num_seqs], the values the
+ *                 device arrays will hold at the paged_attn calls that use
+ *                 this plan
+ * The plan allocates one device buffer (its work lists) with cudaMalloc and
+ * frees it in sa_plan_destroy. Make a new plan whenever the block tables or
+ * lengths change. A plan with no shared runs is valid and costs nothing.
+ * On success *out receives the plan.
+ */
+SA_API int sa_plan_create(const sa_dims *dims, const int32_t *block_table_host,
+                   const int32_t *seq_lens_host, const int32_t *q_lens_host, sa_plan **out);
+SA_API void sa_plan_destroy(sa_plan *plan);
+/* Host-only dry run of sa_plan_create for inspection and tests: no CUDA call.
+ * Fills, per sequence, the number of leading pages the shared-prefix path
+ * would cover (skip_pages_out) and the partial slots it would write
+ * (run_slots_out), and the numbers of shared runs and tensor-core work items
+ * for a device with sm_count SMs. Output pointers may be NULL. */
+SA_API int sa_plan_analyze(const sa_dims *dims, const int32_t *block_table_host,
+                    const int32_t *seq_lens_host, const int32_t *q_lens_host, int32_t sm_count,
+                    int32_t *skip_pages_out, int32_t *run_slots_out, int32_t *num_runs,
+                    int32_t *num_tiles);
+/* Shared-run statistics of a plan: runs, member sequences summed over runs,
+ * logical pages summed over runs. Any pointer may be NULL. */
+SA_API int sa_plan_stats(const sa_plan *plan, int32_t *num_runs, int32_t *num_members,
+                  int32_t *num_pages);
+
+/* Bytes of workspace sa_paged_attn needs for these shapes (plan may be NULL). */
+SA_API size_t sa_paged_attn_workspace_size(const sa_dims *dims, const sa_plan *plan);
+
+/*
+ * sa_paged_attn -- attention of the new query tokens over the paged cache.
+ *
+ * For every sequence b, new token i < q_lens[b] and query head h:
+ *   out[row][h] = softmax_t(scale * q[row][h] . K_b[t]) V_b[t],
+ *   t = 0 .. seq_lens[b] - q_lens[b] + i  (causal inside the new tokens),
+ * where row = (sum of q_lens before b) + i, K_b[t] is the row of KV head
+ * h / (Hq / Hkv) at k_pages[block_table[b][t / 256]][.][t % 256], and V_b
+ * likewise. ExLlamaV2 "Dynamic Generator" page, sections "Continuous
+ * batching" (block-table gather) and "Deduplication" (shared pages); Hugging
+ * Face "Assisted Generation" page, section "How Assisted Generation works"
+ * (one forward pass over k+1 tokens scores every position). q_lens[b] = 1 is
+ * plain decode.
+ *   q, out       device bf16 [total_q, num_q_heads, 128]
+ *   k_pages, v_pages, block_table, seq_lens, q_lens  as in sa_kv_append
+ *   scale        softmax scale (1/sqrt(128) for the usual attention)
+ *   plan         NULL, or a plan built from these tables and lengths
+ *   workspace    device, >= sa_paged_attn_workspace_size(dims, plan) bytes
+ * Accumulation is fp32; out is rounded to bf16 (nearest even).
+ * Requires 0 <= q_lens[b] <= min(seq_lens[b], max_q_len). Entries of
+ * block_table past a sequence's last page are never read.
+ */
+SA_API int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_pages,
+                  const uint16_t *v_pages, const int32_t *block_table,
+                  const int32_t *seq_lens, const int32_t *q_lens, float scale, uint16_t *out,
+                  const sa_plan *plan, void *workspace, size_t workspace_bytes,
+                  int32_t *err_flag, void *stream);
+
+/* Number of kernels one sa_paged_attn call with these shapes launches
+ * (diagnostics; the same decomposition the call itself uses). Needs a device. */
+SA_API int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan);
+
+/* Bytes of workspace sa_spec_verify_greedy needs. */
+SA_API size_t sa_spec_verify_workspace_size(int32_t num_seqs, int32_t k_max, int32_t vocab);
+
+/*
+ * sa_spec_verify_greedy -- greedy acceptance of draft tokens.
+ *
+ * Hugging Face "Assisted Generation" page, section "Assisted Generation loop",
+ * steps 3-5. Per sequence b with c = candidates[b], n = n_cand[b]:
+ *   t_j = lowest index of the largest logits[b][j][:], j = 0..n
+ *         (NaN never wins; an all-NaN row gives 0; -0.0 == +0.0)
+ *   accepted[b] = largest a <= n with c_j == t_j for every j < a
+ *   next_tok[b] = t_{accepted[b]}  (the correction, or the bonus token when
+ *                 all n candidates matched)
+ *   window[b]  <- window[b] + 2 if accepted[b] == n, else max(1, window[b] - 1)
+ *   logits       device fp32 [num_seqs, k_max + 1, vocab]
+ *   candidates   device int32 [num_seqs, k_max]
+ *   n_cand       device int32 [num_seqs], each in 0..k_max
+ *   accepted, next_tok  device int32 [num_seqs] (outputs)
+ *   window       device int32 [num_seqs], updated in place; may be NULL
+ *   workspace    device, >= sa_spec_verify_workspace_size(...) bytes
+ * Results are exact (integer); k_max <= 15.
+ */
+SA_API int sa_spec_verify_greedy(const float *logits, const int32_t *candidates, const int32_t *n_cand,
+                          int32_t num_seqs, int32_t k_max, int32_t vocab, int32_t *accepted,
+                          int32_t *next_tok, int32_t *window, void *workspace,
+                          size_t workspace_bytes, int32_t *err_flag, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECATTN_H */

@@ -1,0 +1,354 @@
+// api.cu -- the C ABI (include/specattn.h): argument checks, work
+// decomposition, tensor maps and kernel launches. Host code only.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "plan.h"
+
+namespace sa {
+
+namespace {
+
+bool debug_sync() {
+    static const bool on = [] {
+        const char *v = std::getenv("SA_DEBUG");
+        return v != nullptr && std::strcmp(v, "1") == 0;
+    }();
+    return on;
+}
+
+// Under SA_DEBUG=1: wait for the stream and turn the device flag into a status.
+int finish(cudaStream_t stream, const int32_t *err_flag) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return SA_ERR_CUDA;
+    if (!debug_sync()) return SA_OK;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return SA_ERR_CUDA;
+    if (err_flag == nullptr) return SA_OK;
+    int32_t flag = 0;
+    if (cudaMemcpy(&flag, err_flag, sizeof flag, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SA_ERR_CUDA;
+    for (int s = 1; s < 31; ++s)
+        if (flag & (1 << s)) return s;
+    return SA_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_dims(const sa_dims *d) {
+    if (d == nullptr) return SA_ERR_ARG;
+    if (d->num_seqs < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->num_pages < 0 ||
+        d->max_pages_per_seq < 0 || d->total_q < 0 || d->max_q_len < 0)
+        return SA_ERR_ARG;
+    if (d->num_q_heads % d->num_kv_heads != 0) return SA_ERR_ARG;
+    if (d->head_dim != kHeadDim || d->page_size != kPageSize) return SA_ERR_UNSUPPORTED;
+    if (d->max_q_len > kMaxQLen) return SA_ERR_UNSUPPORTED;
+    // the pool is addressed as num_pages * Hkv * 256 rows with 32-bit coordinates
+    if (static_cast<int64_t>(d->num_pages) * d->num_kv_heads * kPageSize >= (int64_t{1} << 31))
+        return SA_ERR_UNSUPPORTED;
+    if (d->num_q_heads / d->num_kv_heads * d->max_q_len > 16 * kMaxQLen) return SA_ERR_UNSUPPORTED;
+    return SA_OK;
+}
+
+// Work decomposition of the split kernel; a pure function of the shapes and
+// the SM count so that workspace sizing and launch agree.
+struct SplitConfig {
+    int R, nrb, pps, n_splits, run_slots, n_slots;
+    int64_t n_units;
+};
+
+constexpr int kMaxSplits = 64;
+
+SplitConfig split_config(const sa_dims &d, const sa_plan *plan, int sms) {
+    SplitConfig c{};
+    const int G = d.num_q_heads / d.num_kv_heads;
+    const int rows = G * std::max(1, d.max_q_len);
+    c.R = rows <= 4 ? 4 : rows <= 8 ? 8 : rows <= 12 ? 12 : 16;
+    c.nrb = (rows + c.R - 1) / c.R;
+    const int max_pages = std::max(1, d.max_pages_per_seq);
+    const int pps_min = (max_pages + kMaxSplits - 1) / kMaxSplits;
+    // aim for about six units per SM so that the persistent warps stay balanced
+    const int64_t slots = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.nrb * max_pages;
+    const int64_t target = static_cast<int64_t>(std::max(1, sms)) * 6;
+    c.pps = static_cast<int>(std::max<int64_t>(pps_min, std::min<int64_t>(max_pages, slots / target)));
+    c.pps = std::max(c.pps, 1);
+    c.n_splits = (max_pages + c.pps - 1) / c.pps;
+    c.run_slots = plan ? plan_run_slots(plan) : 0;
+    c.n_slots = c.run_slots + c.n_splits;
+    c.n_units = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.nrb * c.n_splits;
+    return c;
+}
+
+// Workspace layout: fp32 accumulators [n_slots][total_q * Hq][128], then
+// (max, sum) pairs [n_slots][total_q * Hq][2]. It is sized for the finest
+// split any device could choose, so sizing needs no device.
+struct WsLayout {
+    int64_t slots_cap;
+    size_t ml_offset, total;
+};
+
+WsLayout attn_ws_layout(const sa_dims &d, const sa_plan *plan) {
+    WsLayout w{};
+    const int max_pages = std::max(1, d.max_pages_per_seq);
+    const int pps_min = (max_pages + kMaxSplits - 1) / kMaxSplits;
+    w.slots_cap = (plan ? plan_run_slots(plan) : 0) + (max_pages + pps_min - 1) / pps_min;
+    const int64_t rows = static_cast<int64_t>(d.total_q) * d.num_q_heads;
+    const size_t acc = static_cast<size_t>(w.slots_cap * rows * kHeadDim * 4);
+    const size_t ml = static_cast<size_t>(w.slots_cap * rows * 2 * 4);
+    w.ml_offset = (acc + 255) / 256 * 256;
+    w.total = w.ml_offset + (ml + 255) / 256 * 256;
+    return w;
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+    static EncodeFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeFn>(p);
+    }();
+    return fn;
+}
+
+}  // namespace
+
+CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base,
+                              uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    EncodeFn fn = encode_fn();
+    if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int device_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+}  // namespace sa
+
+using namespace sa;
+
+extern "C" {
+
+const char *sa_status_string(int status) {
+    switch (status) {
+        case SA_OK: return "ok";
+        case SA_ERR_ARG: return "invalid argument";
+        case SA_ERR_UNSUPPORTED: return "unsupported shape";
+        case SA_ERR_PAGE_OOB: return "block-table entry out of range";
+        case SA_ERR_CUDA: return "CUDA error";
+        case SA_ERR_TIMEOUT: return "bounded wait timed out inside a kernel";
+        case SA_ERR_WORKSPACE: return "workspace missing or too small";
+        case SA_ERR_QLEN: return "query length or candidate count out of range";
+        default: return "unknown status";
+    }
+}
+
+int sa_device_sm_count(void) { return device_sm_count(); }
+
+int sa_kv_append(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_new,
+                 uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,
+                 const int32_t *seq_lens, const int32_t *q_lens, int32_t *err_flag, void *stream) {
+    int rc = check_dims(dims);
+    if (rc) return rc;
+    if (dims->num_seqs == 0 || dims->total_q == 0) return SA_OK;
+    if (!k_new || !v_new || !k_pages || !v_pages || !block_table || !seq_lens || !q_lens)
+        return SA_ERR_ARG;
+    if (!aligned(k_new, 8) || !aligned(v_new, 8) || !aligned(k_pages, 8) || !aligned(v_pages, 8))
+        return SA_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_kv_append(*dims, k_new, v_new, k_pages, v_pages, block_table, seq_lens, q_lens,
+                         err_flag, s) != cudaSuccess)
+        return SA_ERR_CUDA;
+    return finish(s, err_flag);
+}
+
+size_t sa_paged_attn_workspace_size(const sa_dims *dims, const sa_plan *plan) {
+    if (check_dims(dims) != SA_OK) return 0;
+    return attn_ws_layout(*dims, plan).total;
+}
+
+int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_pages,
+                  const uint16_t *v_pages, const int32_t *block_table, const int32_t *seq_lens,
+                  const int32_t *q_lens, float scale, uint16_t *out, const sa_plan *plan,
+                  void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream) {
+    int rc = check_dims(dims);
+    if (rc) return rc;
+    const sa_dims &d = *dims;
+    if (d.num_seqs == 0 || d.total_q == 0) return SA_OK;
+    if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !q_lens || !out)
+        return SA_ERR_ARG;
+    if (d.num_pages == 0 || d.max_pages_per_seq == 0) return SA_ERR_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16))
+        return SA_ERR_ARG;
+    if (plan && !plan_matches(plan, d)) return SA_ERR_ARG;
+    const WsLayout wl = attn_ws_layout(d, plan);
+    if (workspace == nullptr || workspace_bytes < wl.total || !aligned(workspace, 256))
+        return SA_ERR_WORKSPACE;
+    const int sms = device_sm_count();
+    if (sms <= 0) return SA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    const SplitConfig c = split_config(d, plan, sms);
+    const int64_t rows_total = static_cast<int64_t>(d.total_q) * d.num_q_heads;
+    float *ws_acc = static_cast<float *>(workspace);
+    float *ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.ml_offset);
+
+    CUtensorMap tmk, tmv;
+    const uint64_t pool_rows = static_cast<uint64_t>(d.num_pages) * d.num_kv_heads * kPageSize;
+    if (encode_tensor_map_2d(&tmk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(k_pages),
+                             kHeadDim, pool_rows, kHeadDim * 2, 64, 32,
+                             CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode_tensor_map_2d(&tmv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(v_pages),
+                             kHeadDim, pool_rows, kHeadDim * 2, 64, 32,
+                             CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return SA_ERR_CUDA;
+
+    const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
+    if (pd && pd->num_tiles > 0) {
+        if (launch_prefix_tc(d, *pd, q, k_pages, v_pages, scale, ws_acc, ws_ml, rows_total,
+                             err_flag, s) != cudaSuccess)
+            return SA_ERR_CUDA;
+    }
+
+    SplitParams p{};
+    p.q = q;
+    p.out = out;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.q_lens = q_lens;
+    p.skip_pages = pd ? pd->skip_pages : nullptr;
+    p.run_slots = pd ? pd->run_slots : nullptr;
+    p.ws_acc = ws_acc;
+    p.ws_ml = ws_ml;
+    p.err = err_flag;
+    p.B = d.num_seqs;
+    p.Hq = d.num_q_heads;
+    p.Hkv = d.num_kv_heads;
+    p.G = d.num_q_heads / d.num_kv_heads;
+    p.num_pages = d.num_pages;
+    p.max_pages = d.max_pages_per_seq;
+    p.total_q = d.total_q;
+    p.max_q_len = d.max_q_len;
+    p.rows_per_block = c.R;
+    p.n_row_blocks = c.nrb;
+    p.pages_per_split = c.pps;
+    p.n_splits = c.n_splits;
+    p.slot_base = c.run_slots;
+    p.n_rows_total = static_cast<int32_t>(rows_total);
+    p.n_units = c.n_units;
+    p.qscale = scale * 1.4426950408889634f;
+    p.evict_first = c.nrb == 1;
+
+    int per_sm = 0;
+    if (split_occupancy(c.R, 1, &per_sm) != cudaSuccess || per_sm <= 0) return SA_ERR_CUDA;
+    const int64_t ctas = std::min<int64_t>(static_cast<int64_t>(sms) * per_sm, c.n_units);
+    if (ctas > 0 && launch_split_attn(p, tmk, tmv, static_cast<int>(ctas), 1, s) != cudaSuccess)
+        return SA_ERR_CUDA;
+
+    if (c.n_splits > 1 || c.run_slots > 0) {
+        CombineParams cp{};
+        cp.out = out;
+        cp.seq_lens = seq_lens;
+        cp.q_lens = q_lens;
+        cp.skip_pages = p.skip_pages;
+        cp.run_slots = p.run_slots;
+        cp.ws_acc = ws_acc;
+        cp.ws_ml = ws_ml;
+        cp.B = d.num_seqs;
+        cp.Hq = d.num_q_heads;
+        cp.max_q_len = d.max_q_len;
+        cp.total_q = d.total_q;
+        cp.pages_per_split = c.pps;
+        cp.slot_base = c.run_slots;
+        cp.n_rows_total = static_cast<int32_t>(rows_total);
+        if (launch_combine(cp, s) != cudaSuccess) return SA_ERR_CUDA;
+    }
+    return finish(s, err_flag);
+}
+
+int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan) {
+    if (check_dims(dims) != SA_OK) return -1;
+    const int sms = device_sm_count();
+    if (sms <= 0) return -1;
+    const SplitConfig c = split_config(*dims, plan, sms);
+    const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
+    return 1 + ((c.n_splits > 1 || c.run_slots > 0) ? 1 : 0) + ((pd && pd->num_tiles > 0) ? 1 : 0);
+}
+
+size_t sa_spec_verify_workspace_size(int32_t num_seqs, int32_t k_max, int32_t vocab) {
+    if (num_seqs < 0 || k_max < 0 || k_max > kMaxKMax || vocab <= 0) return 0;
+    const int64_t chunks = (static_cast<int64_t>(vocab) + 1023) / 1024;
+    const int64_t parts = static_cast<int64_t>(num_seqs) * (k_max + 1) * chunks;
+    const size_t a = ((static_cast<size_t>(parts) * 4 + 255) / 256) * 256;
+    const size_t c = ((static_cast<size_t>(num_seqs) * 4 + 255) / 256) * 256;
+    return 2 * a + c;
+}
+
+int sa_spec_verify_greedy(const float *logits, const int32_t *candidates, const int32_t *n_cand,
+                          int32_t num_seqs, int32_t k_max, int32_t vocab, int32_t *accepted,
+                          int32_t *next_tok, int32_t *window, void *workspace,
+                          size_t workspace_bytes, int32_t *err_flag, void *stream) {
+    if (num_seqs < 0 || k_max < 0 || vocab <= 0) return SA_ERR_ARG;
+    if (k_max > kMaxKMax) return SA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return SA_OK;
+    if (!logits || !n_cand || !accepted || !next_tok || (k_max > 0 && !candidates))
+        return SA_ERR_ARG;
+    if (!aligned(logits, 16)) return SA_ERR_ARG;
+    const size_t need = sa_spec_verify_workspace_size(num_seqs, k_max, vocab);
+    if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+        return SA_ERR_WORKSPACE;
+    const int sms = device_sm_count();
+    if (sms <= 0) return SA_ERR_CUDA;
+    const int64_t rows = static_cast<int64_t>(num_seqs) * (k_max + 1);
+    const int64_t max_chunks = (static_cast<int64_t>(vocab) + 1023) / 1024;
+    // about four CTAs per SM in total, each chunk a multiple of 1024 elements
+    int64_t n_chunks = std::min<int64_t>(max_chunks, std::max<int64_t>(1, (4 * sms + rows - 1) / rows));
+    const int64_t chunk = ((vocab + n_chunks - 1) / n_chunks + 1023) / 1024 * 1024;
+    n_chunks = (vocab + chunk - 1) / chunk;
+    const int64_t parts = rows * max_chunks;
+    const size_t a = ((static_cast<size_t>(parts) * 4 + 255) / 256) * 256;
+
+    VerifyParams p{};
+    p.logits = logits;
+    p.candidates = candidates;
+    p.n_cand = n_cand;
+    p.accepted = accepted;
+    p.next_tok = next_tok;
+    p.window = window;
+    p.part_val = static_cast<float *>(workspace);
+    p.part_idx = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + a);
+    p.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + 2 * a);
+    p.err = err_flag;
+    p.B = num_seqs;
+    p.k_max = k_max;
+    p.V = vocab;
+    p.n_chunks = static_cast<int32_t>(n_chunks);
+    p.chunk = static_cast<int32_t>(chunk);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_verify(p, s) != cudaSuccess) return SA_ERR_CUDA;
+    return finish(s, err_flag);
+}
+
+}  // extern "C"

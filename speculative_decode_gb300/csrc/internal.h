@@ -1,0 +1,106 @@
+// internal.h -- declarations shared by the library's translation units
+// (host side). Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "specattn.h"
+
+namespace sa {
+
+constexpr int kHeadDim = 128;
+constexpr int kPageSize = 256;
+constexpr int kMaxQLen = 16;
+constexpr int kMaxKMax = 15;
+
+constexpr int32_t kErrBitPageOOB = 1 << SA_ERR_PAGE_OOB;
+constexpr int32_t kErrBitTimeout = 1 << SA_ERR_TIMEOUT;
+constexpr int32_t kErrBitQlen = 1 << SA_ERR_QLEN;
+
+// Device-side description of a plan's shared-prefix work (all arrays live in
+// the plan's device buffer).
+struct PlanDevice {
+    int32_t num_runs;        // shared runs
+    int32_t num_tiles;       // tensor-core work items (run, kv head, row tile, page chunk)
+    int32_t max_run_slots;   // workspace partial slots used by runs per row
+    const int32_t *skip_pages;  // [B] leading logical pages covered by runs
+    const int32_t *run_slots;   // [B] number of run partials of each sequence
+    const int32_t *run_desc;    // per run: page_lo, page_hi, row_begin, row_count, first member
+    const int32_t *run_rows;    // per run row: packed query token, q head (within kv head), key limit, slot
+    const int32_t *tiles;       // per work item: run, row tile, page chunk lo, page chunk hi, slot
+};
+
+// Parameters of the split-K kernel (page-streamed attention on CUDA cores).
+struct SplitParams {
+    const uint16_t *q;
+    uint16_t *out;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const int32_t *q_lens;
+    const int32_t *skip_pages;  // nullable: pages [0, skip) handled by the shared-prefix path
+    const int32_t *run_slots;   // nullable: partials the shared-prefix path writes per sequence
+    float *ws_acc;              // [n_slots][total_q * Hq][128] fp32 unnormalised accumulators
+    float *ws_ml;               // [n_slots][total_q * Hq][2] running max (log2 units), sum
+    int32_t *err;
+    int32_t B, Hq, Hkv, G, num_pages, max_pages, total_q, max_q_len;
+    int32_t rows_per_block;     // R, rows of one work unit
+    int32_t n_row_blocks;
+    int32_t pages_per_split;
+    int32_t n_splits;
+    int32_t slot_base;          // first workspace slot used by splits
+    int32_t n_rows_total;       // total_q * Hq (row stride of a workspace slot)
+    int64_t n_units;
+    float qscale;               // scale * log2(e)
+    int32_t evict_first;
+};
+
+size_t split_smem_bytes(int R, int stages);
+int max_rows_per_block();
+cudaError_t launch_split_attn(const SplitParams &p, const CUtensorMap &tmap_k,
+                              const CUtensorMap &tmap_v, int num_ctas, int warps_per_cta,
+                              cudaStream_t stream);
+cudaError_t split_occupancy(int R, int warps_per_cta, int *ctas_per_sm);
+
+struct CombineParams {
+    uint16_t *out;
+    const int32_t *seq_lens;
+    const int32_t *q_lens;
+    const int32_t *skip_pages;
+    const int32_t *run_slots;
+    const float *ws_acc;
+    const float *ws_ml;
+    int32_t B, Hq, max_q_len, total_q, pages_per_split, slot_base, n_rows_total;
+};
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
+
+cudaError_t launch_kv_append(const sa_dims &d, const uint16_t *k_new, const uint16_t *v_new,
+                             uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,
+                             const int32_t *seq_lens, const int32_t *q_lens, int32_t *err,
+                             cudaStream_t stream);
+
+struct VerifyParams {
+    const float *logits;
+    const int32_t *candidates;
+    const int32_t *n_cand;
+    int32_t *accepted;
+    int32_t *next_tok;
+    int32_t *window;
+    float *part_val;      // [B * (k_max + 1)][n_chunks]
+    int32_t *part_idx;    // same shape
+    int32_t *counters;    // [B], zero between calls
+    int32_t *err;
+    int32_t B, k_max, V, n_chunks, chunk;
+};
+cudaError_t launch_verify(const VerifyParams &p, cudaStream_t stream);
+
+// Driver entry point for tensor-map encoding (resolved once, no -lcuda).
+CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base,
+                              uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+int device_sm_count();
+
+}  // namespace sa

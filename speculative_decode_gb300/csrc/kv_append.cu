@@ -1,0 +1,76 @@
+// kv_append.cu -- write the new tokens' K/V rows into their pages.
+//
+// ExLlamaV2 "Dynamic Generator" page, "Continuous batching": a sequence's
+// keys and values live in fixed 256-token pages that its block table names;
+// new token i of sequence b sits at position seq_len - q_len + i and goes to
+// page block_table[b][pos / 256], slot pos % 256, for every KV head.
+//
+// One CTA per (query token slot, sequence); one warp per KV head copies the
+// 256-byte K row and V row with 8-byte coalesced accesses. Pure bandwidth.
+#include "common.cuh"
+
+namespace sa {
+
+namespace {
+
+__global__ void __launch_bounds__(256) kv_append_kernel(
+    const uint16_t *__restrict__ k_new, const uint16_t *__restrict__ v_new,
+    uint16_t *__restrict__ k_pages, uint16_t *__restrict__ v_pages,
+    const int32_t *__restrict__ block_table, const int32_t *__restrict__ seq_lens,
+    const int32_t *__restrict__ q_lens, int32_t *err, int Hkv, int num_pages, int max_pages,
+    int max_q_len, int total_q) {
+    const int i = blockIdx.x;
+    const int b = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int n = q_lens[b];
+    const int T = seq_lens[b];
+    if (i >= n) return;
+    if (n > T || n > max_q_len) {
+        if (threadIdx.x == 0) flag_error(err, kErrBitQlen);
+        return;
+    }
+    const int pos = T - n + i;
+    const int j = pos / kPageSize;
+    const int pid = j < max_pages ? block_table[static_cast<int64_t>(b) * max_pages + j] : -1;
+    if (pid < 0 || pid >= num_pages) {
+        if (threadIdx.x == 0) flag_error(err, kErrBitPageOOB);
+        return;
+    }
+    int qstart = 0;  // packed row of token 0 of sequence b
+    for (int k = lane; k < b; k += 32) qstart += q_lens[k];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) qstart += __shfl_xor_sync(0xffffffffu, qstart, o);
+    if (qstart + n > total_q) {  // q_lens disagree with dims.total_q
+        if (threadIdx.x == 0) flag_error(err, kErrBitQlen);
+        return;
+    }
+    const int64_t row = qstart + i;
+    const int slot = pos % kPageSize;
+    for (int g = warp; g < Hkv; g += blockDim.x >> 5) {
+        const int64_t src = (row * Hkv + g) * kHeadDim + lane * 4;
+        const int64_t dst = ((static_cast<int64_t>(pid) * Hkv + g) * kPageSize + slot) * kHeadDim + lane * 4;
+        const uint2 kw = *reinterpret_cast<const uint2 *>(k_new + src);
+        const uint2 vw = *reinterpret_cast<const uint2 *>(v_new + src);
+        *reinterpret_cast<uint2 *>(k_pages + dst) = kw;
+        *reinterpret_cast<uint2 *>(v_pages + dst) = vw;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const sa_dims &d, const uint16_t *k_new, const uint16_t *v_new,
+                             uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,
+                             const int32_t *seq_lens, const int32_t *q_lens, int32_t *err,
+                             cudaStream_t stream) {
+    if (d.num_seqs == 0 || d.max_q_len == 0) return cudaSuccess;
+    const int threads = 32 * (d.num_kv_heads < 8 ? d.num_kv_heads : 8);
+    dim3 grid(d.max_q_len, d.num_seqs);
+    kv_append_kernel<<<grid, threads, 0, stream>>>(k_new, v_new, k_pages, v_pages, block_table,
+                                                   seq_lens, q_lens, err, d.num_kv_heads,
+                                                   d.num_pages, d.max_pages_per_seq, d.max_q_len,
+                                                   d.total_q);
+    return cudaGetLastError();
+}
+
+}  // namespace sa

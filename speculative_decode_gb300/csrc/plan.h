@@ -1,0 +1,50 @@
+// plan.h -- host planner for shared page runs (deduplicated prefixes) and the
+// launcher of the tensor-core shared-prefix kernel. Not part of the public ABI.
+#pragma once
+
+#include <vector>
+
+#include "internal.h"
+
+namespace sa {
+
+// Rows of one shared run, per KV head: member sequences' query tokens x the
+// G query heads of the KV head.
+struct RunRow {
+    int32_t token;      // packed query row (index into q / out)
+    int32_t head_local; // 0 .. G-1; the query head is kv_head * G + head_local
+    int32_t limit;      // last key position this row may see (causal)
+    int32_t slot;       // workspace slot of this row's partial for chunk 0 of the run
+};
+
+struct PlanHost {
+    sa_dims dims;
+    int32_t num_runs = 0, num_members = 0, num_run_pages = 0;
+    int32_t max_run_slots = 0;
+    std::vector<int32_t> skip_pages, run_slots;
+    // per run: page_lo, page_hi, row_begin, row_count, chunk_pages, first member's table row
+    std::vector<int32_t> run_desc;
+    std::vector<RunRow> rows;
+    // per work item: run, kv head, first row of the 128-row tile, page chunk lo, page chunk hi, chunk index
+    std::vector<int32_t> tiles;
+};
+
+int plan_run_slots(const sa_plan *plan);
+bool plan_matches(const sa_plan *plan, const sa_dims &d);
+const PlanDevice *plan_device(const sa_plan *plan);
+
+// Pure host function (no CUDA): find the shared runs of a batch. Runs that
+// would give fewer than `min_rows` rows per KV head stay on the split path.
+PlanHost build_plan(const sa_dims &d, const int32_t *block_table, const int32_t *seq_lens,
+                    const int32_t *q_lens, int sms, int min_rows);
+
+cudaError_t launch_prefix_tc(const sa_dims &d, const PlanDevice &pd, const uint16_t *q,
+                             const uint16_t *k_pages, const uint16_t *v_pages, float scale,
+                             float *ws_acc, float *ws_ml, int64_t rows_total, int32_t *err,
+                             cudaStream_t stream);
+
+constexpr int kRunDescInts = 6;
+constexpr int kTileInts = 6;
+constexpr int kPrefixTileRows = 128;
+
+}  // namespace sa

@@ -1,0 +1,125 @@
+"""CPU checks of the C ABI: the library builds for sm_103a, loads, exports
+every symbol the header declares, and rejects bad arguments on the host
+before any CUDA call. The planner's host logic runs without a GPU."""
+import ctypes
+import os
+import re
+import shutil
+
+import numpy as np
+import pytest
+
+import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specattn.h")
+
+needs_nvcc = pytest.mark.skipif(shutil.which("nvcc") is None and
+                                not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="no CUDA toolkit")
+
+
+@pytest.fixture(scope="module")
+def sa():
+    from speculative_decode_gb300 import build
+    build.build()
+    import speculative_decode_gb300 as mod
+    mod.load_library()
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SA_API\s+[\w\s\*]*?\b(sa_\w+)\s*\(", text)))
+
+
+@needs_nvcc
+def test_every_declared_symbol_is_exported(sa):
+    names = declared_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(sa.library_path())
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+@needs_nvcc
+def test_status_strings(sa):
+    assert sa.status_string(0) == "ok"
+    assert "out of range" in sa.status_string(3)
+    assert sa.status_string(99) == "unknown status"
+
+
+@needs_nvcc
+def test_host_side_argument_checks_need_no_gpu(sa):
+    lib = sa.load_library()
+    d = sa.dims_for(4, 8, 2, 16, 4, 4, 1)
+    d.head_dim = 64
+    assert lib.sa_paged_attn(ctypes.byref(d), *([None] * 6), 0.1, None, None, None, 0, None, None) == 2
+    d = sa.dims_for(4, 8, 3, 16, 4, 4, 1)      # Hq not a multiple of Hkv
+    assert lib.sa_kv_append(ctypes.byref(d), *([None] * 9)) == 1
+    d = sa.dims_for(4, 8, 2, 16, 4, 4, 17)     # max_q_len above 16
+    assert lib.sa_paged_attn(ctypes.byref(d), *([None] * 6), 0.1, None, None, None, 0, None, None) == 2
+    d = sa.dims_for(4, 8, 2, 16, 4, 4, 1)
+    assert lib.sa_paged_attn(ctypes.byref(d), *([None] * 6), 0.1, None, None, None, 0, None, None) == 1
+    assert lib.sa_spec_verify_greedy(None, None, None, 2, 16, 100, *([None] * 4), 0, None, None) == 2
+    assert lib.sa_spec_verify_greedy(None, None, None, -1, 3, 100, *([None] * 4), 0, None, None) == 1
+
+
+@needs_nvcc
+def test_workspace_sizes(sa):
+    w = wl.config(1)
+    d = sa.dims_for(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.num_pages,
+                    w.max_pages_per_seq, w.total_q, 1)
+    n = sa.paged_attn_workspace_size(d)
+    rows = w.total_q * w.num_q_heads
+    assert n >= 4 * rows * 130 * 4          # up to 4 splits of 130 floats per row
+    assert n % 256 == 0
+    assert sa.spec_verify_workspace_size(16, 5, 128256) >= 16 * 6 * 8
+    assert sa.spec_verify_workspace_size(16, 16, 100) == 0
+
+
+@needs_nvcc
+def test_planner_finds_the_shared_prefix(sa):
+    w = wl.config(2)
+    d = sa.dims_for(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.num_pages,
+                    w.max_pages_per_seq, w.total_q, 1)
+    skip, slots, runs, tiles = sa.plan_analyze(d, w.block_table, w.seq_lens, w.q_lens, 148)
+    assert runs == 1
+    assert (skip == 16).all()                 # the 16 shared prefix pages
+    assert (slots == slots[0]).all() and slots[0] >= 1
+    assert tiles >= 148 // 2
+
+
+@needs_nvcc
+def test_planner_nested_runs_and_no_sharing(sa):
+    P = wl.PAGE_SIZE
+    # 40 sequences share pages 0-1; the first 20 of them also share page 2
+    B = 40
+    bt = np.full((B, 5), -1, np.int32)
+    for b in range(B):
+        bt[b, 0], bt[b, 1] = 0, 1
+        bt[b, 2] = 2 if b < 20 else 3 + b
+        bt[b, 3] = 100 + b
+    seq = np.full(B, 3 * P + 10, np.int32)
+    ql = np.ones(B, np.int32)
+    d = sa.dims_for(B, 8, 2, 200, 5, B, 1)
+    skip, slots, runs, _ = sa.plan_analyze(d, bt, seq, ql, 148)
+    assert runs == 2
+    assert (skip[:20] == 3).all() and (skip[20:] == 2).all()
+    assert (slots[:20] > slots[20:].max()).all()
+    # distinct pages everywhere: nothing shared
+    w = wl.config(1)
+    d = sa.dims_for(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.num_pages,
+                    w.max_pages_per_seq, w.total_q, 1)
+    skip, slots, runs, tiles = sa.plan_analyze(d, w.block_table, w.seq_lens, w.q_lens, 148)
+    assert runs == 0 and tiles == 0 and (skip == 0).all()
+
+
+@needs_nvcc
+def test_planner_keeps_small_groups_on_the_split_path(sa):
+    P = wl.PAGE_SIZE
+    bt = np.array([[0, 1], [0, 2]], np.int32)     # two sequences, G=4: 8 rows < threshold
+    d = sa.dims_for(2, 8, 2, 4, 2, 2, 1)
+    skip, _, runs, tiles = sa.plan_analyze(d, bt, np.array([P + 3, P + 9], np.int32),
+                                           np.ones(2, np.int32), 148)
+    assert runs == 0 and tiles == 0 and (skip == 0).all()

@@ -1,0 +1,136 @@
+"""GPU parity of kv_append + paged_attn against the fp64 CPU oracle.
+
+Tolerance (bf16 inputs, fp32 accumulation, bf16 output): max |err| <= 2e-2
+and mean |err| <= 2e-3 against the oracle's fp64 result. kv_append is a byte
+copy and must match bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_path import (assert_attention_close, dev_tensor, dims_of, oracle_attention,
+                      run_attention)
+import speculative_decode_gb300 as sa
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from speculative_decode_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_config_parity_all_rows(cfg):
+    """The five workloads at full size, every output row against the oracle."""
+    w = wl.config(cfg)
+    out, err, _, _ = run_attention(w)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), f"config {cfg}")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_small_cases(seed):
+    rng = np.random.default_rng(seed)
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    w = wl.random_case(100 + seed, num_seqs=int(rng.integers(1, 7)), Hq=G * Hkv, Hkv=Hkv,
+                       max_ctx=int(rng.choice([40, 300, 1300])),
+                       q_len_choices=(0, 1, 2, 3, 6, 16))
+    out, err, _, _ = run_attention(w)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), f"seed {seed}")
+
+
+def test_kv_append_bit_exact():
+    w = wl.random_case(31, num_seqs=5, Hq=8, Hkv=4, max_ctx=900, q_len_choices=(0, 1, 5, 16))
+    _, err, kp, vp = run_attention(w)
+    kref, vref = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table,
+                                  w.pos_start, w.q_lens)
+    assert err == 0
+    assert np.array_equal(kp, kref) and np.array_equal(vp, vref)
+
+
+def test_whole_sequence_is_new_and_single_token_context():
+    """q_len == seq_len (every key is a new token) and seq_len == 1."""
+    w = wl.random_case(41, num_seqs=3, Hq=4, Hkv=2, max_ctx=16, q_len_choices=(16,))
+    w.seq_lens = w.q_lens.copy()
+    w.seq_lens[1] = 1
+    w.q_lens[1] = 1
+    w.q = w.q[: int(w.q_lens.sum())]
+    w.k_new = w.k_new[: int(w.q_lens.sum())]
+    w.v_new = w.v_new[: int(w.q_lens.sum())]
+    out, err, _, _ = run_attention(w)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), "q_len == seq_len")
+
+
+def test_long_sequence_many_splits_and_ragged_tail():
+    w = wl.random_case(43, num_seqs=2, Hq=8, Hkv=1, max_ctx=9000, q_len_choices=(1, 6))
+    out, err, _, _ = run_attention(w)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), "long")
+
+
+def test_repeated_calls_identical():
+    w = wl.config(0)
+    a, _, _, _ = run_attention(w, reps=1)
+    b, _, _, _ = run_attention(w, reps=3)
+    assert np.array_equal(a, b)
+
+
+def test_declared_max_q_len_above_actual():
+    w = wl.random_case(47, num_seqs=4, Hq=8, Hkv=2, max_ctx=700, q_len_choices=(1, 2))
+    out, err, _, _ = run_attention(w, max_q_len=16)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), "max_q_len 16")
+
+
+def test_out_of_range_page_sets_the_flag():
+    w = wl.random_case(51, num_seqs=3, Hq=4, Hkv=2, max_ctx=600, q_len_choices=(1,))
+    w.block_table = w.block_table.copy()
+    w.block_table[1, 0] = w.num_pages + 5
+    _, err, _, _ = run_attention(w, append=False)
+    assert err & (1 << 3)
+
+
+def test_q_len_above_seq_len_sets_the_flag():
+    w = wl.random_case(52, num_seqs=3, Hq=4, Hkv=2, max_ctx=600, q_len_choices=(2,))
+    w.seq_lens = w.seq_lens.copy()
+    w.seq_lens[2] = 1
+    _, err, _, _ = run_attention(w, append=False)
+    assert err & (1 << 7)
+
+
+def test_output_canary_untouched():
+    w = wl.config(0)
+    d = dims_of(w)
+    q = dev_tensor(w.q)
+    out = torch.full((w.total_q + 4, w.num_q_heads, 128), 0x1234, dtype=torch.int16, device="cuda")
+    ws = torch.zeros(sa.paged_attn_workspace_size(d), dtype=torch.uint8, device="cuda")
+    sa.paged_attn(d, q, dev_tensor(w.k_pages), dev_tensor(w.v_pages), dev_tensor(w.block_table),
+                  dev_tensor(w.seq_lens), dev_tensor(w.q_lens), w.scale, out, ws)
+    torch.cuda.synchronize()
+    assert bool((out[w.total_q:] == 0x1234).all())
+
+
+def test_host_argument_errors():
+    w = wl.config(0)
+    d = dims_of(w)
+    q = dev_tensor(w.q)
+    out = torch.zeros_like(q)
+    small = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    args = (q, dev_tensor(w.k_pages), dev_tensor(w.v_pages), dev_tensor(w.block_table),
+            dev_tensor(w.seq_lens), dev_tensor(w.q_lens), w.scale, out)
+    with pytest.raises(sa.SpecAttnError) as e:
+        sa.paged_attn(d, *args, small)
+    assert e.value.code == 6
+    bad = dims_of(w)
+    bad.head_dim = 64
+    with pytest.raises(sa.SpecAttnError) as e:
+        sa.paged_attn(bad, *args, small)
+    assert e.value.code == 2
