@@ -68,13 +68,14 @@ SplitConfig split_config(const sa_dims &d, const sa_plan *plan, int sms) {
     SplitConfig c{};
     const int G = d.num_q_heads / d.num_kv_heads;
     const int rows = G * std::max(1, d.max_q_len);
-    c.R = rows <= 4 ? 4 : rows <= 8 ? 8 : rows <= 12 ? 12 : 16;
+    c.R = rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
     c.nrb = (rows + c.R - 1) / c.R;
     const int max_pages = std::max(1, d.max_pages_per_seq);
     const int pps_min = (max_pages + kMaxSplits - 1) / kMaxSplits;
-    // aim for about six units per SM so that the persistent warps stay balanced
+    // aim for about 24 units per SM (four per resident warp): warps claim units
+    // dynamically, so smaller units balance better, at the price of more partials
     const int64_t slots = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.nrb * max_pages;
-    const int64_t target = static_cast<int64_t>(std::max(1, sms)) * 6;
+    const int64_t target = static_cast<int64_t>(std::max(1, sms)) * 24;
     c.pps = static_cast<int>(std::max<int64_t>(pps_min, std::min<int64_t>(max_pages, slots / target)));
     c.pps = std::max(c.pps, 1);
     c.n_splits = (max_pages + c.pps - 1) / c.pps;
@@ -85,11 +86,13 @@ SplitConfig split_config(const sa_dims &d, const sa_plan *plan, int sms) {
 }
 
 // Workspace layout: fp32 accumulators [n_slots][total_q * Hq][128], then
-// (max, sum) pairs [n_slots][total_q * Hq][2]. It is sized for the finest
-// split any device could choose, so sizing needs no device.
+// (max, sum) pairs [n_slots][total_q * Hq][2], then int32 counters (unit
+// claims, finished warps, per (sequence, KV head, row block) finished splits).
+// It is sized for the finest split any device could choose, so sizing needs
+// no device.
 struct WsLayout {
     int64_t slots_cap;
-    size_t ml_offset, total;
+    size_t ml_offset, ctr_offset, total;
 };
 
 WsLayout attn_ws_layout(const sa_dims &d, const sa_plan *plan) {
@@ -100,8 +103,11 @@ WsLayout attn_ws_layout(const sa_dims &d, const sa_plan *plan) {
     const int64_t rows = static_cast<int64_t>(d.total_q) * d.num_q_heads;
     const size_t acc = static_cast<size_t>(w.slots_cap * rows * kHeadDim * 4);
     const size_t ml = static_cast<size_t>(w.slots_cap * rows * 2 * 4);
+    const SplitConfig c = split_config(d, plan, 1);
+    const size_t ctr = (2 + static_cast<size_t>(d.num_seqs) * d.num_kv_heads * c.nrb) * 4;
     w.ml_offset = (acc + 255) / 256 * 256;
-    w.total = w.ml_offset + (ml + 255) / 256 * 256;
+    w.ctr_offset = w.ml_offset + (ml + 255) / 256 * 256;
+    w.total = w.ctr_offset + (ctr + 255) / 256 * 256;
     return w;
 }
 
@@ -242,6 +248,8 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     p.run_slots = pd ? pd->run_slots : nullptr;
     p.ws_acc = ws_acc;
     p.ws_ml = ws_ml;
+    p.sched = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + wl.ctr_offset);
+    p.merge_ctr = p.sched + 2;
     p.err = err_flag;
     p.B = d.num_seqs;
     p.Hq = d.num_q_heads;
@@ -266,25 +274,6 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     const int64_t ctas = std::min<int64_t>(static_cast<int64_t>(sms) * per_sm, c.n_units);
     if (ctas > 0 && launch_split_attn(p, tmk, tmv, static_cast<int>(ctas), 1, s) != cudaSuccess)
         return SA_ERR_CUDA;
-
-    if (c.n_splits > 1 || c.run_slots > 0) {
-        CombineParams cp{};
-        cp.out = out;
-        cp.seq_lens = seq_lens;
-        cp.q_lens = q_lens;
-        cp.skip_pages = p.skip_pages;
-        cp.run_slots = p.run_slots;
-        cp.ws_acc = ws_acc;
-        cp.ws_ml = ws_ml;
-        cp.B = d.num_seqs;
-        cp.Hq = d.num_q_heads;
-        cp.max_q_len = d.max_q_len;
-        cp.total_q = d.total_q;
-        cp.pages_per_split = c.pps;
-        cp.slot_base = c.run_slots;
-        cp.n_rows_total = static_cast<int32_t>(rows_total);
-        if (launch_combine(cp, s) != cudaSuccess) return SA_ERR_CUDA;
-    }
     return finish(s, err_flag);
 }
 
@@ -294,7 +283,8 @@ int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan) {
     if (sms <= 0) return -1;
     const SplitConfig c = split_config(*dims, plan, sms);
     const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
-    return 1 + ((c.n_splits > 1 || c.run_slots > 0) ? 1 : 0) + ((pd && pd->num_tiles > 0) ? 1 : 0);
+    (void)c;
+    return 1 + ((pd && pd->num_tiles > 0) ? 1 : 0);
 }
 
 size_t sa_spec_verify_workspace_size(int32_t num_seqs, int32_t k_max, int32_t vocab) {

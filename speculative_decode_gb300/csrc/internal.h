@@ -44,9 +44,11 @@ struct SplitParams {
     const int32_t *run_slots;   // nullable: partials the shared-prefix path writes per sequence
     float *ws_acc;              // [n_slots][total_q * Hq][128] fp32 unnormalised accumulators
     float *ws_ml;               // [n_slots][total_q * Hq][2] running max (log2 units), sum
+    int32_t *sched;             // [2] unit claim counter, finished-warp counter (zero between calls)
+    int32_t *merge_ctr;         // [B * Hkv * n_row_blocks] finished splits (zero between calls)
     int32_t *err;
     int32_t B, Hq, Hkv, G, num_pages, max_pages, total_q, max_q_len;
-    int32_t rows_per_block;     // R, rows of one work unit
+    int32_t rows_per_block;     // R, rows of one work unit (4, 8 or 16)
     int32_t n_row_blocks;
     int32_t pages_per_split;
     int32_t n_splits;
@@ -57,24 +59,10 @@ struct SplitParams {
     int32_t evict_first;
 };
 
-size_t split_smem_bytes(int R, int stages);
-int max_rows_per_block();
 cudaError_t launch_split_attn(const SplitParams &p, const CUtensorMap &tmap_k,
                               const CUtensorMap &tmap_v, int num_ctas, int warps_per_cta,
                               cudaStream_t stream);
 cudaError_t split_occupancy(int R, int warps_per_cta, int *ctas_per_sm);
-
-struct CombineParams {
-    uint16_t *out;
-    const int32_t *seq_lens;
-    const int32_t *q_lens;
-    const int32_t *skip_pages;
-    const int32_t *run_slots;
-    const float *ws_acc;
-    const float *ws_ml;
-    int32_t B, Hq, max_q_len, total_q, pages_per_split, slot_base, n_rows_total;
-};
-cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream);
 
 cudaError_t launch_kv_append(const sa_dims &d, const uint16_t *k_new, const uint16_t *v_new,
                              uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,

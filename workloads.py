@@ -172,8 +172,11 @@ def add_verify_inputs(w: Workload, rng: np.random.Generator, k_max: int, vocab: 
         for j in range(k_max + 1):
             logits[b, j, planted[b, j]] = logits[b, j].max() + np.float32(1.0)
     match = rng.random(size=(B, k_max)) < p_match
-    other = rng.integers(0, vocab - 1, size=(B, k_max)).astype(np.int32)
-    other = other + (other >= planted[:, :k_max])  # uniform over tokens != planted
+    if vocab > 1:
+        other = rng.integers(0, vocab - 1, size=(B, k_max)).astype(np.int32)
+        other = other + (other >= planted[:, :k_max])  # uniform over tokens != planted
+    else:
+        other = planted[:, :k_max].copy()             # a one-token vocabulary always matches
     cand = np.where(match, planted[:, :k_max], other).astype(np.int32)
     w.logits = logits
     w.candidates = cand
