@@ -55,33 +55,26 @@ int check_dims(const sa_dims *d) {
     return SA_OK;
 }
 
-// Work decomposition of the split kernel; a pure function of the shapes and
-// the SM count so that workspace sizing and launch agree.
+// Work decomposition of the split kernel: rows per segment and the partial
+// slots pieces may use (a pure function of the shapes).
 struct SplitConfig {
-    int R, nrb, pps, n_splits, run_slots, n_slots;
-    int64_t n_units;
+    int R, nrb, piece_slots, min_tiles, run_slots, n_slots;
 };
 
-constexpr int kMaxSplits = 64;
+constexpr int kPieceSlots = 16;
 
-SplitConfig split_config(const sa_dims &d, const sa_plan *plan, int sms) {
+SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     SplitConfig c{};
     const int G = d.num_q_heads / d.num_kv_heads;
     const int rows = G * std::max(1, d.max_q_len);
     c.R = rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
     c.nrb = (rows + c.R - 1) / c.R;
-    const int max_pages = std::max(1, d.max_pages_per_seq);
-    const int pps_min = (max_pages + kMaxSplits - 1) / kMaxSplits;
-    // aim for about 24 units per SM (four per resident warp): warps claim units
-    // dynamically, so smaller units balance better, at the price of more partials
-    const int64_t slots = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.nrb * max_pages;
-    const int64_t target = static_cast<int64_t>(std::max(1, sms)) * 24;
-    c.pps = static_cast<int>(std::max<int64_t>(pps_min, std::min<int64_t>(max_pages, slots / target)));
-    c.pps = std::max(c.pps, 1);
-    c.n_splits = (max_pages + c.pps - 1) / c.pps;
+    const int max_tiles = std::max(1, d.max_pages_per_seq) * (kPageSize / 32);
+    c.piece_slots = std::min(kPieceSlots, max_tiles);
+    // a segment of s tiles spans at most ceil(s / C) + 1 warps' ranges
+    c.min_tiles = c.piece_slots > 1 ? (max_tiles + c.piece_slots - 2) / (c.piece_slots - 1) : max_tiles;
     c.run_slots = plan ? plan_run_slots(plan) : 0;
-    c.n_slots = c.run_slots + c.n_splits;
-    c.n_units = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.nrb * c.n_splits;
+    c.n_slots = c.run_slots + c.piece_slots;
     return c;
 }
 
@@ -97,14 +90,12 @@ struct WsLayout {
 
 WsLayout attn_ws_layout(const sa_dims &d, const sa_plan *plan) {
     WsLayout w{};
-    const int max_pages = std::max(1, d.max_pages_per_seq);
-    const int pps_min = (max_pages + kMaxSplits - 1) / kMaxSplits;
-    w.slots_cap = (plan ? plan_run_slots(plan) : 0) + (max_pages + pps_min - 1) / pps_min;
+    const SplitConfig c = split_config(d, plan);
+    w.slots_cap = c.n_slots;
     const int64_t rows = static_cast<int64_t>(d.total_q) * d.num_q_heads;
     const size_t acc = static_cast<size_t>(w.slots_cap * rows * kHeadDim * 4);
     const size_t ml = static_cast<size_t>(w.slots_cap * rows * 2 * 4);
-    const SplitConfig c = split_config(d, plan, 1);
-    const size_t ctr = (2 + static_cast<size_t>(d.num_seqs) * d.num_kv_heads * c.nrb) * 4;
+    const size_t ctr = static_cast<size_t>(d.num_seqs) * d.num_kv_heads * c.nrb * 4;
     w.ml_offset = (acc + 255) / 256 * 256;
     w.ctr_offset = w.ml_offset + (ml + 255) / 256 * 256;
     w.total = w.ctr_offset + (ctr + 255) / 256 * 256;
@@ -216,7 +207,7 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     if (sms <= 0) return SA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    const SplitConfig c = split_config(d, plan, sms);
+    const SplitConfig c = split_config(d, plan);
     const int64_t rows_total = static_cast<int64_t>(d.total_q) * d.num_q_heads;
     float *ws_acc = static_cast<float *>(workspace);
     float *ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.ml_offset);
@@ -248,8 +239,7 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     p.run_slots = pd ? pd->run_slots : nullptr;
     p.ws_acc = ws_acc;
     p.ws_ml = ws_ml;
-    p.sched = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + wl.ctr_offset);
-    p.merge_ctr = p.sched + 2;
+    p.merge_ctr = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + wl.ctr_offset);
     p.err = err_flag;
     p.B = d.num_seqs;
     p.Hq = d.num_q_heads;
@@ -261,18 +251,16 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     p.max_q_len = d.max_q_len;
     p.rows_per_block = c.R;
     p.n_row_blocks = c.nrb;
-    p.pages_per_split = c.pps;
-    p.n_splits = c.n_splits;
+    p.min_tiles_per_warp = c.min_tiles;
     p.slot_base = c.run_slots;
     p.n_rows_total = static_cast<int32_t>(rows_total);
-    p.n_units = c.n_units;
     p.qscale = scale * 1.4426950408889634f;
     p.evict_first = c.nrb == 1;
 
     int per_sm = 0;
     if (split_occupancy(c.R, 1, &per_sm) != cudaSuccess || per_sm <= 0) return SA_ERR_CUDA;
-    const int64_t ctas = std::min<int64_t>(static_cast<int64_t>(sms) * per_sm, c.n_units);
-    if (ctas > 0 && launch_split_attn(p, tmk, tmv, static_cast<int>(ctas), 1, s) != cudaSuccess)
+    const int64_t ctas = static_cast<int64_t>(sms) * per_sm;  // one warp per CTA, all resident
+    if (launch_split_attn(p, tmk, tmv, static_cast<int>(ctas), 1, s) != cudaSuccess)
         return SA_ERR_CUDA;
     return finish(s, err_flag);
 }
@@ -281,9 +269,7 @@ int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan) {
     if (check_dims(dims) != SA_OK) return -1;
     const int sms = device_sm_count();
     if (sms <= 0) return -1;
-    const SplitConfig c = split_config(*dims, plan, sms);
     const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
-    (void)c;
     return 1 + ((pd && pd->num_tiles > 0) ? 1 : 0);
 }
 

@@ -1,36 +1,38 @@
-// attn_split.cu -- page-streamed attention on the CUDA cores (split-K over
-// pages) for decode (q_len = 1) and causal multi-query verification
-// (q_len = k + 1).
+// attn_split.cu -- page-streamed attention on the CUDA cores for decode
+// (q_len = 1) and causal multi-query verification (q_len = k + 1).
 //
 // What it computes: for each sequence b, new query token i and query head h,
 // softmax(scale * q . K_b^T) V_b over the keys at positions
 // 0 .. seq_len - q_len + i, with K_b/V_b gathered through the block table
 // (ExLlamaV2 "Dynamic Generator" page, "Continuous batching"; causal rows as
 // in the Hugging Face "Assisted Generation" page, "How Assisted Generation
-// works"). The softmax is evaluated online over 32-token tiles; the pages of a
-// sequence are cut into splits whose partial (max, sum, accumulator) states
-// are merged exactly, in this kernel, by whichever warp finishes a
-// sequence's last split.
+// works"). The softmax is evaluated online over 32-token tiles; where a
+// sequence's keys are cut into pieces, the partial (max, sum, accumulator)
+// states are merged exactly, in this kernel, by whichever warp finishes the
+// last piece.
 //
 // Design (sm_103a):
-//  * Work unit = (sequence, KV head, row block, split of `pages_per_split`
-//    pages). Rows are the G query heads of the KV head times the sequence's
-//    query tokens, so every K/V byte read serves all of them.
-//  * One warp owns a unit from start to finish. Lane 0 streams the unit's
-//    32-token K and V tiles with TMA (2-D tensor copies, 128-byte swizzle)
-//    into the warp's private ring of S stages; warps claim units dynamically
-//    from a global counter and keep copies of their next units in flight
-//    while computing, across unit boundaries.
+//  * Segment = (sequence, KV head, row block): the G query heads of the KV
+//    head times the sequence's new tokens (up to R rows), so every K/V byte
+//    read serves all of them. All segments' 32-token tiles form one sequence
+//    of work that is cut into equal contiguous ranges, one per warp
+//    (stream-K): perfectly balanced whatever the context lengths, with at
+//    most two partial pieces per warp and no scheduling atomics.
+//  * One warp owns its range. Lane 0 streams K and V tiles with TMA (2-D
+//    tensor copies, 128-byte swizzle) into the warp's private ring of S
+//    stages and bulk-copies each piece's query rows ahead of use; all 32
+//    lanes compute.
 //  * Lane mapping: a token is handled by L = 2R lanes (8, 16 or 32), each
-//    owning 128/L head dimensions, so the pre-scaled queries and the output
-//    accumulators live in registers. Q.K partial dots are combined with a
-//    shuffle reduce-scatter, after which each lane holds one (token, row)
-//    score; P.V reuses the same mapping with p broadcast from shared memory.
-//    Products use packed fp32x2 FMAs (bf16 inputs converted exactly).
-//  * Every wait on a TMA barrier is bounded (common.cuh); on timeout the
-//    warp flags SA_ERR_TIMEOUT, drains its copies in flight and leaves.
-#include <cstdlib>
-
+//    owning 128/L head dims, so pre-scaled queries and output accumulators
+//    live in registers. Q.K partial dots are combined with a shuffle
+//    reduce-scatter, after which each lane holds one (token, row) score; P.V
+//    reuses the mapping with p broadcast from shared memory. Products use
+//    packed fp32x2 FMAs on exactly converted bf16 inputs.
+//  * A piece that is not a whole segment stores an fp32 partial and counts
+//    itself with a release atomic whose result is examined one piece later,
+//    so the round trip is hidden; the last piece merges.
+//  * Every wait on a barrier is bounded (common.cuh); on timeout the warp
+//    flags SA_ERR_TIMEOUT, drains its copies in flight and leaves.
 #include "common.cuh"
 
 namespace sa {
@@ -40,7 +42,9 @@ namespace {
 constexpr int kTile = 32;                     // tokens per stage
 constexpr int kHalfBytes = kTile * 128;       // 32 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kStageBytes = 4 * kHalfBytes;   // K[0:64], K[64:128], V[0:64], V[64:128]
-constexpr int kRing = 8;                      // claimed-unit FIFO depth per warp
+constexpr int kStages = 2;                    // pipeline depth per warp
+constexpr int kRing = 4;                      // piece descriptors in flight (>= kStages + 1)
+constexpr int kPieceInts = 16;
 
 template <int R>
 struct Geo {
@@ -50,27 +54,25 @@ struct Geo {
     static constexpr int NW = kHeadDim / L / 2;                // bf16x2 words per lane
 };
 
-template <int R, int S>
+template <int R>
 struct Layout {
-    static constexpr int kPOff = S * kStageBytes;               // fp32 p [32][R]
-    static constexpr int kRowOff = kPOff + kTile * R * 4;       // fp32 [2][R] row exchange
-    static constexpr int kRingOff = kRowOff + 2 * R * 4;        // int32 [kRing]
-    static constexpr int kBarOff = (kRingOff + kRing * 4 + 7) / 8 * 8;
-    static constexpr int kBytes = (kBarOff + S * 8 + 1023) / 1024 * 1024;
+    static constexpr int kQOff = kStages * kStageBytes;                  // bf16 q [S][R][128]
+    static constexpr int kPOff = kQOff + kStages * R * kHeadDim * 2;     // fp32 p [32][R]
+    static constexpr int kRowOff = kPOff + kTile * R * 4;                // fp32 [2][R]
+    static constexpr int kRingOff = kRowOff + 2 * R * 4;                 // int32 [kRing][16]
+    static constexpr int kBarOff = kRingOff + kRing * kPieceInts * 4;    // uint64 [2][kStages]
+    static constexpr int kBytes = (kBarOff + 2 * kStages * 8 + 1023) / 1024 * 1024;
 };
 
-struct Unit {
-    int b, kvh, rb, T, n, qstart, t_lo, t_hi, n_tiles, slot, nsplit, runs;
-    bool direct, ok;
+// A piece: the part of one segment inside this warp's range.
+struct Piece {
+    int b, kvh, rb, T, n, qstart, t_lo, n_tiles, piece, pieces, nvr, runs;
 };
 
-__device__ __forceinline__ int warp_sum_i(int v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
+struct SeqInfo {
+    int T, n, skip_tok, tiles, nrb;
+};
 
-// Packed fp32x2 fused multiply-add: d = a * b + c elementwise, one rounding each.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     unsigned long long ra = *reinterpret_cast<unsigned long long *>(&a);
     unsigned long long rb = *reinterpret_cast<unsigned long long *>(&b);
@@ -111,67 +113,43 @@ __device__ __forceinline__ int lane_dim_of_word(int j, int k) {
     else return 4 * j + 2 * k;
 }
 
-// Packed query rows that precede sequence b (sum of q_lens[0..b)).
-__device__ __forceinline__ int q_row_start(const int32_t *q_lens, int b, int lane) {
-    int s = 0;
-    for (int k = lane; k < b; k += 32) s += q_lens[k];
-    return warp_sum_i(s);
-}
-
-// Decode unit u (warp-uniform; every lane calls). Returns false when the
-// unit has no work; U.ok = false when a page id is out of range.
-template <int R>
-__device__ bool decode_unit(const SplitParams &P, int64_t u, Unit &U, int lane) {
-    const int per_split = P.B * P.Hkv * P.n_row_blocks;
-    const int split = static_cast<int>(u / per_split);
-    int rem = static_cast<int>(u % per_split);
-    U.b = rem / (P.Hkv * P.n_row_blocks);
-    rem %= P.Hkv * P.n_row_blocks;
-    U.kvh = rem / P.n_row_blocks;
-    U.rb = rem % P.n_row_blocks;
-    U.T = P.seq_lens[U.b];
-    U.n = P.q_lens[U.b];
-    if (U.n <= 0) return false;
-    if (U.n > U.T || U.n > P.max_q_len) {
-        if (lane == 0) flag_error(P.err, kErrBitQlen);
-        return false;
-    }
-    if (U.rb * R >= P.G * U.n) return false;
-    const int npages = (U.T + kPageSize - 1) / kPageSize;
-    const int skip = P.skip_pages ? P.skip_pages[U.b] : 0;
-    const int p_lo = skip + split * P.pages_per_split;
-    if (p_lo >= npages) return false;
-    U.qstart = q_row_start(P.q_lens, U.b, lane);
-    if (U.qstart + U.n > P.total_q) {  // q_lens disagree with dims.total_q
-        if (lane == 0) flag_error(P.err, kErrBitQlen);
-        return false;
-    }
-    const int p_hi = min(p_lo + P.pages_per_split, npages);
-    U.t_lo = p_lo * kPageSize;
-    U.t_hi = min(p_hi * kPageSize, U.T);
-    U.n_tiles = (U.t_hi - U.t_lo + kTile - 1) / kTile;
-    U.nsplit = (npages - skip + P.pages_per_split - 1) / P.pages_per_split;
-    U.runs = P.run_slots ? P.run_slots[U.b] : 0;
-    U.direct = (U.nsplit == 1 && U.runs == 0);
-    U.slot = P.slot_base + split;
-    bool ok = npages <= P.max_pages;
-    for (int jp = p_lo + lane; ok && jp < p_hi; jp += 32) {
-        const int id = P.block_table[static_cast<int64_t>(U.b) * P.max_pages + jp];
-        ok = id >= 0 && id < P.num_pages;
-    }
-    U.ok = __all_sync(0xffffffffu, ok);
-    return true;
-}
-
-__device__ __forceinline__ int64_t out_row(const SplitParams &P, const Unit &U, int rr) {
+__device__ __forceinline__ int64_t out_row(const SplitParams &P, const Piece &U, int rr) {
     return static_cast<int64_t>(U.qstart + rr / P.G) * P.Hq + U.kvh * P.G + rr % P.G;
 }
 
-// Merge every partial of rows [rb*R, rb*R + nvr) of (b, kvh): the slots of the
-// shared-prefix runs and of the splits, with exact max-shifted rescaling.
-__device__ void merge_rows(const SplitParams &P, const Unit &U, int R, int nvr, int lane) {
-    const int nslots = U.runs + U.nsplit;
-    for (int r = 0; r < nvr; ++r) {
+// Per-sequence shape of the work; tiles = 0 when the sequence has none.
+template <int R>
+__device__ __forceinline__ SeqInfo seq_info(const SplitParams &P, int b, int qstart, bool flag) {
+    SeqInfo s;
+    s.T = P.seq_lens[b];
+    s.n = P.q_lens[b];
+    s.tiles = 0;
+    s.nrb = 0;
+    s.skip_tok = 0;
+    if (s.n <= 0) return s;
+    const int npages = (s.T + kPageSize - 1) / kPageSize;
+    if (s.n > s.T || s.n > P.max_q_len || qstart + s.n > P.total_q || npages > P.max_pages) {
+        if (flag) flag_error(P.err, kErrBitQlen);
+        return s;
+    }
+    const int skip = P.skip_pages ? P.skip_pages[b] : 0;
+    const int runs = P.run_slots ? P.run_slots[b] : 0;
+    s.skip_tok = skip * kPageSize;
+    const int keys = s.T - s.skip_tok;
+    s.tiles = keys > 0 ? (keys + kTile - 1) / kTile : (runs > 0 ? 1 : 0);  // one empty tile carries the merge
+    s.nrb = (P.G * s.n + R - 1) / R;
+    return s;
+}
+
+__device__ __forceinline__ int64_t seq_work(const SplitParams &P, const SeqInfo &s) {
+    return static_cast<int64_t>(s.tiles) * P.Hkv * s.nrb;
+}
+
+// Merge every partial of the piece's rows: the shared-prefix runs' slots and
+// the pieces' slots, with exact max-shifted rescaling. Lane = 4 head dims.
+__device__ void merge_rows(const SplitParams &P, const Piece &U, int R, int lane) {
+    const int nslots = U.runs + U.pieces;
+    for (int r = 0; r < U.nvr; ++r) {
         const int64_t row = out_row(P, U, U.rb * R + r);
         float M = -INFINITY;
         for (int k = 0; k < nslots; ++k) {
@@ -202,48 +180,122 @@ __device__ void merge_rows(const SplitParams &P, const Unit &U, int R, int nvr, 
     }
 }
 
-// After a split's partial is stored: count it; the last split of (b, kvh,
-// row block) merges all partials and resets the counter for the next call.
-__device__ void count_and_merge(const SplitParams &P, const Unit &U, int R, int nvr, int lane) {
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-        int32_t *ctr = P.merge_ctr + (static_cast<int64_t>(U.b) * P.Hkv + U.kvh) * P.n_row_blocks + U.rb;
-        last = atomicAdd(ctr, 1) == U.nsplit - 1;
-        if (last) atomicExch(ctr, 0);
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence();
-    merge_rows(P, U, R, nvr, lane);
+__device__ __forceinline__ int32_t *merge_counter(const SplitParams &P, const Piece &U) {
+    return P.merge_ctr + (static_cast<int64_t>(U.b) * P.Hkv + U.kvh) * P.n_row_blocks + U.rb;
 }
 
-template <int R, int S>
+// A counted piece whose atomic result is examined later.
+struct Pending {
+    Piece U;
+    int old;
+    bool live;
+};
+
+__device__ void resolve(const SplitParams &P, Pending &pd, int R, int lane) {
+    if (!pd.live) return;
+    pd.live = false;
+    const int old = __shfl_sync(0xffffffffu, pd.old, 0);
+    if (old != pd.U.pieces - 1) return;
+    __threadfence();  // acquire: every other piece's partial is visible
+    merge_rows(P, pd.U, R, lane);
+    if (lane == 0) atomicExch(merge_counter(P, pd.U), 0);
+}
+
+template <int R>
 __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
                                                         const __grid_constant__ CUtensorMap tmk,
                                                         const __grid_constant__ CUtensorMap tmv) {
     using Gm = Geo<R>;
-    using Lay = Layout<R, S>;
+    using Lay = Layout<R>;
     constexpr int L = Gm::L, TG = Gm::TG, NS = Gm::NS, NW = Gm::NW;
+    constexpr int S = kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int lane = threadIdx.x & 31;
     const int tg = lane / L;   // token group
     const int j = lane % L;    // lane within the token group
+    uint16_t *qbuf = reinterpret_cast<uint16_t *>(smem + Lay::kQOff);
     float(*pbuf)[R] = reinterpret_cast<float(*)[R]>(smem + Lay::kPOff);
     float *rowx = reinterpret_cast<float *>(smem + Lay::kRowOff);
     int32_t *ring = reinterpret_cast<int32_t *>(smem + Lay::kRingOff);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::kBarOff);
+    uint64_t *qfull = full + S;
 
     if (lane == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&qfull[s], 1);
+        }
         fence_barrier_init();
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
     }
+
+    // ---- 1. total work and this warp's range [g_begin, g_end) of tiles
+    // lanes take contiguous chunks of sequences; two passes: query offsets, then work
+    const int per = (P.B + 31) / 32;
+    const int c_lo = min(P.B, lane * per), c_hi = min(P.B, c_lo + per);
+    int cq = 0;
+    for (int b = c_lo; b < c_hi; ++b) cq += max(0, P.q_lens[b]);
+    int q_pre = cq;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, q_pre, o);
+        if (lane >= o) q_pre += v;
+    }
+    q_pre -= cq;  // exclusive
+    int64_t cw = 0;
+    {
+        int qs = q_pre;
+        for (int b = c_lo; b < c_hi; ++b) {
+            const SeqInfo si = seq_info<R>(P, b, qs, true);
+            cw += seq_work(P, si);
+            qs += max(0, si.n);
+        }
+    }
+    int64_t w_pre = cw;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t v = __shfl_up_sync(0xffffffffu, w_pre, o);
+        if (lane >= o) w_pre += v;
+    }
+    const int64_t total = __shfl_sync(0xffffffffu, w_pre, 31);
+    w_pre -= cw;
+    const int64_t W = gridDim.x;
+    // at least min_tiles_per_warp, so that no segment splits into more pieces
+    // than the workspace has partial slots
+    const int64_t C = max((total + W - 1) / W, static_cast<int64_t>(max(P.min_tiles_per_warp, 1)));
+    const int64_t g_begin = static_cast<int64_t>(blockIdx.x) * C;
+    const int64_t g_end = min(total, g_begin + C);
     __syncwarp();
+    if (g_begin >= g_end) return;
+
+    // ---- 2. locate the first tile: sequence, segment, tile within segment
+    int b0 = 0, q0 = 0;
+    int64_t ws0 = 0;
+    {
+        const bool mine = cw > 0 && w_pre <= g_begin && g_begin < w_pre + cw;
+        const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+        if (lane == src) {
+            int64_t pos = w_pre;
+            int qs = q_pre;
+            int b = c_lo;
+            for (; b < c_hi; ++b) {
+                const SeqInfo si = seq_info<R>(P, b, qs, false);
+                const int64_t wb = seq_work(P, si);
+                if (g_begin < pos + wb) break;
+                pos += wb;
+                qs += max(0, si.n);
+            }
+            b0 = b;
+            q0 = qs;
+            ws0 = pos;
+        }
+        b0 = __shfl_sync(0xffffffffu, b0, src);
+        q0 = __shfl_sync(0xffffffffu, q0, src);
+        ws0 = __shfl_sync(0xffffffffu, ws0, src);
+    }
 
     // row of the reduce-scatter result this lane ends up holding
     int rj = 0;
@@ -257,42 +309,80 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
     }
     const uint64_t policy = P.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
 
-    // ---- issue side: claims units, pushes them to the ring, streams tiles
-    uint32_t issued = 0, consumed = 0;
-    int ring_head = 0, ring_tail = 0;   // pushed / popped unit counts
-    bool exhausted = false;
-    Unit IU;
-    int itile = 0, intiles = 0;
+    // ---- issue cursor: walks tiles g_begin .. g_end-1 ahead of the consumer
+    int ib = b0, iq = q0;
+    int64_t iws = ws0;
+    SeqInfo isi = seq_info<R>(P, ib, iq, false);
+    int64_t ig = g_begin;
+    int iseg, itile;
+    {
+        const int64_t off = g_begin - iws;
+        iseg = static_cast<int>(off / isi.tiles);
+        itile = static_cast<int>(off % isi.tiles);
+    }
+    uint32_t issued = 0, consumed = 0, pieces_pushed = 0;
     auto issue_next = [&]() -> bool {
-        while (itile >= intiles) {
-            if (exhausted || ring_head - ring_tail >= kRing) return false;
-            int u = 0;
-            if (lane == 0) u = atomicAdd(P.sched, 1);
-            u = __shfl_sync(0xffffffffu, u, 0);
-            if (u >= P.n_units) {
-                exhausted = true;
-                return false;
-            }
-            if (!decode_unit<R>(P, u, IU, lane)) continue;
-            if (lane == 0) ring[ring_head % kRing] = u;
-            ++ring_head;
-            intiles = IU.ok ? IU.n_tiles : 0;
+        if (ig >= g_end) return false;
+        if (itile == isi.tiles) {  // next segment
             itile = 0;
+            if (++iseg == P.Hkv * isi.nrb) {  // next sequence with work
+                iseg = 0;
+                do {
+                    iws += seq_work(P, isi);
+                    iq += max(0, isi.n);
+                    if (++ib >= P.B) return false;  // unreachable while ig < g_end
+                    isi = seq_info<R>(P, ib, iq, false);
+                } while (seq_work(P, isi) == 0);
+            }
         }
-        const int t0 = IU.t_lo + itile * kTile;
-        const int pid = P.block_table[static_cast<int64_t>(IU.b) * P.max_pages + t0 / kPageSize];
-        const int y = (pid * P.Hkv + IU.kvh) * kPageSize + (t0 % kPageSize);
+        const int kvh = iseg / isi.nrb, rb = iseg % isi.nrb;
+        if (ig == g_begin || itile == 0) {
+            // a new piece: describe it for the consumer and fetch its query rows
+            const int64_t seg0 = iws + static_cast<int64_t>(iseg) * isi.tiles;
+            const int64_t seg1 = seg0 + isi.tiles;
+            const int first = static_cast<int>(seg0 / C), last = static_cast<int>((seg1 - 1) / C);
+            const int nvr = min(R, P.G * isi.n - rb * R);
+            const int qs = pieces_pushed % S;
+            if (lane == 0) {
+                int32_t *d = ring + (pieces_pushed % kRing) * kPieceInts;
+                d[0] = ib; d[1] = kvh; d[2] = rb; d[3] = isi.T; d[4] = isi.n; d[5] = iq;
+                d[6] = isi.skip_tok + itile * kTile;
+                d[7] = static_cast<int>(min(seg1, g_end) - ig);
+                d[8] = static_cast<int>(blockIdx.x) - first;
+                d[9] = last - first + 1;
+                d[10] = nvr;
+                d[11] = P.run_slots ? P.run_slots[ib] : 0;
+                mbar_arrive_expect_tx(&qfull[qs], nvr * kHeadDim * 2);
+                const int r0 = rb * R;
+                for (int i = r0 / P.G; i <= (r0 + nvr - 1) / P.G; ++i) {
+                    const int lo = max(r0, i * P.G), hi = min(r0 + nvr, (i + 1) * P.G);
+                    const uint16_t *src = P.q + (static_cast<int64_t>(iq + i) * P.Hq + kvh * P.G + (lo - i * P.G)) * kHeadDim;
+                    bulk_load(qbuf + (qs * R + (lo - r0)) * kHeadDim, src, (hi - lo) * kHeadDim * 2, &qfull[qs]);
+                }
+            }
+            ++pieces_pushed;
+        }
+        // the tile: K and V rows [t0, t0 + 32) of KV head kvh
+        const int t0 = isi.skip_tok + itile * kTile;
         const int s = issued % S;
         if (lane == 0) {
-            uint8_t *dst = smem + s * kStageBytes;
-            mbar_arrive_expect_tx(&full[s], kStageBytes);
-            tma_load_2d(dst, &tmk, &full[s], 0, y, policy);
-            tma_load_2d(dst + kHalfBytes, &tmk, &full[s], 64, y, policy);
-            tma_load_2d(dst + 2 * kHalfBytes, &tmv, &full[s], 0, y, policy);
-            tma_load_2d(dst + 3 * kHalfBytes, &tmv, &full[s], 64, y, policy);
+            int pid = -1;
+            if (t0 < isi.T) pid = P.block_table[static_cast<int64_t>(ib) * P.max_pages + t0 / kPageSize];
+            if (pid >= 0 && pid < P.num_pages) {
+                const int y = (pid * P.Hkv + kvh) * kPageSize + (t0 % kPageSize);
+                uint8_t *dst = smem + s * kStageBytes;
+                mbar_arrive_expect_tx(&full[s], kStageBytes);
+                tma_load_2d(dst, &tmk, &full[s], 0, y, policy);
+                tma_load_2d(dst + kHalfBytes, &tmk, &full[s], 64, y, policy);
+                tma_load_2d(dst + 2 * kHalfBytes, &tmv, &full[s], 0, y, policy);
+                tma_load_2d(dst + 3 * kHalfBytes, &tmv, &full[s], 64, y, policy);
+            } else {
+                mbar_arrive(&full[s]);  // nothing to load: the consumer skips this tile
+            }
         }
         ++issued;
         ++itile;
+        ++ig;
         return true;
     };
     auto top_up = [&]() {
@@ -300,54 +390,45 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
         }
         __syncwarp();
     };
+    uint32_t pieces_done = 0;
+    auto bail_out = [&]() {
+        flag_error(P.err, kErrBitTimeout);
+        for (uint32_t c = consumed; c < issued; ++c) (void)mbar_wait(&full[c % S], (c / S) & 1);
+        for (uint32_t c = pieces_done; c < pieces_pushed; ++c) (void)mbar_wait(&qfull[c % S], (c / S) & 1);
+    };
 
+    Pending pend;
+    pend.live = false;
+    pend.old = 0;
     top_up();
-    while (true) {
-        if (ring_tail == ring_head) top_up();
-        if (ring_tail == ring_head) break;  // nothing claimed and nothing left
-        const int u = ring[ring_tail % kRing];
-        ++ring_tail;
-        Unit U;
-        decode_unit<R>(P, u, U, lane);
-        const int rows = P.G * U.n;
-        const int nvr = min(R, rows - U.rb * R);  // valid rows of this block
-
-        if (!U.ok) {
-            // pages out of range: report, leave an empty partial (or zeros)
-            if (lane == 0) flag_error(P.err, kErrBitPageOOB);
-            for (int r = 0; r < nvr; ++r) {
-                const int64_t row = out_row(P, U, U.rb * R + r);
-                if (U.direct) {
-                    *reinterpret_cast<uint2 *>(P.out + row * kHeadDim + lane * 4) = make_uint2(0, 0);
-                } else {
-                    const int64_t w = static_cast<int64_t>(U.slot) * P.n_rows_total + row;
-                    *reinterpret_cast<float4 *>(P.ws_acc + w * kHeadDim + lane * 4) = make_float4(0, 0, 0, 0);
-                    if (lane == 0) *reinterpret_cast<float2 *>(P.ws_ml + w * 2) = make_float2(-INFINITY, 0.f);
-                }
-            }
-            if (!U.direct) count_and_merge(P, U, R, nvr, lane);
-            continue;
+    while (consumed < issued) {
+        Piece U;
+        {
+            const int32_t *d = ring + (pieces_done % kRing) * kPieceInts;
+            U.b = d[0]; U.kvh = d[1]; U.rb = d[2]; U.T = d[3]; U.n = d[4]; U.qstart = d[5];
+            U.t_lo = d[6]; U.n_tiles = d[7]; U.piece = d[8]; U.pieces = d[9]; U.nvr = d[10]; U.runs = d[11];
         }
+        const bool direct = U.pieces == 1 && U.runs == 0;
 
-        // ---- this lane's slice of the unit's queries, pre-scaled by scale*log2(e)
+        // ---- this piece's queries: bf16 rows in shared memory -> fp32 registers, scaled
+        const int qs = pieces_done % S;
+        if (!__all_sync(0xffffffffu, mbar_wait(&qfull[qs], (pieces_done / S) & 1))) {
+            bail_out();
+            return;
+        }
         float2 q2[R][NW];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int rr = U.rb * R + r;
+            const uint16_t *qrow = qbuf + (qs * R + r) * kHeadDim;
 #pragma unroll
-            for (int k = 0; k < NW; ++k) q2[r][k] = make_float2(0.f, 0.f);
-            if (r < nvr) {
-                const uint16_t *qrow = P.q + out_row(P, U, rr) * kHeadDim;
-#pragma unroll
-                for (int k = 0; k < NW; ++k) {
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(qrow + lane_dim_of_word<L>(j, k));
-                    q2[r][k] = make_float2(bf16_lo(w) * P.qscale, bf16_hi(w) * P.qscale);
-                }
+            for (int k = 0; k < NW; ++k) {
+                const uint32_t w = r < U.nvr ? *reinterpret_cast<const uint32_t *>(qrow + lane_dim_of_word<L>(j, k)) : 0u;
+                q2[r][k] = make_float2(bf16_lo(w) * P.qscale, bf16_hi(w) * P.qscale);
             }
         }
-        const int lim0 = U.T - U.n;                      // last key visible to query token 0
-        const bool row_ok = rj < nvr;
-        const int lim = row_ok ? lim0 + (U.rb * R + rj) / P.G : -1;
+        __syncwarp();
+        ++pieces_done;
+        const int lim = rj < U.nvr ? U.T - U.n + (U.rb * R + rj) / P.G : -1;  // last key of this lane's row
         float m = -INFINITY, lsum = 0.f;
         float2 acc[R][NW];
 #pragma unroll
@@ -358,109 +439,114 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
         for (int kt = 0; kt < U.n_tiles; ++kt) {
             top_up();
             const int s = consumed % S;
-            const bool arrived = mbar_wait(&full[s], (consumed / S) & 1);
-            if (!__all_sync(0xffffffffu, arrived)) {
-                flag_error(P.err, kErrBitTimeout);
-                for (uint32_t c = consumed + 1; c < issued; ++c) (void)mbar_wait(&full[c % S], (c / S) & 1);
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (consumed / S) & 1))) {
+                bail_out();
                 return;
             }
             const uint8_t *st = smem + s * kStageBytes;
             const int t0 = U.t_lo + kt * kTile;
-
-            // ---- scores: partial dots over this lane's dims, reduce-scatter over L lanes
-            float sv[NS];
-#pragma unroll
-            for (int step = 0; step < NS; ++step) {
-                const int t = step * TG + tg;
-                uint32_t kw[NW];
-                load_tile_row<L>(st, t, j, kw);
-                float2 a2[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) a2[r] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < NW; ++k) {
-                    const float2 kf = unpack_bf16x2(kw[k]);
-#pragma unroll
-                    for (int r = 0; r < R; ++r) a2[r] = ffma2(q2[r][k], kf, a2[r]);
-                }
-                float v[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) v[r] = a2[r].x + a2[r].y;
-                int n = R;
-#pragma unroll
-                for (int o = L / 2; o >= 2; o >>= 1) {
-                    const int h = n >> 1;
-                    const bool up = (j & o) != 0;
-#pragma unroll
-                    for (int i = 0; i < h; ++i) {
-                        const float send = up ? v[i] : v[i + h];
-                        const float keep = up ? v[i + h] : v[i];
-                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                    }
-                    n = h;
-                }
-                v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-                sv[step] = t0 + t <= lim ? v[0] : -INFINITY;
+            bool loaded = t0 < U.T;
+            if (loaded) {
+                const int pid = P.block_table[static_cast<int64_t>(U.b) * P.max_pages + t0 / kPageSize];
+                loaded = pid >= 0 && pid < P.num_pages;
+                if (!loaded && lane == 0) flag_error(P.err, kErrBitPageOOB);
             }
-
-            // ---- online softmax for this lane's row (log2 units)
-            float tmax = -INFINITY;
+            if (loaded) {
+                // ---- scores: partial dots over this lane's dims, reduce-scatter over L lanes
+                float sv[NS];
 #pragma unroll
-            for (int step = 0; step < NS; ++step) tmax = fmaxf(tmax, sv[step]);
+                for (int step = 0; step < NS; ++step) {
+                    const int t = step * TG + tg;
+                    uint32_t kw[NW];
+                    load_tile_row<L>(st, t, j, kw);
+                    float2 a2[R];
 #pragma unroll
-            for (int o = L; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-            const float m_new = fmaxf(m, tmax);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = exp2f(m - m_use);
-            lsum *= alpha;
-            m = m_new;
-#pragma unroll
-            for (int step = 0; step < NS; ++step) {
-                const float p = exp2f(sv[step] - m_use);
-                lsum += p;
-                if ((j & 1) == 0) pbuf[step * TG + tg][rj] = p;
-            }
-            if (tg == 0 && (j & 1) == 0) rowx[rj] = alpha;
-            __syncwarp();
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const float a = rowx[r];
-#pragma unroll
-                    for (int k = 0; k < NW; ++k) acc[r][k] = make_float2(acc[r][k].x * a, acc[r][k].y * a);
-                }
-            }
-
-            // ---- O += P V over the valid tokens of the tile
-            const int nvalid = min(kTile, U.t_hi - t0);
-#pragma unroll
-            for (int step = 0; step < NS; ++step) {
-                const int t = step * TG + tg;
-                if (t < nvalid) {
-                    uint32_t vw[NW];
-                    load_tile_row<L>(st + 2 * kHalfBytes, t, j, vw);
-                    float pr[R];
-#pragma unroll
-                    for (int r4 = 0; r4 < R / 4; ++r4) {
-                        const float4 pp = *reinterpret_cast<const float4 *>(&pbuf[t][r4 * 4]);
-                        pr[r4 * 4 + 0] = pp.x;
-                        pr[r4 * 4 + 1] = pp.y;
-                        pr[r4 * 4 + 2] = pp.z;
-                        pr[r4 * 4 + 3] = pp.w;
-                    }
+                    for (int r = 0; r < R; ++r) a2[r] = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int k = 0; k < NW; ++k) {
-                        const float2 vf = unpack_bf16x2(vw[k]);
+                        const float2 kf = unpack_bf16x2(kw[k]);
 #pragma unroll
-                        for (int r = 0; r < R; ++r) acc[r][k] = ffma2(make_float2(pr[r], pr[r]), vf, acc[r][k]);
+                        for (int r = 0; r < R; ++r) a2[r] = ffma2(q2[r][k], kf, a2[r]);
+                    }
+                    float v[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) v[r] = a2[r].x + a2[r].y;
+                    int n = R;
+#pragma unroll
+                    for (int o = L / 2; o >= 2; o >>= 1) {
+                        const int h = n >> 1;
+                        const bool up = (j & o) != 0;
+#pragma unroll
+                        for (int i = 0; i < h; ++i) {
+                            const float send = up ? v[i] : v[i + h];
+                            const float keep = up ? v[i + h] : v[i];
+                            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                        }
+                        n = h;
+                    }
+                    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+                    sv[step] = t0 + t <= lim ? v[0] : -INFINITY;
+                }
+
+                // ---- online softmax for this lane's row (log2 units)
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int step = 0; step < NS; ++step) tmax = fmaxf(tmax, sv[step]);
+#pragma unroll
+                for (int o = L; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+                const float m_new = fmaxf(m, tmax);
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = exp2f(m - m_use);
+                lsum *= alpha;
+                m = m_new;
+#pragma unroll
+                for (int step = 0; step < NS; ++step) {
+                    const float p = exp2f(sv[step] - m_use);
+                    lsum += p;
+                    if ((j & 1) == 0) pbuf[step * TG + tg][rj] = p;
+                }
+                if (tg == 0 && (j & 1) == 0) rowx[rj] = alpha;
+                __syncwarp();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float a = rowx[r];
+#pragma unroll
+                        for (int k = 0; k < NW; ++k) acc[r][k] = make_float2(acc[r][k].x * a, acc[r][k].y * a);
+                    }
+                }
+
+                // ---- O += P V over the valid tokens of the tile
+                const int nvalid = min(kTile, U.T - t0);
+#pragma unroll
+                for (int step = 0; step < NS; ++step) {
+                    const int t = step * TG + tg;
+                    if (t < nvalid) {
+                        uint32_t vw[NW];
+                        load_tile_row<L>(st + 2 * kHalfBytes, t, j, vw);
+                        float pr[R];
+#pragma unroll
+                        for (int r4 = 0; r4 < R / 4; ++r4) {
+                            const float4 pp = *reinterpret_cast<const float4 *>(&pbuf[t][r4 * 4]);
+                            pr[r4 * 4 + 0] = pp.x;
+                            pr[r4 * 4 + 1] = pp.y;
+                            pr[r4 * 4 + 2] = pp.z;
+                            pr[r4 * 4 + 3] = pp.w;
+                        }
+#pragma unroll
+                        for (int k = 0; k < NW; ++k) {
+                            const float2 vf = unpack_bf16x2(vw[k]);
+#pragma unroll
+                            for (int r = 0; r < R; ++r) acc[r][k] = ffma2(make_float2(pr[r], pr[r]), vf, acc[r][k]);
+                        }
                     }
                 }
             }
-            __syncwarp();   // stage and p buffer are reused by the next tile
+            __syncwarp();   // stage and p buffer are reused by later tiles
             ++consumed;
         }
 
-        // ---- finish the unit: sum over token groups, then output or partial
+        // ---- finish the piece: sum over token groups, then output or partial
 #pragma unroll
         for (int o = L; o < 32; o <<= 1) {
             lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
@@ -480,9 +566,9 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
         if (tg == 0) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                if (r < nvr) {
+                if (r < U.nvr) {
                     const int64_t row = out_row(P, U, U.rb * R + r);
-                    if (U.direct) {
+                    if (direct) {
                         const float inv = 1.f / rowx[R + r];
 #pragma unroll
                         for (int k = 0; k < NW; ++k) {
@@ -491,7 +577,7 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
                             *reinterpret_cast<uint32_t *>(P.out + row * kHeadDim + lane_dim_of_word<L>(j, k)) = w;
                         }
                     } else {
-                        const int64_t wi = static_cast<int64_t>(U.slot) * P.n_rows_total + row;
+                        const int64_t wi = static_cast<int64_t>(P.slot_base + U.piece) * P.n_rows_total + row;
 #pragma unroll
                         for (int k = 0; k < NW; ++k)
                             *reinterpret_cast<float2 *>(P.ws_acc + wi * kHeadDim + lane_dim_of_word<L>(j, k)) = acc[r][k];
@@ -500,76 +586,62 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
                 }
             }
         }
-        if (!U.direct) count_and_merge(P, U, R, nvr, lane);
         __syncwarp();
-    }
-
-    // ---- last warp out resets the unit counter for the next call
-    if (lane == 0) {
-        __threadfence();
-        if (atomicAdd(P.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
-            atomicExch(P.sched, 0);
-            atomicExch(P.sched + 1, 0);
+        resolve(P, pend, R, lane);  // the previous piece's count has long returned
+        if (!direct) {
+            pend.U = U;
+            pend.live = true;
+            if (lane == 0) pend.old = atomic_add_release(merge_counter(P, U), 1);
         }
     }
+    resolve(P, pend, R, lane);
 }
 
-template <int R, int S>
-constexpr size_t smem_bytes() { return Layout<R, S>::kBytes + 1024; }
+template <int R>
+constexpr size_t smem_bytes() { return Layout<R>::kBytes + 1024; }
 
-template <int R, int S>
+template <int R>
 cudaError_t prepare() {
-    static cudaError_t err = cudaFuncSetAttribute(split_attn_kernel<R, S>,
+    static cudaError_t err = cudaFuncSetAttribute(split_attn_kernel<R>,
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  static_cast<int>(smem_bytes<R, S>()));
+                                                  static_cast<int>(smem_bytes<R>()));
     return err;
 }
 
-template <int R, int S>
-cudaError_t launch_rs(const SplitParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                      int num_ctas, cudaStream_t stream) {
-    cudaError_t e = prepare<R, S>();
+template <int R>
+cudaError_t launch_r(const SplitParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                     int num_ctas, cudaStream_t stream) {
+    cudaError_t e = prepare<R>();
     if (e != cudaSuccess) return e;
-    split_attn_kernel<R, S><<<num_ctas, 32, smem_bytes<R, S>(), stream>>>(p, tk, tv);
+    split_attn_kernel<R><<<num_ctas, 32, smem_bytes<R>(), stream>>>(p, tk, tv);
     return cudaGetLastError();
 }
 
-template <int R, int S>
-cudaError_t occupancy_rs(int *ctas_per_sm) {
-    cudaError_t e = prepare<R, S>();
+template <int R>
+cudaError_t occupancy_r(int *ctas_per_sm) {
+    cudaError_t e = prepare<R>();
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, split_attn_kernel<R, S>, 32,
-                                                         smem_bytes<R, S>());
-}
-
-// Pipeline depth per warp (stages of 16 KiB). SA_SPLIT_STAGES=3 selects three.
-int split_stages() {
-    static const int s = [] {
-        const char *v = std::getenv("SA_SPLIT_STAGES");
-        return (v != nullptr && v[0] == '3') ? 3 : 2;
-    }();
-    return s;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, split_attn_kernel<R>, 32,
+                                                         smem_bytes<R>());
 }
 
 }  // namespace
 
 cudaError_t split_occupancy(int R, int, int *ctas_per_sm) {
-    const bool s3 = split_stages() == 3;
     switch (R) {
-        case 4: return s3 ? occupancy_rs<4, 3>(ctas_per_sm) : occupancy_rs<4, 2>(ctas_per_sm);
-        case 8: return s3 ? occupancy_rs<8, 3>(ctas_per_sm) : occupancy_rs<8, 2>(ctas_per_sm);
-        case 16: return s3 ? occupancy_rs<16, 3>(ctas_per_sm) : occupancy_rs<16, 2>(ctas_per_sm);
+        case 4: return occupancy_r<4>(ctas_per_sm);
+        case 8: return occupancy_r<8>(ctas_per_sm);
+        case 16: return occupancy_r<16>(ctas_per_sm);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_split_attn(const SplitParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                               int num_ctas, int, cudaStream_t stream) {
-    const bool s3 = split_stages() == 3;
     switch (p.rows_per_block) {
-        case 4: return s3 ? launch_rs<4, 3>(p, tk, tv, num_ctas, stream) : launch_rs<4, 2>(p, tk, tv, num_ctas, stream);
-        case 8: return s3 ? launch_rs<8, 3>(p, tk, tv, num_ctas, stream) : launch_rs<8, 2>(p, tk, tv, num_ctas, stream);
-        case 16: return s3 ? launch_rs<16, 3>(p, tk, tv, num_ctas, stream) : launch_rs<16, 2>(p, tk, tv, num_ctas, stream);
+        case 4: return launch_r<4>(p, tk, tv, num_ctas, stream);
+        case 8: return launch_r<8>(p, tk, tv, num_ctas, stream);
+        case 16: return launch_r<16>(p, tk, tv, num_ctas, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -44,17 +44,14 @@ struct SplitParams {
     const int32_t *run_slots;   // nullable: partials the shared-prefix path writes per sequence
     float *ws_acc;              // [n_slots][total_q * Hq][128] fp32 unnormalised accumulators
     float *ws_ml;               // [n_slots][total_q * Hq][2] running max (log2 units), sum
-    int32_t *sched;             // [2] unit claim counter, finished-warp counter (zero between calls)
-    int32_t *merge_ctr;         // [B * Hkv * n_row_blocks] finished splits (zero between calls)
+    int32_t *merge_ctr;         // [B * Hkv * n_row_blocks] finished pieces (zero between calls)
     int32_t *err;
     int32_t B, Hq, Hkv, G, num_pages, max_pages, total_q, max_q_len;
-    int32_t rows_per_block;     // R, rows of one work unit (4, 8 or 16)
-    int32_t n_row_blocks;
-    int32_t pages_per_split;
-    int32_t n_splits;
-    int32_t slot_base;          // first workspace slot used by splits
+    int32_t rows_per_block;     // R, rows of one segment (4, 8 or 16)
+    int32_t n_row_blocks;       // row blocks per (sequence, KV head) at max_q_len
+    int32_t min_tiles_per_warp; // bounds the pieces of a segment by the piece slots
+    int32_t slot_base;          // first workspace slot used by pieces
     int32_t n_rows_total;       // total_q * Hq (row stride of a workspace slot)
-    int64_t n_units;
     float qscale;               // scale * log2(e)
     int32_t evict_first;
 };
