@@ -174,6 +174,8 @@ def timed_steps(batch: GpuBatch, steps: int, warmup: int, flush, parts):
         for p in parts:
             fns[p]()
     torch.cuda.synchronize()
+    if int(batch.err.item()) != 0:
+        raise SystemExit(f"device error flag {int(batch.err.item())} after warm-up; not timing")
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in parts] for _ in range(steps)]
     barrier()

@@ -35,7 +35,9 @@ _lib = None
 
 
 def library_path() -> str:
-    return LIB
+    """The library this process loads: the in-tree build, or the file named by
+    SA_LIBRARY_PATH (a build of the same sources with other tuning constants)."""
+    return os.environ.get("SA_LIBRARY_PATH") or LIB
 
 
 def load_library() -> ctypes.CDLL:
@@ -43,10 +45,11 @@ def load_library() -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB):
-        raise RuntimeError(f"{LIB} is missing: build it with speculative_decode_gb300.build.build() "
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with speculative_decode_gb300.build.build() "
                            "(or __graft_entry__.build()); there is no fallback path")
-    lib = ctypes.CDLL(LIB)
+    lib = ctypes.CDLL(path)
     P, I32, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
     DP = ctypes.POINTER(Dims)
     sig = {

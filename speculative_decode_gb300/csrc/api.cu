@@ -61,7 +61,7 @@ struct SplitConfig {
     int R, nrb, piece_slots, min_tiles, run_slots, n_slots;
 };
 
-constexpr int kPieceSlots = 16;
+constexpr int kPieceSlots = 8;
 
 SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     SplitConfig c{};
@@ -69,7 +69,7 @@ SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     const int rows = G * std::max(1, d.max_q_len);
     c.R = rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
     c.nrb = (rows + c.R - 1) / c.R;
-    const int max_tiles = std::max(1, d.max_pages_per_seq) * (kPageSize / 32);
+    const int max_tiles = std::max(1, d.max_pages_per_seq) * (kPageSize / split_tile_tokens());
     c.piece_slots = std::min(kPieceSlots, max_tiles);
     // a segment of s tiles spans at most ceil(s / C) + 1 warps' ranges
     c.min_tiles = c.piece_slots > 1 ? (max_tiles + c.piece_slots - 2) / (c.piece_slots - 1) : max_tiles;
@@ -215,10 +215,10 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     CUtensorMap tmk, tmv;
     const uint64_t pool_rows = static_cast<uint64_t>(d.num_pages) * d.num_kv_heads * kPageSize;
     if (encode_tensor_map_2d(&tmk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(k_pages),
-                             kHeadDim, pool_rows, kHeadDim * 2, 64, 32,
+                             kHeadDim, pool_rows, kHeadDim * 2, 64, split_tile_tokens(),
                              CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
         encode_tensor_map_2d(&tmv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(v_pages),
-                             kHeadDim, pool_rows, kHeadDim * 2, 64, 32,
+                             kHeadDim, pool_rows, kHeadDim * 2, 64, split_tile_tokens(),
                              CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return SA_ERR_CUDA;
 

@@ -39,16 +39,31 @@ namespace sa {
 
 namespace {
 
-constexpr int kTile = 32;                     // tokens per stage
+// Tuning constants (measured on GB300: 16-token tiles, two stages per warp and
+// 2R lanes per token were fastest for the decode batch).
+#ifndef SA_SPLIT_TILE
+#define SA_SPLIT_TILE 16
+#endif
+#ifndef SA_SPLIT_MIN_WARPS
+#define SA_SPLIT_MIN_WARPS 1
+#endif
+constexpr int kTile = SA_SPLIT_TILE;          // tokens per stage (16 or 32)
 constexpr int kHalfBytes = kTile * 128;       // 32 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kStageBytes = 4 * kHalfBytes;   // K[0:64], K[64:128], V[0:64], V[64:128]
-constexpr int kStages = 2;                    // pipeline depth per warp
-constexpr int kRing = 4;                      // piece descriptors in flight (>= kStages + 1)
+#ifndef SA_SPLIT_STAGES
+#define SA_SPLIT_STAGES 2
+#endif
+constexpr int kStages = SA_SPLIT_STAGES;      // pipeline depth per warp
+constexpr int kRing = kStages + 2;            // piece descriptors in flight (>= kStages + 1)
 constexpr int kPieceInts = 16;
 
+#ifndef SA_SPLIT_LPT
+#define SA_SPLIT_LPT 2
+#endif
 template <int R>
 struct Geo {
-    static constexpr int L = R <= 4 ? 8 : (R <= 8 ? 16 : 32);  // lanes per token
+    static constexpr int L = SA_SPLIT_LPT * R < 32 ? SA_SPLIT_LPT * R : 32;  // lanes per token
+    static constexpr int DUP = L / R;                          // lanes holding each row's score
     static constexpr int TG = 32 / L;                          // tokens per warp step
     static constexpr int NS = kTile / TG;                      // steps per tile
     static constexpr int NW = kHeadDim / L / 2;                // bf16x2 words per lane
@@ -60,7 +75,8 @@ struct Layout {
     static constexpr int kPOff = kQOff + kStages * R * kHeadDim * 2;     // fp32 p [32][R]
     static constexpr int kRowOff = kPOff + kTile * R * 4;                // fp32 [2][R]
     static constexpr int kRingOff = kRowOff + 2 * R * 4;                 // int32 [kRing][16]
-    static constexpr int kBarOff = kRingOff + kRing * kPieceInts * 4;    // uint64 [2][kStages]
+    static constexpr int kFlagOff = kRingOff + kRing * kPieceInts * 4;   // int32 [kStages] tile loaded?
+    static constexpr int kBarOff = (kFlagOff + kStages * 4 + 7) / 8 * 8;  // uint64 [2][kStages]
     static constexpr int kBytes = (kBarOff + 2 * kStages * 8 + 1023) / 1024 * 1024;
 };
 
@@ -202,12 +218,12 @@ __device__ void resolve(const SplitParams &P, Pending &pd, int R, int lane) {
 }
 
 template <int R>
-__global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
+__global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(const SplitParams P,
                                                         const __grid_constant__ CUtensorMap tmk,
                                                         const __grid_constant__ CUtensorMap tmv) {
     using Gm = Geo<R>;
     using Lay = Layout<R>;
-    constexpr int L = Gm::L, TG = Gm::TG, NS = Gm::NS, NW = Gm::NW;
+    constexpr int L = Gm::L, TG = Gm::TG, NS = Gm::NS, NW = Gm::NW, DUP = Gm::DUP;
     constexpr int S = kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -219,6 +235,7 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
     float(*pbuf)[R] = reinterpret_cast<float(*)[R]>(smem + Lay::kPOff);
     float *rowx = reinterpret_cast<float *>(smem + Lay::kRowOff);
     int32_t *ring = reinterpret_cast<int32_t *>(smem + Lay::kRingOff);
+    int32_t *stage_ok = reinterpret_cast<int32_t *>(smem + Lay::kFlagOff);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::kBarOff);
     uint64_t *qfull = full + S;
 
@@ -302,11 +319,14 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
     {
         int n = R;
 #pragma unroll
-        for (int o = L / 2; o >= 2; o >>= 1) {
-            n >>= 1;
-            if (j & o) rj += n;
+        for (int o = L / 2; o >= 1; o >>= 1) {
+            if (n > 1) {
+                n >>= 1;
+                if (j & o) rj += n;
+            }
         }
     }
+    const bool row_writer = (j % DUP) == 0;  // one of the DUP lanes that hold row rj
     const uint64_t policy = P.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
 
     // ---- issue cursor: walks tiles g_begin .. g_end-1 ahead of the consumer
@@ -321,6 +341,18 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
         itile = static_cast<int>(off % isi.tiles);
     }
     uint32_t issued = 0, consumed = 0, pieces_pushed = 0;
+    // physical page of the issue cursor's current logical page, and the next
+    // page's id loaded one page ahead so the block-table read never stalls a tile
+    int pg_b = -1, pg_j = -1, pg_id = -1, pg_next = -1;
+    auto page_id = [&](int b, int jp, int npages) -> int {
+        if (b == pg_b && jp == pg_j) return pg_id;
+        const int64_t base = static_cast<int64_t>(b) * P.max_pages;
+        pg_id = (b == pg_b && jp == pg_j + 1) ? pg_next : P.block_table[base + jp];
+        pg_b = b;
+        pg_j = jp;
+        pg_next = jp + 1 < npages ? P.block_table[base + jp + 1] : -1;
+        return pg_id;
+    };
     auto issue_next = [&]() -> bool {
         if (ig >= g_end) return false;
         if (itile == isi.tiles) {  // next segment
@@ -365,10 +397,12 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
         // the tile: K and V rows [t0, t0 + 32) of KV head kvh
         const int t0 = isi.skip_tok + itile * kTile;
         const int s = issued % S;
+        const int pid = t0 < isi.T ? page_id(ib, t0 / kPageSize, (isi.T + kPageSize - 1) / kPageSize) : -1;
+        const bool ok = pid >= 0 && pid < P.num_pages;
+        if (t0 < isi.T && !ok && lane == 0) flag_error(P.err, kErrBitPageOOB);
         if (lane == 0) {
-            int pid = -1;
-            if (t0 < isi.T) pid = P.block_table[static_cast<int64_t>(ib) * P.max_pages + t0 / kPageSize];
-            if (pid >= 0 && pid < P.num_pages) {
+            stage_ok[s] = ok;
+            if (ok) {
                 const int y = (pid * P.Hkv + kvh) * kPageSize + (t0 % kPageSize);
                 uint8_t *dst = smem + s * kStageBytes;
                 mbar_arrive_expect_tx(&full[s], kStageBytes);
@@ -445,47 +479,58 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
             }
             const uint8_t *st = smem + s * kStageBytes;
             const int t0 = U.t_lo + kt * kTile;
-            bool loaded = t0 < U.T;
-            if (loaded) {
-                const int pid = P.block_table[static_cast<int64_t>(U.b) * P.max_pages + t0 / kPageSize];
-                loaded = pid >= 0 && pid < P.num_pages;
-                if (!loaded && lane == 0) flag_error(P.err, kErrBitPageOOB);
-            }
-            if (loaded) {
-                // ---- scores: partial dots over this lane's dims, reduce-scatter over L lanes
+            if (stage_ok[s]) {
+                // ---- scores: partial dots over this lane's dims for a batch of
+                // steps, then the reduce-scatter over L lanes level by level across
+                // the batch, so that independent shuffles overlap
                 float sv[NS];
+                constexpr int NB = (32 / R) < NS ? (32 / R) : NS;  // steps per batch
 #pragma unroll
-                for (int step = 0; step < NS; ++step) {
-                    const int t = step * TG + tg;
-                    uint32_t kw[NW];
-                    load_tile_row<L>(st, t, j, kw);
-                    float2 a2[R];
+                for (int b0 = 0; b0 < NS; b0 += NB) {
+                    float v[NB][R];
 #pragma unroll
-                    for (int r = 0; r < R; ++r) a2[r] = make_float2(0.f, 0.f);
+                    for (int bi = 0; bi < NB; ++bi) {
+                        const int t = (b0 + bi) * TG + tg;
+                        uint32_t kw[NW];
+                        load_tile_row<L>(st, t, j, kw);
+                        float2 a2[R];
 #pragma unroll
-                    for (int k = 0; k < NW; ++k) {
-                        const float2 kf = unpack_bf16x2(kw[k]);
+                        for (int r = 0; r < R; ++r) a2[r] = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int r = 0; r < R; ++r) a2[r] = ffma2(q2[r][k], kf, a2[r]);
+                        for (int k = 0; k < NW; ++k) {
+                            const float2 kf = unpack_bf16x2(kw[k]);
+#pragma unroll
+                            for (int r = 0; r < R; ++r) a2[r] = ffma2(q2[r][k], kf, a2[r]);
+                        }
+#pragma unroll
+                        for (int r = 0; r < R; ++r) v[bi][r] = a2[r].x + a2[r].y;
                     }
-                    float v[R];
-#pragma unroll
-                    for (int r = 0; r < R; ++r) v[r] = a2[r].x + a2[r].y;
+                    // halve the values while more than one is left, then all-reduce
                     int n = R;
 #pragma unroll
-                    for (int o = L / 2; o >= 2; o >>= 1) {
-                        const int h = n >> 1;
-                        const bool up = (j & o) != 0;
+                    for (int o = L / 2; o >= 1; o >>= 1) {
+                        if (n > 1) {
+                            const int h = n >> 1;
+                            const bool up = (j & o) != 0;
 #pragma unroll
-                        for (int i = 0; i < h; ++i) {
-                            const float send = up ? v[i] : v[i + h];
-                            const float keep = up ? v[i + h] : v[i];
-                            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                            for (int bi = 0; bi < NB; ++bi)
+#pragma unroll
+                                for (int i = 0; i < h; ++i) {
+                                    const float send = up ? v[bi][i] : v[bi][i + h];
+                                    const float keep = up ? v[bi][i + h] : v[bi][i];
+                                    v[bi][i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                                }
+                            n = h;
+                        } else {
+#pragma unroll
+                            for (int bi = 0; bi < NB; ++bi) v[bi][0] += __shfl_xor_sync(0xffffffffu, v[bi][0], o);
                         }
-                        n = h;
                     }
-                    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-                    sv[step] = t0 + t <= lim ? v[0] : -INFINITY;
+#pragma unroll
+                    for (int bi = 0; bi < NB; ++bi) {
+                        const int t = (b0 + bi) * TG + tg;
+                        sv[b0 + bi] = t0 + t <= lim ? v[bi][0] : -INFINITY;
+                    }
                 }
 
                 // ---- online softmax for this lane's row (log2 units)
@@ -503,9 +548,9 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
                 for (int step = 0; step < NS; ++step) {
                     const float p = exp2f(sv[step] - m_use);
                     lsum += p;
-                    if ((j & 1) == 0) pbuf[step * TG + tg][rj] = p;
+                    if (row_writer) pbuf[step * TG + tg][rj] = p;
                 }
-                if (tg == 0 && (j & 1) == 0) rowx[rj] = alpha;
+                if (tg == 0 && row_writer) rowx[rj] = alpha;
                 __syncwarp();
                 if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
@@ -558,7 +603,7 @@ __global__ void __launch_bounds__(32) split_attn_kernel(const SplitParams P,
                     acc[r][k].y += __shfl_xor_sync(0xffffffffu, acc[r][k].y, o);
                 }
         }
-        if (tg == 0 && (j & 1) == 0) {
+        if (tg == 0 && row_writer) {
             rowx[rj] = m;
             rowx[R + rj] = lsum;
         }
@@ -626,6 +671,8 @@ cudaError_t occupancy_r(int *ctas_per_sm) {
 }
 
 }  // namespace
+
+int split_tile_tokens() { return kTile; }
 
 cudaError_t split_occupancy(int R, int, int *ctas_per_sm) {
     switch (R) {

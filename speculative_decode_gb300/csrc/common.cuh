@@ -64,7 +64,7 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // Wait for the phase with the given parity to complete, giving up after
 // kWaitLimitNs of wall time. Returns false on timeout (the caller flags
 // SA_ERR_TIMEOUT and stops using the pipeline); it never spins forever.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kWaitLimitNs = 250000000ull;  // 250 ms: far above any real copy
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
