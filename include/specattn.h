@@ -170,6 +170,30 @@ SA_API int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t 
  * (diagnostics; the same decomposition the call itself uses). Needs a device. */
 SA_API int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan);
 
+/*
+ * sa_paged_attn_noalloc -- sa_paged_attn for callers that cannot allocate.
+ *
+ * The reference pages have no counterpart to this call; it exists for callers
+ * that cannot allocate device memory at all, such as a plugin inside a serving
+ * process whose memory pool owns the whole GPU, or a decode loop that may not
+ * call cudaMalloc because it synchronises the device. It computes exactly what
+ * sa_paged_attn computes (same arguments, no plan), but its scratch is a fixed
+ * 16 MiB array inside the library, reserved on every GPU that loads the
+ * library until the process exits. The caller still passes inputs and outputs.
+ *   - Shapes whose workspace (sa_paged_attn_workspace_size with no plan) is
+ *     above 16 MiB are rejected with SA_ERR_WORKSPACE before any GPU work.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - Every call clears the array's counters on `stream`, then reuses the same
+ *     array: two calls that overlap on the GPU (different streams, or
+ *     different host threads on one device) race and give wrong results.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+SA_API int sa_paged_attn_noalloc(const sa_dims *dims, const uint16_t *q, const uint16_t *k_pages,
+                                 const uint16_t *v_pages, const int32_t *block_table,
+                                 const int32_t *seq_lens, const int32_t *q_lens, float scale,
+                                 uint16_t *out, int32_t *err_flag, void *stream);
+
 /* Bytes of workspace sa_spec_verify_greedy needs. */
 SA_API size_t sa_spec_verify_workspace_size(int32_t num_seqs, int32_t k_max, int32_t vocab);
 

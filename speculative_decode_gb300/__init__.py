@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     load_library,
     paged_attn,
     paged_attn_kernel_count,
+    paged_attn_noalloc,
     paged_attn_workspace_size,
     plan_analyze,
     sm_count,

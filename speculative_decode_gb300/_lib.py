@@ -63,6 +63,7 @@ def load_library() -> ctypes.CDLL:
         "sa_paged_attn_workspace_size": ([DP, P], SZ),
         "sa_paged_attn": ([DP, P, P, P, P, P, P, F, P, P, P, SZ, P, P], ctypes.c_int),
         "sa_paged_attn_kernel_count": ([DP, P], ctypes.c_int),
+        "sa_paged_attn_noalloc": ([DP, P, P, P, P, P, P, F, P, P, P], ctypes.c_int),
         "sa_spec_verify_workspace_size": ([I32, I32, I32], SZ),
         "sa_spec_verify_greedy": ([P, P, P, I32, I32, I32, P, P, P, P, SZ, P, P], ctypes.c_int),
     }
@@ -185,6 +186,17 @@ def paged_attn(dims: Dims, q, k_pages, v_pages, block_table, seq_lens, q_lens, s
                                       float(scale), _ptr(out), plan.handle if plan else None,
                                       _ptr(workspace), nbytes, _ptr(err_flag), _stream(stream))
     _check(rc, "sa_paged_attn")
+
+
+def paged_attn_noalloc(dims: Dims, q, k_pages, v_pages, block_table, seq_lens, q_lens,
+                       scale: float, out, err_flag=None, stream=None) -> None:
+    """sa_paged_attn_noalloc: paged attention using the library's fixed 16 MiB
+    scratch, for callers that cannot allocate device memory."""
+    rc = load_library().sa_paged_attn_noalloc(ctypes.byref(dims), _ptr(q), _ptr(k_pages),
+                                              _ptr(v_pages), _ptr(block_table), _ptr(seq_lens),
+                                              _ptr(q_lens), float(scale), _ptr(out),
+                                              _ptr(err_flag), _stream(stream))
+    _check(rc, "sa_paged_attn_noalloc")
 
 
 def paged_attn_kernel_count(dims: Dims, plan: Optional[Plan] = None) -> int:

@@ -327,4 +327,63 @@ int sa_spec_verify_greedy(const float *logits, const int32_t *candidates, const 
     return finish(s, err_flag);
 }
 
+// ---------------------------------------------------------------------------
+// Paged attention without any allocation by the caller or the library.
+//
+// Some callers cannot allocate device memory at all: a plugin that runs inside
+// a serving process whose memory pool already owns every byte of the GPU, or a
+// decode loop that may not call cudaMalloc because it synchronises the whole
+// device. For them the split kernel's scratch (partial accumulators and merge
+// counters) lives in one fixed array in this file, reserved on every GPU that
+// loads the library until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kStaticScratchBytes = size_t{16} << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void *g_scratch_ptr[kMaxDevices];  // device address of g_static_scratch, per device
+
+// Device address of the fixed scratch on the current device. Looked up once per
+// device, with that device current; the host-side name of the array is not a
+// device address and is never passed to a kernel.
+int static_scratch_address(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return SA_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return SA_OK;
+}
+
+}  // namespace
+
+int sa_paged_attn_noalloc(const sa_dims *dims, const uint16_t *q, const uint16_t *k_pages,
+                          const uint16_t *v_pages, const int32_t *block_table,
+                          const int32_t *seq_lens, const int32_t *q_lens, float scale,
+                          uint16_t *out, int32_t *err_flag, void *stream) {
+    int rc = check_dims(dims);
+    if (rc) return rc;
+    const WsLayout wl = attn_ws_layout(*dims, nullptr);
+    if (wl.total > kStaticScratchBytes) return SA_ERR_WORKSPACE;  // shapes exceed the fixed scratch
+    void *ws = nullptr;
+    rc = static_scratch_address(&ws);
+    if (rc) return rc;
+    // merge counters must start at zero; calls leave them at zero, but clear
+    // them anyway so that an interrupted earlier call cannot leak into this one
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (wl.total > wl.ctr_offset &&
+        cudaMemsetAsync(static_cast<char *>(ws) + wl.ctr_offset, 0, wl.total - wl.ctr_offset, s) != cudaSuccess)
+        return SA_ERR_CUDA;
+    return sa_paged_attn(dims, q, k_pages, v_pages, block_table, seq_lens, q_lens, scale, out,
+                         nullptr, ws, kStaticScratchBytes, err_flag, stream);
+}
+
 }  // extern "C"
