@@ -224,8 +224,17 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
 
     const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
     if (pd && pd->num_tiles > 0) {
-        if (launch_prefix_tc(d, *pd, q, k_pages, v_pages, scale, ws_acc, ws_ml, rows_total,
-                             err_flag, s) != cudaSuccess)
+        // shared runs first: the split kernel's merges read their partials
+        CUtensorMap pk, pv;
+        if (encode_tensor_map_2d(&pk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(k_pages),
+                                 kHeadDim, pool_rows, kHeadDim * 2, 64, prefix_tile_rows(),
+                                 CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+            encode_tensor_map_2d(&pv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(v_pages),
+                                 kHeadDim, pool_rows, kHeadDim * 2, 64, prefix_tile_rows(),
+                                 CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return SA_ERR_CUDA;
+        if (launch_prefix_tc(d, *pd, q, pk, pv, scale, ws_acc, ws_ml, rows_total, err_flag,
+                             block_table, s) != cudaSuccess)
             return SA_ERR_CUDA;
     }
 

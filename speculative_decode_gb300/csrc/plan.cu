@@ -54,8 +54,13 @@ PlanHost build_plan(const sa_dims &d, const int32_t *bt, const int32_t *seq_lens
         if (n <= 0 || n > T || n > d.max_q_len) continue;
         const int np = (T + kPageSize - 1) / kPageSize;
         if (np > d.max_pages_per_seq) continue;
+        // only pages every key of which is in the cache can be shared on the
+        // tensor cores (a partly written page may hold stale, non-finite data
+        // that a zero probability would still multiply); the last partial page
+        // stays on the split kernel
+        const int full = T / kPageSize;
         int cur = -1;
-        for (int j = 0; j < np; ++j) {
+        for (int j = 0; j < full; ++j) {
             const int page = bt[static_cast<int64_t>(b) * d.max_pages_per_seq + j];
             if (page < 0 || page >= d.num_pages) break;  // left to the split kernel, which flags it
             auto key = std::make_pair(cur, page);
@@ -160,9 +165,11 @@ PlanHost build_plan(const sa_dims &d, const int32_t *bt, const int32_t *seq_lens
         const int row_count = static_cast<int>(P.rows.size()) - row_begin;
         P.run_desc.insert(P.run_desc.end(), {runs[r].page_lo, runs[r].page_hi, row_begin, row_count,
                                              run_chunk_pages[r], runs[r].members[0]});
+        // row tiles of one (KV head, page chunk) are adjacent so that they run
+        // together and the second and later ones read the chunk from L2
         for (int g = 0; g < d.num_kv_heads; ++g)
-            for (int t = 0; t < row_count; t += kPrefixTileRows)
-                for (int c = 0; c < run_chunks[r]; ++c) {
+            for (int c = 0; c < run_chunks[r]; ++c)
+                for (int t = 0; t < row_count; t += kPrefixTileRows) {
                     const int lo = runs[r].page_lo + c * run_chunk_pages[r];
                     const int hi = std::min(runs[r].page_hi, lo + run_chunk_pages[r]);
                     P.tiles.insert(P.tiles.end(), {run_index[r], g, t, lo, hi, c});
@@ -190,9 +197,9 @@ using namespace sa;
 namespace {
 
 constexpr int kMinRunRows = 32;
-// The tensor-core shared-prefix kernel is not wired in yet: plans describe the
-// runs (stats, analysis) but hand every page to the split kernel.
-constexpr bool kPrefixPathReady = false;
+// Whether plans hand their shared runs to the tensor-core kernel (otherwise
+// they only describe them and every page goes through the split kernel).
+constexpr bool kPrefixPathReady = true;
 
 int check_plan_args(const sa_dims *d, const int32_t *bt, const int32_t *sl, const int32_t *ql) {
     if (d == nullptr || d->num_seqs < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 ||

@@ -38,10 +38,14 @@ const PlanDevice *plan_device(const sa_plan *plan);
 PlanHost build_plan(const sa_dims &d, const int32_t *block_table, const int32_t *seq_lens,
                     const int32_t *q_lens, int sms, int min_rows);
 
+// Launch the tensor-core shared-prefix kernel over the plan's work items.
+// tmk / tmv view the K / V pools as [num_pages*Hkv*256 rows][128] bf16 with
+// 64 x prefix_tile_rows() boxes and 128-byte swizzle.
 cudaError_t launch_prefix_tc(const sa_dims &d, const PlanDevice &pd, const uint16_t *q,
-                             const uint16_t *k_pages, const uint16_t *v_pages, float scale,
+                             const CUtensorMap &tmk, const CUtensorMap &tmv, float scale,
                              float *ws_acc, float *ws_ml, int64_t rows_total, int32_t *err,
-                             cudaStream_t stream);
+                             const int32_t *block_table, cudaStream_t stream);
+int prefix_tile_rows();
 
 constexpr int kRunDescInts = 6;
 constexpr int kTileInts = 6;

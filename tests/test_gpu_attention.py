@@ -134,3 +134,72 @@ def test_host_argument_errors():
     with pytest.raises(sa.SpecAttnError) as e:
         sa.paged_attn(bad, *args, small)
     assert e.value.code == 2
+
+
+# ------------------------------------------------- shared prefix on tensor cores
+def _plan_stats(w):
+    return sa.Plan(dims_of(w), w.block_table, w.seq_lens, w.q_lens).stats()
+
+
+@pytest.mark.parametrize("seed,nseq,prefix,qlens", [
+    (61, 24, 1, (1,)),          # one shared page, one 128-row tile per KV head
+    (62, 40, 3, (1, 6)),        # causal verify rows inside the shared run
+    (63, 70, 2, (1, 2)),        # two 128-row tiles per KV head
+])
+def test_shared_prefix_runs_match_the_oracle(seed, nseq, prefix, qlens):
+    w = wl.random_case(seed, num_seqs=nseq, Hq=8, Hkv=2, max_ctx=400, q_len_choices=qlens,
+                       shared_prefix_pages=prefix)
+    assert _plan_stats(w)["runs"] >= 1
+    # no kv_append here: new tokens of short sequences would land in shared pages
+    out, err, _, _ = run_attention(w, use_plan=True, append=False)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w, append=False), f"shared prefix seed {seed}")
+
+
+def test_dedup_config_with_plan_all_rows():
+    w = wl.config(2)
+    st = _plan_stats(w)
+    assert st["runs"] == 1 and st["members"] == 100 and st["pages"] == 16
+    out, err, _, _ = run_attention(w, use_plan=True)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), "dedup with plan")
+    plain, _, _, _ = run_attention(w, use_plan=False)
+    assert_attention_close(plain, oracle_attention(w), "dedup without plan")
+
+
+def test_sequences_made_only_of_shared_pages():
+    """Members whose whole context is the shared run: the split kernel has no
+    keys left for them and only merges the tensor-core partials."""
+    w = wl.random_case(64, num_seqs=36, Hq=4, Hkv=1, max_ctx=300, q_len_choices=(1,),
+                       shared_prefix_pages=2)
+    w.seq_lens = w.seq_lens.copy()
+    w.seq_lens[::3] = 2 * wl.PAGE_SIZE          # every third sequence ends with the prefix
+    out, err, _, _ = run_attention(w, use_plan=True, append=False)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w, append=False), "prefix-only members")
+
+
+def test_nested_shared_runs():
+    """A prefix shared by all sequences, then a deeper page shared by half."""
+    rng = np.random.default_rng(65)
+    P = wl.PAGE_SIZE
+    B, Hq, Hkv = 48, 8, 2
+    num_pages = 3 + B + 4
+    bt = np.full((B, 4), -1, np.int32)
+    for b in range(B):
+        bt[b, :2] = [0, 1]
+        bt[b, 2] = 2 if b < B // 2 else 3 + b
+        bt[b, 3] = 3 + B + (b % 4)             # partial last pages (shared by accident, not full)
+    seq = (3 * P + rng.integers(1, 200, size=B)).astype(np.int32)
+    ql = rng.choice([1, 3], size=B).astype(np.int32)
+    tq = int(ql.sum())
+    w = wl.Workload(name="nested", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128, page_size=P,
+                    q=wl.normal_bf16(rng, (tq, Hq, 128)),
+                    k_pages=wl.normal_bf16(rng, (num_pages, Hkv, P, 128)),
+                    v_pages=wl.normal_bf16(rng, (num_pages, Hkv, P, 128)),
+                    block_table=bt, seq_lens=seq, q_lens=ql, scale=0.0883883,
+                    k_new=wl.normal_bf16(rng, (tq, Hkv, 128)), v_new=wl.normal_bf16(rng, (tq, Hkv, 128)))
+    assert _plan_stats(w)["runs"] == 2
+    out, err, _, _ = run_attention(w, use_plan=True, append=False)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w, append=False), "nested runs")
