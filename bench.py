@@ -38,6 +38,7 @@ import workloads as wl  # noqa: E402
 METRIC = "paged-attn KV GB/s (frac of HBM peak); verified tokens/s at 1 GB300"
 DECODE_CFG = 1   # Llama3-8B-shaped decode batch
 VERIFY_CFG = 3   # speculative verification batch
+DEDUP_CFG = 2    # 100 sequences sharing a 16-page prefix
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -113,7 +114,7 @@ class ClockSampler:
 class GpuBatch:
     """A workload resident on the GPU plus everything one step needs."""
 
-    def __init__(self, w: wl.Workload, device):
+    def __init__(self, w: wl.Workload, device, use_plan=False):
         import torch
 
         import speculative_decode_gb300 as sa
@@ -133,9 +134,10 @@ class GpuBatch:
         self.q, self.k_new, self.v_new = T(w.q), T(w.k_new), T(w.v_new)
         self.out = torch.zeros_like(self.q)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
-        self.ws = torch.zeros(sa.paged_attn_workspace_size(self.dims), dtype=torch.uint8,
+        self.plan = sa.Plan(self.dims, w.block_table, w.seq_lens, w.q_lens) if use_plan else None
+        self.ws = torch.zeros(sa.paged_attn_workspace_size(self.dims, self.plan), dtype=torch.uint8,
                               device=device)
-        self.kernels_attn = sa.paged_attn_kernel_count(self.dims)
+        self.kernels_attn = sa.paged_attn_kernel_count(self.dims, self.plan)
         self.verify = w.logits is not None
         if self.verify:
             B, k1, V = w.logits.shape
@@ -153,7 +155,7 @@ class GpuBatch:
 
     def attend(self):
         self.sa.paged_attn(self.dims, self.q, self.kp, self.vp, self.bt, self.sl, self.ql,
-                           self.w.scale, self.out, self.ws, err_flag=self.err)
+                           self.w.scale, self.out, self.ws, plan=self.plan, err_flag=self.err)
 
     def accept(self):
         self.sa.spec_verify_greedy(self.logits, self.cand, self.ncand, self.acc, self.nxt,
@@ -296,6 +298,21 @@ def run_ours(args):
     vq = int(wv.q_lens.sum())
     vbytes = counted_bytes(wv)
 
+    # ---- third block: the dedup batch (100 sequences sharing a 4096-token
+    # prefix), paged_attn with the shared-run plan and without it
+    wd = wl.config(DEDUP_CFG, seed=1000 + DEDUP_CFG + 1 + 7919 * rank)
+    dsteps = max(3, args.steps // 4)
+    dedup = {"workload": wd.name, "unique_bytes": counted_bytes(wd)}
+    for label, use_plan in (("with_plan", True), ("without_plan", False)):
+        db = GpuBatch(wd, dev, use_plan=use_plan)
+        dparts, _ = timed_steps(db, dsteps, args.warmup, flush, ["attend"])
+        t = max_over_ranks(statistics.mean(dparts["attend"]))
+        dedup[label] = {"paged_attn_ms": round(t, 5),
+                        "GBps_unique": round(dedup["unique_bytes"] / (t * 1e-3) / 1e9, 1)}
+        if use_plan:
+            dedup["plan"] = db.plan.stats()
+        del db
+
     peak, peak_kind = hbm_peak()
     achieved = cbytes / (t_attn_max * 1e-3) / 1e9
     line = {
@@ -344,6 +361,7 @@ def run_ours(args):
             "step_ms": round(tv_step, 5),
             "note": "per attention layer: one layer's attention + one greedy accept",
         },
+        "dedup": dedup,
         "e2e": {"value": round(world * cbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 5)},

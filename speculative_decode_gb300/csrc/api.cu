@@ -58,7 +58,7 @@ int check_dims(const sa_dims *d) {
 // Work decomposition of the split kernel: rows per segment and the partial
 // slots pieces may use (a pure function of the shapes).
 struct SplitConfig {
-    int R, nrb, piece_slots, min_tiles, run_slots, n_slots;
+    int R, nrb, piece_slots, run_slots, n_slots;
 };
 
 constexpr int kPieceSlots = 8;
@@ -71,8 +71,6 @@ SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     c.nrb = (rows + c.R - 1) / c.R;
     const int max_tiles = std::max(1, d.max_pages_per_seq) * (kPageSize / split_tile_tokens());
     c.piece_slots = std::min(kPieceSlots, max_tiles);
-    // a segment of s tiles spans at most ceil(s / C) + 1 warps' ranges
-    c.min_tiles = c.piece_slots > 1 ? (max_tiles + c.piece_slots - 2) / (c.piece_slots - 1) : max_tiles;
     c.run_slots = plan ? plan_run_slots(plan) : 0;
     c.n_slots = c.run_slots + c.piece_slots;
     return c;
@@ -260,7 +258,7 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     p.max_q_len = d.max_q_len;
     p.rows_per_block = c.R;
     p.n_row_blocks = c.nrb;
-    p.min_tiles_per_warp = c.min_tiles;
+    p.piece_slots = c.piece_slots;
     p.slot_base = c.run_slots;
     p.n_rows_total = static_cast<int32_t>(rows_total);
     p.qscale = scale * 1.4426950408889634f;

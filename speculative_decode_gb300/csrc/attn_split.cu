@@ -263,14 +263,18 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
     }
     q_pre -= cq;  // exclusive
     int64_t cw = 0;
+    int max_tiles = 0;  // longest segment, in tiles
     {
         int qs = q_pre;
         for (int b = c_lo; b < c_hi; ++b) {
             const SeqInfo si = seq_info<R>(P, b, qs, true);
             cw += seq_work(P, si);
+            max_tiles = max(max_tiles, si.tiles);
             qs += max(0, si.n);
         }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) max_tiles = max(max_tiles, __shfl_xor_sync(0xffffffffu, max_tiles, o));
     int64_t w_pre = cw;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -280,9 +284,11 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
     const int64_t total = __shfl_sync(0xffffffffu, w_pre, 31);
     w_pre -= cw;
     const int64_t W = gridDim.x;
-    // at least min_tiles_per_warp, so that no segment splits into more pieces
-    // than the workspace has partial slots
-    const int64_t C = max((total + W - 1) / W, static_cast<int64_t>(max(P.min_tiles_per_warp, 1)));
+    // a segment of s tiles spans at most ceil(s / C) + 1 ranges: C is at least
+    // ceil(longest / (slots - 1)) so that no segment has more pieces than the
+    // workspace has partial slots
+    const int64_t C_min = P.piece_slots > 1 ? (max_tiles + P.piece_slots - 2) / (P.piece_slots - 1) : max_tiles;
+    const int64_t C = max((total + W - 1) / W, max(C_min, int64_t{1}));
     const int64_t g_begin = static_cast<int64_t>(blockIdx.x) * C;
     const int64_t g_end = min(total, g_begin + C);
     __syncwarp();

@@ -49,7 +49,7 @@ struct SplitParams {
     int32_t B, Hq, Hkv, G, num_pages, max_pages, total_q, max_q_len;
     int32_t rows_per_block;     // R, rows of one segment (4, 8 or 16)
     int32_t n_row_blocks;       // row blocks per (sequence, KV head) at max_q_len
-    int32_t min_tiles_per_warp; // bounds the pieces of a segment by the piece slots
+    int32_t piece_slots;        // partial slots a segment's pieces may use
     int32_t slot_base;          // first workspace slot used by pieces
     int32_t n_rows_total;       // total_q * Hq (row stride of a workspace slot)
     float qscale;               // scale * log2(e)

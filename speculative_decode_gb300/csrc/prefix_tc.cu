@@ -15,11 +15,16 @@
 //
 // CTA = 6 warps: warps 0-3 softmax and epilogue (thread t owns row t, which is
 // tensor-memory lane t), warp 4 the TMA producer, warp 5 allocates tensor
-// memory and issues the MMAs (one elected thread). Operands sit in shared
+// memory and issues the MMAs (one elected thread). S is double-buffered in
+// tensor memory, so Q K^T of the next tile and P V of the previous one run on
+// the tensor cores while the softmax of the current tile runs on the CUDA
+// cores. Operands sit in shared
 // memory in the 128-byte-swizzled K-major layout the TMA writes (Q, K and P)
 // or the MN-major one (V), described to the tensor core by shared-memory
 // matrix descriptors. Every wait is bounded; on timeout the CTA flags
 // SA_ERR_TIMEOUT, drains what it issued and frees its tensor memory.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "plan.h"
 
@@ -34,7 +39,7 @@ constexpr int kQBytes = 2 * kSub;             // Q [128 rows][128 d]
 constexpr int kPBytes = 2 * kSub;             // P [128 rows][128 keys]
 constexpr int kKVStage = 4 * kSub;            // K (2 blocks) + V (2 blocks) = 64 KiB
 constexpr int kStagesTC = 2;
-constexpr int kTmemCols = 256;                // S: columns 0-127, O: 128-255
+constexpr int kTmemCols = 512;                // S0: columns 0-127, S1: 128-255, O: 256-383
 constexpr int kThreads = 192;
 
 constexpr int kOffQ = 0;
@@ -129,14 +134,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint64_t *kv_full = bars;           // [2]
-    uint64_t *kv_empty = bars + 2;      // [2]
-    uint64_t *q_full = bars + 4;
-    uint64_t *s_full = bars + 5;
-    uint64_t *p_full = bars + 6;
-    uint64_t *o_done = bars + 7;
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 8);
-    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(bars + 9);
+    uint64_t *kv_full = bars;           // [2] K/V tile landed
+    uint64_t *kv_empty = bars + 2;      // [2] K/V stage free again
+    uint64_t *q_full = bars + 4;        // Q rows written
+    uint64_t *s_full = bars + 5;        // [2] S buffer holds Q K^T of a tile
+    uint64_t *p_full = bars + 7;        // P written (and its S buffer read)
+    uint64_t *p_free = bars + 8;        // P V finished: P free, O up to date
+    uint64_t *mma_done = bars + 9;      // every MMA finished (before freeing tensor memory)
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 10);
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(bars + 11);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -154,10 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&kv_empty[s], 1);
         }
         mbar_init(q_full, kM);
-        mbar_init(s_full, 1);
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
         mbar_init(p_full, kM);
-        mbar_init(o_done, 1);
-        mbar_init(&bars[10], 1);  // all MMAs complete (before tensor memory is freed)
+        mbar_init(p_free, 1);
+        mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_s = tmem, tmem_o = tmem + kN;
+    const uint32_t tmem_o = tmem + 2 * kN;  // S buffers at columns 0 and kN
 
     const uint32_t sQ = smem_u32(smem + kOffQ), sP = smem_u32(smem + kOffP), sKV = smem_u32(smem + kOffKV);
 
@@ -205,17 +212,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, lsum = 0.f;
         bool ok = true;
         for (int i = 0; i < n_kv && ok; ++i) {
-            ok = __all_sync(0xffffffffu, mbar_wait(s_full, i & 1));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[i & 1], (i >> 1) & 1));
             if (!ok) break;
             tc_fence_after();
             const int pos0 = (pc_lo + (i >> 1)) * kPageSize + (i & 1) * kN;
+            const uint32_t tmem_s = tmem + (i & 1) * kN;
             float x[kN];
+            const bool whole = pos0 + kN - 1 <= limit;  // no key of this tile is masked for row t
 #pragma unroll
             for (int c = 0; c < kN / 32; ++c) {
                 float v[32];
                 tmem_ld32(tmem_s + lane_base + c * 32, v);
+                if (whole) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) x[c * 32 + k] = pos0 + c * 32 + k <= limit ? v[k] * P.qscale : -INFINITY;
+                    for (int k = 0; k < 32; ++k) x[c * 32 + k] = v[k] * P.qscale;
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        x[c * 32 + k] = pos0 + c * 32 + k <= limit ? v[k] * P.qscale : -INFINITY;
+                }
             }
             float tmax = -INFINITY;
 #pragma unroll
@@ -225,38 +240,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool grow = tmax > m_ref + 8.f;
             const float m_new = grow ? tmax : m_ref;
             const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;  // 0 when m_ref was -inf
-            if (__any_sync(0xffffffffu, grow) && i > 0) {
+            const float m_use = m_new == -INFINITY ? 0.f : m_new;
+            // probabilities, packed to bf16 pairs while the tensor cores finish P V
+            uint32_t pw[kN / 2];
+            float psum = 0.f;
 #pragma unroll
-                for (int c = 0; c < kHeadDim / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(tmem_o + lane_base + c * 32, o);
+            for (int k = 0; k < kN / 2; ++k) {
+                const float a = exp2f(x[2 * k] - m_use), b = exp2f(x[2 * k + 1] - m_use);
+                psum += a + b;
+                const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+                pw[k] = *reinterpret_cast<const uint32_t *>(&h);
+            }
+            if (i > 0) {  // P V of the previous tile must be done before P and O change
+                ok = __all_sync(0xffffffffu, mbar_wait(p_free, (i - 1) & 1));
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] *= alpha;
-                    tmem_st32(tmem_o + lane_base + c * 32, o);
+                    for (int c = 0; c < kHeadDim / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(tmem_o + lane_base + c * 32, o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] *= alpha;
+                        tmem_st32(tmem_o + lane_base + c * 32, o);
+                    }
                 }
             }
-            lsum *= alpha;
+            lsum = lsum * alpha + psum;
             m_ref = m_new;
-            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
             // P row t -> shared memory (bf16, 128-byte swizzled K-major)
 #pragma unroll
-            for (int c = 0; c < kN / 8; ++c) {
-                uint32_t w[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint16_t lo = f32_to_bf16_rne(exp2f(x[c * 8 + 2 * k] - m_use));
-                    const uint16_t hi = f32_to_bf16_rne(exp2f(x[c * 8 + 2 * k + 1] - m_use));
-                    lsum += __uint_as_float(static_cast<uint32_t>(lo) << 16) + __uint_as_float(static_cast<uint32_t>(hi) << 16);
-                    w[k] = lo | (static_cast<uint32_t>(hi) << 16);
-                }
+            for (int c = 0; c < kN / 8; ++c)
                 *reinterpret_cast<uint4 *>(smem + kOffP + (c >> 3) * kSub + sw128_offset(t, c & 7)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-            }
+                    make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             mbar_arrive(p_full);
         }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, 0));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(p_free, (n_kv - 1) & 1));  // the last P V
         if (!ok) {
             *abort_flag = 1;
             if (lane == 0) flag_error(P.err, kErrBitTimeout);
@@ -311,11 +332,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (void)mbar_wait(&kv_full[i % kStagesTC], (i / kStagesTC) & 1);
         }
     } else {
-        // ================= MMA issuer (one thread)
+        // ================= MMA issuer (one thread). Order: QK(0), then for
+        // each tile i >= 1: QK(i) into the other S buffer, PV(i-1).
         if (lane == 0) {
             constexpr uint32_t kIdQK = idesc_bf16(false), kIdPV = idesc_bf16(true);
             bool ok = mbar_wait(q_full, 0);
             for (int i = 0; ok && i <= n_kv; ++i) {
+                if (i < n_kv) {  // S[i&1] = Q K(i)^T; S[i&1] was last read by softmax(i-2)
+                    const int s = i % kStagesTC;
+                    ok = mbar_wait(&kv_full[s], (i / kStagesTC) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t sK = sKV + s * kKVStage;
+#pragma unroll
+                    for (int k = 0; k < kHeadDim / 16; ++k) {
+                        const uint64_t a = smem_desc(sQ + (k >> 2) * kSub + (k & 3) * 32, 16, 1024);
+                        const uint64_t b = smem_desc(sK + (k >> 2) * kSub + (k & 3) * 32, 16, 1024);
+                        mma_bf16(tmem + (i & 1) * kN, a, b, kIdQK, k > 0);
+                    }
+                    mma_commit(&s_full[i & 1]);
+                }
                 if (i > 0) {  // O += P(i-1) V(i-1) once the softmax has written P(i-1)
                     ok = mbar_wait(p_full, (i - 1) & 1);
                     if (!ok) break;
@@ -328,21 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16(tmem_o, a, b, kIdPV, i > 1 || k > 0);
                     }
                     mma_commit(&kv_empty[(i - 1) % kStagesTC]);
-                    if (i == n_kv) mma_commit(o_done);
-                }
-                if (i < n_kv) {  // S = Q K(i)^T
-                    const int s = i % kStagesTC;
-                    ok = mbar_wait(&kv_full[s], (i / kStagesTC) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t sK = sKV + s * kKVStage;
-#pragma unroll
-                    for (int k = 0; k < kHeadDim / 16; ++k) {
-                        const uint64_t a = smem_desc(sQ + (k >> 2) * kSub + (k & 3) * 32, 16, 1024);
-                        const uint64_t b = smem_desc(sK + (k >> 2) * kSub + (k & 3) * 32, 16, 1024);
-                        mma_bf16(tmem_s, a, b, kIdQK, k > 0);
-                    }
-                    mma_commit(s_full);
+                    mma_commit(p_free);
                 }
             }
             if (!ok) {
@@ -350,10 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 flag_error(P.err, kErrBitTimeout);
             }
             // every MMA this thread issued completes before tensor memory is freed
-            mma_commit(&bars[10]);
+            mma_commit(mma_done);
         }
     }
-    if (warp == 5 && lane == 0) (void)mbar_wait(&bars[10], 0);
+    if (warp == 5 && lane == 0) (void)mbar_wait(mma_done, 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
