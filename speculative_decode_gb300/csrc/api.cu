@@ -59,9 +59,15 @@ int check_dims(const sa_dims *d) {
 // slots pieces may use (a pure function of the shapes).
 struct SplitConfig {
     int R, nrb, piece_slots, run_slots, n_slots;
+    SeqTcConfig tc;
 };
 
 constexpr int kPieceSlots = 8;
+// Sequences with at least this many query rows per KV head (G heads x new
+// tokens: q_len = k+1 verification) are a dense contraction: without a plan
+// they go to the tensor cores, in chunks of kTcChunkPages pages.
+constexpr int kTcMinRows = 16;
+constexpr int kTcChunkPages = 8;
 
 SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     SplitConfig c{};
@@ -71,7 +77,14 @@ SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     c.nrb = (rows + c.R - 1) / c.R;
     const int max_tiles = std::max(1, d.max_pages_per_seq) * (kPageSize / split_tile_tokens());
     c.piece_slots = std::min(kPieceSlots, max_tiles);
-    c.run_slots = plan ? plan_run_slots(plan) : 0;
+    c.tc = SeqTcConfig{0, 0, 0, 0};
+    if (plan == nullptr && G * std::max(1, d.max_q_len) >= kTcMinRows) {
+        c.tc.min_rows = kTcMinRows;
+        c.tc.mtiles = (rows + prefix_tile_rows() - 1) / prefix_tile_rows();
+        c.tc.chunk_pages = kTcChunkPages;
+        c.tc.max_chunks = (std::max(1, d.max_pages_per_seq) + kTcChunkPages - 1) / kTcChunkPages;
+    }
+    c.run_slots = plan ? plan_run_slots(plan) : c.tc.max_chunks;
     c.n_slots = c.run_slots + c.piece_slots;
     return c;
 }
@@ -221,8 +234,8 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
         return SA_ERR_CUDA;
 
     const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
-    if (pd && pd->num_tiles > 0) {
-        // shared runs first: the split kernel's merges read their partials
+    if ((pd && pd->num_tiles > 0) || c.tc.min_rows > 0) {
+        // tensor-core work first: the split kernel's merges read its partials
         CUtensorMap pk, pv;
         if (encode_tensor_map_2d(&pk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(k_pages),
                                  kHeadDim, pool_rows, kHeadDim * 2, 64, prefix_tile_rows(),
@@ -231,8 +244,13 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
                                  kHeadDim, pool_rows, kHeadDim * 2, 64, prefix_tile_rows(),
                                  CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return SA_ERR_CUDA;
-        if (launch_prefix_tc(d, *pd, q, pk, pv, scale, ws_acc, ws_ml, rows_total, err_flag,
+        if (pd && pd->num_tiles > 0 &&
+            launch_prefix_tc(d, *pd, q, pk, pv, scale, ws_acc, ws_ml, rows_total, err_flag,
                              block_table, s) != cudaSuccess)
+            return SA_ERR_CUDA;
+        if (c.tc.min_rows > 0 &&
+            launch_seq_tc(d, c.tc, q, pk, pv, scale, ws_acc, ws_ml, rows_total, err_flag,
+                          block_table, seq_lens, q_lens, s) != cudaSuccess)
             return SA_ERR_CUDA;
     }
 
@@ -259,6 +277,8 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     p.rows_per_block = c.R;
     p.n_row_blocks = c.nrb;
     p.piece_slots = c.piece_slots;
+    p.tc_min_rows = c.tc.min_rows;
+    p.tc_chunk_pages = c.tc.chunk_pages > 0 ? c.tc.chunk_pages : 1;
     p.slot_base = c.run_slots;
     p.n_rows_total = static_cast<int32_t>(rows_total);
     p.qscale = scale * 1.4426950408889634f;
@@ -277,7 +297,8 @@ int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan) {
     const int sms = device_sm_count();
     if (sms <= 0) return -1;
     const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
-    return 1 + ((pd && pd->num_tiles > 0) ? 1 : 0);
+    const SplitConfig c = split_config(*dims, plan);
+    return 1 + ((pd && pd->num_tiles > 0) ? 1 : 0) + (c.tc.min_rows > 0 ? 1 : 0);
 }
 
 size_t sa_spec_verify_workspace_size(int32_t num_seqs, int32_t k_max, int32_t vocab) {

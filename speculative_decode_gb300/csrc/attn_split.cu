@@ -86,7 +86,7 @@ struct Piece {
 };
 
 struct SeqInfo {
-    int T, n, skip_tok, tiles, nrb;
+    int T, n, skip_tok, tiles, nrb, runs;
 };
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -142,14 +142,20 @@ __device__ __forceinline__ SeqInfo seq_info(const SplitParams &P, int b, int qst
     s.tiles = 0;
     s.nrb = 0;
     s.skip_tok = 0;
+    s.runs = 0;
     if (s.n <= 0) return s;
     const int npages = (s.T + kPageSize - 1) / kPageSize;
     if (s.n > s.T || s.n > P.max_q_len || qstart + s.n > P.total_q || npages > P.max_pages) {
         if (flag) flag_error(P.err, kErrBitQlen);
         return s;
     }
-    const int skip = P.skip_pages ? P.skip_pages[b] : 0;
-    const int runs = P.run_slots ? P.run_slots[b] : 0;
+    int skip = P.skip_pages ? P.skip_pages[b] : 0;
+    int runs = P.run_slots ? P.run_slots[b] : 0;
+    if (P.tc_min_rows > 0 && P.G * s.n >= P.tc_min_rows) {  // attended on the tensor cores
+        skip = npages;
+        runs = (npages + P.tc_chunk_pages - 1) / P.tc_chunk_pages;
+    }
+    s.runs = runs;
     s.skip_tok = skip * kPageSize;
     const int keys = s.T - s.skip_tok;
     s.tiles = keys > 0 ? (keys + kTile - 1) / kTile : (runs > 0 ? 1 : 0);  // one empty tile carries the merge
@@ -340,11 +346,13 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
     int64_t iws = ws0;
     SeqInfo isi = seq_info<R>(P, ib, iq, false);
     int64_t ig = g_begin;
-    int iseg, itile;
+    int iseg, itile, ikvh, irb;
     {
         const int64_t off = g_begin - iws;
         iseg = static_cast<int>(off / isi.tiles);
         itile = static_cast<int>(off % isi.tiles);
+        ikvh = iseg / isi.nrb;
+        irb = iseg % isi.nrb;
     }
     uint32_t issued = 0, consumed = 0, pieces_pushed = 0;
     // physical page of the issue cursor's current logical page, and the next
@@ -363,8 +371,15 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         if (ig >= g_end) return false;
         if (itile == isi.tiles) {  // next segment
             itile = 0;
-            if (++iseg == P.Hkv * isi.nrb) {  // next sequence with work
+            ++iseg;
+            if (++irb == isi.nrb) {
+                irb = 0;
+                ++ikvh;
+            }
+            if (iseg == P.Hkv * isi.nrb) {  // next sequence with work
                 iseg = 0;
+                ikvh = 0;
+                irb = 0;
                 do {
                     iws += seq_work(P, isi);
                     iq += max(0, isi.n);
@@ -373,7 +388,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                 } while (seq_work(P, isi) == 0);
             }
         }
-        const int kvh = iseg / isi.nrb, rb = iseg % isi.nrb;
+        const int kvh = ikvh, rb = irb;
         if (ig == g_begin || itile == 0) {
             // a new piece: describe it for the consumer and fetch its query rows
             const int64_t seg0 = iws + static_cast<int64_t>(iseg) * isi.tiles;
@@ -389,7 +404,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                 d[8] = static_cast<int>(blockIdx.x) - first;
                 d[9] = last - first + 1;
                 d[10] = nvr;
-                d[11] = P.run_slots ? P.run_slots[ib] : 0;
+                d[11] = isi.runs;
                 mbar_arrive_expect_tx(&qfull[qs], nvr * kHeadDim * 2);
                 const int r0 = rb * R;
                 for (int i = r0 / P.G; i <= (r0 + nvr - 1) / P.G; ++i) {
@@ -545,9 +560,13 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                 for (int step = 0; step < NS; ++step) tmax = fmaxf(tmax, sv[step]);
 #pragma unroll
                 for (int o = L; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-                const float m_new = fmaxf(m, tmax);
+                // the reference max m only moves when the tile max exceeds it by
+                // more than 2^8, so p stays below 256 and the accumulators are
+                // rescaled a few times per segment instead of on most tiles
+                const bool grow = tmax > m + 8.f;
+                const float m_new = grow ? tmax : m;
+                const float alpha = grow ? exp2f(m - m_new) : 1.f;  // 0 when m was -inf
                 const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                const float alpha = exp2f(m - m_use);
                 lsum *= alpha;
                 m = m_new;
 #pragma unroll
@@ -556,9 +575,9 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                     lsum += p;
                     if (row_writer) pbuf[step * TG + tg][rj] = p;
                 }
-                if (tg == 0 && row_writer) rowx[rj] = alpha;
-                __syncwarp();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                if (__any_sync(0xffffffffu, grow)) {
+                    if (tg == 0 && row_writer) rowx[rj] = alpha;
+                    __syncwarp();
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
                         const float a = rowx[r];
@@ -566,6 +585,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                         for (int k = 0; k < NW; ++k) acc[r][k] = make_float2(acc[r][k].x * a, acc[r][k].y * a);
                     }
                 }
+                __syncwarp();  // p visible to the whole warp
 
                 // ---- O += P V over the valid tokens of the tile
                 const int nvalid = min(kTile, U.T - t0);

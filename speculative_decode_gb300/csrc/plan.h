@@ -47,6 +47,23 @@ cudaError_t launch_prefix_tc(const sa_dims &d, const PlanDevice &pd, const uint1
                              const int32_t *block_table, cudaStream_t stream);
 int prefix_tile_rows();
 
+// Sequence mode of the tensor-core kernel: sequences with at least min_rows
+// query rows per KV head (G heads x new tokens, e.g. q_len = k+1 verification)
+// are attended entirely on the tensor cores, one work item per (sequence, KV
+// head, 128-row tile, chunk of chunk_pages pages); the split kernel only merges
+// their partials (slot = chunk index).
+struct SeqTcConfig {
+    int min_rows;    // 0 disables the mode
+    int mtiles;      // 128-row tiles at max_q_len
+    int chunk_pages;
+    int max_chunks;  // ceil(max_pages_per_seq / chunk_pages)
+};
+cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t *q,
+                          const CUtensorMap &tmk, const CUtensorMap &tmv, float scale,
+                          float *ws_acc, float *ws_ml, int64_t rows_total, int32_t *err,
+                          const int32_t *block_table, const int32_t *seq_lens,
+                          const int32_t *q_lens, cudaStream_t stream);
+
 constexpr int kRunDescInts = 6;
 constexpr int kTileInts = 6;
 constexpr int kPrefixTileRows = 128;

@@ -116,9 +116,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 struct PrefixParams {
     const uint16_t *q;
     const int32_t *block_table;
+    // plan mode: work items and rows from a shared-run plan
     const int32_t *run_desc;
     const int32_t *run_rows;
     const int32_t *tiles;
+    // sequence mode: one work item per (sequence, KV head, row tile, page chunk)
+    const int32_t *seq_lens;
+    const int32_t *q_lens;
+    int32_t seq_mode, B, max_q_len, total_q, min_rows, mtiles, max_chunks, chunk_pages;
     float *ws_acc;
     float *ws_ml;
     int32_t *err;
@@ -147,12 +152,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
 
-    // ---- the work item: (run, KV head, 128-row tile, page chunk)
-    const int32_t *it = P.tiles + static_cast<int64_t>(blockIdx.x) * kTileInts;
-    const int run = it[0], g = it[1], row0 = it[2], pc_lo = it[3], pc_hi = it[4], chunk = it[5];
-    const int32_t *rd = P.run_desc + static_cast<int64_t>(run) * kRunDescInts;
-    const int rows_begin = rd[2], row_count = rd[3], member = rd[5];
-    const int n_kv = 2 * (pc_hi - pc_lo);  // 128-key tiles
+    // ---- the work item
+    int g, row0, pc_lo, pc_hi, chunk, member, row_count, rows_begin = 0;
+    int key_end = 0x7fffffff;  // keys at or past this position are not in the cache
+    int seq_n = 0, seq_qstart = 0;
+    if (!P.seq_mode) {  // (run, KV head, 128-row tile, page chunk) from the plan
+        const int32_t *it = P.tiles + static_cast<int64_t>(blockIdx.x) * kTileInts;
+        const int run = it[0];
+        g = it[1];
+        row0 = it[2];
+        pc_lo = it[3];
+        pc_hi = it[4];
+        chunk = it[5];
+        const int32_t *rd = P.run_desc + static_cast<int64_t>(run) * kRunDescInts;
+        rows_begin = rd[2];
+        row_count = rd[3];
+        member = rd[5];
+    } else {  // (sequence, KV head, 128-row tile, page chunk): rows = G heads x new tokens
+        int idx = blockIdx.x;
+        chunk = idx % P.max_chunks;
+        idx /= P.max_chunks;
+        const int mt = idx % P.mtiles;
+        idx /= P.mtiles;
+        g = idx % P.Hkv;
+        member = idx / P.Hkv;
+        const int T = P.seq_lens[member];
+        seq_n = P.q_lens[member];
+        const int npages = (T + kPageSize - 1) / kPageSize;
+        row_count = P.G * seq_n;
+        row0 = mt * kM;
+        pc_lo = chunk * P.chunk_pages;
+        pc_hi = min(npages, pc_lo + P.chunk_pages);
+        key_end = T;
+        // packed query row of the sequence's first new token (block reduction)
+        __shared__ int red[kThreads / 32];
+        int part = 0;
+        for (int k = tid; k < member; k += kThreads) part += P.q_lens[k];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) red[warp] = part;
+        __syncthreads();
+        for (int w = 0; w < kThreads / 32; ++w) seq_qstart += red[w];
+        // the same eligibility rule as the split kernel's, which merges these partials
+        const bool work = seq_n > 0 && seq_n <= T && seq_n <= P.max_q_len && npages <= P.max_pages &&
+                          row_count >= P.min_rows && seq_qstart + seq_n <= P.total_q && pc_lo < pc_hi &&
+                          row0 < row_count;
+        if (!work) return;  // uniform over the CTA: nothing allocated yet
+    }
+    // 128-key tiles of the chunk that hold keys below key_end
+    const int n_kv = (min(pc_hi * kPageSize, key_end) - pc_lo * kPageSize + kN - 1) / kN;
 
     if (tid == 0) {
         for (int s = 0; s < kStagesTC; ++s) {
@@ -188,13 +236,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = tid;
         const int r = row0 + t;
         const bool valid = r < row_count;
+        const bool warp_valid = __any_sync(0xffffffffu, valid);  // warps without rows skip the softmax
         int32_t token = 0, hl = 0, limit = -1, slot = 0;
         if (valid) {
-            const int32_t *rr = P.run_rows + static_cast<int64_t>(rows_begin + r) * 4;
-            token = rr[0];
-            hl = rr[1];
-            limit = rr[2];
-            slot = rr[3] + chunk;
+            if (!P.seq_mode) {
+                const int32_t *rr = P.run_rows + static_cast<int64_t>(rows_begin + r) * 4;
+                token = rr[0];
+                hl = rr[1];
+                limit = rr[2];
+                slot = rr[3] + chunk;
+            } else {
+                token = seq_qstart + r / P.G;
+                hl = r % P.G;
+                limit = key_end - seq_n + r / P.G;
+                slot = chunk;
+            }
+        }
+        if (!warp_valid) {  // P rows of rows that do not exist stay zero
+#pragma unroll
+            for (int c = 0; c < kN / 8; ++c)
+                *reinterpret_cast<uint4 *>(smem + kOffP + (c >> 3) * kSub + sw128_offset(t, c & 7)) = make_uint4(0, 0, 0, 0);
         }
         // Q row t -> shared memory, 128-byte swizzled K-major (two 64-column blocks)
         {
@@ -215,7 +276,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(&s_full[i & 1], (i >> 1) & 1));
             if (!ok) break;
             tc_fence_after();
-            const int pos0 = (pc_lo + (i >> 1)) * kPageSize + (i & 1) * kN;
+            const int pos0 = pc_lo * kPageSize + i * kN;
+            if (!warp_valid) {
+                if (i > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(p_free, (i - 1) & 1));
+                    if (!ok) break;
+                }
+                if (pos0 + t >= key_end) {  // keys past the end may hold stale data: zero their V row
+                    uint8_t *vrow = smem + kOffKV + (i % kStagesTC) * kKVStage + 2 * kSub + t * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        *reinterpret_cast<uint4 *>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(vrow + kSub + c * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tc_fence_before();
+                mbar_arrive(p_full);
+                continue;
+            }
             const uint32_t tmem_s = tmem + (i & 1) * kN;
             float x[kN];
             const bool whole = pos0 + kN - 1 <= limit;  // no key of this tile is masked for row t
@@ -273,6 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kN / 8; ++c)
                 *reinterpret_cast<uint4 *>(smem + kOffP + (c >> 3) * kSub + sw128_offset(t, c & 7)) =
                     make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+            if (pos0 + t >= key_end) {  // keys past the end may hold stale data: zero their V row
+                uint8_t *vrow = smem + kOffKV + (i % kStagesTC) * kKVStage + 2 * kSub + t * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    *reinterpret_cast<uint4 *>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(vrow + kSub + c * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             mbar_arrive(p_full);
@@ -281,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) {
             *abort_flag = 1;
             if (lane == 0) flag_error(P.err, kErrBitTimeout);
-        } else {
+        } else if (warp_valid) {
             tc_fence_after();
             // epilogue: fp32 partial (O, m, l) of this row for the merge
             const int64_t orow = static_cast<int64_t>(token) * P.Hq + g * P.G + hl;
@@ -313,6 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (*abort_flag) break;
                 const int page = pc_lo + (i >> 1);
                 const int pid = P.block_table[static_cast<int64_t>(member) * P.max_pages + page];
+                // (sequence mode: the last tile may reach past the sequence's keys; the
+                // rows past the end are zeroed in shared memory before P V)
                 uint8_t *dst = smem + kOffKV + s * kKVStage;
                 if (pid < 0 || pid >= P.num_pages) {  // the planner only takes valid pages
                     flag_error(P.err, kErrBitPageOOB);
@@ -410,6 +499,43 @@ cudaError_t launch_prefix_tc(const sa_dims &d, const PlanDevice &pd, const uint1
     p.n_rows_total = rows_total;
     p.qscale = scale * 1.4426950408889634f;
     prefix_tc_kernel<<<pd.num_tiles, kThreads, kSmemBytes, stream>>>(p, tmk, tmv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t *q,
+                          const CUtensorMap &tmk, const CUtensorMap &tmv, float scale,
+                          float *ws_acc, float *ws_ml, int64_t rows_total, int32_t *err,
+                          const int32_t *block_table, const int32_t *seq_lens,
+                          const int32_t *q_lens, cudaStream_t stream) {
+    static cudaError_t attr = cudaFuncSetAttribute(prefix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   kSmemBytes);
+    if (attr != cudaSuccess) return attr;
+    PrefixParams p{};
+    p.q = q;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.q_lens = q_lens;
+    p.seq_mode = 1;
+    p.B = d.num_seqs;
+    p.max_q_len = d.max_q_len;
+    p.total_q = d.total_q;
+    p.min_rows = c.min_rows;
+    p.mtiles = c.mtiles;
+    p.max_chunks = c.max_chunks;
+    p.chunk_pages = c.chunk_pages;
+    p.ws_acc = ws_acc;
+    p.ws_ml = ws_ml;
+    p.err = err;
+    p.Hq = d.num_q_heads;
+    p.Hkv = d.num_kv_heads;
+    p.G = d.num_q_heads / d.num_kv_heads;
+    p.max_pages = d.max_pages_per_seq;
+    p.num_pages = d.num_pages;
+    p.n_rows_total = rows_total;
+    p.qscale = scale * 1.4426950408889634f;
+    const int64_t grid = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.mtiles * c.max_chunks;
+    if (grid == 0) return cudaSuccess;
+    prefix_tc_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(p, tmk, tmv);
     return cudaGetLastError();
 }
 

@@ -203,3 +203,19 @@ def test_nested_shared_runs():
     out, err, _, _ = run_attention(w, use_plan=True, append=False)
     assert err == 0
     assert_attention_close(out, oracle_attention(w, append=False), "nested runs")
+
+
+# ----------------------------------- multi-query rows on tensor cores (no plan)
+@pytest.mark.parametrize("seed,G,Hkv,qlens,max_ctx", [
+    (71, 4, 2, (6,), 3000),          # 24 rows per KV head: the verify shape
+    (72, 8, 1, (1, 6), 2500),        # mixed: q_len 1 rows on the split kernel, q_len 6 on tensor cores
+    (73, 16, 2, (16,), 700),         # 256 rows per KV head: two 128-row tiles
+    (74, 4, 4, (4, 5, 16), 129),     # short contexts: partial 128-key tiles past the end
+])
+def test_multi_query_rows_on_tensor_cores(seed, G, Hkv, qlens, max_ctx):
+    w = wl.random_case(seed, num_seqs=5, Hq=G * Hkv, Hkv=Hkv, max_ctx=max_ctx, q_len_choices=qlens)
+    d = dims_of(w)
+    assert sa.paged_attn_kernel_count(d) == 2      # tensor-core sequence pass + split/merge pass
+    out, err, _, _ = run_attention(w)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), f"multi-query seed {seed}")
