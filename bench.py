@@ -261,12 +261,19 @@ def run_ours(args):
     barrier()
     dev = torch.device("cuda", local)
 
-    # L2 flush buffer: twice the L2 size, rewritten before every timed step
+    # L2 flush before every timed step: write a buffer twice the L2 size, then
+    # read another one of the same size. The write evicts everything; the read
+    # leaves the L2 holding clean lines of unrelated data, so the timed kernels
+    # neither find their inputs cached nor pay for writing back the flush's own
+    # dirty lines.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_buf = torch.empty(max(2 * l2, 1 << 20), dtype=torch.uint8, device=dev)
+    nflush = max(2 * l2, 1 << 20) // 8 * 8
+    flush_w = torch.empty(nflush, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(nflush, dtype=torch.uint8, device=dev)
 
     def flush():
-        flush_buf.zero_()
+        flush_w.zero_()
+        flush_r.view(torch.int64).sum()
 
     # ---- headline: decode step on the Llama3-8B-shaped batch
     w = wl.config(DECODE_CFG, seed=1000 + DECODE_CFG + 1 + 7919 * rank)
@@ -336,7 +343,7 @@ def run_ours(args):
             "ctx": "uniform[512,1024]", "q_len": 1,
             "step": "kv_append + paged_attn",
             "value_counts": "paged_attn algorithmic bytes / paged_attn device time",
-            "l2": "flushed (2x L2 write) before every step",
+            "l2": "flushed before every step: 2x L2 written, then 2x L2 of other data read",
             "parallelism": f"replicas x{world} (independent batches, no collective)",
         },
         "counted_bytes_per_step": cbytes,

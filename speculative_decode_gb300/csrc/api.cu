@@ -81,12 +81,20 @@ SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     if (plan == nullptr && G * std::max(1, d.max_q_len) >= kTcMinRows) {
         c.tc.min_rows = kTcMinRows;
         c.tc.mtiles = (rows + prefix_tile_rows() - 1) / prefix_tile_rows();
-        c.tc.chunk_pages = kTcChunkPages;
-        c.tc.max_chunks = (std::max(1, d.max_pages_per_seq) + kTcChunkPages - 1) / kTcChunkPages;
+        // at most 8 chunks per sequence, so that a row has at most 16 partials to merge
+        const int mp = std::max(1, d.max_pages_per_seq);
+        c.tc.chunk_pages = std::max(kTcChunkPages, (mp + 7) / 8);
+        c.tc.max_chunks = (mp + c.tc.chunk_pages - 1) / c.tc.chunk_pages;
     }
     c.run_slots = plan ? plan_run_slots(plan) : c.tc.max_chunks;
     c.n_slots = c.run_slots + c.piece_slots;
     return c;
+}
+
+// Partials one output row may have to merge (the split kernel merges at most
+// kMaxMergeSlotsHost of them).
+constexpr int kMaxMergeSlotsHost = 16;
+bool merge_fits(const SplitConfig &c) { return c.n_slots <= kMaxMergeSlotsHost;
 }
 
 // Workspace layout: fp32 accumulators [n_slots][total_q * Hq][128], then
@@ -219,20 +227,12 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     const SplitConfig c = split_config(d, plan);
+    if (!merge_fits(c)) return SA_ERR_UNSUPPORTED;  // too many partials per row to merge
     const int64_t rows_total = static_cast<int64_t>(d.total_q) * d.num_q_heads;
     float *ws_acc = static_cast<float *>(workspace);
     float *ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.ml_offset);
 
-    CUtensorMap tmk, tmv;
     const uint64_t pool_rows = static_cast<uint64_t>(d.num_pages) * d.num_kv_heads * kPageSize;
-    if (encode_tensor_map_2d(&tmk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(k_pages),
-                             kHeadDim, pool_rows, kHeadDim * 2, 64, split_tile_tokens(),
-                             CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-        encode_tensor_map_2d(&tmv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(v_pages),
-                             kHeadDim, pool_rows, kHeadDim * 2, 64, split_tile_tokens(),
-                             CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-        return SA_ERR_CUDA;
-
     const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
     if ((pd && pd->num_tiles > 0) || c.tc.min_rows > 0) {
         // tensor-core work first: the split kernel's merges read its partials
@@ -256,6 +256,8 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
 
     SplitParams p{};
     p.q = q;
+    p.k_pages = k_pages;
+    p.v_pages = v_pages;
     p.out = out;
     p.block_table = block_table;
     p.seq_lens = seq_lens;
@@ -287,7 +289,7 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     int per_sm = 0;
     if (split_occupancy(c.R, 1, &per_sm) != cudaSuccess || per_sm <= 0) return SA_ERR_CUDA;
     const int64_t ctas = static_cast<int64_t>(sms) * per_sm;  // one warp per CTA, all resident
-    if (launch_split_attn(p, tmk, tmv, static_cast<int>(ctas), 1, s) != cudaSuccess)
+    if (launch_split_attn(p, static_cast<int>(ctas), s) != cudaSuccess)
         return SA_ERR_CUDA;
     return finish(s, err_flag);
 }

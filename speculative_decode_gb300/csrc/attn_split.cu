@@ -18,10 +18,10 @@
 //    of work that is cut into equal contiguous ranges, one per warp
 //    (stream-K): perfectly balanced whatever the context lengths, with at
 //    most two partial pieces per warp and no scheduling atomics.
-//  * One warp owns its range. Lane 0 streams K and V tiles with TMA (2-D
-//    tensor copies, 128-byte swizzle) into the warp's private ring of S
-//    stages and bulk-copies each piece's query rows ahead of use; all 32
-//    lanes compute.
+//  * One warp owns its range. Lane 0 streams each tile's K rows and V rows
+//    (each one contiguous run inside a page) with two 1-D bulk copies into
+//    the warp's private ring of S stages, and bulk-copies each piece's query
+//    rows ahead of use; all 32 lanes compute.
 //  * Lane mapping: a token is handled by L = 2R lanes (8, 16 or 32), each
 //    owning 128/L head dims, so pre-scaled queries and output accumulators
 //    live in registers. Q.K partial dots are combined with a shuffle
@@ -48,8 +48,9 @@ namespace {
 #define SA_SPLIT_MIN_WARPS 1
 #endif
 constexpr int kTile = SA_SPLIT_TILE;          // tokens per stage (16 or 32)
-constexpr int kHalfBytes = kTile * 128;       // 32 rows x 64 bf16 (one 128-byte swizzle span)
-constexpr int kStageBytes = 4 * kHalfBytes;   // K[0:64], K[64:128], V[0:64], V[64:128]
+constexpr int kRowBytes = kHeadDim * 2;       // one K or V row: 256 bytes
+constexpr int kKVBytes = kTile * kRowBytes;   // K (or V) rows of one tile, contiguous in a page
+constexpr int kStageBytes = 2 * kKVBytes;     // K tile, then V tile
 #ifndef SA_SPLIT_STAGES
 #define SA_SPLIT_STAGES 2
 #endif
@@ -100,23 +101,24 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
 
-// Load this lane's bf16 words of row t from a swizzled two-half tile. Lane j
-// of an L-lane token group owns: L=8 -> d 8j..8j+7 and 64+8j..64+8j+7;
-// L=16 -> d 64(j/8)+8(j%8) .. +7; L=32 -> d 4j..4j+3. Each quarter-warp then
-// touches eight distinct 16-byte chunks of the swizzle span (conflict-free).
+// Load this lane's bf16 words of row t of a tile held as plain 256-byte rows.
+// Lane j of an L-lane token group owns: L=8 -> d 8j..8j+7 and 64+8j..64+8j+7;
+// L=16 -> d 8j..8j+7; L=32 -> d 4j..4j+3. The lanes of a token group read
+// consecutive 16-byte (8-byte) pieces of one row, so each quarter-warp touches
+// one 128-byte span: no bank conflicts.
 template <int L>
 __device__ __forceinline__ void load_tile_row(const uint8_t *tile, int t, int j, uint32_t (&w)[64 / L]) {
+    const uint8_t *row = tile + t * kRowBytes;
     if constexpr (L == 8) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(tile + sw128_offset(t, j));
-        const uint4 b = *reinterpret_cast<const uint4 *>(tile + kHalfBytes + sw128_offset(t, j));
+        const uint4 a = *reinterpret_cast<const uint4 *>(row + j * 16);
+        const uint4 b = *reinterpret_cast<const uint4 *>(row + 128 + j * 16);
         w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
         w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
     } else if constexpr (L == 16) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(tile + (j >> 3) * kHalfBytes + sw128_offset(t, j & 7));
+        const uint4 a = *reinterpret_cast<const uint4 *>(row + j * 16);
         w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
     } else {
-        const uint2 a = *reinterpret_cast<const uint2 *>(tile + (j >> 4) * kHalfBytes +
-                                                         sw128_offset(t, (j & 15) >> 1) + (j & 1) * 8);
+        const uint2 a = *reinterpret_cast<const uint2 *>(row + j * 8);
         w[0] = a.x; w[1] = a.y;
     }
 }
@@ -125,7 +127,7 @@ __device__ __forceinline__ void load_tile_row(const uint8_t *tile, int t, int j,
 template <int L>
 __device__ __forceinline__ int lane_dim_of_word(int j, int k) {
     if constexpr (L == 8) return (k < 4 ? 8 * j : 64 + 8 * j) + 2 * (k & 3);
-    else if constexpr (L == 16) return 64 * (j >> 3) + 8 * (j & 7) + 2 * k;
+    else if constexpr (L == 16) return 8 * j + 2 * k;
     else return 4 * j + 2 * k;
 }
 
@@ -167,38 +169,70 @@ __device__ __forceinline__ int64_t seq_work(const SplitParams &P, const SeqInfo 
     return static_cast<int64_t>(s.tiles) * P.Hkv * s.nrb;
 }
 
-// Merge every partial of the piece's rows: the shared-prefix runs' slots and
-// the pieces' slots, with exact max-shifted rescaling. Lane = 4 head dims.
+// Merge every partial of the piece's rows: the tensor-core runs' slots and the
+// pieces' slots, with exact max-shifted rescaling. Eight lanes per row (16
+// head dims each), four rows at a time, every load of a row's slots in flight
+// together so the merge costs about two memory round trips per four rows.
+constexpr int kMaxMergeSlots = 16;
+
+__device__ __forceinline__ const float *ws_slot_row(const SplitParams &P, const Piece &U, int k, int64_t row,
+                                                    const float *base, int width) {
+    const int slot = k < U.runs ? k : P.slot_base + (k - U.runs);
+    return base + (static_cast<int64_t>(slot) * P.n_rows_total + row) * width;
+}
+
 __device__ void merge_rows(const SplitParams &P, const Piece &U, int R, int lane) {
     const int nslots = U.runs + U.pieces;
-    for (int r = 0; r < U.nvr; ++r) {
+    const int sub = lane & 7;
+    for (int r0 = 0; r0 < U.nvr; r0 += 4) {
+        const int r = r0 + (lane >> 3);
+        if (r >= U.nvr) continue;
         const int64_t row = out_row(P, U, U.rb * R + r);
+        float ms[kMaxMergeSlots], ls[kMaxMergeSlots];
         float M = -INFINITY;
-        for (int k = 0; k < nslots; ++k) {
-            const int slot = k < U.runs ? k : P.slot_base + (k - U.runs);
-            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-                P.ws_ml + (static_cast<int64_t>(slot) * P.n_rows_total + row) * 2));
-            if (ml.y > 0.f) M = fmaxf(M, ml.x);
+#pragma unroll
+        for (int k = 0; k < kMaxMergeSlots; ++k) {
+            ms[k] = -INFINITY;
+            ls[k] = 0.f;
+            if (k < nslots) {
+                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(ws_slot_row(P, U, k, row, P.ws_ml, 2)));
+                ms[k] = ml.x;
+                ls[k] = ml.y;
+            }
         }
+#pragma unroll
+        for (int k = 0; k < kMaxMergeSlots; ++k)
+            if (ls[k] > 0.f) M = fmaxf(M, ms[k]);
         float Lsum = 0.f;
-        float4 o = make_float4(0, 0, 0, 0);
-        for (int k = 0; k < nslots; ++k) {
-            const int slot = k < U.runs ? k : P.slot_base + (k - U.runs);
-            const int64_t wi = static_cast<int64_t>(slot) * P.n_rows_total + row;
-            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(P.ws_ml + wi * 2));
-            if (!(ml.y > 0.f)) continue;
-            const float sc = exp2f(ml.x - M);
-            const float4 a = __ldcg(reinterpret_cast<const float4 *>(P.ws_acc + wi * kHeadDim + lane * 4));
-            Lsum += ml.y * sc;
-            o.x += a.x * sc;
-            o.y += a.y * sc;
-            o.z += a.z * sc;
-            o.w += a.w * sc;
+        float4 o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) o[q] = make_float4(0, 0, 0, 0);
+#pragma unroll
+        for (int k = 0; k < kMaxMergeSlots; ++k) {
+            if (ls[k] > 0.f) {
+                const float w = exp2f(ms[k] - M);
+                Lsum += ls[k] * w;
+                const float4 *a = reinterpret_cast<const float4 *>(ws_slot_row(P, U, k, row, P.ws_acc, kHeadDim) + sub * 16);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 v = __ldcg(a + q);
+                    o[q].x += v.x * w;
+                    o[q].y += v.y * w;
+                    o[q].z += v.z * w;
+                    o[q].w += v.w * w;
+                }
+            }
         }
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-        const uint32_t lo = f32_to_bf16_rne(o.x * inv) | (static_cast<uint32_t>(f32_to_bf16_rne(o.y * inv)) << 16);
-        const uint32_t hi = f32_to_bf16_rne(o.z * inv) | (static_cast<uint32_t>(f32_to_bf16_rne(o.w * inv)) << 16);
-        *reinterpret_cast<uint2 *>(P.out + row * kHeadDim + lane * 4) = make_uint2(lo, hi);
+        uint32_t wv[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            wv[2 * q] = f32_to_bf16_rne(o[q].x * inv) | (static_cast<uint32_t>(f32_to_bf16_rne(o[q].y * inv)) << 16);
+            wv[2 * q + 1] = f32_to_bf16_rne(o[q].z * inv) | (static_cast<uint32_t>(f32_to_bf16_rne(o[q].w * inv)) << 16);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(P.out + row * kHeadDim + sub * 16);
+        dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
     }
 }
 
@@ -218,15 +252,13 @@ __device__ void resolve(const SplitParams &P, Pending &pd, int R, int lane) {
     pd.live = false;
     const int old = __shfl_sync(0xffffffffu, pd.old, 0);
     if (old != pd.U.pieces - 1) return;
-    __threadfence();  // acquire: every other piece's partial is visible
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");  // acquire: every other piece's partial is visible
     merge_rows(P, pd.U, R, lane);
     if (lane == 0) atomicExch(merge_counter(P, pd.U), 0);
 }
 
 template <int R>
-__global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(const SplitParams P,
-                                                        const __grid_constant__ CUtensorMap tmk,
-                                                        const __grid_constant__ CUtensorMap tmv) {
+__global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(const SplitParams P) {
     using Gm = Geo<R>;
     using Lay = Layout<R>;
     constexpr int L = Gm::L, TG = Gm::TG, NS = Gm::NS, NW = Gm::NW, DUP = Gm::DUP;
@@ -251,8 +283,6 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
             mbar_init(&qfull[s], 1);
         }
         fence_barrier_init();
-        prefetch_tensormap(&tmk);
-        prefetch_tensormap(&tmv);
     }
 
     // ---- 1. total work and this warp's range [g_begin, g_end) of tiles
@@ -424,13 +454,12 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         if (lane == 0) {
             stage_ok[s] = ok;
             if (ok) {
-                const int y = (pid * P.Hkv + kvh) * kPageSize + (t0 % kPageSize);
+                // the tile's K rows and V rows are each one contiguous run in the page
+                const int64_t row = static_cast<int64_t>(pid * P.Hkv + kvh) * kPageSize + (t0 % kPageSize);
                 uint8_t *dst = smem + s * kStageBytes;
                 mbar_arrive_expect_tx(&full[s], kStageBytes);
-                tma_load_2d(dst, &tmk, &full[s], 0, y, policy);
-                tma_load_2d(dst + kHalfBytes, &tmk, &full[s], 64, y, policy);
-                tma_load_2d(dst + 2 * kHalfBytes, &tmv, &full[s], 0, y, policy);
-                tma_load_2d(dst + 3 * kHalfBytes, &tmv, &full[s], 64, y, policy);
+                bulk_load_hint(dst, P.k_pages + row * kHeadDim, kKVBytes, &full[s], policy);
+                bulk_load_hint(dst + kKVBytes, P.v_pages + row * kHeadDim, kKVBytes, &full[s], policy);
             } else {
                 mbar_arrive(&full[s]);  // nothing to load: the consumer skips this tile
             }
@@ -594,7 +623,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                     const int t = step * TG + tg;
                     if (t < nvalid) {
                         uint32_t vw[NW];
-                        load_tile_row<L>(st + 2 * kHalfBytes, t, j, vw);
+                        load_tile_row<L>(st + kKVBytes, t, j, vw);
                         float pr[R];
 #pragma unroll
                         for (int r4 = 0; r4 < R / 4; ++r4) {
@@ -680,11 +709,10 @@ cudaError_t prepare() {
 }
 
 template <int R>
-cudaError_t launch_r(const SplitParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                     int num_ctas, cudaStream_t stream) {
+cudaError_t launch_r(const SplitParams &p, int num_ctas, cudaStream_t stream) {
     cudaError_t e = prepare<R>();
     if (e != cudaSuccess) return e;
-    split_attn_kernel<R><<<num_ctas, 32, smem_bytes<R>(), stream>>>(p, tk, tv);
+    split_attn_kernel<R><<<num_ctas, 32, smem_bytes<R>(), stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -709,12 +737,11 @@ cudaError_t split_occupancy(int R, int, int *ctas_per_sm) {
     }
 }
 
-cudaError_t launch_split_attn(const SplitParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                              int num_ctas, int, cudaStream_t stream) {
+cudaError_t launch_split_attn(const SplitParams &p, int num_ctas, cudaStream_t stream) {
     switch (p.rows_per_block) {
-        case 4: return launch_r<4>(p, tk, tv, num_ctas, stream);
-        case 8: return launch_r<8>(p, tk, tv, num_ctas, stream);
-        case 16: return launch_r<16>(p, tk, tv, num_ctas, stream);
+        case 4: return launch_r<4>(p, num_ctas, stream);
+        case 8: return launch_r<8>(p, num_ctas, stream);
+        case 16: return launch_r<16>(p, num_ctas, stream);
         default: return cudaErrorInvalidValue;
     }
 }

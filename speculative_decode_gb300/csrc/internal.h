@@ -36,6 +36,8 @@ struct PlanDevice {
 // Parameters of the split-K kernel (page-streamed attention on CUDA cores).
 struct SplitParams {
     const uint16_t *q;
+    const uint16_t *k_pages;    // [num_pages, Hkv, 256, 128]
+    const uint16_t *v_pages;
     uint16_t *out;
     const int32_t *block_table;
     const int32_t *seq_lens;
@@ -59,11 +61,9 @@ struct SplitParams {
     int32_t evict_first;
 };
 
-cudaError_t launch_split_attn(const SplitParams &p, const CUtensorMap &tmap_k,
-                              const CUtensorMap &tmap_v, int num_ctas, int warps_per_cta,
-                              cudaStream_t stream);
+cudaError_t launch_split_attn(const SplitParams &p, int num_ctas, cudaStream_t stream);
 cudaError_t split_occupancy(int R, int warps_per_cta, int *ctas_per_sm);
-int split_tile_tokens();  // tokens per K/V tile of the split kernel (TMA box rows)
+int split_tile_tokens();  // tokens per K/V tile of the split kernel
 
 cudaError_t launch_kv_append(const sa_dims &d, const uint16_t *k_new, const uint16_t *v_new,
                              uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,

@@ -127,7 +127,20 @@ PlanHost build_plan(const sa_dims &d, const int32_t *bt, const int32_t *seq_lens
     int64_t base_items = 0;
     for (auto &r : runs)
         if (r.taken) base_items += static_cast<int64_t>(d.num_kv_heads) * ((r.rows + kPrefixTileRows - 1) / kPrefixTileRows);
-    const int64_t chunks_wanted = std::max<int64_t>(1, (std::max(sms, 1) + base_items - 1) / base_items);
+    // a member's runs together use at most 8 partial slots (the merge takes 16
+    // per row, 8 of which belong to the split kernel's pieces)
+    int max_runs_per_seq = 1;
+    for (int b = 0; b < B; ++b) {
+        int k = 0;
+        for (int r : runs_of[b]) {
+            if (!runs[r].taken) break;
+            ++k;
+        }
+        max_runs_per_seq = std::max(max_runs_per_seq, k);
+    }
+    const int64_t chunk_cap = std::max(1, 8 / max_runs_per_seq);
+    const int64_t chunks_wanted = std::min<int64_t>(
+        chunk_cap, std::max<int64_t>(1, (std::max(sms, 1) + base_items - 1) / base_items));
 
     std::vector<int> run_index(runs.size(), -1), run_chunk_pages(runs.size(), 0), run_chunks(runs.size(), 0);
     std::vector<int> slot_base_of;  // filled per (run, member) below
