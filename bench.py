@@ -252,6 +252,9 @@ def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    # a stream of our own (not the legacy default stream), on which the
+    # combine pass can start as a programmatic dependent of the split kernel
+    torch.cuda.set_stream(torch.cuda.Stream(device=torch.device("cuda", local)))
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))

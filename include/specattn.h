@@ -21,10 +21,11 @@
  *     caller clears the flag and reads it when it chooses. err_flag may be
  *     NULL, in which case such errors are dropped silently.
  *   - Workspaces are caller-owned device buffers of at least the size the
- *     matching *_workspace_size call returns, 256-byte aligned, ZERO-FILLED
- *     BEFORE THEIR FIRST USE. Every call leaves the workspace's counters at
- *     zero again, so a workspace can be reused call after call on one stream;
- *     two calls in flight at once need two workspaces.
+ *     matching *_workspace_size call returns, 256-byte aligned. The
+ *     sa_paged_attn workspace needs no initialisation; the sa_spec_verify_greedy
+ *     workspace must be ZERO-FILLED BEFORE ITS FIRST USE, and every call leaves
+ *     its counters at zero again. A workspace can be reused call after call on
+ *     one stream; two calls in flight at once need two workspaces.
  */
 #ifndef SPECATTN_H
 #define SPECATTN_H
@@ -184,9 +185,9 @@ SA_API int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan);
  *     above 16 MiB are rejected with SA_ERR_WORKSPACE before any GPU work.
  *   - The first call on a device looks up the array's device address with that
  *     device current; make that first call before any stream capture.
- *   - Every call clears the array's counters on `stream`, then reuses the same
- *     array: two calls that overlap on the GPU (different streams, or
- *     different host threads on one device) race and give wrong results.
+ *   - Every call reuses the same array (partial accumulators, no counters):
+ *     two calls that overlap on the GPU (different streams, or different host
+ *     threads on one device) race and give wrong results.
  *   - No cudaMalloc, cudaFree or other allocating routine is called.
  */
 SA_API int sa_paged_attn_noalloc(const sa_dims *dims, const uint16_t *q, const uint16_t *k_pages,

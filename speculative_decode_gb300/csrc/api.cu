@@ -91,20 +91,20 @@ SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     return c;
 }
 
-// Partials one output row may have to merge (the split kernel merges at most
+// Partials one output row may have to merge (the combine pass merges at most
 // kMaxMergeSlotsHost of them).
 constexpr int kMaxMergeSlotsHost = 16;
 bool merge_fits(const SplitConfig &c) { return c.n_slots <= kMaxMergeSlotsHost;
 }
 
 // Workspace layout: fp32 accumulators [n_slots][total_q * Hq][128], then
-// (max, sum) pairs [n_slots][total_q * Hq][2], then int32 counters (unit
-// claims, finished warps, per (sequence, KV head, row block) finished splits).
+// (max, sum) pairs [n_slots][total_q * Hq][2]. Every slot a call reads was
+// written earlier in the same call, so the workspace needs no initialisation.
 // It is sized for the finest split any device could choose, so sizing needs
 // no device.
 struct WsLayout {
     int64_t slots_cap;
-    size_t ml_offset, ctr_offset, total;
+    size_t ml_offset, total;
 };
 
 WsLayout attn_ws_layout(const sa_dims &d, const sa_plan *plan) {
@@ -114,10 +114,8 @@ WsLayout attn_ws_layout(const sa_dims &d, const sa_plan *plan) {
     const int64_t rows = static_cast<int64_t>(d.total_q) * d.num_q_heads;
     const size_t acc = static_cast<size_t>(w.slots_cap * rows * kHeadDim * 4);
     const size_t ml = static_cast<size_t>(w.slots_cap * rows * 2 * 4);
-    const size_t ctr = static_cast<size_t>(d.num_seqs) * d.num_kv_heads * c.nrb * 4;
     w.ml_offset = (acc + 255) / 256 * 256;
-    w.ctr_offset = w.ml_offset + (ml + 255) / 256 * 256;
-    w.total = w.ctr_offset + (ctr + 255) / 256 * 256;
+    w.total = w.ml_offset + (ml + 255) / 256 * 256;
     return w;
 }
 
@@ -228,6 +226,10 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
 
     const SplitConfig c = split_config(d, plan);
     if (!merge_fits(c)) return SA_ERR_UNSUPPORTED;  // too many partials per row to merge
+    // the split kernel counts work in 16-token tiles with 32-bit offsets
+    const int64_t max_work = static_cast<int64_t>(d.num_seqs) * d.max_pages_per_seq *
+                             (kPageSize / split_tile_tokens()) * d.num_kv_heads * c.nrb;
+    if (max_work > INT32_MAX) return SA_ERR_UNSUPPORTED;
     const int64_t rows_total = static_cast<int64_t>(d.total_q) * d.num_q_heads;
     float *ws_acc = static_cast<float *>(workspace);
     float *ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.ml_offset);
@@ -235,7 +237,7 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     const uint64_t pool_rows = static_cast<uint64_t>(d.num_pages) * d.num_kv_heads * kPageSize;
     const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
     if ((pd && pd->num_tiles > 0) || c.tc.min_rows > 0) {
-        // tensor-core work first: the split kernel's merges read its partials
+        // tensor-core work first: the combine pass reads its partials
         CUtensorMap pk, pv;
         if (encode_tensor_map_2d(&pk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(k_pages),
                                  kHeadDim, pool_rows, kHeadDim * 2, 64, prefix_tile_rows(),
@@ -266,7 +268,6 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     p.run_slots = pd ? pd->run_slots : nullptr;
     p.ws_acc = ws_acc;
     p.ws_ml = ws_ml;
-    p.merge_ctr = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + wl.ctr_offset);
     p.err = err_flag;
     p.B = d.num_seqs;
     p.Hq = d.num_q_heads;
@@ -288,8 +289,8 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
 
     int per_sm = 0;
     if (split_occupancy(c.R, 1, &per_sm) != cudaSuccess || per_sm <= 0) return SA_ERR_CUDA;
-    const int64_t ctas = static_cast<int64_t>(sms) * per_sm;  // one warp per CTA, all resident
-    if (launch_split_attn(p, static_cast<int>(ctas), s) != cudaSuccess)
+    p.split_ctas = sms * per_sm;  // one warp per CTA, all resident
+    if (launch_split_attn(p, s) != cudaSuccess)
         return SA_ERR_CUDA;
     return finish(s, err_flag);
 }
@@ -300,7 +301,7 @@ int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan) {
     if (sms <= 0) return -1;
     const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
     const SplitConfig c = split_config(*dims, plan);
-    return 1 + ((pd && pd->num_tiles > 0) ? 1 : 0) + (c.tc.min_rows > 0 ? 1 : 0);
+    return 2 + ((pd && pd->num_tiles > 0) ? 1 : 0) + (c.tc.min_rows > 0 ? 1 : 0);
 }
 
 size_t sa_spec_verify_workspace_size(int32_t num_seqs, int32_t k_max, int32_t vocab) {
@@ -363,8 +364,8 @@ int sa_spec_verify_greedy(const float *logits, const int32_t *candidates, const 
 // Some callers cannot allocate device memory at all: a plugin that runs inside
 // a serving process whose memory pool already owns every byte of the GPU, or a
 // decode loop that may not call cudaMalloc because it synchronises the whole
-// device. For them the split kernel's scratch (partial accumulators and merge
-// counters) lives in one fixed array in this file, reserved on every GPU that
+// device. For them the split kernel's scratch (partial accumulators and their
+// maxima and sums) lives in one fixed array in this file, reserved on every GPU that
 // loads the library until the process exits.
 // ---------------------------------------------------------------------------
 constexpr size_t kStaticScratchBytes = size_t{16} << 20;  // 16 MiB
@@ -406,12 +407,6 @@ int sa_paged_attn_noalloc(const sa_dims *dims, const uint16_t *q, const uint16_t
     void *ws = nullptr;
     rc = static_scratch_address(&ws);
     if (rc) return rc;
-    // merge counters must start at zero; calls leave them at zero, but clear
-    // them anyway so that an interrupted earlier call cannot leak into this one
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (wl.total > wl.ctr_offset &&
-        cudaMemsetAsync(static_cast<char *>(ws) + wl.ctr_offset, 0, wl.total - wl.ctr_offset, s) != cudaSuccess)
-        return SA_ERR_CUDA;
     return sa_paged_attn(dims, q, k_pages, v_pages, block_table, seq_lens, q_lens, scale, out,
                          nullptr, ws, kStaticScratchBytes, err_flag, stream);
 }

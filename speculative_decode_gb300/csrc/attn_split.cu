@@ -6,15 +6,14 @@
 // 0 .. seq_len - q_len + i, with K_b/V_b gathered through the block table
 // (ExLlamaV2 "Dynamic Generator" page, "Continuous batching"; causal rows as
 // in the Hugging Face "Assisted Generation" page, "How Assisted Generation
-// works"). The softmax is evaluated online over 32-token tiles; where a
+// works"). The softmax is evaluated online over 16-token tiles; where a
 // sequence's keys are cut into pieces, the partial (max, sum, accumulator)
-// states are merged exactly, in this kernel, by whichever warp finishes the
-// last piece.
+// states are merged exactly by a combine pass, a second kernel.
 //
 // Design (sm_103a):
 //  * Segment = (sequence, KV head, row block): the G query heads of the KV
 //    head times the sequence's new tokens (up to R rows), so every K/V byte
-//    read serves all of them. All segments' 32-token tiles form one sequence
+//    read serves all of them. All segments' 16-token tiles form one sequence
 //    of work that is cut into equal contiguous ranges, one per warp
 //    (stream-K): perfectly balanced whatever the context lengths, with at
 //    most two partial pieces per warp and no scheduling atomics.
@@ -28,9 +27,11 @@
 //    reduce-scatter, after which each lane holds one (token, row) score; P.V
 //    reuses the mapping with p broadcast from shared memory. Products use
 //    packed fp32x2 FMAs on exactly converted bf16 inputs.
-//  * A piece that is not a whole segment stores an fp32 partial and counts
-//    itself with a release atomic whose result is examined one piece later,
-//    so the round trip is hidden; the last piece merges.
+//  * A piece that is not a whole segment stores an fp32 partial; nothing in
+//    the split kernel waits on another warp. The combine kernel, launched as
+//    a programmatic dependent, repeats the (cheap) work scan while the split
+//    kernel runs, waits for the grid, and merges each cut segment's partials
+//    (and the tensor-core kernels' partials) in one or two memory round trips.
 //  * Every wait on a barrier is bounded (common.cuh); on timeout the warp
 //    flags SA_ERR_TIMEOUT, drains its copies in flight and leaves.
 #include "common.cuh"
@@ -90,7 +91,16 @@ struct SeqInfo {
     int T, n, skip_tok, tiles, nrb, runs;
 };
 
+#ifndef SA_SPLIT_SCALAR_FMA
+#define SA_SPLIT_SCALAR_FMA 0
+#endif
+#ifndef SA_SPLIT_QK_BATCH
+#define SA_SPLIT_QK_BATCH 32
+#endif
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+#if SA_SPLIT_SCALAR_FMA
+    return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y));
+#endif
     unsigned long long ra = *reinterpret_cast<unsigned long long *>(&a);
     unsigned long long rb = *reinterpret_cast<unsigned long long *>(&b);
     unsigned long long rc = *reinterpret_cast<unsigned long long *>(&c);
@@ -135,24 +145,39 @@ __device__ __forceinline__ int64_t out_row(const SplitParams &P, const Piece &U,
     return static_cast<int64_t>(U.qstart + rr / P.G) * P.Hq + U.kvh * P.G + rr % P.G;
 }
 
-// Per-sequence shape of the work; tiles = 0 when the sequence has none.
+// Per-sequence shape of the work; tiles = 0 when the sequence has none. The
+// packed query rows of all sequences are checked against total_q once, by the
+// caller of this function, so no per-sequence query offset is needed here.
+constexpr int kScanBatch = 4;  // sequences per lane handled with all loads in flight
+
 template <int R>
-__device__ __forceinline__ SeqInfo seq_info(const SplitParams &P, int b, int qstart, bool flag) {
+__device__ __forceinline__ SeqInfo seq_info_from(const SplitParams &P, int T, int n, int skip_pages,
+                                                 int run_slots, bool flag);
+
+template <int R>
+__device__ __forceinline__ SeqInfo seq_info(const SplitParams &P, int b, bool flag) {
+    return seq_info_from<R>(P, P.seq_lens[b], P.q_lens[b], P.skip_pages ? P.skip_pages[b] : 0,
+                            P.run_slots ? P.run_slots[b] : 0, flag);
+}
+
+template <int R>
+__device__ __forceinline__ SeqInfo seq_info_from(const SplitParams &P, int T, int n, int skip_pages,
+                                                 int run_slots, bool flag) {
     SeqInfo s;
-    s.T = P.seq_lens[b];
-    s.n = P.q_lens[b];
+    s.T = T;
+    s.n = n;
     s.tiles = 0;
     s.nrb = 0;
     s.skip_tok = 0;
     s.runs = 0;
     if (s.n <= 0) return s;
     const int npages = (s.T + kPageSize - 1) / kPageSize;
-    if (s.n > s.T || s.n > P.max_q_len || qstart + s.n > P.total_q || npages > P.max_pages) {
+    if (s.n > s.T || s.n > P.max_q_len || npages > P.max_pages) {
         if (flag) flag_error(P.err, kErrBitQlen);
         return s;
     }
-    int skip = P.skip_pages ? P.skip_pages[b] : 0;
-    int runs = P.run_slots ? P.run_slots[b] : 0;
+    int skip = skip_pages;
+    int runs = run_slots;
     if (P.tc_min_rows > 0 && P.G * s.n >= P.tc_min_rows) {  // attended on the tensor cores
         skip = npages;
         runs = (npages + P.tc_chunk_pages - 1) / P.tc_chunk_pages;
@@ -160,19 +185,37 @@ __device__ __forceinline__ SeqInfo seq_info(const SplitParams &P, int b, int qst
     s.runs = runs;
     s.skip_tok = skip * kPageSize;
     const int keys = s.T - s.skip_tok;
-    s.tiles = keys > 0 ? (keys + kTile - 1) / kTile : (runs > 0 ? 1 : 0);  // one empty tile carries the merge
+    s.tiles = keys > 0 ? (keys + kTile - 1) / kTile : 0;  // tensor-core partials only: merged by the combine pass
     s.nrb = (P.G * s.n + R - 1) / R;
     return s;
 }
 
-__device__ __forceinline__ int64_t seq_work(const SplitParams &P, const SeqInfo &s) {
-    return static_cast<int64_t>(s.tiles) * P.Hkv * s.nrb;
+// The cut of the tile sequence [0, total) into one contiguous range per warp:
+// every warp gets C or C + 1 tiles (the first `rem` get C + 1) when that keeps
+// C >= C_min; otherwise ranges of C_min tiles and the last warps stay idle.
+// Work offsets are counted in tiles in 32 bits: the host rejects shapes whose
+// largest possible total reaches 2^31.
+struct Ranges {
+    int C, rem;
+    __device__ __forceinline__ int begin(int w) const { return w * C + min(w, rem); }
+    __device__ __forceinline__ int range_of(int t) const {
+        const int big = rem * (C + 1);
+        return t < big ? t / (C + 1) : rem + (t - big) / C;
+    }
+};
+
+__device__ __forceinline__ Ranges make_ranges(int total, int W, int C_min) {
+    const int even = total / W;
+    if (even >= C_min) return Ranges{even, total - even * W};
+    return Ranges{C_min, 0};
 }
 
-// Merge every partial of the piece's rows: the tensor-core runs' slots and the
-// pieces' slots, with exact max-shifted rescaling. Eight lanes per row (16
-// head dims each), four rows at a time, every load of a row's slots in flight
-// together so the merge costs about two memory round trips per four rows.
+__device__ __forceinline__ int seq_work(const SplitParams &P, const SeqInfo &s) {
+    return s.tiles * P.Hkv * s.nrb;
+}
+
+// Merging a row's partials (the tensor-core runs' slots, then the pieces'
+// slots) with exact max-shifted rescaling.
 constexpr int kMaxMergeSlots = 16;
 
 __device__ __forceinline__ const float *ws_slot_row(const SplitParams &P, const Piece &U, int k, int64_t row,
@@ -181,37 +224,71 @@ __device__ __forceinline__ const float *ws_slot_row(const SplitParams &P, const 
     return base + (static_cast<int64_t>(slot) * P.n_rows_total + row) * width;
 }
 
-__device__ void merge_rows(const SplitParams &P, const Piece &U, int R, int lane) {
+// 16 head dims (sub*16 ..) of an output row: o / Lsum rounded to bf16.
+__device__ __forceinline__ void store_row(const SplitParams &P, int64_t row, int sub, const float4 (&o)[4], float Lsum) {
+    const float inv = Lsum > 0.f ? __frcp_rn(Lsum) : 0.f;
+    uint4 *dst = reinterpret_cast<uint4 *>(P.out + row * kHeadDim + sub * 16);
+    dst[0] = make_uint4(pack_bf16x2(o[0].x * inv, o[0].y * inv), pack_bf16x2(o[0].z * inv, o[0].w * inv),
+                        pack_bf16x2(o[1].x * inv, o[1].y * inv), pack_bf16x2(o[1].z * inv, o[1].w * inv));
+    dst[1] = make_uint4(pack_bf16x2(o[2].x * inv, o[2].y * inv), pack_bf16x2(o[2].z * inv, o[2].w * inv),
+                        pack_bf16x2(o[3].x * inv, o[3].y * inv), pack_bf16x2(o[3].z * inv, o[3].w * inv));
+}
+
+// Rows r4*4 .. r4*4+3 of a segment: eight lanes per row, 16 head dims each.
+// Up to four partials are read in one round trip (every (max, sum) and
+// accumulator in flight together); more take two (the maxima, then the
+// accumulators).
+__device__ void merge_rows(const SplitParams &P, const Piece &U, int R, int r4, int lane) {
     const int nslots = U.runs + U.pieces;
     const int sub = lane & 7;
-    for (int r0 = 0; r0 < U.nvr; r0 += 4) {
-        const int r = r0 + (lane >> 3);
-        if (r >= U.nvr) continue;
-        const int64_t row = out_row(P, U, U.rb * R + r);
-        float ms[kMaxMergeSlots], ls[kMaxMergeSlots];
-        float M = -INFINITY;
+    const int r = r4 * 4 + (lane >> 3);
+    if (r >= U.nvr) return;
+    const int64_t row = out_row(P, U, U.rb * R + r);
+    float M = -INFINITY, Lsum = 0.f;
+    float4 o[4];
 #pragma unroll
-        for (int k = 0; k < kMaxMergeSlots; ++k) {
-            ms[k] = -INFINITY;
-            ls[k] = 0.f;
+    for (int q = 0; q < 4; ++q) o[q] = make_float4(0, 0, 0, 0);
+    if (nslots <= 4) {
+        float2 ml[4];
+        float4 av[4][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            ml[k] = make_float2(-INFINITY, 0.f);
             if (k < nslots) {
-                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(ws_slot_row(P, U, k, row, P.ws_ml, 2)));
-                ms[k] = ml.x;
-                ls[k] = ml.y;
+                ml[k] = __ldcg(reinterpret_cast<const float2 *>(ws_slot_row(P, U, k, row, P.ws_ml, 2)));
+                const float4 *a = reinterpret_cast<const float4 *>(ws_slot_row(P, U, k, row, P.ws_acc, kHeadDim) + sub * 16);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) av[k][q] = __ldcg(a + q);
             }
         }
 #pragma unroll
-        for (int k = 0; k < kMaxMergeSlots; ++k)
-            if (ls[k] > 0.f) M = fmaxf(M, ms[k]);
-        float Lsum = 0.f;
-        float4 o[4];
+        for (int k = 0; k < 4; ++k)
+            if (ml[k].y > 0.f) M = fmaxf(M, ml[k].x);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) o[q] = make_float4(0, 0, 0, 0);
+        for (int k = 0; k < 4; ++k) {
+            if (ml[k].y > 0.f) {
+                const float w = exp2f(ml[k].x - M);
+                Lsum += ml[k].y * w;
 #pragma unroll
-        for (int k = 0; k < kMaxMergeSlots; ++k) {
-            if (ls[k] > 0.f) {
-                const float w = exp2f(ms[k] - M);
-                Lsum += ls[k] * w;
+                for (int q = 0; q < 4; ++q) {
+                    o[q].x += av[k][q].x * w;
+                    o[q].y += av[k][q].y * w;
+                    o[q].z += av[k][q].z * w;
+                    o[q].w += av[k][q].w * w;
+                }
+            }
+        }
+    } else {
+        // the maxima first (all loads in flight), then the accumulators
+        for (int k = 0; k < nslots; ++k) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(ws_slot_row(P, U, k, row, P.ws_ml, 2)));
+            if (ml.y > 0.f) M = fmaxf(M, ml.x);
+        }
+        for (int k = 0; k < nslots; ++k) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(ws_slot_row(P, U, k, row, P.ws_ml, 2)));
+            if (ml.y > 0.f) {
+                const float w = exp2f(ml.x - M);
+                Lsum += ml.y * w;
                 const float4 *a = reinterpret_cast<const float4 *>(ws_slot_row(P, U, k, row, P.ws_acc, kHeadDim) + sub * 16);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -223,38 +300,134 @@ __device__ void merge_rows(const SplitParams &P, const Piece &U, int R, int lane
                 }
             }
         }
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-        uint32_t wv[8];
+    }
+    store_row(P, row, sub, o, Lsum);
+}
+
+// ---- the work scan shared by the split and combine kernels
+// Lanes take contiguous chunks of sequences; with at most kScanBatch per lane
+// every length is loaded in one round and kept in registers.
+struct WorkScan {
+    int c_lo, c_hi;
+    bool fast;
+    int Ts[kScanBatch], ns[kScanBatch], sk[kScanBatch], rs[kScanBatch];
+    int cw, w_pre, total;      // this lane's work, work before its chunk, all work (tiles)
+    int cq, q_pre, q_total;    // the same for query tokens
+    int max_tiles;             // longest segment, in tiles
+};
+
+template <int R>
+__device__ __forceinline__ void scan_work(const SplitParams &P, int lane, bool flag, WorkScan &sc) {
+    const int per = (P.B + 31) / 32;
+    sc.c_lo = min(P.B, lane * per);
+    sc.c_hi = min(P.B, sc.c_lo + per);
+    sc.fast = per <= kScanBatch;
+    sc.cq = 0;
+    sc.cw = 0;
+    int max_tiles = 0;
+    if (sc.fast) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            wv[2 * q] = f32_to_bf16_rne(o[q].x * inv) | (static_cast<uint32_t>(f32_to_bf16_rne(o[q].y * inv)) << 16);
-            wv[2 * q + 1] = f32_to_bf16_rne(o[q].z * inv) | (static_cast<uint32_t>(f32_to_bf16_rne(o[q].w * inv)) << 16);
+        for (int k = 0; k < kScanBatch; ++k) {
+            const int b = sc.c_lo + k;
+            const bool in = b < sc.c_hi;
+            sc.Ts[k] = in ? P.seq_lens[b] : 0;
+            sc.ns[k] = in ? P.q_lens[b] : 0;
+            sc.sk[k] = in && P.skip_pages ? P.skip_pages[b] : 0;
+            sc.rs[k] = in && P.run_slots ? P.run_slots[b] : 0;
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(P.out + row * kHeadDim + sub * 16);
-        dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+#pragma unroll
+        for (int k = 0; k < kScanBatch; ++k) {
+            if (sc.c_lo + k < sc.c_hi) {
+                const SeqInfo si = seq_info_from<R>(P, sc.Ts[k], sc.ns[k], sc.sk[k], sc.rs[k], flag);
+                sc.cw += seq_work(P, si);
+                max_tiles = max(max_tiles, si.tiles);
+                sc.cq += max(0, si.n);
+            }
+        }
+    } else {
+        for (int b = sc.c_lo; b < sc.c_hi; ++b) {
+            const SeqInfo si = seq_info<R>(P, b, flag);
+            sc.cw += seq_work(P, si);
+            max_tiles = max(max_tiles, si.tiles);
+            sc.cq += max(0, si.n);
+        }
+    }
+    int q_pre = sc.cq;
+    int w_pre = sc.cw;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, q_pre, o);
+        const int wv = __shfl_up_sync(0xffffffffu, w_pre, o);
+        if (lane >= o) {
+            q_pre += v;
+            w_pre += wv;
+        }
+        max_tiles = max(max_tiles, __shfl_xor_sync(0xffffffffu, max_tiles, o));
+    }
+    sc.q_total = __shfl_sync(0xffffffffu, q_pre, 31);
+    sc.total = __shfl_sync(0xffffffffu, w_pre, 31);
+    sc.q_pre = q_pre - sc.cq;  // exclusive
+    sc.w_pre = w_pre - sc.cw;
+    sc.max_tiles = max_tiles;
+}
+
+// The cut of the work into W warp ranges. A segment of s tiles spans at most
+// ceil(s / C) + 1 ranges: C is at least ceil(longest / (slots - 1)) so that no
+// segment has more pieces than the workspace has partial slots.
+__device__ __forceinline__ Ranges split_ranges(const SplitParams &P, const WorkScan &sc, int W) {
+    const int mt = sc.max_tiles;
+    const int C_min = P.piece_slots > 1 ? (mt + P.piece_slots - 2) / (P.piece_slots - 1) : mt;
+    return make_ranges(sc.total, W, max(C_min, 1));
+}
+
+// Walk this lane's chunk of sequences to the one whose work holds tile g
+// (by_work) or to sequence bt: its index, work offset, query offset and shape.
+template <int R>
+__device__ __forceinline__ void walk_chunk(const SplitParams &P, const WorkScan &sc, bool by_work, int g,
+                                           int bt, int &b_out, int &pos, int &qs, SeqInfo &si_out) {
+    pos = sc.w_pre;
+    qs = sc.q_pre;
+    b_out = sc.c_lo;
+    if (sc.fast) {
+        bool found = false;
+#pragma unroll
+        for (int k = 0; k < kScanBatch; ++k) {
+            if (!found && sc.c_lo + k < sc.c_hi) {
+                const SeqInfo si = seq_info_from<R>(P, sc.Ts[k], sc.ns[k], sc.sk[k], sc.rs[k], false);
+                const int wb = seq_work(P, si);
+                if (by_work ? g < pos + wb : sc.c_lo + k == bt) {
+                    found = true;
+                    b_out = sc.c_lo + k;
+                    si_out = si;
+                } else {
+                    pos += wb;
+                    qs += max(0, si.n);
+                }
+            }
+        }
+    } else {
+        for (int b = sc.c_lo; b < sc.c_hi; ++b) {
+            const SeqInfo si = seq_info<R>(P, b, false);
+            const int wb = seq_work(P, si);
+            if (by_work ? g < pos + wb : b == bt) {
+                b_out = b;
+                si_out = si;
+                return;
+            }
+            pos += wb;
+            qs += max(0, si.n);
+        }
     }
 }
 
-__device__ __forceinline__ int32_t *merge_counter(const SplitParams &P, const Piece &U) {
-    return P.merge_ctr + (static_cast<int64_t>(U.b) * P.Hkv + U.kvh) * P.n_row_blocks + U.rb;
-}
-
-// A counted piece whose atomic result is examined later.
-struct Pending {
-    Piece U;
-    int old;
-    bool live;
-};
-
-__device__ void resolve(const SplitParams &P, Pending &pd, int R, int lane) {
-    if (!pd.live) return;
-    pd.live = false;
-    const int old = __shfl_sync(0xffffffffu, pd.old, 0);
-    if (old != pd.U.pieces - 1) return;
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");  // acquire: every other piece's partial is visible
-    merge_rows(P, pd.U, R, lane);
-    if (lane == 0) atomicExch(merge_counter(P, pd.U), 0);
+__device__ __forceinline__ SeqInfo shfl_seq_info(SeqInfo si, int src) {
+    si.T = __shfl_sync(0xffffffffu, si.T, src);
+    si.n = __shfl_sync(0xffffffffu, si.n, src);
+    si.skip_tok = __shfl_sync(0xffffffffu, si.skip_tok, src);
+    si.tiles = __shfl_sync(0xffffffffu, si.tiles, src);
+    si.nrb = __shfl_sync(0xffffffffu, si.nrb, src);
+    si.runs = __shfl_sync(0xffffffffu, si.runs, src);
+    return si;
 }
 
 template <int R>
@@ -285,75 +458,47 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         fence_barrier_init();
     }
 
+    // the combine kernel may be scheduled now: it waits for this grid's
+    // partials before reading them
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // ---- 1. total work and this warp's range [g_begin, g_end) of tiles
-    // lanes take contiguous chunks of sequences; two passes: query offsets, then work
-    const int per = (P.B + 31) / 32;
-    const int c_lo = min(P.B, lane * per), c_hi = min(P.B, c_lo + per);
-    int cq = 0;
-    for (int b = c_lo; b < c_hi; ++b) cq += max(0, P.q_lens[b]);
-    int q_pre = cq;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, q_pre, o);
-        if (lane >= o) q_pre += v;
+    WorkScan sc;
+    scan_work<R>(P, lane, true, sc);
+    if (sc.q_total > P.total_q) {  // q_lens disagree with dims.total_q: reject the whole call
+        if (lane == 0) flag_error(P.err, kErrBitQlen);
+        return;
     }
-    q_pre -= cq;  // exclusive
-    int64_t cw = 0;
-    int max_tiles = 0;  // longest segment, in tiles
-    {
-        int qs = q_pre;
-        for (int b = c_lo; b < c_hi; ++b) {
-            const SeqInfo si = seq_info<R>(P, b, qs, true);
-            cw += seq_work(P, si);
-            max_tiles = max(max_tiles, si.tiles);
-            qs += max(0, si.n);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) max_tiles = max(max_tiles, __shfl_xor_sync(0xffffffffu, max_tiles, o));
-    int64_t w_pre = cw;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int64_t v = __shfl_up_sync(0xffffffffu, w_pre, o);
-        if (lane >= o) w_pre += v;
-    }
-    const int64_t total = __shfl_sync(0xffffffffu, w_pre, 31);
-    w_pre -= cw;
-    const int64_t W = gridDim.x;
-    // a segment of s tiles spans at most ceil(s / C) + 1 ranges: C is at least
-    // ceil(longest / (slots - 1)) so that no segment has more pieces than the
-    // workspace has partial slots
-    const int64_t C_min = P.piece_slots > 1 ? (max_tiles + P.piece_slots - 2) / (P.piece_slots - 1) : max_tiles;
-    const int64_t C = max((total + W - 1) / W, max(C_min, int64_t{1}));
-    const int64_t g_begin = static_cast<int64_t>(blockIdx.x) * C;
-    const int64_t g_end = min(total, g_begin + C);
+    const Ranges rg = split_ranges(P, sc, gridDim.x);
+    const int g_begin = rg.begin(blockIdx.x);
+    const int g_end = min(sc.total, rg.begin(blockIdx.x + 1));
     __syncwarp();
     if (g_begin >= g_end) return;
 
-    // ---- 2. locate the first tile: sequence, segment, tile within segment
+    // ---- 2. locate the first tile (the lane whose sequences hold g_begin walks
+    // them from registers) and read its page id at once
     int b0 = 0, q0 = 0;
-    int64_t ws0 = 0;
+    int ws0 = 0;
+    SeqInfo si0{};
+    int pid0 = -1, pid1 = -1, j0 = 0;
     {
-        const bool mine = cw > 0 && w_pre <= g_begin && g_begin < w_pre + cw;
+        const bool mine = sc.cw > 0 && sc.w_pre <= g_begin && g_begin < sc.w_pre + sc.cw;
         const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
         if (lane == src) {
-            int64_t pos = w_pre;
-            int qs = q_pre;
-            int b = c_lo;
-            for (; b < c_hi; ++b) {
-                const SeqInfo si = seq_info<R>(P, b, qs, false);
-                const int64_t wb = seq_work(P, si);
-                if (g_begin < pos + wb) break;
-                pos += wb;
-                qs += max(0, si.n);
-            }
-            b0 = b;
-            q0 = qs;
-            ws0 = pos;
+            walk_chunk<R>(P, sc, true, g_begin, 0, b0, ws0, q0, si0);
+            const int t0 = si0.skip_tok + static_cast<int>((g_begin - ws0) % si0.tiles) * kTile;
+            j0 = t0 / kPageSize;
+            const int npg = (si0.T + kPageSize - 1) / kPageSize;
+            if (t0 < si0.T) pid0 = P.block_table[static_cast<int64_t>(b0) * P.max_pages + j0];
+            if (j0 + 1 < npg) pid1 = P.block_table[static_cast<int64_t>(b0) * P.max_pages + j0 + 1];
         }
         b0 = __shfl_sync(0xffffffffu, b0, src);
         q0 = __shfl_sync(0xffffffffu, q0, src);
         ws0 = __shfl_sync(0xffffffffu, ws0, src);
+        si0 = shfl_seq_info(si0, src);
+        pid0 = __shfl_sync(0xffffffffu, pid0, src);
+        pid1 = __shfl_sync(0xffffffffu, pid1, src);
+        j0 = __shfl_sync(0xffffffffu, j0, src);
     }
 
     // row of the reduce-scatter result this lane ends up holding
@@ -373,25 +518,42 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
 
     // ---- issue cursor: walks tiles g_begin .. g_end-1 ahead of the consumer
     int ib = b0, iq = q0;
-    int64_t iws = ws0;
-    SeqInfo isi = seq_info<R>(P, ib, iq, false);
-    int64_t ig = g_begin;
+    int iws = ws0;
+    SeqInfo isi = si0;
+    int ig = g_begin;
     int iseg, itile, ikvh, irb;
     {
-        const int64_t off = g_begin - iws;
+        const int off = g_begin - iws;
         iseg = static_cast<int>(off / isi.tiles);
         itile = static_cast<int>(off % isi.tiles);
         ikvh = iseg / isi.nrb;
         irb = iseg % isi.nrb;
     }
     uint32_t issued = 0, consumed = 0, pieces_pushed = 0;
-    // physical page of the issue cursor's current logical page, and the next
-    // page's id loaded one page ahead so the block-table read never stalls a tile
-    int pg_b = -1, pg_j = -1, pg_id = -1, pg_next = -1;
+    // Page ids and lengths the issue cursor needs, each read well before its
+    // first use so that no block-table or length load stalls the issue of a
+    // tile: the current page's id and the next page's; the current sequence's
+    // first page (every KV head's segment starts there); the next sequence's
+    // lengths and, without a plan, its first page.
+    int pg_b = b0, pg_j = j0, pg_id = pid0, pg_next = pid1;  // primed by the locating lane
+    int f_b = b0, f_j = si0.skip_tok / kPageSize;
+    int f_pid = j0 == f_j ? pid0 : P.block_table[static_cast<int64_t>(b0) * P.max_pages + f_j];
+    const bool plain = P.skip_pages == nullptr && P.run_slots == nullptr;  // sequences start at page 0
+    int nx_b = -1, nx_T = 0, nx_n = 0, nx_sk = 0, nx_rs = 0, nx_pid = -1;
+    auto prefetch_next = [&](int b) {
+        nx_b = b + 1 < P.B ? b + 1 : -1;
+        if (nx_b < 0) return;
+        nx_T = P.seq_lens[nx_b];
+        nx_n = P.q_lens[nx_b];
+        nx_sk = P.skip_pages ? P.skip_pages[nx_b] : 0;
+        nx_rs = P.run_slots ? P.run_slots[nx_b] : 0;
+        nx_pid = plain ? P.block_table[static_cast<int64_t>(nx_b) * P.max_pages] : -1;
+    };
+    prefetch_next(b0);
     auto page_id = [&](int b, int jp, int npages) -> int {
         if (b == pg_b && jp == pg_j) return pg_id;
         const int64_t base = static_cast<int64_t>(b) * P.max_pages;
-        pg_id = (b == pg_b && jp == pg_j + 1) ? pg_next : P.block_table[base + jp];
+        pg_id = (b == pg_b && jp == pg_j + 1) ? pg_next : (b == f_b && jp == f_j) ? f_pid : P.block_table[base + jp];
         pg_b = b;
         pg_j = jp;
         pg_next = jp + 1 < npages ? P.block_table[base + jp + 1] : -1;
@@ -414,16 +576,20 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                     iws += seq_work(P, isi);
                     iq += max(0, isi.n);
                     if (++ib >= P.B) return false;  // unreachable while ig < g_end
-                    isi = seq_info<R>(P, ib, iq, false);
+                    isi = ib == nx_b ? seq_info_from<R>(P, nx_T, nx_n, nx_sk, nx_rs, false) : seq_info<R>(P, ib, false);
                 } while (seq_work(P, isi) == 0);
+                f_b = ib;
+                f_j = isi.skip_tok / kPageSize;
+                f_pid = (ib == nx_b && plain && f_j == 0) ? nx_pid : P.block_table[static_cast<int64_t>(ib) * P.max_pages + f_j];
+                prefetch_next(ib);
             }
         }
         const int kvh = ikvh, rb = irb;
         if (ig == g_begin || itile == 0) {
             // a new piece: describe it for the consumer and fetch its query rows
-            const int64_t seg0 = iws + static_cast<int64_t>(iseg) * isi.tiles;
-            const int64_t seg1 = seg0 + isi.tiles;
-            const int first = static_cast<int>(seg0 / C), last = static_cast<int>((seg1 - 1) / C);
+            const int seg0 = iws + iseg * isi.tiles;
+            const int seg1 = seg0 + isi.tiles;
+            const int first = rg.range_of(seg0), last = rg.range_of(seg1 - 1);
             const int nvr = min(R, P.G * isi.n - rb * R);
             const int qs = pieces_pushed % S;
             if (lane == 0) {
@@ -481,9 +647,6 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         for (uint32_t c = pieces_done; c < pieces_pushed; ++c) (void)mbar_wait(&qfull[c % S], (c / S) & 1);
     };
 
-    Pending pend;
-    pend.live = false;
-    pend.old = 0;
     top_up();
     while (consumed < issued) {
         Piece U;
@@ -534,7 +697,8 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                 // steps, then the reduce-scatter over L lanes level by level across
                 // the batch, so that independent shuffles overlap
                 float sv[NS];
-                constexpr int NB = (32 / R) < NS ? (32 / R) : NS;  // steps per batch
+                constexpr int NB0 = (SA_SPLIT_QK_BATCH / R) < NS ? (SA_SPLIT_QK_BATCH / R) : NS;
+                constexpr int NB = NB0 > 0 ? NB0 : 1;  // steps per batch
 #pragma unroll
                 for (int b0 = 0; b0 < NS; b0 += NB) {
                     float v[NB][R];
@@ -646,55 +810,125 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
             ++consumed;
         }
 
-        // ---- finish the piece: sum over token groups, then output or partial
+        // ---- finish the piece. The token groups' accumulators are summed in
+        // shared memory, in the stage of the piece's last tile (free until the
+        // next top-up), as [TG][R][128] fp32; then each lane owns 4R head dims
+        // of one row and writes them out (bf16) or as a partial (fp32).
 #pragma unroll
-        for (int o = L; o < 32; o <<= 1) {
-            lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int k = 0; k < NW; ++k) {
-                    acc[r][k].x += __shfl_xor_sync(0xffffffffu, acc[r][k].x, o);
-                    acc[r][k].y += __shfl_xor_sync(0xffffffffu, acc[r][k].y, o);
-                }
-        }
+        for (int o = L; o < 32; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
         if (tg == 0 && row_writer) {
             rowx[rj] = m;
             rowx[R + rj] = lsum;
         }
+        float *red = reinterpret_cast<float *>(smem + ((consumed - 1) % S) * kStageBytes);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int k = 0; k < NW; k += 2)
+                *reinterpret_cast<float4 *>(red + (tg * R + r) * kHeadDim + lane_dim_of_word<L>(j, k)) =
+                    make_float4(acc[r][k].x, acc[r][k].y, acc[r][k + 1].x, acc[r][k + 1].y);
         __syncwarp();
-        if (tg == 0) {
+        {
+            constexpr int DPL = 4 * R;              // head dims per lane
+            constexpr int LPR = kHeadDim / DPL;     // lanes per row
+            const int r = lane / LPR, d0 = (lane % LPR) * DPL;
+            if (r < U.nvr) {
+                float4 o[DPL / 4];
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                if (r < U.nvr) {
-                    const int64_t row = out_row(P, U, U.rb * R + r);
-                    if (direct) {
-                        const float inv = 1.f / rowx[R + r];
+                for (int v = 0; v < DPL / 4; ++v) {
+                    o[v] = *reinterpret_cast<const float4 *>(red + r * kHeadDim + d0 + 4 * v);
 #pragma unroll
-                        for (int k = 0; k < NW; ++k) {
-                            const uint32_t w = f32_to_bf16_rne(acc[r][k].x * inv) |
-                                               (static_cast<uint32_t>(f32_to_bf16_rne(acc[r][k].y * inv)) << 16);
-                            *reinterpret_cast<uint32_t *>(P.out + row * kHeadDim + lane_dim_of_word<L>(j, k)) = w;
-                        }
-                    } else {
-                        const int64_t wi = static_cast<int64_t>(P.slot_base + U.piece) * P.n_rows_total + row;
-#pragma unroll
-                        for (int k = 0; k < NW; ++k)
-                            *reinterpret_cast<float2 *>(P.ws_acc + wi * kHeadDim + lane_dim_of_word<L>(j, k)) = acc[r][k];
-                        if (j == 0) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(rowx[r], rowx[R + r]);
+                    for (int g = 1; g < TG; ++g) {
+                        const float4 a = *reinterpret_cast<const float4 *>(red + (g * R + r) * kHeadDim + d0 + 4 * v);
+                        o[v].x += a.x;
+                        o[v].y += a.y;
+                        o[v].z += a.z;
+                        o[v].w += a.w;
                     }
+                }
+                const int64_t row = out_row(P, U, U.rb * R + r);
+                if (direct) {
+                    const float inv = __frcp_rn(rowx[R + r]);
+                    uint4 *dst = reinterpret_cast<uint4 *>(P.out + row * kHeadDim + d0);
+#pragma unroll
+                    for (int v = 0; v < DPL / 8; ++v)
+                        dst[v] = make_uint4(pack_bf16x2(o[2 * v].x * inv, o[2 * v].y * inv),
+                                            pack_bf16x2(o[2 * v].z * inv, o[2 * v].w * inv),
+                                            pack_bf16x2(o[2 * v + 1].x * inv, o[2 * v + 1].y * inv),
+                                            pack_bf16x2(o[2 * v + 1].z * inv, o[2 * v + 1].w * inv));
+                } else {
+                    const int64_t wi = static_cast<int64_t>(P.slot_base + U.piece) * P.n_rows_total + row;
+                    float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + d0);
+#pragma unroll
+                    for (int v = 0; v < DPL / 4; ++v) dst[v] = o[v];
+                    if (d0 == 0) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(rowx[r], rowx[R + r]);
                 }
             }
         }
         __syncwarp();
-        resolve(P, pend, R, lane);  // the previous piece's count has long returned
-        if (!direct) {
-            pend.U = U;
-            pend.live = true;
-            if (lane == 0) pend.old = atomic_add_release(merge_counter(P, U), 1);
-        }
     }
-    resolve(P, pend, R, lane);
+}
+
+// ---- the combine pass: one warp per (sequence, KV head, row block, group of
+// four rows) merges the partials of a segment that was cut into pieces or
+// has tensor-core partials. It repeats the split kernel's scan (before the
+// grid dependency wait, so this overlaps the split kernel) to find the pieces.
+// One warp per CTA and at most 128 registers, so that a combine CTA fits beside
+// the eight resident split CTAs of an SM and can be scheduled early.
+#ifndef SA_COMBINE_WARPS
+#define SA_COMBINE_WARPS 1
+#endif
+#ifndef SA_COMBINE_MIN_CTAS
+#define SA_COMBINE_MIN_CTAS 16
+#endif
+constexpr int kCombineWarps = SA_COMBINE_WARPS;
+
+template <int R>
+__global__ void __launch_bounds__(kCombineWarps * 32, SA_COMBINE_MIN_CTAS) combine_kernel(const SplitParams P) {
+    const int lane = threadIdx.x & 31;
+    constexpr int RG = R / 4;
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * kCombineWarps + threadIdx.x / 32;
+    const int64_t per_seq = static_cast<int64_t>(P.Hkv) * P.n_row_blocks * RG;
+    const int bt = static_cast<int>(unit / per_seq);
+    if (bt >= P.B) return;
+    int rem = static_cast<int>(unit % per_seq);
+    const int kvh = rem / (P.n_row_blocks * RG);
+    rem %= P.n_row_blocks * RG;
+    const int rb = rem / RG, r4 = rem % RG;
+
+    WorkScan sc;
+    scan_work<R>(P, lane, false, sc);
+    if (sc.q_total > P.total_q) return;  // flagged by the split kernel
+    int b = 0, qs = 0;
+    int pos = 0;
+    SeqInfo si{};
+    {
+        const int src = __ffs(__ballot_sync(0xffffffffu, sc.c_lo <= bt && bt < sc.c_hi)) - 1;
+        if (lane == src) walk_chunk<R>(P, sc, false, 0, bt, b, pos, qs, si);
+        qs = __shfl_sync(0xffffffffu, qs, src);
+        pos = __shfl_sync(0xffffffffu, pos, src);
+        si = shfl_seq_info(si, src);
+    }
+    if (si.n <= 0 || rb >= si.nrb) return;
+    const int nvr = min(R, P.G * si.n - rb * R);
+    if (r4 * 4 >= nvr) return;
+    int pieces = 0;
+    if (si.tiles > 0) {
+        const Ranges rg = split_ranges(P, sc, P.split_ctas);
+        const int seg0 = pos + (kvh * si.nrb + rb) * si.tiles;
+        pieces = rg.range_of(seg0 + si.tiles - 1) - rg.range_of(seg0) + 1;
+    }
+    if (si.runs == 0 && pieces <= 1) return;  // written directly by the split kernel
+    Piece U{};
+    U.b = bt;
+    U.kvh = kvh;
+    U.rb = rb;
+    U.qstart = qs;
+    U.pieces = pieces;
+    U.runs = si.runs;
+    U.nvr = nvr;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the split kernel's partials are complete
+    merge_rows(P, U, R, r4, lane);
 }
 
 template <int R>
@@ -709,11 +943,26 @@ cudaError_t prepare() {
 }
 
 template <int R>
-cudaError_t launch_r(const SplitParams &p, int num_ctas, cudaStream_t stream) {
+cudaError_t launch_r(const SplitParams &p, cudaStream_t stream) {
     cudaError_t e = prepare<R>();
     if (e != cudaSuccess) return e;
-    split_attn_kernel<R><<<num_ctas, 32, smem_bytes<R>(), stream>>>(p);
-    return cudaGetLastError();
+    split_attn_kernel<R><<<p.split_ctas, 32, smem_bytes<R>(), stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the combine pass, launched as a programmatic dependent of the split
+    // kernel: its scan runs while the split kernel finishes
+    const int64_t units = static_cast<int64_t>(p.B) * p.Hkv * p.n_row_blocks * (R / 4);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>((units + kCombineWarps - 1) / kCombineWarps));
+    cfg.blockDim = dim3(kCombineWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel<R>, p);
 }
 
 template <int R>
@@ -737,11 +986,11 @@ cudaError_t split_occupancy(int R, int, int *ctas_per_sm) {
     }
 }
 
-cudaError_t launch_split_attn(const SplitParams &p, int num_ctas, cudaStream_t stream) {
+cudaError_t launch_split_attn(const SplitParams &p, cudaStream_t stream) {
     switch (p.rows_per_block) {
-        case 4: return launch_r<4>(p, num_ctas, stream);
-        case 8: return launch_r<8>(p, num_ctas, stream);
-        case 16: return launch_r<16>(p, num_ctas, stream);
+        case 4: return launch_r<4>(p, stream);
+        case 8: return launch_r<8>(p, stream);
+        case 16: return launch_r<16>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -62,15 +62,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Wait for the phase with the given parity to complete, giving up after
-// kWaitLimitNs of wall time. Returns false on timeout (the caller flags
-// SA_ERR_TIMEOUT and stops using the pipeline); it never spins forever.
-constexpr uint64_t kWaitLimitNs = 250000000ull;  // 250 ms: far above any real copy
+// about kWaitLimitCycles SM clock cycles (~250 ms at 2 GHz). Returns false on
+// timeout (the caller flags SA_ERR_TIMEOUT and stops using the pipeline); it
+// never spins forever. The SM cycle counter is cheap to read, so the wait
+// returns as soon as the phase completes.
+constexpr long long kWaitLimitCycles = 500000000ll;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
+    const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (clock64() - t0 > kWaitLimitCycles) return false;
     }
     return true;
 }
@@ -143,13 +145,13 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// float -> bf16 bits, round to nearest even (NaN kept quiet).
-__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
-    uint32_t u = __float_as_uint(f);
-    if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((u >> 16) | 0x40u);
-    u += 0x7fffu + ((u >> 16) & 1u);
-    return static_cast<uint16_t>(u >> 16);
+// Two floats -> packed bf16x2 (lo in bits 0..15), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
+
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile that
 // the TMA wrote with 128-byte swizzling: 128-byte rows, chunk index XOR-ed

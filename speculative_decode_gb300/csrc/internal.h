@@ -46,7 +46,6 @@ struct SplitParams {
     const int32_t *run_slots;   // nullable: partials the shared-prefix path writes per sequence
     float *ws_acc;              // [n_slots][total_q * Hq][128] fp32 unnormalised accumulators
     float *ws_ml;               // [n_slots][total_q * Hq][2] running max (log2 units), sum
-    int32_t *merge_ctr;         // [B * Hkv * n_row_blocks] finished pieces (zero between calls)
     int32_t *err;
     int32_t B, Hq, Hkv, G, num_pages, max_pages, total_q, max_q_len;
     int32_t rows_per_block;     // R, rows of one segment (4, 8 or 16)
@@ -54,14 +53,18 @@ struct SplitParams {
     int32_t piece_slots;        // partial slots a segment's pieces may use
     int32_t tc_min_rows;        // > 0: sequences with >= this many rows per KV head were
     int32_t tc_chunk_pages;     //   attended on the tensor cores in chunks of this many pages;
-                                //   this kernel only merges their partials
+                                //   the combine pass merges their partials
     int32_t slot_base;          // first workspace slot used by pieces
     int32_t n_rows_total;       // total_q * Hq (row stride of a workspace slot)
     float qscale;               // scale * log2(e)
     int32_t evict_first;
+    int32_t split_ctas;         // grid of the split kernel (one warp each); the combine
+                                // pass recomputes the same cut of the work
 };
 
-cudaError_t launch_split_attn(const SplitParams &p, int num_ctas, cudaStream_t stream);
+// Split kernel over p.split_ctas one-warp CTAs, then the combine pass that
+// merges the partials of segments cut into pieces (two kernels).
+cudaError_t launch_split_attn(const SplitParams &p, cudaStream_t stream);
 cudaError_t split_occupancy(int R, int warps_per_cta, int *ctas_per_sm);
 int split_tile_tokens();  // tokens per K/V tile of the split kernel
 
