@@ -148,7 +148,6 @@ __device__ __forceinline__ int64_t out_row(const SplitParams &P, const Piece &U,
 // Per-sequence shape of the work; tiles = 0 when the sequence has none. The
 // packed query rows of all sequences are checked against total_q once, by the
 // caller of this function, so no per-sequence query offset is needed here.
-constexpr int kScanBatch = 4;  // sequences per lane handled with all loads in flight
 
 template <int R>
 __device__ __forceinline__ SeqInfo seq_info_from(const SplitParams &P, int T, int n, int skip_pages,
@@ -304,71 +303,58 @@ __device__ void merge_rows(const SplitParams &P, const Piece &U, int R, int r4, 
     store_row(P, row, sub, o, Lsum);
 }
 
+__device__ __forceinline__ SeqInfo shfl_seq_info(SeqInfo si, int src) {
+    si.T = __shfl_sync(0xffffffffu, si.T, src);
+    si.n = __shfl_sync(0xffffffffu, si.n, src);
+    si.skip_tok = __shfl_sync(0xffffffffu, si.skip_tok, src);
+    si.tiles = __shfl_sync(0xffffffffu, si.tiles, src);
+    si.nrb = __shfl_sync(0xffffffffu, si.nrb, src);
+    si.runs = __shfl_sync(0xffffffffu, si.runs, src);
+    return si;
+}
+
 // ---- the work scan shared by the split and combine kernels
-// Lanes take contiguous chunks of sequences; with at most kScanBatch per lane
-// every length is loaded in one round and kept in registers.
+// Lane i looks after sequences i, i + 32, ...; each round of 32 sequences is
+// reduced with warp-wide integer reductions, and the next round's lengths are
+// loaded before the current round is reduced. The code is kept small on
+// purpose: it runs once per warp, so its instructions are fetched cold.
 struct WorkScan {
-    int c_lo, c_hi;
-    bool fast;
-    int Ts[kScanBatch], ns[kScanBatch], sk[kScanBatch], rs[kScanBatch];
-    int cw, w_pre, total;      // this lane's work, work before its chunk, all work (tiles)
-    int cq, q_pre, q_total;    // the same for query tokens
-    int max_tiles;             // longest segment, in tiles
+    int total;      // all work, in tiles
+    int q_total;    // all query tokens
+    int max_tiles;  // longest segment, in tiles
 };
 
 template <int R>
+__device__ __forceinline__ SeqInfo seq_of(const SplitParams &P, int b, bool flag) {
+    if (b >= P.B) return SeqInfo{0, 0, 0, 0, 0, 0};
+    return seq_info<R>(P, b, flag);
+}
+
+// A sequence's raw lengths (no work when b is past the batch).
+struct SeqRaw {
+    int T, n, sk, rs;
+};
+
+__device__ __forceinline__ SeqRaw load_raw(const SplitParams &P, int b) {
+    if (b >= P.B) return SeqRaw{0, 0, 0, 0};
+    return SeqRaw{P.seq_lens[b], P.q_lens[b], P.skip_pages ? P.skip_pages[b] : 0, P.run_slots ? P.run_slots[b] : 0};
+}
+
+template <int R>
 __device__ __forceinline__ void scan_work(const SplitParams &P, int lane, bool flag, WorkScan &sc) {
-    const int per = (P.B + 31) / 32;
-    sc.c_lo = min(P.B, lane * per);
-    sc.c_hi = min(P.B, sc.c_lo + per);
-    sc.fast = per <= kScanBatch;
-    sc.cq = 0;
-    sc.cw = 0;
-    int max_tiles = 0;
-    if (sc.fast) {
-#pragma unroll
-        for (int k = 0; k < kScanBatch; ++k) {
-            const int b = sc.c_lo + k;
-            const bool in = b < sc.c_hi;
-            sc.Ts[k] = in ? P.seq_lens[b] : 0;
-            sc.ns[k] = in ? P.q_lens[b] : 0;
-            sc.sk[k] = in && P.skip_pages ? P.skip_pages[b] : 0;
-            sc.rs[k] = in && P.run_slots ? P.run_slots[b] : 0;
-        }
-#pragma unroll
-        for (int k = 0; k < kScanBatch; ++k) {
-            if (sc.c_lo + k < sc.c_hi) {
-                const SeqInfo si = seq_info_from<R>(P, sc.Ts[k], sc.ns[k], sc.sk[k], sc.rs[k], flag);
-                sc.cw += seq_work(P, si);
-                max_tiles = max(max_tiles, si.tiles);
-                sc.cq += max(0, si.n);
-            }
-        }
-    } else {
-        for (int b = sc.c_lo; b < sc.c_hi; ++b) {
-            const SeqInfo si = seq_info<R>(P, b, flag);
-            sc.cw += seq_work(P, si);
-            max_tiles = max(max_tiles, si.tiles);
-            sc.cq += max(0, si.n);
-        }
+    sc.total = 0;
+    sc.q_total = 0;
+    sc.max_tiles = 0;
+    SeqRaw nxt = load_raw(P, lane);
+#pragma unroll 1
+    for (int base = 0; base < P.B; base += 32) {
+        const SeqRaw cur = nxt;
+        if (base + 32 < P.B) nxt = load_raw(P, base + 32 + lane);  // in flight while this round is reduced
+        const SeqInfo si = seq_info_from<R>(P, cur.T, cur.n, cur.sk, cur.rs, flag);
+        sc.total += __reduce_add_sync(0xffffffffu, static_cast<unsigned>(seq_work(P, si)));
+        sc.q_total += __reduce_add_sync(0xffffffffu, static_cast<unsigned>(max(0, si.n)));
+        sc.max_tiles = max(sc.max_tiles, static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(si.tiles))));
     }
-    int q_pre = sc.cq;
-    int w_pre = sc.cw;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, q_pre, o);
-        const int wv = __shfl_up_sync(0xffffffffu, w_pre, o);
-        if (lane >= o) {
-            q_pre += v;
-            w_pre += wv;
-        }
-        max_tiles = max(max_tiles, __shfl_xor_sync(0xffffffffu, max_tiles, o));
-    }
-    sc.q_total = __shfl_sync(0xffffffffu, q_pre, 31);
-    sc.total = __shfl_sync(0xffffffffu, w_pre, 31);
-    sc.q_pre = q_pre - sc.cq;  // exclusive
-    sc.w_pre = w_pre - sc.cw;
-    sc.max_tiles = max_tiles;
 }
 
 // The cut of the work into W warp ranges. A segment of s tiles spans at most
@@ -380,55 +366,43 @@ __device__ __forceinline__ Ranges split_ranges(const SplitParams &P, const WorkS
     return make_ranges(sc.total, W, max(C_min, 1));
 }
 
-// Walk this lane's chunk of sequences to the one whose work holds tile g
-// (by_work) or to sequence bt: its index, work offset, query offset and shape.
+// The sequence whose work holds tile g (by_work) or sequence bt: its index,
+// work offset, query offset and shape, the same on every lane. A second pass
+// over the lengths, which the scan left in L1.
 template <int R>
-__device__ __forceinline__ void walk_chunk(const SplitParams &P, const WorkScan &sc, bool by_work, int g,
-                                           int bt, int &b_out, int &pos, int &qs, SeqInfo &si_out) {
-    pos = sc.w_pre;
-    qs = sc.q_pre;
-    b_out = sc.c_lo;
-    if (sc.fast) {
-        bool found = false;
+__device__ __forceinline__ void locate_seq(const SplitParams &P, int lane, bool by_work, int g, int bt,
+                                           int &b_out, int &pos, int &qs, SeqInfo &si_out) {
+    int w_base = 0, q_base = 0;
+#pragma unroll 1
+    for (int base = 0; base < P.B; base += 32) {
+        const int b = base + lane;
+        const SeqInfo si = seq_of<R>(P, b, false);
+        const int w = seq_work(P, si), qn = max(0, si.n);
+        int wi = w, qi = qn;  // inclusive prefix sums over the lanes
 #pragma unroll
-        for (int k = 0; k < kScanBatch; ++k) {
-            if (!found && sc.c_lo + k < sc.c_hi) {
-                const SeqInfo si = seq_info_from<R>(P, sc.Ts[k], sc.ns[k], sc.sk[k], sc.rs[k], false);
-                const int wb = seq_work(P, si);
-                if (by_work ? g < pos + wb : sc.c_lo + k == bt) {
-                    found = true;
-                    b_out = sc.c_lo + k;
-                    si_out = si;
-                } else {
-                    pos += wb;
-                    qs += max(0, si.n);
-                }
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, wi, o), c = __shfl_up_sync(0xffffffffu, qi, o);
+            if (lane >= o) {
+                wi += a;
+                qi += c;
             }
         }
-    } else {
-        for (int b = sc.c_lo; b < sc.c_hi; ++b) {
-            const SeqInfo si = seq_info<R>(P, b, false);
-            const int wb = seq_work(P, si);
-            if (by_work ? g < pos + wb : b == bt) {
-                b_out = b;
-                si_out = si;
-                return;
-            }
-            pos += wb;
-            qs += max(0, si.n);
+        const int wx = w_base + wi - w, qx = q_base + qi - qn;
+        const unsigned hit = __ballot_sync(0xffffffffu, by_work ? (w > 0 && wx <= g && g < wx + w) : b == bt);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            b_out = base + src;
+            pos = __shfl_sync(0xffffffffu, wx, src);
+            qs = __shfl_sync(0xffffffffu, qx, src);
+            si_out = shfl_seq_info(si, src);
+            return;
         }
+        w_base += __shfl_sync(0xffffffffu, wi, 31);
+        q_base += __shfl_sync(0xffffffffu, qi, 31);
     }
+    b_out = P.B;  // not found (only when g is past all work)
 }
 
-__device__ __forceinline__ SeqInfo shfl_seq_info(SeqInfo si, int src) {
-    si.T = __shfl_sync(0xffffffffu, si.T, src);
-    si.n = __shfl_sync(0xffffffffu, si.n, src);
-    si.skip_tok = __shfl_sync(0xffffffffu, si.skip_tok, src);
-    si.tiles = __shfl_sync(0xffffffffu, si.tiles, src);
-    si.nrb = __shfl_sync(0xffffffffu, si.nrb, src);
-    si.runs = __shfl_sync(0xffffffffu, si.runs, src);
-    return si;
-}
 
 template <int R>
 __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(const SplitParams P) {
@@ -458,8 +432,13 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         fence_barrier_init();
     }
 
-    // the combine kernel may be scheduled now: it waits for this grid's
-    // partials before reading them
+    // The combine kernel may be scheduled now: it waits for this grid before
+    // it reads the partials. This kernel itself may have been started while
+    // the kernel before it (kv_append) still runs: everything up to the grid
+    // dependency wait below reads only lengths and block tables, which that
+    // kernel does not write; queries and pages are read after the wait. Every
+    // warp waits before it exits, so this grid completes after its
+    // predecessor.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- 1. total work and this warp's range [g_begin, g_end) of tiles
@@ -467,39 +446,27 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
     scan_work<R>(P, lane, true, sc);
     if (sc.q_total > P.total_q) {  // q_lens disagree with dims.total_q: reject the whole call
         if (lane == 0) flag_error(P.err, kErrBitQlen);
+        grid_dependency_wait();
         return;
     }
     const Ranges rg = split_ranges(P, sc, gridDim.x);
     const int g_begin = rg.begin(blockIdx.x);
     const int g_end = min(sc.total, rg.begin(blockIdx.x + 1));
     __syncwarp();
-    if (g_begin >= g_end) return;
-
-    // ---- 2. locate the first tile (the lane whose sequences hold g_begin walks
-    // them from registers) and read its page id at once
-    int b0 = 0, q0 = 0;
-    int ws0 = 0;
-    SeqInfo si0{};
-    int pid0 = -1, pid1 = -1, j0 = 0;
-    {
-        const bool mine = sc.cw > 0 && sc.w_pre <= g_begin && g_begin < sc.w_pre + sc.cw;
-        const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
-        if (lane == src) {
-            walk_chunk<R>(P, sc, true, g_begin, 0, b0, ws0, q0, si0);
-            const int t0 = si0.skip_tok + static_cast<int>((g_begin - ws0) % si0.tiles) * kTile;
-            j0 = t0 / kPageSize;
-            const int npg = (si0.T + kPageSize - 1) / kPageSize;
-            if (t0 < si0.T) pid0 = P.block_table[static_cast<int64_t>(b0) * P.max_pages + j0];
-            if (j0 + 1 < npg) pid1 = P.block_table[static_cast<int64_t>(b0) * P.max_pages + j0 + 1];
-        }
-        b0 = __shfl_sync(0xffffffffu, b0, src);
-        q0 = __shfl_sync(0xffffffffu, q0, src);
-        ws0 = __shfl_sync(0xffffffffu, ws0, src);
-        si0 = shfl_seq_info(si0, src);
-        pid0 = __shfl_sync(0xffffffffu, pid0, src);
-        pid1 = __shfl_sync(0xffffffffu, pid1, src);
-        j0 = __shfl_sync(0xffffffffu, j0, src);
+    if (g_begin >= g_end) {
+        grid_dependency_wait();
+        return;
     }
+
+    // ---- 2. locate the first tile and read its page id (and the next page's)
+    int b0 = 0, q0 = 0, ws0 = 0;
+    SeqInfo si0{};
+    locate_seq<R>(P, lane, true, g_begin, 0, b0, ws0, q0, si0);
+    const int t0_first = si0.skip_tok + ((g_begin - ws0) % si0.tiles) * kTile;
+    const int j0 = t0_first / kPageSize;
+    const int64_t bt0 = static_cast<int64_t>(b0) * P.max_pages;
+    const int pid0 = t0_first < si0.T ? P.block_table[bt0 + j0] : -1;
+    const int pid1 = j0 + 1 < (si0.T + kPageSize - 1) / kPageSize ? P.block_table[bt0 + j0 + 1] : -1;
 
     // row of the reduce-scatter result this lane ends up holding
     int rj = 0;
@@ -647,6 +614,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         for (uint32_t c = pieces_done; c < pieces_pushed; ++c) (void)mbar_wait(&qfull[c % S], (c / S) & 1);
     };
 
+    grid_dependency_wait();  // the pages written by the previous kernel are complete
     top_up();
     while (consumed < issued) {
         Piece U;
@@ -899,16 +867,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32, SA_COMBINE_MIN_CTAS) combi
     WorkScan sc;
     scan_work<R>(P, lane, false, sc);
     if (sc.q_total > P.total_q) return;  // flagged by the split kernel
-    int b = 0, qs = 0;
-    int pos = 0;
+    int b = 0, qs = 0, pos = 0;
     SeqInfo si{};
-    {
-        const int src = __ffs(__ballot_sync(0xffffffffu, sc.c_lo <= bt && bt < sc.c_hi)) - 1;
-        if (lane == src) walk_chunk<R>(P, sc, false, 0, bt, b, pos, qs, si);
-        qs = __shfl_sync(0xffffffffu, qs, src);
-        pos = __shfl_sync(0xffffffffu, pos, src);
-        si = shfl_seq_info(si, src);
-    }
+    locate_seq<R>(P, lane, false, 0, bt, b, pos, qs, si);
     if (si.n <= 0 || rb >= si.nrb) return;
     const int nvr = min(R, P.G * si.n - rb * R);
     if (r4 * 4 >= nvr) return;
@@ -927,7 +888,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, SA_COMBINE_MIN_CTAS) combi
     U.pieces = pieces;
     U.runs = si.runs;
     U.nvr = nvr;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the split kernel's partials are complete
+    grid_dependency_wait();  // the split kernel's partials are complete
     merge_rows(P, U, R, r4, lane);
 }
 
@@ -942,27 +903,36 @@ cudaError_t prepare() {
     return err;
 }
 
-template <int R>
-cudaError_t launch_r(const SplitParams &p, cudaStream_t stream) {
-    cudaError_t e = prepare<R>();
-    if (e != cudaSuccess) return e;
-    split_attn_kernel<R><<<p.split_ctas, 32, smem_bytes<R>(), stream>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // the combine pass, launched as a programmatic dependent of the split
-    // kernel: its scan runs while the split kernel finishes
-    const int64_t units = static_cast<int64_t>(p.B) * p.Hkv * p.n_row_blocks * (R / 4);
+// Launch as a programmatic dependent of whatever precedes it on the stream:
+// the kernel may start once its predecessor has signalled (kv_append does at
+// once; any other kernel at its end) and waits for the predecessor's
+// completion itself (griddepcontrol.wait) before reading its results.
+template <typename Kernel>
+cudaError_t launch_dependent(Kernel kernel, int grid, int threads, size_t smem, cudaStream_t stream,
+                             const SplitParams &p) {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>((units + kCombineWarps - 1) / kCombineWarps));
-    cfg.blockDim = dim3(kCombineWarps * 32);
-    cfg.dynamicSmemBytes = 0;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel<R>, p);
+    return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+template <int R>
+cudaError_t launch_r(const SplitParams &p, cudaStream_t stream) {
+    cudaError_t e = prepare<R>();
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(split_attn_kernel<R>, p.split_ctas, 32, smem_bytes<R>(), stream, p);
+    if (e != cudaSuccess) return e;
+    // the combine pass: its scan runs while the split kernel finishes
+    const int64_t units = static_cast<int64_t>(p.B) * p.Hkv * p.n_row_blocks * (R / 4);
+    return launch_dependent(combine_kernel<R>, static_cast<int>((units + kCombineWarps - 1) / kCombineWarps),
+                            kCombineWarps * 32, 0, stream, p);
 }
 
 template <int R>

@@ -145,6 +145,11 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible (returns at once when the
+// kernel was not launched as a dependent).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Two floats -> packed bf16x2 (lo in bits 0..15), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t d;

@@ -19,39 +19,40 @@ __global__ void __launch_bounds__(256) kv_append_kernel(
     const int32_t *__restrict__ block_table, const int32_t *__restrict__ seq_lens,
     const int32_t *__restrict__ q_lens, int32_t *err, int Hkv, int num_pages, int max_pages,
     int max_q_len, int total_q) {
+    // the attention kernel that follows may start its set-up now: it reads
+    // the pages only after this grid has completed
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int i = blockIdx.x;
     const int b = blockIdx.y;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
+    // one round of independent loads: this sequence's lengths and the query
+    // counts of the sequences before it (for its first packed row)
     const int n = q_lens[b];
     const int T = seq_lens[b];
+    int qstart = 0;
+    for (int k = lane; k < b; k += 32) qstart += q_lens[k];
+    qstart = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(qstart)));
     if (i >= n) return;
-    if (n > T || n > max_q_len) {
+    if (n > T || n > max_q_len || qstart + n > total_q) {  // q_lens disagree with seq_lens or dims
         if (threadIdx.x == 0) flag_error(err, kErrBitQlen);
         return;
     }
+    // second round: the page id and the new rows, independent of each other
     const int pos = T - n + i;
     const int j = pos / kPageSize;
     const int pid = j < max_pages ? block_table[static_cast<int64_t>(b) * max_pages + j] : -1;
-    if (pid < 0 || pid >= num_pages) {
-        if (threadIdx.x == 0) flag_error(err, kErrBitPageOOB);
-        return;
-    }
-    int qstart = 0;  // packed row of token 0 of sequence b
-    for (int k = lane; k < b; k += 32) qstart += q_lens[k];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) qstart += __shfl_xor_sync(0xffffffffu, qstart, o);
-    if (qstart + n > total_q) {  // q_lens disagree with dims.total_q
-        if (threadIdx.x == 0) flag_error(err, kErrBitQlen);
-        return;
-    }
     const int64_t row = qstart + i;
     const int slot = pos % kPageSize;
     for (int g = warp; g < Hkv; g += blockDim.x >> 5) {
         const int64_t src = (row * Hkv + g) * kHeadDim + lane * 4;
-        const int64_t dst = ((static_cast<int64_t>(pid) * Hkv + g) * kPageSize + slot) * kHeadDim + lane * 4;
         const uint2 kw = *reinterpret_cast<const uint2 *>(k_new + src);
         const uint2 vw = *reinterpret_cast<const uint2 *>(v_new + src);
+        if (pid < 0 || pid >= num_pages) {
+            if (threadIdx.x == 0) flag_error(err, kErrBitPageOOB);
+            return;
+        }
+        const int64_t dst = ((static_cast<int64_t>(pid) * Hkv + g) * kPageSize + slot) * kHeadDim + lane * 4;
         *reinterpret_cast<uint2 *>(k_pages + dst) = kw;
         *reinterpret_cast<uint2 *>(v_pages + dst) = vw;
     }
