@@ -226,9 +226,10 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
 
     const SplitConfig c = split_config(d, plan);
     if (!merge_fits(c)) return SA_ERR_UNSUPPORTED;  // too many partials per row to merge
-    // the split kernel counts work in 16-token tiles with 32-bit offsets
-    const int64_t max_work = static_cast<int64_t>(d.num_seqs) * d.max_pages_per_seq *
-                             (kPageSize / split_tile_tokens()) * d.num_kv_heads * c.nrb;
+    // the split kernel counts work in 32-bit balancing units
+    const int64_t max_work = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.nrb *
+                             (static_cast<int64_t>(d.max_pages_per_seq) * (kPageSize / split_tile_tokens()) *
+                                  split_units_per_tile() + split_segment_cost());
     if (max_work > INT32_MAX) return SA_ERR_UNSUPPORTED;
     const int64_t rows_total = static_cast<int64_t>(d.total_q) * d.num_q_heads;
     float *ws_acc = static_cast<float *>(workspace);

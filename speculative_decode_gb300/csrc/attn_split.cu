@@ -192,10 +192,10 @@ __device__ __forceinline__ SeqInfo seq_info_from(const SplitParams &P, int T, in
 // The cut of the tile sequence [0, total) into one contiguous range per warp:
 // every warp gets C or C + 1 tiles (the first `rem` get C + 1) when that keeps
 // C >= C_min; otherwise ranges of C_min tiles and the last warps stay idle.
-// Work offsets are counted in tiles in 32 bits: the host rejects shapes whose
-// largest possible total reaches 2^31.
+// Work offsets are counted in balancing units in 32 bits: the host rejects
+// shapes whose largest possible total reaches 2^31.
 struct Ranges {
-    int C, rem;
+    int C, rem;  // warp w gets C + 1 units if w < rem, else C
     __device__ __forceinline__ int begin(int w) const { return w * C + min(w, rem); }
     __device__ __forceinline__ int range_of(int t) const {
         const int big = rem * (C + 1);
@@ -203,19 +203,36 @@ struct Ranges {
     }
 };
 
+// Every warp gets C or C + 1 units when that keeps C >= C_min; otherwise
+// ranges of C_min units and the last warps stay idle.
 __device__ __forceinline__ Ranges make_ranges(int total, int W, int C_min) {
     const int even = total / W;
     if (even >= C_min) return Ranges{even, total - even * W};
     return Ranges{C_min, 0};
 }
 
+// The work of a segment in balancing units: kUnitsPerTile per tile plus
+// kSegmentCost for the segment's start (closing the previous piece, loading
+// and converting new queries), so that a warp whose range crosses into a new
+// segment gets fewer tiles. Tile t of a segment that starts at unit u sits at
+// unit u + kSegmentCost + kUnitsPerTile * t and belongs to the warp whose range
+// holds that unit.
+#ifndef SA_SPLIT_SEG_COST
+#define SA_SPLIT_SEG_COST 8
+#endif
+constexpr int kUnitsPerTile = 4;
+constexpr int kSegmentCost = SA_SPLIT_SEG_COST;
+
+__device__ __forceinline__ int segment_units(const SeqInfo &s) {
+    return s.tiles > 0 ? kSegmentCost + kUnitsPerTile * s.tiles : 0;
+}
+
 __device__ __forceinline__ int seq_work(const SplitParams &P, const SeqInfo &s) {
-    return s.tiles * P.Hkv * s.nrb;
+    return segment_units(s) * P.Hkv * s.nrb;
 }
 
 // Merging a row's partials (the tensor-core runs' slots, then the pieces'
 // slots) with exact max-shifted rescaling.
-constexpr int kMaxMergeSlots = 16;
 
 __device__ __forceinline__ const float *ws_slot_row(const SplitParams &P, const Piece &U, int k, int64_t row,
                                                     const float *base, int width) {
@@ -237,7 +254,7 @@ __device__ __forceinline__ void store_row(const SplitParams &P, int64_t row, int
 // Up to four partials are read in one round trip (every (max, sum) and
 // accumulator in flight together); more take two (the maxima, then the
 // accumulators).
-__device__ void merge_rows(const SplitParams &P, const Piece &U, int R, int r4, int lane) {
+__device__ __forceinline__ void merge_rows(const SplitParams &P, const Piece &U, int R, int r4, int lane, bool store) {
     const int nslots = U.runs + U.pieces;
     const int sub = lane & 7;
     const int r = r4 * 4 + (lane >> 3);
@@ -300,7 +317,7 @@ __device__ void merge_rows(const SplitParams &P, const Piece &U, int R, int r4, 
             }
         }
     }
-    store_row(P, row, sub, o, Lsum);
+    if (store) store_row(P, row, sub, o, Lsum);
 }
 
 __device__ __forceinline__ SeqInfo shfl_seq_info(SeqInfo si, int src) {
@@ -357,13 +374,19 @@ __device__ __forceinline__ void scan_work(const SplitParams &P, int lane, bool f
     }
 }
 
-// The cut of the work into W warp ranges. A segment of s tiles spans at most
-// ceil(s / C) + 1 ranges: C is at least ceil(longest / (slots - 1)) so that no
+// The cut of the work into W warp ranges. A segment of u units spans at most
+// ceil(u / C) + 1 ranges: C is at least ceil(longest / (slots - 1)) so that no
 // segment has more pieces than the workspace has partial slots.
 __device__ __forceinline__ Ranges split_ranges(const SplitParams &P, const WorkScan &sc, int W) {
-    const int mt = sc.max_tiles;
-    const int C_min = P.piece_slots > 1 ? (mt + P.piece_slots - 2) / (P.piece_slots - 1) : mt;
+    const int mu = kSegmentCost + kUnitsPerTile * sc.max_tiles;
+    const int C_min = P.piece_slots > 1 ? (mu + P.piece_slots - 2) / (P.piece_slots - 1) : mu;
     return make_ranges(sc.total, W, max(C_min, 1));
+}
+
+// Pieces (warp ranges) that a segment starting at unit u0 with `tiles` tiles is cut into.
+__device__ __forceinline__ void segment_ranges(const Ranges &rg, int u0, int tiles, int &first, int &last) {
+    first = rg.range_of(u0 + kSegmentCost);
+    last = rg.range_of(u0 + kSegmentCost + kUnitsPerTile * (tiles - 1));
 }
 
 // The sequence whose work holds tile g (by_work) or sequence bt: its index,
@@ -458,15 +481,21 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         return;
     }
 
-    // ---- 2. locate the first tile and read its page id (and the next page's)
+    // ---- 2. locate the first tile (the first tile unit at or after g_begin)
+    // and read its page id and the next page's
     int b0 = 0, q0 = 0, ws0 = 0;
     SeqInfo si0{};
     locate_seq<R>(P, lane, true, g_begin, 0, b0, ws0, q0, si0);
-    const int t0_first = si0.skip_tok + ((g_begin - ws0) % si0.tiles) * kTile;
+    const int seg_units0 = segment_units(si0);
+    const int iseg0 = (g_begin - ws0) / seg_units0;
+    const int in_seg = (g_begin - ws0) - iseg0 * seg_units0;
+    const int tile0 = in_seg <= kSegmentCost ? 0 : (in_seg - kSegmentCost + kUnitsPerTile - 1) / kUnitsPerTile;
+    const bool primed = tile0 < si0.tiles;  // else the first tile is in the next segment
+    const int t0_first = si0.skip_tok + tile0 * kTile;
     const int j0 = t0_first / kPageSize;
     const int64_t bt0 = static_cast<int64_t>(b0) * P.max_pages;
-    const int pid0 = t0_first < si0.T ? P.block_table[bt0 + j0] : -1;
-    const int pid1 = j0 + 1 < (si0.T + kPageSize - 1) / kPageSize ? P.block_table[bt0 + j0 + 1] : -1;
+    const int pid0 = primed && t0_first < si0.T ? P.block_table[bt0 + j0] : -1;
+    const int pid1 = primed && j0 + 1 < (si0.T + kPageSize - 1) / kPageSize ? P.block_table[bt0 + j0 + 1] : -1;
 
     // row of the reduce-scatter result this lane ends up holding
     int rj = 0;
@@ -483,28 +512,24 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
     const bool row_writer = (j % DUP) == 0;  // one of the DUP lanes that hold row rj
     const uint64_t policy = P.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
 
-    // ---- issue cursor: walks tiles g_begin .. g_end-1 ahead of the consumer
+    // ---- issue cursor: walks this warp's tiles ahead of the consumer; ig is
+    // the unit of the next tile
     int ib = b0, iq = q0;
     int iws = ws0;
     SeqInfo isi = si0;
-    int ig = g_begin;
-    int iseg, itile, ikvh, irb;
-    {
-        const int off = g_begin - iws;
-        iseg = static_cast<int>(off / isi.tiles);
-        itile = static_cast<int>(off % isi.tiles);
-        ikvh = iseg / isi.nrb;
-        irb = iseg % isi.nrb;
-    }
+    int iseg = iseg0, itile = tile0;
+    int ikvh = iseg / isi.nrb, irb = iseg % isi.nrb;
+    int ig = ws0 + iseg * seg_units0 + kSegmentCost + kUnitsPerTile * tile0;
+    bool first_piece = true;
     uint32_t issued = 0, consumed = 0, pieces_pushed = 0;
     // Page ids and lengths the issue cursor needs, each read well before its
     // first use so that no block-table or length load stalls the issue of a
     // tile: the current page's id and the next page's; the current sequence's
     // first page (every KV head's segment starts there); the next sequence's
     // lengths and, without a plan, its first page.
-    int pg_b = b0, pg_j = j0, pg_id = pid0, pg_next = pid1;  // primed by the locating lane
+    int pg_b = primed ? b0 : -1, pg_j = j0, pg_id = pid0, pg_next = pid1;  // primed after locating
     int f_b = b0, f_j = si0.skip_tok / kPageSize;
-    int f_pid = j0 == f_j ? pid0 : P.block_table[static_cast<int64_t>(b0) * P.max_pages + f_j];
+    int f_pid = primed && j0 == f_j ? pid0 : P.block_table[static_cast<int64_t>(b0) * P.max_pages + f_j];
     const bool plain = P.skip_pages == nullptr && P.run_slots == nullptr;  // sequences start at page 0
     int nx_b = -1, nx_T = 0, nx_n = 0, nx_sk = 0, nx_rs = 0, nx_pid = -1;
     auto prefetch_next = [&](int b) {
@@ -530,6 +555,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         if (ig >= g_end) return false;
         if (itile == isi.tiles) {  // next segment
             itile = 0;
+            ig += kSegmentCost;
             ++iseg;
             if (++irb == isi.nrb) {
                 irb = 0;
@@ -550,20 +576,21 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                 f_pid = (ib == nx_b && plain && f_j == 0) ? nx_pid : P.block_table[static_cast<int64_t>(ib) * P.max_pages + f_j];
                 prefetch_next(ib);
             }
+            if (ig >= g_end) return false;
         }
         const int kvh = ikvh, rb = irb;
-        if (ig == g_begin || itile == 0) {
+        if (first_piece || itile == 0) {
             // a new piece: describe it for the consumer and fetch its query rows
-            const int seg0 = iws + iseg * isi.tiles;
-            const int seg1 = seg0 + isi.tiles;
-            const int first = rg.range_of(seg0), last = rg.range_of(seg1 - 1);
+            first_piece = false;
+            int first, last;
+            segment_ranges(rg, iws + iseg * segment_units(isi), isi.tiles, first, last);
             const int nvr = min(R, P.G * isi.n - rb * R);
             const int qs = pieces_pushed % S;
             if (lane == 0) {
                 int32_t *d = ring + (pieces_pushed % kRing) * kPieceInts;
                 d[0] = ib; d[1] = kvh; d[2] = rb; d[3] = isi.T; d[4] = isi.n; d[5] = iq;
                 d[6] = isi.skip_tok + itile * kTile;
-                d[7] = static_cast<int>(min(seg1, g_end) - ig);
+                d[7] = min(isi.tiles - itile, (g_end - ig + kUnitsPerTile - 1) / kUnitsPerTile);
                 d[8] = static_cast<int>(blockIdx.x) - first;
                 d[9] = last - first + 1;
                 d[10] = nvr;
@@ -599,7 +626,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         }
         ++issued;
         ++itile;
-        ++ig;
+        ig += kUnitsPerTile;
         return true;
     };
     auto top_up = [&]() {
@@ -876,8 +903,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32, SA_COMBINE_MIN_CTAS) combi
     int pieces = 0;
     if (si.tiles > 0) {
         const Ranges rg = split_ranges(P, sc, P.split_ctas);
-        const int seg0 = pos + (kvh * si.nrb + rb) * si.tiles;
-        pieces = rg.range_of(seg0 + si.tiles - 1) - rg.range_of(seg0) + 1;
+        int first, last;
+        segment_ranges(rg, pos + (kvh * si.nrb + rb) * segment_units(si), si.tiles, first, last);
+        pieces = last - first + 1;
     }
     if (si.runs == 0 && pieces <= 1) return;  // written directly by the split kernel
     Piece U{};
@@ -888,8 +916,15 @@ __global__ void __launch_bounds__(kCombineWarps * 32, SA_COMBINE_MIN_CTAS) combi
     U.pieces = pieces;
     U.runs = si.runs;
     U.nvr = nvr;
-    grid_dependency_wait();  // the split kernel's partials are complete
-    merge_rows(P, U, R, r4, lane);
+    // Pass 0 runs the merge on whatever the workspace holds now and stores
+    // nothing: it brings the merge's instructions and address translations on
+    // chip while the split kernel finishes. Pass 1, after the grid dependency
+    // wait (the split kernel's partials are complete), is the merge.
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        if (pass == 1) grid_dependency_wait();
+        merge_rows(P, U, R, r4, lane, pass == 1);
+    }
 }
 
 template <int R>
@@ -946,6 +981,8 @@ cudaError_t occupancy_r(int *ctas_per_sm) {
 }  // namespace
 
 int split_tile_tokens() { return kTile; }
+int split_units_per_tile() { return kUnitsPerTile; }
+int split_segment_cost() { return kSegmentCost; }
 
 cudaError_t split_occupancy(int R, int, int *ctas_per_sm) {
     switch (R) {

@@ -67,6 +67,8 @@ struct SplitParams {
 cudaError_t launch_split_attn(const SplitParams &p, cudaStream_t stream);
 cudaError_t split_occupancy(int R, int warps_per_cta, int *ctas_per_sm);
 int split_tile_tokens();  // tokens per K/V tile of the split kernel
+int split_units_per_tile();  // balancing units of one tile and of a segment start
+int split_segment_cost();
 
 cudaError_t launch_kv_append(const sa_dims &d, const uint16_t *k_new, const uint16_t *v_new,
                              uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,
