@@ -199,6 +199,12 @@ def timed_steps(batch: GpuBatch, steps: int, warmup: int, flush, parts):
     return per_part, wall
 
 
+# DRAM bytes of one split_attn_kernel<4> launch on the decode batch, from the
+# ncu capture summarised in profiles/split_attn_kernel_R4_llama3_8b_decode.md
+# (200.35 MB read + 3.60 MB written). Set to None when the kernel changes.
+SPLIT_TRAFFIC_BYTES = 203_950_336
+
+
 def timed_sequence(batch: GpuBatch, steps: int, warmup: int, flush, parts):
     """Run warmup + steps of the named parts launched back to back (no event
     between them, so a kernel may start while its predecessor finishes); per
@@ -396,7 +402,9 @@ def run_ours(args):
         "frac_of_hbm_peak": round(achieved / peak, 4),
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None,
+            "frac": round(achieved / peak, 4), "traffic": SPLIT_TRAFFIC_BYTES,
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of split_attn_kernel<4>, "
+                              "one capture of this build (profiles/split_attn_kernel_R4_llama3_8b_decode.md)",
             "kernel": "paged_attn call (split_attn_kernel + combine_kernel)",
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback 6.8 TB/s",
