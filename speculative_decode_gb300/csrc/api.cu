@@ -67,7 +67,10 @@ constexpr int kPieceSlots = 8;
 // tokens: q_len = k+1 verification) are a dense contraction: without a plan
 // they go to the tensor cores, in chunks of kTcChunkPages pages.
 constexpr int kTcMinRows = 16;
-constexpr int kTcChunkPages = 8;
+#ifndef SA_TC_CHUNK_PAGES
+#define SA_TC_CHUNK_PAGES 8
+#endif
+constexpr int kTcChunkPages = SA_TC_CHUNK_PAGES;
 
 SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     SplitConfig c{};
@@ -241,10 +244,10 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
         // tensor-core work first: the combine pass reads its partials
         CUtensorMap pk, pv;
         if (encode_tensor_map_2d(&pk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(k_pages),
-                                 kHeadDim, pool_rows, kHeadDim * 2, 64, prefix_tile_rows(),
+                                 kHeadDim, pool_rows, kHeadDim * 2, 64, prefix_key_tile(),
                                  CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
             encode_tensor_map_2d(&pv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(v_pages),
-                                 kHeadDim, pool_rows, kHeadDim * 2, 64, prefix_tile_rows(),
+                                 kHeadDim, pool_rows, kHeadDim * 2, 64, prefix_key_tile(),
                                  CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return SA_ERR_CUDA;
         if (pd && pd->num_tiles > 0 &&

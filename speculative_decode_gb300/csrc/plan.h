@@ -40,12 +40,13 @@ PlanHost build_plan(const sa_dims &d, const int32_t *block_table, const int32_t 
 
 // Launch the tensor-core shared-prefix kernel over the plan's work items.
 // tmk / tmv view the K / V pools as [num_pages*Hkv*256 rows][128] bf16 with
-// 64 x prefix_tile_rows() boxes and 128-byte swizzle.
+// 64 x prefix_key_tile() boxes and 128-byte swizzle.
 cudaError_t launch_prefix_tc(const sa_dims &d, const PlanDevice &pd, const uint16_t *q,
                              const CUtensorMap &tmk, const CUtensorMap &tmv, float scale,
                              float *ws_acc, float *ws_ml, int64_t rows_total, int32_t *err,
                              const int32_t *block_table, cudaStream_t stream);
-int prefix_tile_rows();
+int prefix_tile_rows();  // query rows per work item (tensor-memory lanes)
+int prefix_key_tile();   // keys per K/V tile
 
 // Sequence mode of the tensor-core kernel: sequences with at least min_rows
 // query rows per KV head (G heads x new tokens, e.g. q_len = k+1 verification)

@@ -4,26 +4,32 @@
 // the same physical pages for a common prefix. Attention over such a run of
 // pages is one dense contraction: the query rows of every member sequence
 // (G heads x its new tokens, all for one KV head) against the run's keys and
-// values. This kernel streams each shared 128-token K/V tile from HBM once per
+// values. This kernel streams each shared 64-token K/V tile from HBM once per
 // 128-row tile of queries (row tiles of one run share their tiles through L2)
 // and computes
 //     S = Q K^T          (tcgen05.mma, bf16 x bf16 -> fp32 in tensor memory)
 //     P = exp2(S*scale*log2e - m)  online, one thread per row, bf16 to smem
 //     O += P V           (tcgen05.mma, fp32 accumulator in tensor memory)
-// and stores, per row, an fp32 partial (O, m, l) that the split kernel merges
+// and stores, per row, an fp32 partial (O, m, l) that the combine kernel merges
 // with the rest of the sequence's keys.
 //
 // CTA = 6 warps: warps 0-3 softmax and epilogue (thread t owns row t, which is
 // tensor-memory lane t), warp 4 the TMA producer, warp 5 allocates tensor
-// memory and issues the MMAs (one elected thread). S is double-buffered in
-// tensor memory, so Q K^T of the next tile and P V of the previous one run on
-// the tensor cores while the softmax of the current tile runs on the CUDA
-// cores. Operands sit in shared
+// memory and issues the MMAs (one elected thread). K/V tiles of 64 keys
+// (32 KiB) stream through five stages, so four loads are in flight while a
+// tile is consumed; S (tensor memory, three buffers) and P (shared memory, two)
+// are multi-buffered, so Q K^T runs up to two tiles ahead and P V of the
+// previous tile runs on the tensor cores while the softmax of the current tile
+// runs on the CUDA cores. With at most 32 query rows (q_len = k+1
+// verification of one sequence) every row is held four times and each copy's
+// softmax takes a quarter of a tile's keys. Operands sit in shared
 // memory in the 128-byte-swizzled K-major layout the TMA writes (Q, K and P)
 // or the MN-major one (V), described to the tensor core by shared-memory
 // matrix descriptors. Every wait is bounded; on timeout the CTA flags
 // SA_ERR_TIMEOUT, drains what it issued and frees its tensor memory.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "plan.h"
@@ -33,18 +39,23 @@ namespace sa {
 namespace {
 
 constexpr int kM = 128;                       // rows per tile (tensor-memory lanes)
-constexpr int kN = 128;                       // keys per K/V tile
-constexpr int kSub = kN * 128;                // one 64-wide bf16 column block: 128 rows x 128 B = 16 KiB
-constexpr int kQBytes = 2 * kSub;             // Q [128 rows][128 d]
-constexpr int kPBytes = 2 * kSub;             // P [128 rows][128 keys]
-constexpr int kKVStage = 4 * kSub;            // K (2 blocks) + V (2 blocks) = 64 KiB
-constexpr int kStagesTC = 2;
-constexpr int kTmemCols = 512;                // S0: columns 0-127, S1: 128-255, O: 256-383
+constexpr int kN = 64;                        // keys per K/V tile
+constexpr int kRowBlk = kM * 128;             // one 64-wide bf16 column block of 128 rows: 16 KiB
+constexpr int kKVBlk = kN * 128;              // one 64-wide bf16 column block of a K or V tile: 8 KiB
+constexpr int kQBytes = 2 * kRowBlk;          // Q [128 rows][128 d]
+constexpr int kPBytes = kRowBlk;              // P [128 rows][64 keys], double-buffered
+constexpr int kKVStage = 4 * kKVBlk;          // K (2 blocks) + V (2 blocks) = 32 KiB
+#ifndef SA_TC_STAGES
+#define SA_TC_STAGES 5
+#endif
+constexpr int kStagesTC = SA_TC_STAGES;
+constexpr int kSBufs = 3;                     // S buffers: Q K^T runs up to two tiles ahead of the softmax
+constexpr int kTmemCols = 512;                // S buffers: columns 0 .. 3*64-1, O: the next 128
 constexpr int kThreads = 192;
 
 constexpr int kOffQ = 0;
 constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffKV = kOffP + kPBytes;
+constexpr int kOffKV = kOffP + 2 * kPBytes;
 constexpr int kOffBar = kOffKV + kStagesTC * kKVStage;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, tensor-memory address, alignment slack
 
@@ -57,10 +68,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 
 // Instruction descriptor for kind::f16: fp32 accumulate, bf16 A and B, A
-// K-major, B K-major or MN-major, M = 128, N = 128.
-__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
+// K-major, B K-major or MN-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major, int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) |
-           (static_cast<uint32_t>(kN >> 3) << 17) | (static_cast<uint32_t>(kM >> 4) << 24);
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kM >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -113,6 +124,37 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// N consecutive 32-bit columns (16, 32 or 64) of this thread's lane, one wait.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float *v) {
+    uint32_t r[N];
+    if constexpr (N == 16) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr));
+    } else {
+#pragma unroll
+        for (int h = 0; h < N / 32; ++h)
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                : "=r"(r[32 * h + 0]), "=r"(r[32 * h + 1]), "=r"(r[32 * h + 2]), "=r"(r[32 * h + 3]),
+                  "=r"(r[32 * h + 4]), "=r"(r[32 * h + 5]), "=r"(r[32 * h + 6]), "=r"(r[32 * h + 7]),
+                  "=r"(r[32 * h + 8]), "=r"(r[32 * h + 9]), "=r"(r[32 * h + 10]), "=r"(r[32 * h + 11]),
+                  "=r"(r[32 * h + 12]), "=r"(r[32 * h + 13]), "=r"(r[32 * h + 14]), "=r"(r[32 * h + 15]),
+                  "=r"(r[32 * h + 16]), "=r"(r[32 * h + 17]), "=r"(r[32 * h + 18]), "=r"(r[32 * h + 19]),
+                  "=r"(r[32 * h + 20]), "=r"(r[32 * h + 21]), "=r"(r[32 * h + 22]), "=r"(r[32 * h + 23]),
+                  "=r"(r[32 * h + 24]), "=r"(r[32 * h + 25]), "=r"(r[32 * h + 26]), "=r"(r[32 * h + 27]),
+                  "=r"(r[32 * h + 28]), "=r"(r[32 * h + 29]), "=r"(r[32 * h + 30]), "=r"(r[32 * h + 31])
+                : "r"(taddr + 32 * h));
+    }
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 struct PrefixParams {
     const uint16_t *q;
     const int32_t *block_table;
@@ -139,15 +181,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    uint64_t *kv_full = bars;           // [2] K/V tile landed
-    uint64_t *kv_empty = bars + 2;      // [2] K/V stage free again
-    uint64_t *q_full = bars + 4;        // Q rows written
-    uint64_t *s_full = bars + 5;        // [2] S buffer holds Q K^T of a tile
-    uint64_t *p_full = bars + 7;        // P written (and its S buffer read)
-    uint64_t *p_free = bars + 8;        // P V finished: P free, O up to date
-    uint64_t *mma_done = bars + 9;      // every MMA finished (before freeing tensor memory)
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + 10);
-    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(bars + 11);
+    uint64_t *kv_full = bars;                   // [kStagesTC] K/V tile landed
+    uint64_t *kv_empty = bars + kStagesTC;      // [kStagesTC] K/V stage free again
+    uint64_t *q_full = bars + 2 * kStagesTC;    // Q rows written
+    uint64_t *s_full = q_full + 1;              // [kSBufs] S buffer holds Q K^T of a tile
+    uint64_t *p_full = s_full + kSBufs;         // [2] P buffer written (and its S buffer read)
+    uint64_t *p_free = p_full + 2;              // [2] P V of that buffer finished (O up to date with it)
+    uint64_t *mma_done = p_free + 2;            // every MMA finished (before freeing tensor memory)
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(mma_done + 1);
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(mma_done + 2);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -208,10 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&kv_empty[s], 1);
         }
         mbar_init(q_full, kM);
-        mbar_init(&s_full[0], 1);
-        mbar_init(&s_full[1], 1);
-        mbar_init(p_full, kM);
-        mbar_init(p_free, 1);
+        for (int b = 0; b < kSBufs; ++b) mbar_init(&s_full[b], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&p_full[b], kM);
+            mbar_init(&p_free[b], 1);
+        }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -227,44 +270,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o = tmem + 2 * kN;  // S buffers at columns 0 and kN
+    const uint32_t tmem_o = tmem + kSBufs * kN;  // S buffers at columns 0, kN, 2 kN; O after them
 
     const uint32_t sQ = smem_u32(smem + kOffQ), sP = smem_u32(smem + kOffP), sKV = smem_u32(smem + kOffKV);
 
     if (warp < 4) {
-        // ================= softmax / epilogue warps: thread t owns row t
+        // ================= softmax / epilogue warps: thread t owns tensor-memory
+        // lane t. With at most 32 rows (sequence mode), every row is held by
+        // four lanes, one in each softmax warp (the Q tile holds four copies of
+        // the rows), and copy c takes keys [16c, 16c + 16) of every tile: a
+        // warp's per-tile softmax work is four times smaller. The P rows of a
+        // copy are zero outside its keys, so P V sums each copy's keys into its
+        // own lanes of O, with its own running max; the epilogue merges the
+        // four copies of each row.
+        const int rf = (P.seq_mode && row_count - row0 <= kM / 4) ? 4 : 1;  // copies per row
+        const int rpc = kM / rf;                                           // rows per copy
         const int t = tid;
-        const int r = row0 + t;
+        const int cp = t / rpc;
+        auto row_of = [&](int rr, int32_t &token, int32_t &hl, int32_t &limit, int32_t &slot) {
+            if (!P.seq_mode) {
+                const int32_t *rrow = P.run_rows + static_cast<int64_t>(rows_begin + rr) * 4;
+                token = rrow[0];
+                hl = rrow[1];
+                limit = rrow[2];
+                slot = rrow[3] + chunk;
+            } else {
+                token = seq_qstart + rr / P.G;
+                hl = rr % P.G;
+                limit = key_end - seq_n + rr / P.G;
+                slot = chunk;
+            }
+        };
+        const int r = row0 + t % rpc;
         const bool valid = r < row_count;
         const bool warp_valid = __any_sync(0xffffffffu, valid);  // warps without rows skip the softmax
         int32_t token = 0, hl = 0, limit = -1, slot = 0;
-        if (valid) {
-            if (!P.seq_mode) {
-                const int32_t *rr = P.run_rows + static_cast<int64_t>(rows_begin + r) * 4;
-                token = rr[0];
-                hl = rr[1];
-                limit = rr[2];
-                slot = rr[3] + chunk;
-            } else {
-                token = seq_qstart + r / P.G;
-                hl = r % P.G;
-                limit = key_end - seq_n + r / P.G;
-                slot = chunk;
-            }
-        }
-        if (!warp_valid) {  // P rows of rows that do not exist stay zero
+        if (valid) row_of(r, token, hl, limit, slot);
+        // P rows start at zero in both buffers (a copy writes only its own keys)
 #pragma unroll
-            for (int c = 0; c < kN / 8; ++c)
-                *reinterpret_cast<uint4 *>(smem + kOffP + (c >> 3) * kSub + sw128_offset(t, c & 7)) = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < kN / 8; ++c) {
+            *reinterpret_cast<uint4 *>(smem + kOffP + sw128_offset(t, c)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(smem + kOffP + kPBytes + sw128_offset(t, c)) = make_uint4(0, 0, 0, 0);
         }
-        // Q row t -> shared memory, 128-byte swizzled K-major (two 64-column blocks)
+        // Q row of lane t -> shared memory, 128-byte swizzled K-major (two 64-column blocks)
         {
             const uint4 *src = reinterpret_cast<const uint4 *>(
                 P.q + (static_cast<int64_t>(token) * P.Hq + g * P.G + hl) * kHeadDim);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const uint4 w = valid ? src[c] : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(smem + kOffQ + (c >> 3) * kSub + sw128_offset(t, c & 7)) = w;
+                *reinterpret_cast<uint4 *>(smem + kOffQ + (c >> 3) * kRowBlk + sw128_offset(t, c & 7)) = w;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(q_full);
@@ -272,69 +327,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         float m_ref = -INFINITY, lsum = 0.f;
         bool ok = true;
-        for (int i = 0; i < n_kv && ok; ++i) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[i & 1], (i >> 1) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            const int pos0 = pc_lo * kPageSize + i * kN;
-            if (!warp_valid) {
-                if (i > 0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(p_free, (i - 1) & 1));
-                    if (!ok) break;
-                }
-                if (pos0 + t >= key_end) {  // keys past the end may hold stale data: zero their V row
-                    uint8_t *vrow = smem + kOffKV + (i % kStagesTC) * kKVStage + 2 * kSub + t * 128;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        *reinterpret_cast<uint4 *>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(vrow + kSub + c * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                tc_fence_before();
-                mbar_arrive(p_full);
-                continue;
-            }
-            const uint32_t tmem_s = tmem + (i & 1) * kN;
-            float x[kN];
-            const bool whole = pos0 + kN - 1 <= limit;  // no key of this tile is masked for row t
-#pragma unroll
-            for (int c = 0; c < kN / 32; ++c) {
-                float v[32];
-                tmem_ld32(tmem_s + lane_base + c * 32, v);
-                if (whole) {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) x[c * 32 + k] = v[k] * P.qscale;
-                } else {
-#pragma unroll
-                    for (int k = 0; k < 32; ++k)
-                        x[c * 32 + k] = pos0 + c * 32 + k <= limit ? v[k] * P.qscale : -INFINITY;
-                }
-            }
-            float tmax = -INFINITY;
-#pragma unroll
-            for (int k = 0; k < kN; ++k) tmax = fmaxf(tmax, x[k]);
-            // move the reference max only when it grows by more than 2^8, so
-            // that tensor-memory O is rarely rescaled (p stays below 256)
-            const bool grow = tmax > m_ref + 8.f;
-            const float m_new = grow ? tmax : m_ref;
-            const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;  // 0 when m_ref was -inf
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            // probabilities, packed to bf16 pairs while the tensor cores finish P V
-            uint32_t pw[kN / 2];
-            float psum = 0.f;
-#pragma unroll
-            for (int k = 0; k < kN / 2; ++k) {
-                const float a = exp2f(x[2 * k] - m_use), b = exp2f(x[2 * k + 1] - m_use);
-                psum += a + b;
-                const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-                pw[k] = *reinterpret_cast<const uint32_t *>(&h);
-            }
-            if (i > 0) {  // P V of the previous tile must be done before P and O change
-                ok = __all_sync(0xffffffffu, mbar_wait(p_free, (i - 1) & 1));
+        // P buffer b = i & 1 is free again once P V of tile i - 2 has run;
+        // that P V is the ((i - 2) >> 1)-th commit on p_free[b]
+        auto wait_pv = [&](int j) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(&p_free[j & 1], (j >> 1) & 1));
+        };
+        auto softmax_tiles = [&](auto kpc_tag) {
+            constexpr int KPC = decltype(kpc_tag)::value;  // keys of a tile this lane's copy takes
+            const int koff = cp * KPC;
+            for (int i = 0; i < n_kv && ok; ++i) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[i % kSBufs], (i / kSBufs) & 1));
                 if (!ok) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, grow)) {
+                const int pos0 = pc_lo * kPageSize + i * kN;
+                uint8_t *pbuf = smem + kOffP + (i & 1) * kPBytes;
+                uint8_t *vstage = smem + kOffKV + (i % kStagesTC) * kKVStage + 2 * kKVBlk;
+                if (!warp_valid) {
+                    // arrivals on p_full[i & 1] must not run ahead of the phase that
+                    // tile i - 2 completes there: wait, like the rows with data do,
+                    // until P V of tile i - 2 (which follows that phase) is done
+                    if (i >= 2) {
+                        ok = wait_pv(i - 2);
+                        if (!ok) break;
+                    }
+                    if (t < kN && pos0 + t >= key_end) {  // keys past the end may hold stale data: zero their V row
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            *reinterpret_cast<uint4 *>(vstage + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(vstage + kKVBlk + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    tc_fence_before();
+                    mbar_arrive(&p_full[i & 1]);
+                    continue;
+                }
+                float x[KPC];
+                tmem_ld_cols<KPC>(tmem + (i % kSBufs) * kN + koff + lane_base, x);
+                const bool whole = pos0 + kN - 1 <= limit;  // no key of this tile is masked for this row
+#pragma unroll
+                for (int k = 0; k < KPC; ++k)
+                    x[k] = (whole || pos0 + koff + k <= limit) ? x[k] * P.qscale : -INFINITY;
+                // row max as a tree (independent partial maxima, short dependency chains)
+                float mx[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mx[k] = x[k];
+#pragma unroll
+                for (int k = 8; k < KPC; ++k) mx[k & 7] = fmaxf(mx[k & 7], x[k]);
+                const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                // move the reference max only when it grows by more than 2^8, so
+                // that tensor-memory O is rarely rescaled (p stays below 256)
+                const bool grow = tmax > m_ref + 8.f;
+                const float m_new = grow ? tmax : m_ref;
+                const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;  // 0 when m_ref was -inf
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                // probabilities, packed to bf16 pairs while the tensor cores run P V
+                uint32_t pw[KPC / 2];
+                float ps[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+#pragma unroll
+                for (int k = 0; k < KPC / 2; ++k) {
+                    const float a = exp2f(x[2 * k] - m_use), b = exp2f(x[2 * k + 1] - m_use);
+                    ps[k & 7] += a + b;
+                    pw[k] = pack_bf16x2(a, b);
+                }
+                const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                if (i >= 2) {  // P V of tile i - 2 must be done before its P buffer is rewritten
+                    ok = wait_pv(i - 2);
+                    if (!ok) break;
+                }
+                if (i >= 1 && __any_sync(0xffffffffu, grow)) {  // O must hold every earlier P V before it is rescaled
+                    ok = wait_pv(i - 1);
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
                     for (int c = 0; c < kHeadDim / 32; ++c) {
                         float o[32];
@@ -344,46 +411,107 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st32(tmem_o + lane_base + c * 32, o);
                     }
                 }
-            }
-            lsum = lsum * alpha + psum;
-            m_ref = m_new;
-            // P row t -> shared memory (bf16, 128-byte swizzled K-major)
+                lsum = lsum * alpha + psum;
+                m_ref = m_new;
+                // this copy's keys of P row t -> shared memory (bf16, 128-byte swizzled K-major)
 #pragma unroll
-            for (int c = 0; c < kN / 8; ++c)
-                *reinterpret_cast<uint4 *>(smem + kOffP + (c >> 3) * kSub + sw128_offset(t, c & 7)) =
-                    make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-            if (pos0 + t >= key_end) {  // keys past the end may hold stale data: zero their V row
-                uint8_t *vrow = smem + kOffKV + (i % kStagesTC) * kKVStage + 2 * kSub + t * 128;
+                for (int c = 0; c < KPC / 8; ++c)
+                    *reinterpret_cast<uint4 *>(pbuf + sw128_offset(t, koff / 8 + c)) =
+                        make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+                if (t < kN && pos0 + t >= key_end) {  // keys past the end may hold stale data: zero their V row
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    *reinterpret_cast<uint4 *>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(vrow + kSub + c * 16) = make_uint4(0, 0, 0, 0);
+                    for (int c = 0; c < 8; ++c) {
+                        *reinterpret_cast<uint4 *>(vstage + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(vstage + kKVBlk + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                    }
                 }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tc_fence_before();
+                mbar_arrive(&p_full[i & 1]);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc_fence_before();
-            mbar_arrive(p_full);
-        }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(p_free, (n_kv - 1) & 1));  // the last P V
+        };
+        if (rf == 4) softmax_tiles(std::integral_constant<int, kN / 4>{});
+        else softmax_tiles(std::integral_constant<int, kN>{});
+        if (ok && n_kv > 0) ok = wait_pv(n_kv - 1);  // the last P V (every earlier one before it)
         if (!ok) {
             *abort_flag = 1;
             if (lane == 0) flag_error(P.err, kErrBitTimeout);
-        } else if (warp_valid) {
+        } else if (rf == 1) {
+            if (warp_valid) {  // epilogue with one copy per row
+                tc_fence_after();
+                // epilogue: fp32 partial (O, m, l) of this row for the merge
+                const int64_t orow = static_cast<int64_t>(token) * P.Hq + g * P.G + hl;
+                const int64_t wi = static_cast<int64_t>(slot) * P.n_rows_total + orow;
+#pragma unroll
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem_o + lane_base + c * 32, o);
+                    if (valid) {
+                        float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + c * 32);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                    }
+                }
+                if (valid) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(m_ref, lsum);
+            }
+        }
+        if (rf != 1) {
+            // epilogue with four copies: stage every lane's O row, max and sum in
+            // shared memory (the K/V stages are idle now), then thread t merges
+            // columns [32 (t / 32), +32) of row t % 32 over the copies. Every
+            // softmax warp reaches the barrier, whatever its status.
             tc_fence_after();
-            // epilogue: fp32 partial (O, m, l) of this row for the merge
-            const int64_t orow = static_cast<int64_t>(token) * P.Hq + g * P.G + hl;
-            const int64_t wi = static_cast<int64_t>(slot) * P.n_rows_total + orow;
+            constexpr int kOStride = kHeadDim + 4;  // floats; breaks bank conflicts
+            float *ost = reinterpret_cast<float *>(smem + kOffKV);
+            float *mls = ost + kM * kOStride;
 #pragma unroll
             for (int c = 0; c < kHeadDim / 32; ++c) {
                 float o[32];
                 tmem_ld32(tmem_o + lane_base + c * 32, o);
-                if (valid) {
-                    float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + c * 32);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                }
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<float4 *>(ost + t * kOStride + c * 32 + 4 * k) =
+                        make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
             }
-            if (valid) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(m_ref, lsum);
+            mls[2 * t] = m_ref;
+            mls[2 * t + 1] = lsum;
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps only
+            const int rl = t % rpc, q4 = t / rpc;
+            const int rr = row0 + rl;
+            if (ok && rr < row_count) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (mls[2 * (c * rpc + rl) + 1] > 0.f) M = fmaxf(M, mls[2 * (c * rpc + rl)]);
+                float L = 0.f;
+                float4 o[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float lc = mls[2 * (c * rpc + rl) + 1];
+                    if (lc > 0.f) {
+                        const float wgt = exp2f(mls[2 * (c * rpc + rl)] - M);
+                        L += lc * wgt;
+                        const float *src = ost + (c * rpc + rl) * kOStride + q4 * 32;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float4 v = *reinterpret_cast<const float4 *>(src + 4 * k);
+                            o[k].x += v.x * wgt;
+                            o[k].y += v.y * wgt;
+                            o[k].z += v.z * wgt;
+                            o[k].w += v.w * wgt;
+                        }
+                    }
+                }
+                int32_t tk, hh, lim, sl;
+                row_of(rr, tk, hh, lim, sl);
+                const int64_t wi = static_cast<int64_t>(sl) * P.n_rows_total + static_cast<int64_t>(tk) * P.Hq + g * P.G + hh;
+                float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + q4 * 32);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) dst[k] = o[k];
+                if (q4 == 0) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(M, L);
+            }
         }
     } else if (warp == 4) {
         // ================= TMA producer
@@ -398,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 if (*abort_flag) break;
-                const int page = pc_lo + (i >> 1);
+                const int page = pc_lo + i / (kPageSize / kN);
                 const int pid = P.block_table[static_cast<int64_t>(member) * P.max_pages + page];
                 // (sequence mode: the last tile may reach past the sequence's keys; the
                 // rows past the end are zeroed in shared memory before P V)
@@ -407,12 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     flag_error(P.err, kErrBitPageOOB);
                     mbar_arrive(&kv_full[s]);
                 } else {
-                    const int y = (pid * P.Hkv + g) * kPageSize + (i & 1) * kN;
+                    const int y = (pid * P.Hkv + g) * kPageSize + (i % (kPageSize / kN)) * kN;
                     mbar_arrive_expect_tx(&kv_full[s], kKVStage);
                     tma_load_2d(dst, &tmk, &kv_full[s], 0, y, policy);
-                    tma_load_2d(dst + kSub, &tmk, &kv_full[s], 64, y, policy);
-                    tma_load_2d(dst + 2 * kSub, &tmv, &kv_full[s], 0, y, policy);
-                    tma_load_2d(dst + 3 * kSub, &tmv, &kv_full[s], 64, y, policy);
+                    tma_load_2d(dst + kKVBlk, &tmk, &kv_full[s], 64, y, policy);
+                    tma_load_2d(dst + 2 * kKVBlk, &tmv, &kv_full[s], 0, y, policy);
+                    tma_load_2d(dst + 3 * kKVBlk, &tmv, &kv_full[s], 64, y, policy);
                 }
                 ++issued;
             }
@@ -421,40 +549,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (void)mbar_wait(&kv_full[i % kStagesTC], (i / kStagesTC) & 1);
         }
     } else {
-        // ================= MMA issuer (one thread). Order: QK(0), then for
-        // each tile i >= 1: QK(i) into the other S buffer, PV(i-1).
+        // ================= MMA issuer (one thread). Q K^T of tile j goes into S
+        // buffer j % kSBufs once the softmax has read that buffer's previous
+        // tile (its P V has been issued, so its P was written); P V of tile j
+        // once the softmax has written P(j). Q K^T therefore runs up to
+        // kSBufs - 1 tiles ahead of the softmax.
         if (lane == 0) {
-            constexpr uint32_t kIdQK = idesc_bf16(false), kIdPV = idesc_bf16(true);
+            constexpr uint32_t kIdQK = idesc_bf16(false, kN), kIdPV = idesc_bf16(true, kHeadDim);
+            // Descriptors are linear in the start address (its 14-bit field holds
+            // address / 16 and shared-memory offsets stay below 256 KiB), so every
+            // operand's descriptor is a base plus a byte offset / 16, computed
+            // once: a lone issuing thread pays for each dependent instruction.
+            const uint64_t dQ = smem_desc(sQ, 16, 1024), dK = smem_desc(sKV, 16, 1024);
+            const uint64_t dP = smem_desc(sP, 16, 1024), dV = smem_desc(sKV + 2 * kKVBlk, kKVBlk, 1024);
             bool ok = mbar_wait(q_full, 0);
-            for (int i = 0; ok && i <= n_kv; ++i) {
-                if (i < n_kv) {  // S[i&1] = Q K(i)^T; S[i&1] was last read by softmax(i-2)
-                    const int s = i % kStagesTC;
-                    ok = mbar_wait(&kv_full[s], (i / kStagesTC) & 1);
+            int qk = 0;
+            for (int j = 0; ok && j < n_kv; ++j) {
+                for (; ok && qk < n_kv && qk < j + kSBufs; ++qk) {
+                    const int s = qk % kStagesTC;
+                    ok = mbar_wait(&kv_full[s], (qk / kStagesTC) & 1);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t sK = sKV + s * kKVStage;
+                    const uint64_t dKs = dK + ((s * kKVStage) >> 4);
+                    const uint32_t d_s = tmem + (qk % kSBufs) * kN;
 #pragma unroll
-                    for (int k = 0; k < kHeadDim / 16; ++k) {
-                        const uint64_t a = smem_desc(sQ + (k >> 2) * kSub + (k & 3) * 32, 16, 1024);
-                        const uint64_t b = smem_desc(sK + (k >> 2) * kSub + (k & 3) * 32, 16, 1024);
-                        mma_bf16(tmem + (i & 1) * kN, a, b, kIdQK, k > 0);
-                    }
-                    mma_commit(&s_full[i & 1]);
+                    for (int k = 0; k < kHeadDim / 16; ++k)
+                        mma_bf16(d_s, dQ + (((k >> 2) * kRowBlk + (k & 3) * 32) >> 4),
+                                 dKs + (((k >> 2) * kKVBlk + (k & 3) * 32) >> 4), kIdQK, k > 0);
+                    mma_commit(&s_full[qk % kSBufs]);
                 }
-                if (i > 0) {  // O += P(i-1) V(i-1) once the softmax has written P(i-1)
-                    ok = mbar_wait(p_full, (i - 1) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t sV = sKV + ((i - 1) % kStagesTC) * kKVStage + 2 * kSub;
+                if (!ok) break;
+                // O += P(j) V(j) once the softmax has written P(j)
+                ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dVs = dV + (((j % kStagesTC) * kKVStage) >> 4);
+                const uint64_t dPj = dP + (((j & 1) * kPBytes) >> 4);
 #pragma unroll
-                    for (int k = 0; k < kN / 16; ++k) {
-                        const uint64_t a = smem_desc(sP + (k >> 2) * kSub + (k & 3) * 32, 16, 1024);
-                        const uint64_t b = smem_desc(sV + k * 16 * 128, kSub, 1024);
-                        mma_bf16(tmem_o, a, b, kIdPV, i > 1 || k > 0);
-                    }
-                    mma_commit(&kv_empty[(i - 1) % kStagesTC]);
-                    mma_commit(p_free);
-                }
+                for (int k = 0; k < kN / 16; ++k)
+                    mma_bf16(tmem_o, dPj + ((k * 32) >> 4), dVs + ((k * 16 * 128) >> 4), kIdPV, j > 0 || k > 0);
+                mma_commit(&kv_empty[j % kStagesTC]);
+                mma_commit(&p_free[j & 1]);
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -539,6 +674,7 @@ cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t
     return cudaGetLastError();
 }
 
-int prefix_tile_rows() { return kN; }
+int prefix_tile_rows() { return kM; }
+int prefix_key_tile() { return kN; }
 
 }  // namespace sa
