@@ -95,6 +95,8 @@ SA_API int sa_device_sm_count(void);
  *   seq_lens, q_lens  device int32 [num_seqs]; seq_lens include the new tokens
  * Writing into a page that another sequence also indexes is the caller's
  * responsibility (copy-on-write is the scheduler's job); it is not checked.
+ * The kernel allows the next kernel on the stream to start early
+ * (programmatic dependent launch); sa_paged_attn uses that, see there.
  */
 SA_API int sa_kv_append(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_new,
                  uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,
@@ -160,6 +162,12 @@ SA_API size_t sa_paged_attn_workspace_size(const sa_dims *dims, const sa_plan *p
  * Accumulation is fp32; out is rounded to bf16 (nearest even).
  * Requires 0 <= q_lens[b] <= min(seq_lens[b], max_q_len). Entries of
  * block_table past a sequence's last page are never read.
+ * Ordering: the call's kernels are launched as programmatic dependents, so
+ * when the previous kernel on the stream is sa_kv_append (which allows an
+ * early start) they begin while it runs. Before waiting for it they read only
+ * the lengths and the block tables (which sa_kv_append does not write); q and
+ * the pages are read after it has completed. After any other kernel, which
+ * does not allow an early start, the call starts when that kernel ends.
  */
 SA_API int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_pages,
                   const uint16_t *v_pages, const int32_t *block_table,
