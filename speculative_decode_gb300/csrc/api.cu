@@ -10,6 +10,7 @@
 
 #include "internal.h"
 #include "plan.h"
+#include "tc_work.cuh"
 
 namespace sa {
 
@@ -65,12 +66,8 @@ struct SplitConfig {
 constexpr int kPieceSlots = 8;
 // Sequences with at least this many query rows per KV head (G heads x new
 // tokens: q_len = k+1 verification) are a dense contraction: without a plan
-// they go to the tensor cores, in chunks of kTcChunkPages pages.
+// they go to the tensor cores (persistent CTAs over an even cut of their tiles).
 constexpr int kTcMinRows = 16;
-#ifndef SA_TC_CHUNK_PAGES
-#define SA_TC_CHUNK_PAGES 8
-#endif
-constexpr int kTcChunkPages = SA_TC_CHUNK_PAGES;
 
 SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     SplitConfig c{};
@@ -80,16 +77,9 @@ SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     c.nrb = (rows + c.R - 1) / c.R;
     const int max_tiles = std::max(1, d.max_pages_per_seq) * (kPageSize / split_tile_tokens());
     c.piece_slots = std::min(kPieceSlots, max_tiles);
-    c.tc = SeqTcConfig{0, 0, 0, 0};
-    if (plan == nullptr && G * std::max(1, d.max_q_len) >= kTcMinRows) {
-        c.tc.min_rows = kTcMinRows;
-        c.tc.mtiles = (rows + prefix_tile_rows() - 1) / prefix_tile_rows();
-        // at most 8 chunks per sequence, so that a row has at most 16 partials to merge
-        const int mp = std::max(1, d.max_pages_per_seq);
-        c.tc.chunk_pages = std::max(kTcChunkPages, (mp + 7) / 8);
-        c.tc.max_chunks = (mp + c.tc.chunk_pages - 1) / c.tc.chunk_pages;
-    }
-    c.run_slots = plan ? plan_run_slots(plan) : c.tc.max_chunks;
+    c.tc = SeqTcConfig{0, 0};  // grid is set at launch (one CTA per SM)
+    if (plan == nullptr && G * std::max(1, d.max_q_len) >= kTcMinRows) c.tc.min_rows = kTcMinRows;
+    c.run_slots = plan ? plan_run_slots(plan) : (c.tc.min_rows > 0 ? kTcMaxPieces : 0);
     c.n_slots = c.run_slots + c.piece_slots;
     return c;
 }
@@ -255,7 +245,7 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
                              block_table, s) != cudaSuccess)
             return SA_ERR_CUDA;
         if (c.tc.min_rows > 0 &&
-            launch_seq_tc(d, c.tc, q, pk, pv, scale, ws_acc, ws_ml, rows_total, err_flag,
+            launch_seq_tc(d, SeqTcConfig{c.tc.min_rows, sms}, q, pk, pv, scale, ws_acc, ws_ml, rows_total, err_flag,
                           block_table, seq_lens, q_lens, s) != cudaSuccess)
             return SA_ERR_CUDA;
     }
@@ -285,7 +275,7 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     p.n_row_blocks = c.nrb;
     p.piece_slots = c.piece_slots;
     p.tc_min_rows = c.tc.min_rows;
-    p.tc_chunk_pages = c.tc.chunk_pages > 0 ? c.tc.chunk_pages : 1;
+    p.tc_grid = sms;
     p.slot_base = c.run_slots;
     p.n_rows_total = static_cast<int32_t>(rows_total);
     p.qscale = scale * 1.4426950408889634f;
@@ -334,8 +324,8 @@ int sa_spec_verify_greedy(const float *logits, const int32_t *candidates, const 
     if (sms <= 0) return SA_ERR_CUDA;
     const int64_t rows = static_cast<int64_t>(num_seqs) * (k_max + 1);
     const int64_t max_chunks = (static_cast<int64_t>(vocab) + 1023) / 1024;
-    // about four CTAs per SM in total, each chunk a multiple of 1024 elements
-    int64_t n_chunks = std::min<int64_t>(max_chunks, std::max<int64_t>(1, (4 * sms + rows - 1) / rows));
+    // about five CTAs per SM in total (one wave), each chunk a multiple of 1024 elements
+    int64_t n_chunks = std::min<int64_t>(max_chunks, std::max<int64_t>(1, (5 * sms + rows - 1) / rows));
     const int64_t chunk = ((vocab + n_chunks - 1) / n_chunks + 1023) / 1024 * 1024;
     n_chunks = (vocab + chunk - 1) / chunk;
     const int64_t parts = rows * max_chunks;

@@ -35,6 +35,7 @@
 //  * Every wait on a barrier is bounded (common.cuh); on timeout the warp
 //    flags SA_ERR_TIMEOUT, drains its copies in flight and leaves.
 #include "common.cuh"
+#include "tc_work.cuh"
 
 namespace sa {
 
@@ -89,6 +90,7 @@ struct Piece {
 
 struct SeqInfo {
     int T, n, skip_tok, tiles, nrb, runs;
+    int tc;  // attended on the tensor cores (runs are then per segment: tc_work.cuh)
 };
 
 #ifndef SA_SPLIT_SCALAR_FMA
@@ -169,6 +171,7 @@ __device__ __forceinline__ SeqInfo seq_info_from(const SplitParams &P, int T, in
     s.nrb = 0;
     s.skip_tok = 0;
     s.runs = 0;
+    s.tc = 0;
     if (s.n <= 0) return s;
     const int npages = (s.T + kPageSize - 1) / kPageSize;
     if (s.n > s.T || s.n > P.max_q_len || npages > P.max_pages) {
@@ -177,9 +180,11 @@ __device__ __forceinline__ SeqInfo seq_info_from(const SplitParams &P, int T, in
     }
     int skip = skip_pages;
     int runs = run_slots;
+    s.tc = 0;
     if (P.tc_min_rows > 0 && P.G * s.n >= P.tc_min_rows) {  // attended on the tensor cores
         skip = npages;
-        runs = (npages + P.tc_chunk_pages - 1) / P.tc_chunk_pages;
+        runs = 0;
+        s.tc = 1;
     }
     s.runs = runs;
     s.skip_tok = skip * kPageSize;
@@ -327,6 +332,7 @@ __device__ __forceinline__ SeqInfo shfl_seq_info(SeqInfo si, int src) {
     si.tiles = __shfl_sync(0xffffffffu, si.tiles, src);
     si.nrb = __shfl_sync(0xffffffffu, si.nrb, src);
     si.runs = __shfl_sync(0xffffffffu, si.runs, src);
+    si.tc = __shfl_sync(0xffffffffu, si.tc, src);
     return si;
 }
 
@@ -343,7 +349,7 @@ struct WorkScan {
 
 template <int R>
 __device__ __forceinline__ SeqInfo seq_of(const SplitParams &P, int b, bool flag) {
-    if (b >= P.B) return SeqInfo{0, 0, 0, 0, 0, 0};
+    if (b >= P.B) return SeqInfo{0, 0, 0, 0, 0, 0, 0};
     return seq_info<R>(P, b, flag);
 }
 
@@ -864,6 +870,39 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
     }
 }
 
+// Pieces the tensor-core sequence mode cut segment (bt, kvh, mt) into: a scan
+// over the sequences gives the tile sequence's total, its longest segment and
+// the segment's first unit, and the same cut as the tensor-core kernel's.
+template <int R>
+__device__ int tc_pieces(const SplitParams &P, int lane, int bt, int kvh, int mt) {
+    int total = 0, max_tiles = 0, u0 = 0;
+    TcSeq wb{0, 0, 0};
+#pragma unroll 1
+    for (int base = 0; base < P.B; base += 32) {
+        const int b = base + lane;
+        const int T = b < P.B ? P.seq_lens[b] : 0, n = b < P.B ? P.q_lens[b] : 0;
+        const TcSeq w = tc_seq(T, n, P.G, P.Hkv, P.max_q_len, P.max_pages, P.tc_min_rows);
+        int ui = w.units;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, ui, o);
+            if (lane >= o) ui += a;
+        }
+        const int src = bt - base;
+        if (src >= 0 && src < 32) {
+            u0 = total + __shfl_sync(0xffffffffu, ui - w.units, src);
+            wb.tiles = __shfl_sync(0xffffffffu, w.tiles, src);
+            wb.mtiles = __shfl_sync(0xffffffffu, w.mtiles, src);
+        }
+        total += __shfl_sync(0xffffffffu, ui, 31);
+        max_tiles = max(max_tiles, static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(w.tiles))));
+    }
+    if (wb.tiles == 0) return 0;
+    const TcRanges rg = make_tc_ranges(total, P.tc_grid, max_tiles);
+    const int s0 = u0 + (kvh * wb.mtiles + mt) * wb.tiles;
+    return rg.range_of(s0 + wb.tiles - 1) - rg.range_of(s0) + 1;
+}
+
 // ---- the combine pass: one warp per (sequence, KV head, row block, group of
 // four rows) merges the partials of a segment that was cut into pieces or
 // has tensor-core partials. It repeats the split kernel's scan (before the
@@ -907,14 +946,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32, SA_COMBINE_MIN_CTAS) combi
         segment_ranges(rg, pos + (kvh * si.nrb + rb) * segment_units(si), si.tiles, first, last);
         pieces = last - first + 1;
     }
-    if (si.runs == 0 && pieces <= 1) return;  // written directly by the split kernel
+    int runs = si.runs;
+    if (si.tc) runs = tc_pieces<R>(P, lane, bt, kvh, (rb * R) / kTcRowTile);
+    if (runs == 0 && pieces <= 1) return;  // written directly by the split kernel
     Piece U{};
     U.b = bt;
     U.kvh = kvh;
     U.rb = rb;
     U.qstart = qs;
     U.pieces = pieces;
-    U.runs = si.runs;
+    U.runs = runs;
     U.nvr = nvr;
     // Pass 0 runs the merge on whatever the workspace holds now and stores
     // nothing: it brings the merge's instructions and address translations on

@@ -52,8 +52,8 @@ struct SplitParams {
     int32_t n_row_blocks;       // row blocks per (sequence, KV head) at max_q_len
     int32_t piece_slots;        // partial slots a segment's pieces may use
     int32_t tc_min_rows;        // > 0: sequences with >= this many rows per KV head were
-    int32_t tc_chunk_pages;     //   attended on the tensor cores in chunks of this many pages;
-                                //   the combine pass merges their partials
+    int32_t tc_grid;            //   attended on the tensor cores by this many persistent CTAs
+                                //   (tc_work.cuh); the combine pass merges their partials
     int32_t slot_base;          // first workspace slot used by pieces
     int32_t n_rows_total;       // total_q * Hq (row stride of a workspace slot)
     float qscale;               // scale * log2(e)

@@ -50,14 +50,13 @@ int prefix_key_tile();   // keys per K/V tile
 
 // Sequence mode of the tensor-core kernel: sequences with at least min_rows
 // query rows per KV head (G heads x new tokens, e.g. q_len = k+1 verification)
-// are attended entirely on the tensor cores, one work item per (sequence, KV
-// head, 128-row tile, chunk of chunk_pages pages); the split kernel only merges
-// their partials (slot = chunk index).
+// are attended entirely on the tensor cores by `grid` persistent CTAs, each
+// walking one contiguous range of the sequence of (sequence, KV head, 128-row
+// tile) segments' 64-key tiles (tc_work.cuh); the combine pass merges their
+// partials (up to kTcMaxPieces per segment).
 struct SeqTcConfig {
-    int min_rows;    // 0 disables the mode
-    int mtiles;      // 128-row tiles at max_q_len
-    int chunk_pages;
-    int max_chunks;  // ceil(max_pages_per_seq / chunk_pages)
+    int min_rows;  // 0 disables the mode
+    int grid;      // CTAs (one per SM)
 };
 cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t *q,
                           const CUtensorMap &tmk, const CUtensorMap &tmv, float scale,

@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "plan.h"
+#include "tc_work.cuh"
 
 namespace sa {
 
@@ -50,14 +51,19 @@ constexpr int kKVStage = 4 * kKVBlk;          // K (2 blocks) + V (2 blocks) = 3
 #endif
 constexpr int kStagesTC = SA_TC_STAGES;
 constexpr int kSBufs = 3;                     // S buffers: Q K^T runs up to two tiles ahead of the softmax
-constexpr int kTmemCols = 512;                // S buffers: columns 0 .. 3*64-1, O: the next 128
+constexpr int kTmemCols = 512;                // S buffers: columns 0 .. 3*64-1, two O buffers: the next 2*128
 constexpr int kThreads = 192;
 
 constexpr int kOffQ = 0;
 constexpr int kOffP = kOffQ + kQBytes;
 constexpr int kOffKV = kOffP + 2 * kPBytes;
 constexpr int kOffBar = kOffKV + kStagesTC * kKVStage;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, tensor-memory address, alignment slack
+constexpr int kOffML = kOffBar + 256;             // epilogue: (max, sum) of the 128 lanes
+constexpr int kOffStart = kOffML + kM * 2 * 4;    // sequence mode: where this CTA's range starts
+constexpr int kSmemBytes = kOffStart + 128 + 1024;  // + alignment slack
+
+static_assert(kN == kTcKeyTile && kM == kTcRowTile, "tile shapes shared with the combine pass");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 
 // ------------------------------------------------------------ tcgen05 helpers
 // Shared-memory matrix descriptor: start address, leading / stride byte
@@ -158,20 +164,92 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float *v) {
 struct PrefixParams {
     const uint16_t *q;
     const int32_t *block_table;
-    // plan mode: work items and rows from a shared-run plan
+    // plan mode: work items and rows from a shared-run plan (one item per CTA)
     const int32_t *run_desc;
     const int32_t *run_rows;
     const int32_t *tiles;
-    // sequence mode: one work item per (sequence, KV head, row tile, page chunk)
+    // sequence mode: the cut of the tile sequence (tc_work.cuh), one range per CTA
     const int32_t *seq_lens;
     const int32_t *q_lens;
-    int32_t seq_mode, B, max_q_len, total_q, min_rows, mtiles, max_chunks, chunk_pages;
+    int32_t seq_mode, B, max_q_len, total_q, min_rows;
     float *ws_acc;
     float *ws_ml;
     int32_t *err;
     int32_t Hq, Hkv, G, max_pages, num_pages;
     int64_t n_rows_total;
     float qscale;  // scale * log2(e)
+};
+
+// A piece: the tiles of one segment that this CTA attends.
+struct TcPiece {
+    int member;                       // block-table row whose pages are read
+    int g;                            // KV head
+    int row0, row_count, rows_begin;  // rows [row0, min(row0 + 128, row_count)) of the segment
+    int pc_lo;                        // page of tile 0
+    int t_lo, t_hi;                   // 64-key tiles [t_lo, t_hi) counted from page pc_lo
+    int key_end;                      // keys at or past this position are not in the cache
+    int seq_n, qstart;                // sequence mode: new tokens, packed row of the first
+    int slot;                         // sequence mode: partial slot; plan mode: page chunk
+};
+
+// Start of this CTA's range in sequence mode, found by warp 0 and shared.
+struct TcStart {
+    int has_work, b, qstart, seg, tile, unit, end;
+    TcRanges rg;
+};
+
+// The walk over the pieces of this CTA's range (sequence mode); every role
+// runs its own copy and they see the same pieces.
+struct TcCursor {
+    int b, qstart, seg, tile, unit, end, T, n;
+    TcSeq w;
+    TcRanges rg;
+
+    __device__ __forceinline__ void load(const PrefixParams &P) {
+        T = P.seq_lens[b];
+        n = P.q_lens[b];
+        w = tc_seq(T, n, P.G, P.Hkv, P.max_q_len, P.max_pages, P.min_rows);
+    }
+    __device__ __forceinline__ void init(const PrefixParams &P, const TcStart &s) {
+        b = s.b;
+        qstart = s.qstart;
+        seg = s.seg;
+        tile = s.tile;
+        unit = s.unit;
+        end = s.end;
+        rg = s.rg;
+        if (unit < end) load(P);
+    }
+    __device__ __forceinline__ bool next(const PrefixParams &P, TcPiece &pc) {
+        if (unit >= end) return false;
+        const int mt = seg % w.mtiles;
+        pc.member = b;
+        pc.g = seg / w.mtiles;
+        pc.row0 = mt * kTcRowTile;
+        pc.row_count = P.G * n;
+        pc.rows_begin = 0;
+        pc.pc_lo = 0;
+        pc.t_lo = tile;
+        pc.t_hi = min(w.tiles, tile + (end - unit));
+        pc.key_end = T;
+        pc.seq_n = n;
+        pc.qstart = qstart;
+        pc.slot = static_cast<int>(blockIdx.x) - rg.range_of(unit - tile);
+        unit += pc.t_hi - tile;
+        tile = pc.t_hi;
+        if (tile == w.tiles && unit < end) {  // the next segment (of the next tensor-core sequence)
+            tile = 0;
+            if (++seg == P.Hkv * w.mtiles) {
+                seg = 0;
+                do {
+                    qstart += max(0, n);
+                    ++b;
+                    load(P);
+                } while (w.units == 0 && b + 1 < P.B);
+            }
+        }
+        return true;
+    }
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -183,66 +261,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *kv_full = bars;                   // [kStagesTC] K/V tile landed
     uint64_t *kv_empty = bars + kStagesTC;      // [kStagesTC] K/V stage free again
-    uint64_t *q_full = bars + 2 * kStagesTC;    // Q rows written
+    uint64_t *q_full = bars + 2 * kStagesTC;    // Q rows of a piece written
     uint64_t *s_full = q_full + 1;              // [kSBufs] S buffer holds Q K^T of a tile
     uint64_t *p_full = s_full + kSBufs;         // [2] P buffer written (and its S buffer read)
     uint64_t *p_free = p_full + 2;              // [2] P V of that buffer finished (O up to date with it)
-    uint64_t *mma_done = p_free + 2;            // every MMA finished (before freeing tensor memory)
+    uint64_t *o_free = p_free + 2;              // [2] O buffer read by its piece's epilogue
+    uint64_t *mma_done = o_free + 2;            // every MMA finished (before freeing tensor memory)
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(mma_done + 1);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(mma_done + 2);
+    TcStart *start = reinterpret_cast<TcStart *>(smem + kOffStart);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
 
-    // ---- the work item
-    int g, row0, pc_lo, pc_hi, chunk, member, row_count, rows_begin = 0;
-    int key_end = 0x7fffffff;  // keys at or past this position are not in the cache
-    int seq_n = 0, seq_qstart = 0;
+    // ---- the work: plan mode, this CTA's item; sequence mode, this CTA's range
+    TcPiece plan_piece{};
     if (!P.seq_mode) {  // (run, KV head, 128-row tile, page chunk) from the plan
         const int32_t *it = P.tiles + static_cast<int64_t>(blockIdx.x) * kTileInts;
-        const int run = it[0];
-        g = it[1];
-        row0 = it[2];
-        pc_lo = it[3];
-        pc_hi = it[4];
-        chunk = it[5];
-        const int32_t *rd = P.run_desc + static_cast<int64_t>(run) * kRunDescInts;
-        rows_begin = rd[2];
-        row_count = rd[3];
-        member = rd[5];
-    } else {  // (sequence, KV head, 128-row tile, page chunk): rows = G heads x new tokens
-        int idx = blockIdx.x;
-        chunk = idx % P.max_chunks;
-        idx /= P.max_chunks;
-        const int mt = idx % P.mtiles;
-        idx /= P.mtiles;
-        g = idx % P.Hkv;
-        member = idx / P.Hkv;
-        const int T = P.seq_lens[member];
-        seq_n = P.q_lens[member];
-        const int npages = (T + kPageSize - 1) / kPageSize;
-        row_count = P.G * seq_n;
-        row0 = mt * kM;
-        pc_lo = chunk * P.chunk_pages;
-        pc_hi = min(npages, pc_lo + P.chunk_pages);
-        key_end = T;
-        // packed query row of the sequence's first new token (block reduction)
-        __shared__ int red[kThreads / 32];
-        int part = 0;
-        for (int k = tid; k < member; k += kThreads) part += P.q_lens[k];
+        const int32_t *rd = P.run_desc + static_cast<int64_t>(it[0]) * kRunDescInts;
+        plan_piece.member = rd[5];
+        plan_piece.g = it[1];
+        plan_piece.row0 = it[2];
+        plan_piece.row_count = rd[3];
+        plan_piece.rows_begin = rd[2];
+        plan_piece.pc_lo = it[3];
+        plan_piece.t_lo = 0;
+        plan_piece.t_hi = ((it[4] - it[3]) * kPageSize + kN - 1) / kN;
+        plan_piece.key_end = 0x7fffffff;
+        plan_piece.slot = it[5];
+    } else if (warp == 0) {
+        // lane-per-sequence scan: the total work, the longest segment, the queries
+        int total = 0, max_tiles = 0, q_total = 0;
+#pragma unroll 1
+        for (int base = 0; base < P.B; base += 32) {
+            const int b = base + lane;
+            const int T = b < P.B ? P.seq_lens[b] : 0, n = b < P.B ? P.q_lens[b] : 0;
+            const TcSeq w = tc_seq(T, n, P.G, P.Hkv, P.max_q_len, P.max_pages, P.min_rows);
+            total += __reduce_add_sync(0xffffffffu, static_cast<unsigned>(w.units));
+            max_tiles = max(max_tiles, static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(w.tiles))));
+            q_total += __reduce_add_sync(0xffffffffu, static_cast<unsigned>(max(0, n)));
+        }
+        const TcRanges rg = make_tc_ranges(total, gridDim.x, max_tiles);
+        const int c_begin = rg.begin(blockIdx.x), c_end = min(total, rg.begin(blockIdx.x + 1));
+        int has = q_total <= P.total_q && c_begin < c_end;  // else the split kernel flags the lengths
+        int fb = 0, fq = 0, fu = 0;
+        if (has) {  // the sequence whose units hold c_begin
+            int u_base = 0, q_base = 0;
+            has = 0;
+#pragma unroll 1
+            for (int base = 0; base < P.B && !has; base += 32) {
+                const int b = base + lane;
+                const int T = b < P.B ? P.seq_lens[b] : 0, n = b < P.B ? P.q_lens[b] : 0;
+                const int u = tc_seq(T, n, P.G, P.Hkv, P.max_q_len, P.max_pages, P.min_rows).units;
+                const int qn = max(0, n);
+                int ui = u, qi = qn;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (lane == 0) red[warp] = part;
-        __syncthreads();
-        for (int w = 0; w < kThreads / 32; ++w) seq_qstart += red[w];
-        // the same eligibility rule as the split kernel's, which merges these partials
-        const bool work = seq_n > 0 && seq_n <= T && seq_n <= P.max_q_len && npages <= P.max_pages &&
-                          row_count >= P.min_rows && seq_qstart + seq_n <= P.total_q && pc_lo < pc_hi &&
-                          row0 < row_count;
-        if (!work) return;  // uniform over the CTA: nothing allocated yet
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int a = __shfl_up_sync(0xffffffffu, ui, o), c = __shfl_up_sync(0xffffffffu, qi, o);
+                    if (lane >= o) {
+                        ui += a;
+                        qi += c;
+                    }
+                }
+                const int ux = u_base + ui - u, qx = q_base + qi - qn;
+                const unsigned hit = __ballot_sync(0xffffffffu, u > 0 && ux <= c_begin && c_begin < ux + u);
+                if (hit) {
+                    const int src = __ffs(hit) - 1;
+                    fb = base + src;
+                    fu = __shfl_sync(0xffffffffu, ux, src);
+                    fq = __shfl_sync(0xffffffffu, qx, src);
+                    has = 1;
+                }
+                u_base += __shfl_sync(0xffffffffu, ui, 31);
+                q_base += __shfl_sync(0xffffffffu, qi, 31);
+            }
+        }
+        if (lane == 0) {
+            start->has_work = has;
+            start->rg = rg;
+            if (has) {
+                const TcSeq w = tc_seq(P.seq_lens[fb], P.q_lens[fb], P.G, P.Hkv, P.max_q_len, P.max_pages, P.min_rows);
+                const int off = c_begin - fu;
+                start->b = fb;
+                start->qstart = fq;
+                start->seg = off / w.tiles;
+                start->tile = off % w.tiles;
+                start->unit = c_begin;
+                start->end = c_end;
+            }
+        }
     }
-    // 128-key tiles of the chunk that hold keys below key_end
-    const int n_kv = (min(pc_hi * kPageSize, key_end) - pc_lo * kPageSize + kN - 1) / kN;
+    if (P.seq_mode) {
+        __syncthreads();
+        if (!start->has_work) return;  // uniform over the CTA: nothing allocated yet
+    }
+    auto first_piece = [&](TcCursor &cur, TcPiece &pc) -> bool {
+        if (!P.seq_mode) {
+            pc = plan_piece;
+            return true;
+        }
+        cur.init(P, *start);
+        return cur.next(P, pc);
+    };
+    auto next_piece = [&](TcCursor &cur, TcPiece &pc) -> bool { return P.seq_mode && cur.next(P, pc); };
 
     if (tid == 0) {
         for (int s = 0; s < kStagesTC; ++s) {
@@ -254,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&p_full[b], kM);
             mbar_init(&p_free[b], 1);
+            mbar_init(&o_free[b], kM);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -270,87 +392,163 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o = tmem + kSBufs * kN;  // S buffers at columns 0, kN, 2 kN; O after them
+    const uint32_t tmem_o0 = tmem + kSBufs * kN;  // S buffers at columns 0, kN, 2 kN; two O buffers after them
 
     const uint32_t sQ = smem_u32(smem + kOffQ), sP = smem_u32(smem + kOffP), sKV = smem_u32(smem + kOffKV);
 
     if (warp < 4) {
         // ================= softmax / epilogue warps: thread t owns tensor-memory
-        // lane t. With at most 32 rows (sequence mode), every row is held by
-        // four lanes, one in each softmax warp (the Q tile holds four copies of
-        // the rows), and copy c takes keys [16c, 16c + 16) of every tile: a
-        // warp's per-tile softmax work is four times smaller. The P rows of a
-        // copy are zero outside its keys, so P V sums each copy's keys into its
-        // own lanes of O, with its own running max; the epilogue merges the
-        // four copies of each row.
-        const int rf = (P.seq_mode && row_count - row0 <= kM / 4) ? 4 : 1;  // copies per row
-        const int rpc = kM / rf;                                           // rows per copy
+        // lane t. With at most 32 rows in a piece, every row is held by four
+        // lanes, one in each softmax warp (the Q tile holds four copies of the
+        // rows), and copy c takes keys [16c, 16c + 16) of every tile: a warp's
+        // per-tile softmax work is four times smaller. The P rows of a copy are
+        // zero outside its keys, so P V sums each copy's keys into its own lanes
+        // of O, with its own running max; the epilogue merges the four copies.
         const int t = tid;
-        const int cp = t / rpc;
-        auto row_of = [&](int rr, int32_t &token, int32_t &hl, int32_t &limit, int32_t &slot) {
-            if (!P.seq_mode) {
-                const int32_t *rrow = P.run_rows + static_cast<int64_t>(rows_begin + rr) * 4;
-                token = rrow[0];
-                hl = rrow[1];
-                limit = rrow[2];
-                slot = rrow[3] + chunk;
-            } else {
-                token = seq_qstart + rr / P.G;
-                hl = rr % P.G;
-                limit = key_end - seq_n + rr / P.G;
-                slot = chunk;
-            }
-        };
-        const int r = row0 + t % rpc;
-        const bool valid = r < row_count;
-        const bool warp_valid = __any_sync(0xffffffffu, valid);  // warps without rows skip the softmax
-        int32_t token = 0, hl = 0, limit = -1, slot = 0;
-        if (valid) row_of(r, token, hl, limit, slot);
-        // P rows start at zero in both buffers (a copy writes only its own keys)
-#pragma unroll
-        for (int c = 0; c < kN / 8; ++c) {
-            *reinterpret_cast<uint4 *>(smem + kOffP + sw128_offset(t, c)) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(smem + kOffP + kPBytes + sw128_offset(t, c)) = make_uint4(0, 0, 0, 0);
-        }
-        // Q row of lane t -> shared memory, 128-byte swizzled K-major (two 64-column blocks)
-        {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                P.q + (static_cast<int64_t>(token) * P.Hq + g * P.G + hl) * kHeadDim);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 w = valid ? src[c] : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(smem + kOffQ + (c >> 3) * kRowBlk + sw128_offset(t, c & 7)) = w;
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(q_full);
-        }
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        float m_ref = -INFINITY, lsum = 0.f;
         bool ok = true;
         // P buffer b = i & 1 is free again once P V of tile i - 2 has run;
         // that P V is the ((i - 2) >> 1)-th commit on p_free[b]
         auto wait_pv = [&](int j) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(&p_free[j & 1], (j >> 1) & 1));
         };
-        auto softmax_tiles = [&](auto kpc_tag) {
-            constexpr int KPC = decltype(kpc_tag)::value;  // keys of a tile this lane's copy takes
-            const int koff = cp * KPC;
-            for (int i = 0; i < n_kv && ok; ++i) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[i % kSBufs], (i / kSBufs) & 1));
-                if (!ok) break;
-                tc_fence_after();
-                const int pos0 = pc_lo * kPageSize + i * kN;
-                uint8_t *pbuf = smem + kOffP + (i & 1) * kPBytes;
-                uint8_t *vstage = smem + kOffKV + (i % kStagesTC) * kKVStage + 2 * kKVBlk;
-                if (!warp_valid) {
-                    // arrivals on p_full[i & 1] must not run ahead of the phase that
-                    // tile i - 2 completes there: wait, like the rows with data do,
-                    // until P V of tile i - 2 (which follows that phase) is done
-                    if (i >= 2) {
+        int i = 0;  // tile index over all pieces of this CTA
+        int p = 0;  // piece index
+        TcCursor cur;
+        TcPiece pc;
+        for (bool more = first_piece(cur, pc); more && ok; more = next_piece(cur, pc), ++p) {
+            const int rf = (P.seq_mode && pc.row_count - pc.row0 <= kM / 4) ? 4 : 1;  // copies per row
+            const int rpc = kM / rf;                                                 // rows per copy
+            const int cp = t / rpc;
+            auto row_of = [&](int rr, int32_t &token, int32_t &hl, int32_t &limit, int32_t &slot) {
+                if (!P.seq_mode) {
+                    const int32_t *rrow = P.run_rows + static_cast<int64_t>(pc.rows_begin + rr) * 4;
+                    token = rrow[0];
+                    hl = rrow[1];
+                    limit = rrow[2];
+                    slot = rrow[3] + pc.slot;
+                } else {
+                    token = pc.qstart + rr / P.G;
+                    hl = rr % P.G;
+                    limit = pc.key_end - pc.seq_n + rr / P.G;
+                    slot = pc.slot;
+                }
+            };
+            const int r = pc.row0 + t % rpc;
+            const bool valid = r < pc.row_count;
+            const bool warp_valid = __any_sync(0xffffffffu, valid);  // warps without rows skip the softmax
+            int32_t token = 0, hl = 0, limit = -1, slot = 0;
+            if (valid) row_of(r, token, hl, limit, slot);
+            // P rows start each piece at zero in both buffers (a copy writes only
+            // its own keys); every P V of the previous piece has completed
+#pragma unroll
+            for (int c = 0; c < kN / 8; ++c) {
+                *reinterpret_cast<uint4 *>(smem + kOffP + sw128_offset(t, c)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(smem + kOffP + kPBytes + sw128_offset(t, c)) = make_uint4(0, 0, 0, 0);
+            }
+            // Q row of lane t -> shared memory, 128-byte swizzled K-major (two
+            // 64-column blocks); every Q K^T of the previous piece has completed
+            {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    P.q + (static_cast<int64_t>(token) * P.Hq + pc.g * P.G + hl) * kHeadDim);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 w = valid ? src[c] : make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(smem + kOffQ + (c >> 3) * kRowBlk + sw128_offset(t, c & 7)) = w;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(q_full);
+            }
+            const uint32_t tmem_o = tmem_o0 + (p & 1) * kHeadDim;
+            float m_ref = -INFINITY, lsum = 0.f;
+            const int i_first = i;
+            auto softmax_tiles = [&](auto kpc_tag) {
+                constexpr int KPC = decltype(kpc_tag)::value;  // keys of a tile this lane's copy takes
+                const int koff = cp * KPC;
+                for (int tt = pc.t_lo; tt < pc.t_hi && ok; ++tt, ++i) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&s_full[i % kSBufs], (i / kSBufs) & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const int pos0 = pc.pc_lo * kPageSize + tt * kN;
+                    uint8_t *pbuf = smem + kOffP + (i & 1) * kPBytes;
+                    uint8_t *vstage = smem + kOffKV + (i % kStagesTC) * kKVStage + 2 * kKVBlk;
+                    if (!warp_valid) {
+                        // arrivals on p_full[i & 1] must not run ahead of the phase that
+                        // tile i - 2 completes there: wait, like the rows with data do,
+                        // until P V of tile i - 2 (which follows that phase) is done
+                        if (i >= 2) {
+                            ok = wait_pv(i - 2);
+                            if (!ok) break;
+                        }
+                        if (t < kN && pos0 + t >= pc.key_end) {  // keys past the end may hold stale data: zero their V row
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                *reinterpret_cast<uint4 *>(vstage + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                                *reinterpret_cast<uint4 *>(vstage + kKVBlk + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                            }
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        tc_fence_before();
+                        mbar_arrive(&p_full[i & 1]);
+                        continue;
+                    }
+                    float x[KPC];
+                    tmem_ld_cols<KPC>(tmem + (i % kSBufs) * kN + koff + lane_base, x);
+                    const bool whole = pos0 + kN - 1 <= limit;  // no key of this tile is masked for this row
+#pragma unroll
+                    for (int k = 0; k < KPC; ++k)
+                        x[k] = (whole || pos0 + koff + k <= limit) ? x[k] * P.qscale : -INFINITY;
+                    // row max as a tree (independent partial maxima, short dependency chains)
+                    float mx[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mx[k] = x[k];
+#pragma unroll
+                    for (int k = 8; k < KPC; ++k) mx[k & 7] = fmaxf(mx[k & 7], x[k]);
+                    const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    // move the reference max only when it grows by more than 2^8, so
+                    // that tensor-memory O is rarely rescaled (p stays below 256)
+                    const bool grow = tmax > m_ref + 8.f;
+                    const float m_new = grow ? tmax : m_ref;
+                    const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;  // 0 when m_ref was -inf
+                    const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                    // probabilities, packed to bf16 pairs while the tensor cores run P V
+                    uint32_t pw[KPC / 2];
+                    float ps[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+#pragma unroll
+                    for (int k = 0; k < KPC / 2; ++k) {
+                        const float a = exp2f(x[2 * k] - m_use), b = exp2f(x[2 * k + 1] - m_use);
+                        ps[k & 7] += a + b;
+                        pw[k] = pack_bf16x2(a, b);
+                    }
+                    const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                    if (i >= 2) {  // P V of tile i - 2 must be done before its P buffer is rewritten
                         ok = wait_pv(i - 2);
                         if (!ok) break;
                     }
-                    if (t < kN && pos0 + t >= key_end) {  // keys past the end may hold stale data: zero their V row
+                    if (i > i_first && __any_sync(0xffffffffu, grow)) {  // O must hold every earlier P V of the piece
+                        ok = wait_pv(i - 1);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < kHeadDim / 32; ++c) {
+                            float o[32];
+                            tmem_ld32(tmem_o + lane_base + c * 32, o);
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] *= alpha;
+                            tmem_st32(tmem_o + lane_base + c * 32, o);
+                        }
+                    }
+                    lsum = lsum * alpha + psum;
+                    m_ref = m_new;
+                    // this copy's keys of P row t -> shared memory (bf16, 128-byte swizzled K-major)
+#pragma unroll
+                    for (int c = 0; c < KPC / 8; ++c)
+                        *reinterpret_cast<uint4 *>(pbuf + sw128_offset(t, koff / 8 + c)) =
+                            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+                    if (t < kN && pos0 + t >= pc.key_end) {  // keys past the end may hold stale data: zero their V row
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             *reinterpret_cast<uint4 *>(vstage + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
@@ -360,200 +558,150 @@ __global__ void __launch_bounds__(kThreads, 1)
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     tc_fence_before();
                     mbar_arrive(&p_full[i & 1]);
-                    continue;
                 }
-                float x[KPC];
-                tmem_ld_cols<KPC>(tmem + (i % kSBufs) * kN + koff + lane_base, x);
-                const bool whole = pos0 + kN - 1 <= limit;  // no key of this tile is masked for this row
-#pragma unroll
-                for (int k = 0; k < KPC; ++k)
-                    x[k] = (whole || pos0 + koff + k <= limit) ? x[k] * P.qscale : -INFINITY;
-                // row max as a tree (independent partial maxima, short dependency chains)
-                float mx[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) mx[k] = x[k];
-#pragma unroll
-                for (int k = 8; k < KPC; ++k) mx[k & 7] = fmaxf(mx[k & 7], x[k]);
-                const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                // move the reference max only when it grows by more than 2^8, so
-                // that tensor-memory O is rarely rescaled (p stays below 256)
-                const bool grow = tmax > m_ref + 8.f;
-                const float m_new = grow ? tmax : m_ref;
-                const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;  // 0 when m_ref was -inf
-                const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                // probabilities, packed to bf16 pairs while the tensor cores run P V
-                uint32_t pw[KPC / 2];
-                float ps[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) ps[k] = 0.f;
-#pragma unroll
-                for (int k = 0; k < KPC / 2; ++k) {
-                    const float a = exp2f(x[2 * k] - m_use), b = exp2f(x[2 * k + 1] - m_use);
-                    ps[k & 7] += a + b;
-                    pw[k] = pack_bf16x2(a, b);
-                }
-                const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-                if (i >= 2) {  // P V of tile i - 2 must be done before its P buffer is rewritten
-                    ok = wait_pv(i - 2);
-                    if (!ok) break;
-                }
-                if (i >= 1 && __any_sync(0xffffffffu, grow)) {  // O must hold every earlier P V before it is rescaled
-                    ok = wait_pv(i - 1);
-                    if (!ok) break;
-                    tc_fence_after();
+            };
+            if (rf == 4) softmax_tiles(std::integral_constant<int, kN / 4>{});
+            else softmax_tiles(std::integral_constant<int, kN>{});
+            if (ok && i > i_first) ok = wait_pv(i - 1);  // the piece's last P V (every earlier one before it)
+            if (!ok) {
+                *abort_flag = 1;
+                if (lane == 0) flag_error(P.err, kErrBitTimeout);
+                break;
+            }
+            tc_fence_after();
+            if (rf == 1) {
+                if (warp_valid) {  // epilogue with one copy per row: fp32 partial (O, m, l) of this row
+                    const int64_t orow = static_cast<int64_t>(token) * P.Hq + pc.g * P.G + hl;
+                    const int64_t wi = static_cast<int64_t>(slot) * P.n_rows_total + orow;
 #pragma unroll
                     for (int c = 0; c < kHeadDim / 32; ++c) {
                         float o[32];
                         tmem_ld32(tmem_o + lane_base + c * 32, o);
+                        if (valid) {
+                            float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + c * 32);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] *= alpha;
-                        tmem_st32(tmem_o + lane_base + c * 32, o);
+                            for (int k = 0; k < 8; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                        }
                     }
+                    if (valid) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(m_ref, lsum);
                 }
-                lsum = lsum * alpha + psum;
-                m_ref = m_new;
-                // this copy's keys of P row t -> shared memory (bf16, 128-byte swizzled K-major)
-#pragma unroll
-                for (int c = 0; c < KPC / 8; ++c)
-                    *reinterpret_cast<uint4 *>(pbuf + sw128_offset(t, koff / 8 + c)) =
-                        make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-                if (t < kN && pos0 + t >= key_end) {  // keys past the end may hold stale data: zero their V row
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        *reinterpret_cast<uint4 *>(vstage + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(vstage + kKVBlk + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                tc_fence_before();
-                mbar_arrive(&p_full[i & 1]);
-            }
-        };
-        if (rf == 4) softmax_tiles(std::integral_constant<int, kN / 4>{});
-        else softmax_tiles(std::integral_constant<int, kN>{});
-        if (ok && n_kv > 0) ok = wait_pv(n_kv - 1);  // the last P V (every earlier one before it)
-        if (!ok) {
-            *abort_flag = 1;
-            if (lane == 0) flag_error(P.err, kErrBitTimeout);
-        } else if (rf == 1) {
-            if (warp_valid) {  // epilogue with one copy per row
-                tc_fence_after();
-                // epilogue: fp32 partial (O, m, l) of this row for the merge
-                const int64_t orow = static_cast<int64_t>(token) * P.Hq + g * P.G + hl;
-                const int64_t wi = static_cast<int64_t>(slot) * P.n_rows_total + orow;
+            } else {
+                // epilogue with four copies: stage every lane's O row, max and sum
+                // in shared memory (the Q and P buffers: every Q K^T and P V of the
+                // piece is done), then thread t merges columns [32 (t / 32), +32) of
+                // row t % 32 over the copies
+                float *ost = reinterpret_cast<float *>(smem + kOffQ);  // [128 lanes][128], 16-byte chunks xor-swizzled
+                float *mls = reinterpret_cast<float *>(smem + kOffML);
 #pragma unroll
                 for (int c = 0; c < kHeadDim / 32; ++c) {
                     float o[32];
                     tmem_ld32(tmem_o + lane_base + c * 32, o);
-                    if (valid) {
-                        float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + c * 32);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                    }
+                    for (int k = 0; k < 8; ++k)
+                        *reinterpret_cast<float4 *>(ost + t * kHeadDim + (((c * 8 + k) ^ (t & 7)) * 4)) =
+                            make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
                 }
-                if (valid) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(m_ref, lsum);
-            }
-        }
-        if (rf != 1) {
-            // epilogue with four copies: stage every lane's O row, max and sum in
-            // shared memory (the K/V stages are idle now), then thread t merges
-            // columns [32 (t / 32), +32) of row t % 32 over the copies. Every
-            // softmax warp reaches the barrier, whatever its status.
-            tc_fence_after();
-            constexpr int kOStride = kHeadDim + 4;  // floats; breaks bank conflicts
-            float *ost = reinterpret_cast<float *>(smem + kOffKV);
-            float *mls = ost + kM * kOStride;
+                mls[2 * t] = m_ref;
+                mls[2 * t + 1] = lsum;
+                asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps only
+                const int rl = t % rpc, q4 = t / rpc;
+                const int rr = pc.row0 + rl;
+                if (rr < pc.row_count) {
+                    float M = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kHeadDim / 32; ++c) {
-                float o[32];
-                tmem_ld32(tmem_o + lane_base + c * 32, o);
+                    for (int c = 0; c < 4; ++c)
+                        if (mls[2 * (c * rpc + rl) + 1] > 0.f) M = fmaxf(M, mls[2 * (c * rpc + rl)]);
+                    float L = 0.f;
+                    float4 o[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    *reinterpret_cast<float4 *>(ost + t * kOStride + c * 32 + 4 * k) =
-                        make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-            }
-            mls[2 * t] = m_ref;
-            mls[2 * t + 1] = lsum;
-            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps only
-            const int rl = t % rpc, q4 = t / rpc;
-            const int rr = row0 + rl;
-            if (ok && rr < row_count) {
-                float M = -INFINITY;
+                    for (int k = 0; k < 8; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    if (mls[2 * (c * rpc + rl) + 1] > 0.f) M = fmaxf(M, mls[2 * (c * rpc + rl)]);
-                float L = 0.f;
-                float4 o[8];
+                    for (int c = 0; c < 4; ++c) {
+                        const int ln = c * rpc + rl;
+                        const float lc = mls[2 * ln + 1];
+                        if (lc > 0.f) {
+                            const float wgt = exp2f(mls[2 * ln] - M);
+                            L += lc * wgt;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float lc = mls[2 * (c * rpc + rl) + 1];
-                    if (lc > 0.f) {
-                        const float wgt = exp2f(mls[2 * (c * rpc + rl)] - M);
-                        L += lc * wgt;
-                        const float *src = ost + (c * rpc + rl) * kOStride + q4 * 32;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const float4 v = *reinterpret_cast<const float4 *>(src + 4 * k);
-                            o[k].x += v.x * wgt;
-                            o[k].y += v.y * wgt;
-                            o[k].z += v.z * wgt;
-                            o[k].w += v.w * wgt;
+                            for (int k = 0; k < 8; ++k) {
+                                const float4 v = *reinterpret_cast<const float4 *>(ost + ln * kHeadDim + (((q4 * 8 + k) ^ (ln & 7)) * 4));
+                                o[k].x += v.x * wgt;
+                                o[k].y += v.y * wgt;
+                                o[k].z += v.z * wgt;
+                                o[k].w += v.w * wgt;
+                            }
                         }
                     }
-                }
-                int32_t tk, hh, lim, sl;
-                row_of(rr, tk, hh, lim, sl);
-                const int64_t wi = static_cast<int64_t>(sl) * P.n_rows_total + static_cast<int64_t>(tk) * P.Hq + g * P.G + hh;
-                float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + q4 * 32);
+                    int32_t tk, hh, lim, sl;
+                    row_of(rr, tk, hh, lim, sl);
+                    const int64_t wi = static_cast<int64_t>(sl) * P.n_rows_total + static_cast<int64_t>(tk) * P.Hq + pc.g * P.G + hh;
+                    float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + q4 * 32);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) dst[k] = o[k];
-                if (q4 == 0) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(M, L);
+                    for (int k = 0; k < 8; ++k) dst[k] = o[k];
+                    if (q4 == 0) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(M, L);
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");  // staging read before the next piece's Q
             }
+            tc_fence_before();
+            mbar_arrive(&o_free[p & 1]);  // this piece's O buffer may be overwritten
         }
     } else if (warp == 4) {
         // ================= TMA producer
         if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_last();  // row tiles of the run re-read these
-            int issued = 0;
-            for (int i = 0; i < n_kv; ++i) {
-                const int s = i % kStagesTC;
-                if (i >= kStagesTC && !mbar_wait(&kv_empty[s], ((i / kStagesTC) - 1) & 1)) {
-                    *abort_flag = 1;
-                    flag_error(P.err, kErrBitTimeout);
-                    break;
+            const uint64_t policy = P.seq_mode ? l2_policy_evict_first() : l2_policy_evict_last();  // plan: row tiles re-read
+            int i = 0;
+            bool ok = true;
+            TcCursor cur;
+            TcPiece pc;
+            for (bool more = first_piece(cur, pc); more && ok; more = next_piece(cur, pc)) {
+                if (P.seq_mode && i > 0) {
+                    // the softmax warps load this piece's query rows when the previous
+                    // piece ends; bring them into L2 now, while that piece still runs
+                    for (int k = 0; k < pc.seq_n; ++k)
+                        bulk_prefetch_l2(P.q + (static_cast<int64_t>(pc.qstart + k) * P.Hq + pc.g * P.G) * kHeadDim,
+                                         P.G * kHeadDim * 2);
                 }
-                if (*abort_flag) break;
-                const int page = pc_lo + i / (kPageSize / kN);
-                const int pid = P.block_table[static_cast<int64_t>(member) * P.max_pages + page];
-                // (sequence mode: the last tile may reach past the sequence's keys; the
-                // rows past the end are zeroed in shared memory before P V)
-                uint8_t *dst = smem + kOffKV + s * kKVStage;
-                if (pid < 0 || pid >= P.num_pages) {  // the planner only takes valid pages
-                    flag_error(P.err, kErrBitPageOOB);
-                    mbar_arrive(&kv_full[s]);
-                } else {
-                    const int y = (pid * P.Hkv + g) * kPageSize + (i % (kPageSize / kN)) * kN;
-                    mbar_arrive_expect_tx(&kv_full[s], kKVStage);
-                    tma_load_2d(dst, &tmk, &kv_full[s], 0, y, policy);
-                    tma_load_2d(dst + kKVBlk, &tmk, &kv_full[s], 64, y, policy);
-                    tma_load_2d(dst + 2 * kKVBlk, &tmv, &kv_full[s], 0, y, policy);
-                    tma_load_2d(dst + 3 * kKVBlk, &tmv, &kv_full[s], 64, y, policy);
+                for (int tt = pc.t_lo; tt < pc.t_hi; ++tt, ++i) {
+                    const int s = i % kStagesTC;
+                    if (i >= kStagesTC && !mbar_wait(&kv_empty[s], ((i / kStagesTC) - 1) & 1)) {
+                        *abort_flag = 1;
+                        flag_error(P.err, kErrBitTimeout);
+                        ok = false;
+                        break;
+                    }
+                    if (*abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    const int page = pc.pc_lo + tt / (kPageSize / kN);
+                    const int pid = P.block_table[static_cast<int64_t>(pc.member) * P.max_pages + page];
+                    // (the last tile may reach past the sequence's keys; the rows past
+                    // the end are zeroed in shared memory before P V)
+                    uint8_t *dst = smem + kOffKV + s * kKVStage;
+                    if (pid < 0 || pid >= P.num_pages) {
+                        flag_error(P.err, kErrBitPageOOB);
+                        mbar_arrive(&kv_full[s]);
+                    } else {
+                        const int y = (pid * P.Hkv + pc.g) * kPageSize + (tt % (kPageSize / kN)) * kN;
+                        mbar_arrive_expect_tx(&kv_full[s], kKVStage);
+                        tma_load_2d(dst, &tmk, &kv_full[s], 0, y, policy);
+                        tma_load_2d(dst + kKVBlk, &tmk, &kv_full[s], 64, y, policy);
+                        tma_load_2d(dst + 2 * kKVBlk, &tmv, &kv_full[s], 0, y, policy);
+                        tma_load_2d(dst + 3 * kKVBlk, &tmv, &kv_full[s], 64, y, policy);
+                    }
                 }
-                ++issued;
             }
             // copies still in flight finish before the CTA can leave
-            for (int i = issued - kStagesTC < 0 ? 0 : issued - kStagesTC; i < issued; ++i)
-                (void)mbar_wait(&kv_full[i % kStagesTC], (i / kStagesTC) & 1);
+            for (int k = i - kStagesTC < 0 ? 0 : i - kStagesTC; k < i; ++k)
+                (void)mbar_wait(&kv_full[k % kStagesTC], (k / kStagesTC) & 1);
         }
     } else {
         // ================= MMA issuer (one thread). Q K^T of tile j goes into S
         // buffer j % kSBufs once the softmax has read that buffer's previous
         // tile (its P V has been issued, so its P was written); P V of tile j
-        // once the softmax has written P(j). Q K^T therefore runs up to
-        // kSBufs - 1 tiles ahead of the softmax.
+        // once the softmax has written P(j), into the O buffer of its piece.
+        // Q K^T therefore runs up to kSBufs - 1 tiles ahead of the softmax,
+        // within a piece (the next piece's Q is written after this one ends).
         if (lane == 0) {
             constexpr uint32_t kIdQK = idesc_bf16(false, kN), kIdPV = idesc_bf16(true, kHeadDim);
             // Descriptors are linear in the start address (its 14-bit field holds
@@ -562,34 +710,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             // once: a lone issuing thread pays for each dependent instruction.
             const uint64_t dQ = smem_desc(sQ, 16, 1024), dK = smem_desc(sKV, 16, 1024);
             const uint64_t dP = smem_desc(sP, 16, 1024), dV = smem_desc(sKV + 2 * kKVBlk, kKVBlk, 1024);
-            bool ok = mbar_wait(q_full, 0);
-            int qk = 0;
-            for (int j = 0; ok && j < n_kv; ++j) {
-                for (; ok && qk < n_kv && qk < j + kSBufs; ++qk) {
-                    const int s = qk % kStagesTC;
-                    ok = mbar_wait(&kv_full[s], (qk / kStagesTC) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t dKs = dK + ((s * kKVStage) >> 4);
-                    const uint32_t d_s = tmem + (qk % kSBufs) * kN;
-#pragma unroll
-                    for (int k = 0; k < kHeadDim / 16; ++k)
-                        mma_bf16(d_s, dQ + (((k >> 2) * kRowBlk + (k & 3) * 32) >> 4),
-                                 dKs + (((k >> 2) * kKVBlk + (k & 3) * 32) >> 4), kIdQK, k > 0);
-                    mma_commit(&s_full[qk % kSBufs]);
-                }
-                if (!ok) break;
-                // O += P(j) V(j) once the softmax has written P(j)
-                ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1);
+            bool ok = true;
+            int i = 0, p = 0;
+            TcCursor cur;
+            TcPiece pc;
+            for (bool more = first_piece(cur, pc); more && ok; more = next_piece(cur, pc), ++p) {
+                ok = mbar_wait(q_full, p & 1);  // this piece's Q rows
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t dVs = dV + (((j % kStagesTC) * kKVStage) >> 4);
-                const uint64_t dPj = dP + (((j & 1) * kPBytes) >> 4);
+                const int i0 = i, i1 = i + (pc.t_hi - pc.t_lo);
+                const uint32_t tmem_o = tmem_o0 + (p & 1) * kHeadDim;
+                int qk = i0;
+                for (int j = i0; ok && j < i1; ++j) {
+                    for (; ok && qk < i1 && qk < j + kSBufs; ++qk) {
+                        const int s = qk % kStagesTC;
+                        ok = mbar_wait(&kv_full[s], (qk / kStagesTC) & 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint64_t dKs = dK + ((s * kKVStage) >> 4);
+                        const uint32_t d_s = tmem + (qk % kSBufs) * kN;
 #pragma unroll
-                for (int k = 0; k < kN / 16; ++k)
-                    mma_bf16(tmem_o, dPj + ((k * 32) >> 4), dVs + ((k * 16 * 128) >> 4), kIdPV, j > 0 || k > 0);
-                mma_commit(&kv_empty[j % kStagesTC]);
-                mma_commit(&p_free[j & 1]);
+                        for (int k = 0; k < kHeadDim / 16; ++k)
+                            mma_bf16(d_s, dQ + (((k >> 2) * kRowBlk + (k & 3) * 32) >> 4),
+                                     dKs + (((k >> 2) * kKVBlk + (k & 3) * 32) >> 4), kIdQK, k > 0);
+                        mma_commit(&s_full[qk % kSBufs]);
+                    }
+                    if (!ok) break;
+                    if (j == i0 && p >= 2) {  // the epilogue of piece p - 2 has read this O buffer
+                        ok = mbar_wait(&o_free[p & 1], ((p - 2) >> 1) & 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    // O += P(j) V(j) once the softmax has written P(j)
+                    ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t dVs = dV + (((j % kStagesTC) * kKVStage) >> 4);
+                    const uint64_t dPj = dP + (((j & 1) * kPBytes) >> 4);
+#pragma unroll
+                    for (int k = 0; k < kN / 16; ++k)
+                        mma_bf16(tmem_o, dPj + ((k * 32) >> 4), dVs + ((k * 16 * 128) >> 4), kIdPV, j > i0 || k > 0);
+                    mma_commit(&kv_empty[j % kStagesTC]);
+                    mma_commit(&p_free[j & 1]);
+                }
+                i = i1;
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -655,9 +819,6 @@ cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t
     p.max_q_len = d.max_q_len;
     p.total_q = d.total_q;
     p.min_rows = c.min_rows;
-    p.mtiles = c.mtiles;
-    p.max_chunks = c.max_chunks;
-    p.chunk_pages = c.chunk_pages;
     p.ws_acc = ws_acc;
     p.ws_ml = ws_ml;
     p.err = err;
@@ -668,9 +829,9 @@ cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t
     p.num_pages = d.num_pages;
     p.n_rows_total = rows_total;
     p.qscale = scale * 1.4426950408889634f;
-    const int64_t grid = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.mtiles * c.max_chunks;
-    if (grid == 0) return cudaSuccess;
-    prefix_tc_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(p, tmk, tmv);
+    if (d.num_seqs == 0 || c.grid <= 0) return cudaSuccess;
+    // persistent: one CTA per SM, each walks its range of the tile sequence
+    prefix_tc_kernel<<<static_cast<unsigned>(c.grid), kThreads, kSmemBytes, stream>>>(p, tmk, tmv);
     return cudaGetLastError();
 }
 

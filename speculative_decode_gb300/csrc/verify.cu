@@ -56,24 +56,45 @@ __global__ void __launch_bounds__(256) argmax_accept_kernel(const VerifyParams P
         float bv = -INFINITY;
         int bi = INT_MAX;
         if ((P.V & 3) == 0) {
-            // rows are 16-byte aligned and chunk bounds are multiples of 4
-            for (int64_t e = lo + threadIdx.x * 4; e < hi; e += 4 * 1024) {
-                float4 x[4];
+            // rows are 16-byte aligned and chunk bounds are multiples of 4.
+            // Four 16-byte loads per thread per step with the next step's
+            // loads in flight while this step is reduced, into four
+            // independent (value, index) pairs merged at the end (the order
+            // (larger value, then lower index) makes the merge exact).
+            constexpr int kStep = 4 * 4 * 256;  // elements per CTA step
+            float4 cur[4], nxt[4];
+            float pv[4];
+            int pi[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                pv[u] = -INFINITY;
+                pi[u] = INT_MAX;
+            }
+            auto load_step = [&](int64_t e, float4 (&x)[4]) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int64_t eu = e + u * 1024;
                     x[u] = eu < hi ? __ldcs(reinterpret_cast<const float4 *>(row + eu))
                                    : make_float4(NAN, NAN, NAN, NAN);
                 }
+            };
+            int64_t e = lo + threadIdx.x * 4;
+            load_step(e, cur);
+            for (; e < hi; e += kStep) {
+                load_step(e + kStep, nxt);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int base = static_cast<int>(e + u * 1024);
-                    take_if_better(x[u].x, base, bv, bi);
-                    take_if_better(x[u].y, base + 1, bv, bi);
-                    take_if_better(x[u].z, base + 2, bv, bi);
-                    take_if_better(x[u].w, base + 3, bv, bi);
+                    take_if_better(cur[u].x, base, pv[u], pi[u]);
+                    take_if_better(cur[u].y, base + 1, pv[u], pi[u]);
+                    take_if_better(cur[u].z, base + 2, pv[u], pi[u]);
+                    take_if_better(cur[u].w, base + 3, pv[u], pi[u]);
                 }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
             }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) take_if_better(pv[u], pi[u], bv, bi);
         } else {
             for (int64_t e = lo + threadIdx.x; e < hi; e += blockDim.x)
                 take_if_better(__ldcs(row + e), static_cast<int>(e), bv, bi);
