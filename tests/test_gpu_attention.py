@@ -219,3 +219,22 @@ def test_multi_query_rows_on_tensor_cores(seed, G, Hkv, qlens, max_ctx):
     out, err, _, _ = run_attention(w)
     assert err == 0
     assert_attention_close(out, oracle_attention(w), f"multi-query seed {seed}")
+
+
+def test_tensor_core_pieces_with_mixed_row_counts():
+    """Sequences of 24 rows (four row copies) and 64 rows (one copy) per KV
+    head on the tensor cores: persistent CTAs walk pieces of both kinds."""
+    w = wl.random_case(75, num_seqs=8, Hq=8, Hkv=2, max_ctx=1500, q_len_choices=(6, 16))
+    assert sa.paged_attn_kernel_count(dims_of(w)) == 3
+    out, err, _, _ = run_attention(w)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), "mixed tensor-core row counts")
+
+
+def test_tensor_core_many_short_segments():
+    """Many short verify sequences between decode ones: a CTA's range holds
+    many tensor-core segments and skips the sequences that are not its."""
+    w = wl.random_case(76, num_seqs=40, Hq=16, Hkv=2, max_ctx=200, q_len_choices=(1, 6))
+    out, err, _, _ = run_attention(w)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), "short tensor-core segments")
