@@ -247,9 +247,16 @@ def max_over_ranks(x: float) -> float:
     import torch.distributed as dist
     if not (dist.is_available() and dist.is_initialized()):
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(cfg: int, rank: int) -> int:
+    """Seed of rank's batch of workload cfg: rank 0 uses the workload's own
+    seed, every other rank an independent batch of the same shapes."""
+    return 1000 + cfg + 1 + 7919 * rank
 
 
 def e2e_steps(batch: GpuBatch, steps: int, warmup: int):
@@ -318,7 +325,7 @@ def run_ours(args):
         flush_r.view(torch.int64).sum()
 
     # ---- headline: decode step on the Llama3-8B-shaped batch
-    w = wl.config(DECODE_CFG, seed=1000 + DECODE_CFG + 1 + 7919 * rank)
+    w = wl.config(DECODE_CFG, seed=rank_seed(DECODE_CFG, rank))
     batch = GpuBatch(w, dev)
     cbytes = counted_bytes(w)
     sbytes = cbytes + append_bytes(w)
@@ -339,7 +346,7 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e2e_ms)
 
     # ---- second block: speculative verification step
-    wv = wl.config(VERIFY_CFG, seed=1000 + VERIFY_CFG + 1 + 7919 * rank)
+    wv = wl.config(VERIFY_CFG, seed=rank_seed(VERIFY_CFG, rank))
     vb = GpuBatch(wv, dev)
     vsteps = max(3, args.steps // 4)
     vparts, _ = timed_steps(vb, vsteps, args.warmup, flush, ["append", "attend", "accept"])
@@ -354,7 +361,7 @@ def run_ours(args):
 
     # ---- third block: the dedup batch (100 sequences sharing a 4096-token
     # prefix), paged_attn with the shared-run plan and without it
-    wd = wl.config(DEDUP_CFG, seed=1000 + DEDUP_CFG + 1 + 7919 * rank)
+    wd = wl.config(DEDUP_CFG, seed=rank_seed(DEDUP_CFG, rank))
     dsteps = max(3, args.steps // 4)
     dedup = {"workload": wd.name, "unique_bytes": counted_bytes(wd)}
     for label, use_plan in (("with_plan", True), ("without_plan", False)):
