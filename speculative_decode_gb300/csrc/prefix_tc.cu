@@ -13,9 +13,9 @@
 // and stores, per row, an fp32 partial (O, m, l) that the combine kernel merges
 // with the rest of the sequence's keys.
 //
-// CTA = 6 warps: warps 0-3 softmax and epilogue (thread t owns row t, which is
-// tensor-memory lane t), warp 4 the TMA producer, warp 5 allocates tensor
-// memory and issues the MMAs (one elected thread). K/V tiles of 64 keys
+// CTA = 7 warps: warps 0-3 softmax and epilogue (thread t owns tensor-memory
+// lane t), warp 4 the TMA producer, warp 5 allocates tensor memory and issues
+// Q K^T, warp 6 issues P V (one thread each). K/V tiles of 64 keys
 // (32 KiB) stream through five stages, so four loads are in flight while a
 // tile is consumed; S (tensor memory, three buffers) and P (shared memory, two)
 // are multi-buffered, so Q K^T runs up to two tiles ahead and P V of the
@@ -52,7 +52,7 @@ constexpr int kKVStage = 4 * kKVBlk;          // K (2 blocks) + V (2 blocks) = 3
 constexpr int kStagesTC = SA_TC_STAGES;
 constexpr int kSBufs = 3;                     // S buffers: Q K^T runs up to two tiles ahead of the softmax
 constexpr int kTmemCols = 512;                // S buffers: columns 0 .. 3*64-1, two O buffers: the next 2*128
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 
 constexpr int kOffQ = 0;
 constexpr int kOffP = kOffQ + kQBytes;
@@ -266,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *p_full = s_full + kSBufs;         // [2] P buffer written (and its S buffer read)
     uint64_t *p_free = p_full + 2;              // [2] P V of that buffer finished (O up to date with it)
     uint64_t *o_free = p_free + 2;              // [2] O buffer read by its piece's epilogue
-    uint64_t *mma_done = o_free + 2;            // every MMA finished (before freeing tensor memory)
+    uint64_t *s_free = o_free + 2;              // [kSBufs] S buffer read by the softmax
+    uint64_t *mma_done = s_free + kSBufs;       // every MMA of both issuers finished
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(mma_done + 1);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(mma_done + 2);
     TcStart *start = reinterpret_cast<TcStart *>(smem + kOffStart);
@@ -377,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&p_free[b], 1);
             mbar_init(&o_free[b], kM);
         }
-        mbar_init(mma_done, 1);
+        for (int b = 0; b < kSBufs; ++b) mbar_init(&s_free[b], kM);
+        mbar_init(mma_done, 2);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -473,6 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *pbuf = smem + kOffP + (i & 1) * kPBytes;
                     uint8_t *vstage = smem + kOffKV + (i % kStagesTC) * kKVStage + 2 * kKVBlk;
                     if (!warp_valid) {
+                        tc_fence_before();
+                        mbar_arrive(&s_free[i % kSBufs]);
                         // arrivals on p_full[i & 1] must not run ahead of the phase that
                         // tile i - 2 completes there: wait, like the rows with data do,
                         // until P V of tile i - 2 (which follows that phase) is done
@@ -494,6 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     float x[KPC];
                     tmem_ld_cols<KPC>(tmem + (i % kSBufs) * kN + koff + lane_base, x);
+                    tc_fence_before();
+                    mbar_arrive(&s_free[i % kSBufs]);  // Q K^T of tile i + kSBufs may overwrite it
                     const bool whole = pos0 + kN - 1 <= limit;  // no key of this tile is masked for this row
 #pragma unroll
                     for (int k = 0; k < KPC; ++k)
@@ -695,53 +701,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = i - kStagesTC < 0 ? 0 : i - kStagesTC; k < i; ++k)
                 (void)mbar_wait(&kv_full[k % kStagesTC], (k / kStagesTC) & 1);
         }
-    } else {
-        // ================= MMA issuer (one thread). Q K^T of tile j goes into S
-        // buffer j % kSBufs once the softmax has read that buffer's previous
-        // tile (its P V has been issued, so its P was written); P V of tile j
-        // once the softmax has written P(j), into the O buffer of its piece.
-        // Q K^T therefore runs up to kSBufs - 1 tiles ahead of the softmax,
-        // within a piece (the next piece's Q is written after this one ends).
+    } else if (warp == 5) {
+        // ================= Q K^T issuer (one thread): tile qk into S buffer
+        // qk % kSBufs once its K has landed and the softmax has read that
+        // buffer's previous tile, so Q K^T runs up to kSBufs tiles ahead of
+        // the softmax within a piece (the next piece's Q is written after this
+        // one ends). Descriptors are linear in the start address (its 14-bit
+        // field holds address / 16; shared-memory offsets stay below 256 KiB),
+        // so each is a base plus a byte offset / 16, computed once.
         if (lane == 0) {
-            constexpr uint32_t kIdQK = idesc_bf16(false, kN), kIdPV = idesc_bf16(true, kHeadDim);
-            // Descriptors are linear in the start address (its 14-bit field holds
-            // address / 16 and shared-memory offsets stay below 256 KiB), so every
-            // operand's descriptor is a base plus a byte offset / 16, computed
-            // once: a lone issuing thread pays for each dependent instruction.
+            constexpr uint32_t kIdQK = idesc_bf16(false, kN);
             const uint64_t dQ = smem_desc(sQ, 16, 1024), dK = smem_desc(sKV, 16, 1024);
-            const uint64_t dP = smem_desc(sP, 16, 1024), dV = smem_desc(sKV + 2 * kKVBlk, kKVBlk, 1024);
             bool ok = true;
-            int i = 0, p = 0;
+            int qk = 0, p = 0;
             TcCursor cur;
             TcPiece pc;
             for (bool more = first_piece(cur, pc); more && ok; more = next_piece(cur, pc), ++p) {
                 ok = mbar_wait(q_full, p & 1);  // this piece's Q rows
                 if (!ok) break;
                 tc_fence_after();
-                const int i0 = i, i1 = i + (pc.t_hi - pc.t_lo);
-                const uint32_t tmem_o = tmem_o0 + (p & 1) * kHeadDim;
-                int qk = i0;
-                for (int j = i0; ok && j < i1; ++j) {
-                    for (; ok && qk < i1 && qk < j + kSBufs; ++qk) {
-                        const int s = qk % kStagesTC;
-                        ok = mbar_wait(&kv_full[s], (qk / kStagesTC) & 1);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint64_t dKs = dK + ((s * kKVStage) >> 4);
-                        const uint32_t d_s = tmem + (qk % kSBufs) * kN;
-#pragma unroll
-                        for (int k = 0; k < kHeadDim / 16; ++k)
-                            mma_bf16(d_s, dQ + (((k >> 2) * kRowBlk + (k & 3) * 32) >> 4),
-                                     dKs + (((k >> 2) * kKVBlk + (k & 3) * 32) >> 4), kIdQK, k > 0);
-                        mma_commit(&s_full[qk % kSBufs]);
-                    }
+                for (int tt = pc.t_lo; ok && tt < pc.t_hi; ++tt, ++qk) {
+                    const int s = qk % kStagesTC;
+                    ok = mbar_wait(&kv_full[s], (qk / kStagesTC) & 1);
+                    if (ok && qk >= kSBufs) ok = mbar_wait(&s_free[qk % kSBufs], ((qk / kSBufs) - 1) & 1);
                     if (!ok) break;
-                    if (j == i0 && p >= 2) {  // the epilogue of piece p - 2 has read this O buffer
+                    tc_fence_after();
+                    const uint64_t dKs = dK + ((s * kKVStage) >> 4);
+                    const uint32_t d_s = tmem + (qk % kSBufs) * kN;
+#pragma unroll
+                    for (int k = 0; k < kHeadDim / 16; ++k)
+                        mma_bf16(d_s, dQ + (((k >> 2) * kRowBlk + (k & 3) * 32) >> 4),
+                                 dKs + (((k >> 2) * kKVBlk + (k & 3) * 32) >> 4), kIdQK, k > 0);
+                    mma_commit(&s_full[qk % kSBufs]);
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                flag_error(P.err, kErrBitTimeout);
+            }
+            mma_commit(mma_done);  // every MMA this thread issued completes before tensor memory is freed
+        }
+    } else {
+        // ================= P V issuer (one thread): tile j once the softmax has
+        // written P(j), into the O buffer of its piece (overwriting it on the
+        // piece's first tile, after the epilogue of the piece two back read it).
+        if (lane == 0) {
+            constexpr uint32_t kIdPV = idesc_bf16(true, kHeadDim);
+            const uint64_t dP = smem_desc(sP, 16, 1024), dV = smem_desc(sKV + 2 * kKVBlk, kKVBlk, 1024);
+            bool ok = true;
+            int j = 0, p = 0;
+            TcCursor cur;
+            TcPiece pc;
+            for (bool more = first_piece(cur, pc); more && ok; more = next_piece(cur, pc), ++p) {
+                const uint32_t tmem_o = tmem_o0 + (p & 1) * kHeadDim;
+                const int j0 = j;
+                for (int tt = pc.t_lo; ok && tt < pc.t_hi; ++tt, ++j) {
+                    if (j == j0 && p >= 2) {  // the epilogue of piece p - 2 has read this O buffer
                         ok = mbar_wait(&o_free[p & 1], ((p - 2) >> 1) & 1);
                         if (!ok) break;
-                        tc_fence_after();
                     }
-                    // O += P(j) V(j) once the softmax has written P(j)
                     ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1);
                     if (!ok) break;
                     tc_fence_after();
@@ -749,17 +767,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t dPj = dP + (((j & 1) * kPBytes) >> 4);
 #pragma unroll
                     for (int k = 0; k < kN / 16; ++k)
-                        mma_bf16(tmem_o, dPj + ((k * 32) >> 4), dVs + ((k * 16 * 128) >> 4), kIdPV, j > i0 || k > 0);
+                        mma_bf16(tmem_o, dPj + ((k * 32) >> 4), dVs + ((k * 16 * 128) >> 4), kIdPV, j > j0 || k > 0);
                     mma_commit(&kv_empty[j % kStagesTC]);
                     mma_commit(&p_free[j & 1]);
                 }
-                i = i1;
             }
             if (!ok) {
                 *abort_flag = 1;
                 flag_error(P.err, kErrBitTimeout);
             }
-            // every MMA this thread issued completes before tensor memory is freed
             mma_commit(mma_done);
         }
     }
