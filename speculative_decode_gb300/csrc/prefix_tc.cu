@@ -414,59 +414,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto wait_pv = [&](int j) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(&p_free[j & 1], (j >> 1) & 1));
         };
-        int i = 0;  // tile index over all pieces of this CTA
-        int p = 0;  // piece index
-        TcCursor cur;
-        TcPiece pc;
-        for (bool more = first_piece(cur, pc); more && ok; more = next_piece(cur, pc), ++p) {
-            const int rf = (P.seq_mode && pc.row_count - pc.row0 <= kM / 4) ? 4 : 1;  // copies per row
-            const int rpc = kM / rf;                                                 // rows per copy
-            const int cp = t / rpc;
-            auto row_of = [&](int rr, int32_t &token, int32_t &hl, int32_t &limit, int32_t &slot) {
-                if (!P.seq_mode) {
-                    const int32_t *rrow = P.run_rows + static_cast<int64_t>(pc.rows_begin + rr) * 4;
-                    token = rrow[0];
-                    hl = rrow[1];
-                    limit = rrow[2];
-                    slot = rrow[3] + pc.slot;
-                } else {
-                    token = pc.qstart + rr / P.G;
-                    hl = rr % P.G;
-                    limit = pc.key_end - pc.seq_n + rr / P.G;
-                    slot = pc.slot;
-                }
-            };
-            const int r = pc.row0 + t % rpc;
-            const bool valid = r < pc.row_count;
-            const bool warp_valid = __any_sync(0xffffffffu, valid);  // warps without rows skip the softmax
-            int32_t token = 0, hl = 0, limit = -1, slot = 0;
-            if (valid) row_of(r, token, hl, limit, slot);
-            // P rows start each piece at zero in both buffers (a copy writes only
-            // its own keys); every P V of the previous piece has completed
+        // the rows of a piece that lane t holds
+        struct RowMap {
+            int rf, rpc, cp, r;
+            bool valid, warp_valid;
+            int32_t token, hl, limit, slot;
+        };
+        auto row_of = [&](const TcPiece &pc, int rr, int32_t &token, int32_t &hl, int32_t &limit, int32_t &slot) {
+            if (!P.seq_mode) {
+                const int32_t *rrow = P.run_rows + static_cast<int64_t>(pc.rows_begin + rr) * 4;
+                token = rrow[0];
+                hl = rrow[1];
+                limit = rrow[2];
+                slot = rrow[3] + pc.slot;
+            } else {
+                token = pc.qstart + rr / P.G;
+                hl = rr % P.G;
+                limit = pc.key_end - pc.seq_n + rr / P.G;
+                slot = pc.slot;
+            }
+        };
+        auto map_rows = [&](const TcPiece &pc) -> RowMap {
+            RowMap m{};
+            m.rf = (P.seq_mode && pc.row_count - pc.row0 <= kM / 4) ? 4 : 1;  // copies per row
+            m.rpc = kM / m.rf;                                               // rows per copy
+            m.cp = t / m.rpc;
+            m.r = pc.row0 + t % m.rpc;
+            m.valid = m.r < pc.row_count;
+            m.warp_valid = __any_sync(0xffffffffu, m.valid);  // warps without rows skip the softmax
+            m.token = 0;
+            m.hl = 0;
+            m.limit = -1;
+            m.slot = 0;
+            if (m.valid) row_of(pc, m.r, m.token, m.hl, m.limit, m.slot);
+            return m;
+        };
+        // Q row of lane t -> shared memory, 128-byte swizzled K-major (two
+        // 64-column blocks); every Q K^T of the previous piece has completed
+        auto write_q = [&](const TcPiece &pc, const RowMap &m) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                P.q + (static_cast<int64_t>(m.token) * P.Hq + pc.g * P.G + m.hl) * kHeadDim);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint4 w = m.valid ? src[c] : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(smem + kOffQ + (c >> 3) * kRowBlk + sw128_offset(t, c & 7)) = w;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(q_full);
+        };
+        // P rows start each piece at zero in both buffers (a copy writes only
+        // its own keys); every P V of the previous piece has completed
+        auto zero_p = [&]() {
 #pragma unroll
             for (int c = 0; c < kN / 8; ++c) {
                 *reinterpret_cast<uint4 *>(smem + kOffP + sw128_offset(t, c)) = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4 *>(smem + kOffP + kPBytes + sw128_offset(t, c)) = make_uint4(0, 0, 0, 0);
             }
-            // Q row of lane t -> shared memory, 128-byte swizzled K-major (two
-            // 64-column blocks); every Q K^T of the previous piece has completed
-            {
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    P.q + (static_cast<int64_t>(token) * P.Hq + pc.g * P.G + hl) * kHeadDim);
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint4 w = valid ? src[c] : make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(smem + kOffQ + (c >> 3) * kRowBlk + sw128_offset(t, c & 7)) = w;
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(q_full);
-            }
+        };
+        int i = 0;  // tile index over all pieces of this CTA
+        int p = 0;  // piece index
+        TcCursor cur;
+        TcPiece pc;
+        bool more = first_piece(cur, pc);
+        RowMap rm = map_rows(pc);
+        zero_p();
+        write_q(pc, rm);
+        while (more && ok) {
             const uint32_t tmem_o = tmem_o0 + (p & 1) * kHeadDim;
             float m_ref = -INFINITY, lsum = 0.f;
             const int i_first = i;
             auto softmax_tiles = [&](auto kpc_tag) {
                 constexpr int KPC = decltype(kpc_tag)::value;  // keys of a tile this lane's copy takes
-                const int koff = cp * KPC;
+                const int koff = rm.cp * KPC;
                 for (int tt = pc.t_lo; tt < pc.t_hi && ok; ++tt, ++i) {
                     ok = __all_sync(0xffffffffu, mbar_wait(&s_full[i % kSBufs], (i / kSBufs) & 1));
                     if (!ok) break;
@@ -474,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int pos0 = pc.pc_lo * kPageSize + tt * kN;
                     uint8_t *pbuf = smem + kOffP + (i & 1) * kPBytes;
                     uint8_t *vstage = smem + kOffKV + (i % kStagesTC) * kKVStage + 2 * kKVBlk;
-                    if (!warp_valid) {
+                    if (!rm.warp_valid) {
                         tc_fence_before();
                         mbar_arrive(&s_free[i % kSBufs]);
                         // arrivals on p_full[i & 1] must not run ahead of the phase that
@@ -500,10 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_cols<KPC>(tmem + (i % kSBufs) * kN + koff + lane_base, x);
                     tc_fence_before();
                     mbar_arrive(&s_free[i % kSBufs]);  // Q K^T of tile i + kSBufs may overwrite it
-                    const bool whole = pos0 + kN - 1 <= limit;  // no key of this tile is masked for this row
+                    const bool whole = pos0 + kN - 1 <= rm.limit;  // no key of this tile is masked for this row
 #pragma unroll
                     for (int k = 0; k < KPC; ++k)
-                        x[k] = (whole || pos0 + koff + k <= limit) ? x[k] * P.qscale : -INFINITY;
+                        x[k] = (whole || pos0 + koff + k <= rm.limit) ? x[k] * P.qscale : -INFINITY;
                     // row max as a tree (independent partial maxima, short dependency chains)
                     float mx[8];
 #pragma unroll
@@ -566,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&p_full[i & 1]);
                 }
             };
-            if (rf == 4) softmax_tiles(std::integral_constant<int, kN / 4>{});
+            if (rm.rf == 4) softmax_tiles(std::integral_constant<int, kN / 4>{});
             else softmax_tiles(std::integral_constant<int, kN>{});
             if (ok && i > i_first) ok = wait_pv(i - 1);  // the piece's last P V (every earlier one before it)
             if (!ok) {
@@ -575,81 +594,103 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            if (rf == 1) {
-                if (warp_valid) {  // epilogue with one copy per row: fp32 partial (O, m, l) of this row
-                    const int64_t orow = static_cast<int64_t>(token) * P.Hq + pc.g * P.G + hl;
-                    const int64_t wi = static_cast<int64_t>(slot) * P.n_rows_total + orow;
+            // the next piece's queries first, so that its Q K^T runs during this epilogue
+            TcPiece nx{};
+            const bool has_next = next_piece(cur, nx);
+            RowMap rn{};
+            if (has_next) {
+                rn = map_rows(nx);
+                write_q(nx, rn);
+            }
+            if (rm.rf == 1) {
+                if (rm.warp_valid) {  // epilogue with one copy per row: fp32 partial (O, m, l) of this row
+                    const int64_t orow = static_cast<int64_t>(rm.token) * P.Hq + pc.g * P.G + rm.hl;
+                    const int64_t wi = static_cast<int64_t>(rm.slot) * P.n_rows_total + orow;
 #pragma unroll
                     for (int c = 0; c < kHeadDim / 32; ++c) {
                         float o[32];
                         tmem_ld32(tmem_o + lane_base + c * 32, o);
-                        if (valid) {
+                        if (rm.valid) {
                             float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + c * 32);
 #pragma unroll
                             for (int k = 0; k < 8; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
                         }
                     }
-                    if (valid) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(m_ref, lsum);
+                    if (rm.valid) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(m_ref, lsum);
                 }
             } else {
-                // epilogue with four copies: stage every lane's O row, max and sum
-                // in shared memory (the Q and P buffers: every Q K^T and P V of the
-                // piece is done), then thread t merges columns [32 (t / 32), +32) of
-                // row t % 32 over the copies
-                float *ost = reinterpret_cast<float *>(smem + kOffQ);  // [128 lanes][128], 16-byte chunks xor-swizzled
+                // epilogue with four copies, in two halves of 64 columns staged
+                // in the P buffers (idle until the next piece's softmax): every
+                // lane stages its half row, then thread t merges 16 columns of
+                // row t % 32 over the copies. Every softmax warp reaches the
+                // barriers.
+                float *ost = reinterpret_cast<float *>(smem + kOffP);  // [128 lanes][64], 16-byte chunks xor-swizzled
                 float *mls = reinterpret_cast<float *>(smem + kOffML);
-#pragma unroll
-                for (int c = 0; c < kHeadDim / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(tmem_o + lane_base + c * 32, o);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        *reinterpret_cast<float4 *>(ost + t * kHeadDim + (((c * 8 + k) ^ (t & 7)) * 4)) =
-                            make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                }
                 mls[2 * t] = m_ref;
                 mls[2 * t + 1] = lsum;
-                asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps only
-                const int rl = t % rpc, q4 = t / rpc;
+                const int rl = t % rm.rpc, q4 = t / rm.rpc;
                 const int rr = pc.row0 + rl;
-                if (rr < pc.row_count) {
-                    float M = -INFINITY;
+                float M = -INFINITY, L = 0.f, wgt[4];
+                int64_t wi = 0;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (mls[2 * (c * rpc + rl) + 1] > 0.f) M = fmaxf(M, mls[2 * (c * rpc + rl)]);
-                    float L = 0.f;
-                    float4 o[8];
+                    for (int c = 0; c < 2; ++c) {
+                        float o[32];
+                        tmem_ld32(tmem_o + lane_base + h * 64 + c * 32, o);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int k = 0; k < 8; ++k)
+                            *reinterpret_cast<float4 *>(ost + t * 64 + (((c * 8 + k) ^ (t & 7)) * 4)) =
+                                make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps only
+                    if (rr < pc.row_count) {
+                        if (h == 0) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int ln = c * rpc + rl;
-                        const float lc = mls[2 * ln + 1];
-                        if (lc > 0.f) {
-                            const float wgt = exp2f(mls[2 * ln] - M);
-                            L += lc * wgt;
+                            for (int c = 0; c < 4; ++c)
+                                if (mls[2 * (c * rm.rpc + rl) + 1] > 0.f) M = fmaxf(M, mls[2 * (c * rm.rpc + rl)]);
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                const float4 v = *reinterpret_cast<const float4 *>(ost + ln * kHeadDim + (((q4 * 8 + k) ^ (ln & 7)) * 4));
-                                o[k].x += v.x * wgt;
-                                o[k].y += v.y * wgt;
-                                o[k].z += v.z * wgt;
-                                o[k].w += v.w * wgt;
+                            for (int c = 0; c < 4; ++c) {
+                                const float lc = mls[2 * (c * rm.rpc + rl) + 1];
+                                wgt[c] = lc > 0.f ? exp2f(mls[2 * (c * rm.rpc + rl)] - M) : 0.f;
+                                L += lc * wgt[c];
+                            }
+                            int32_t tk, hh, lim, sl;
+                            row_of(pc, rr, tk, hh, lim, sl);
+                            wi = static_cast<int64_t>(sl) * P.n_rows_total + static_cast<int64_t>(tk) * P.Hq + pc.g * P.G + hh;
+                            if (q4 == 0) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(M, L);
+                        }
+                        float4 o[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            if (wgt[c] > 0.f) {
+                                const int ln = c * rm.rpc + rl;
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const float4 v = *reinterpret_cast<const float4 *>(ost + ln * 64 + (((q4 * 4 + k) ^ (ln & 7)) * 4));
+                                    o[k].x += v.x * wgt[c];
+                                    o[k].y += v.y * wgt[c];
+                                    o[k].z += v.z * wgt[c];
+                                    o[k].w += v.w * wgt[c];
+                                }
                             }
                         }
-                    }
-                    int32_t tk, hh, lim, sl;
-                    row_of(rr, tk, hh, lim, sl);
-                    const int64_t wi = static_cast<int64_t>(sl) * P.n_rows_total + static_cast<int64_t>(tk) * P.Hq + pc.g * P.G + hh;
-                    float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + q4 * 32);
+                        float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + h * 64 + q4 * 16);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) dst[k] = o[k];
-                    if (q4 == 0) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(M, L);
+                        for (int k = 0; k < 4; ++k) dst[k] = o[k];
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");  // staging read before it is rewritten
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");  // staging read before the next piece's Q
             }
             tc_fence_before();
             mbar_arrive(&o_free[p & 1]);  // this piece's O buffer may be overwritten
+            if (!has_next) break;
+            zero_p();
+            pc = nx;
+            rm = rn;
+            ++p;
         }
     } else if (warp == 4) {
         // ================= TMA producer
