@@ -284,6 +284,7 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
     int per_sm = 0;
     if (split_occupancy(c.R, 1, &per_sm) != cudaSuccess || per_sm <= 0) return SA_ERR_CUDA;
     p.split_ctas = sms * per_sm;  // one warp per CTA, all resident
+    p.pages_ready = ((pd && pd->num_tiles > 0) || c.tc.min_rows > 0) ? 1 : 0;
     if (launch_split_attn(p, s) != cudaSuccess)
         return SA_ERR_CUDA;
     return finish(s, err_flag);

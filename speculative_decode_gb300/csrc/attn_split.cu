@@ -463,11 +463,13 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
 
     // The combine kernel may be scheduled now: it waits for this grid before
     // it reads the partials. This kernel itself may have been started while
-    // the kernel before it (kv_append) still runs: everything up to the grid
-    // dependency wait below reads only lengths and block tables, which that
-    // kernel does not write; queries and pages are read after the wait. Every
+    // the kernel before it still runs. After kv_append, everything up to the
+    // grid dependency wait below reads only lengths and block tables, which
+    // kv_append does not write; queries and pages are read after the wait.
+    // After a tensor-core kernel of this call (which started once the pages
+    // were complete and writes only partials), pages are read at once. Every
     // warp waits before it exits, so this grid completes after its
-    // predecessor.
+    // predecessor and the combine pass sees the tensor-core partials.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- 1. total work and this warp's range [g_begin, g_end) of tiles
@@ -643,11 +645,14 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
     uint32_t pieces_done = 0;
     auto bail_out = [&]() {
         flag_error(P.err, kErrBitTimeout);
+        if (P.pages_ready) grid_dependency_wait();
         for (uint32_t c = consumed; c < issued; ++c) (void)mbar_wait(&full[c % S], (c / S) & 1);
         for (uint32_t c = pieces_done; c < pieces_pushed; ++c) (void)mbar_wait(&qfull[c % S], (c / S) & 1);
     };
 
-    grid_dependency_wait();  // the pages written by the previous kernel are complete
+    // the pages written by the previous kernel are complete (when a tensor-core
+    // kernel of this call ran first, it started after them: no wait needed here)
+    if (!P.pages_ready) grid_dependency_wait();
     top_up();
     while (consumed < issued) {
         Piece U;
@@ -868,6 +873,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         }
         __syncwarp();
     }
+    if (P.pages_ready) grid_dependency_wait();  // every warp waits before it exits
 }
 
 // Pieces the tensor-core sequence mode cut segment (bt, kvh, mt) into: a scan

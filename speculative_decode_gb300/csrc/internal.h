@@ -60,6 +60,8 @@ struct SplitParams {
     int32_t evict_first;
     int32_t split_ctas;         // grid of the split kernel (one warp each); the combine
                                 // pass recomputes the same cut of the work
+    int32_t pages_ready;        // 1: a kernel of this call that started after the pages were
+                                // written ran first, so pages are read without waiting for it
 };
 
 // Split kernel over p.split_ctas one-warp CTAs, then the combine pass that

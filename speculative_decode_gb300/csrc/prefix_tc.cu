@@ -274,6 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    // the split kernel that follows reads nothing this kernel writes (the
+    // combine pass reads the partials after both grids), so it may start on
+    // SMs this grid leaves free
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- the work: plan mode, this CTA's item; sequence mode, this CTA's range
     TcPiece plan_piece{};
@@ -449,15 +453,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (m.valid) row_of(pc, m.r, m.token, m.hl, m.limit, m.slot);
             return m;
         };
-        // Q row of lane t -> shared memory, 128-byte swizzled K-major (two
-        // 64-column blocks); every Q K^T of the previous piece has completed
+        // the piece's Q rows -> shared memory, 128-byte swizzled K-major (two
+        // 64-column blocks), one copy per row group; every Q K^T of the
+        // previous piece has completed. The 128 threads read the rows together,
+        // 16 bytes each (16 threads per row), and write every copy. Lanes past
+        // the piece's rows keep whatever they hold: their S, P and O lanes are
+        // never read for output.
         auto write_q = [&](const TcPiece &pc, const RowMap &m) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                P.q + (static_cast<int64_t>(m.token) * P.Hq + pc.g * P.G + m.hl) * kHeadDim);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 w = m.valid ? src[c] : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(smem + kOffQ + (c >> 3) * kRowBlk + sw128_offset(t, c & 7)) = w;
+            const int nrow = min(m.rpc, pc.row_count - pc.row0);
+            for (int idx = t; idx < nrow * 16; idx += kM) {
+                const int rr = idx >> 4, c = idx & 15;
+                int32_t tk, hh, lim, sl;
+                row_of(pc, pc.row0 + rr, tk, hh, lim, sl);
+                const uint4 w = *reinterpret_cast<const uint4 *>(
+                    P.q + (static_cast<int64_t>(tk) * P.Hq + pc.g * P.G + hh) * kHeadDim + c * 8);
+                for (int cp = 0; cp < m.rf; ++cp)
+                    *reinterpret_cast<uint4 *>(smem + kOffQ + (c >> 3) * kRowBlk + sw128_offset(cp * m.rpc + rr, c & 7)) = w;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(q_full);
