@@ -616,19 +616,25 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         // the tile: K and V rows [t0, t0 + 32) of KV head kvh
         const int t0 = isi.skip_tok + itile * kTile;
         const int s = issued % S;
-        const int pid = t0 < isi.T ? page_id(ib, t0 / kPageSize, (isi.T + kPageSize - 1) / kPageSize) : -1;
-        const bool ok = pid >= 0 && pid < P.num_pages;
-        if (t0 < isi.T && !ok && lane == 0) flag_error(P.err, kErrBitPageOOB);
-        if (lane == 0) {
-            stage_ok[s] = ok;
+        // (t0 < T for every tile of a segment: tiles = ceil(keys / kTile))
+        const int pid = page_id(ib, t0 / kPageSize, (isi.T + kPageSize - 1) / kPageSize);
+        const bool ok = static_cast<unsigned>(pid) < static_cast<unsigned>(P.num_pages);
+        if (!ok && lane == 0) flag_error(P.err, kErrBitPageOOB);
+        if (lane < 2) {
             if (ok) {
-                // the tile's K rows and V rows are each one contiguous run in the page
+                // The tile's K rows and V rows are each one contiguous run in the
+                // page: lane 0 copies the K rows, lane 1 the V rows, in one
+                // instruction (the copy instruction's issue is slow; two lanes
+                // take the time of one).
                 const int64_t row = static_cast<int64_t>(pid * P.Hkv + kvh) * kPageSize + (t0 % kPageSize);
-                uint8_t *dst = smem + s * kStageBytes;
-                mbar_arrive_expect_tx(&full[s], kStageBytes);
-                bulk_load_hint(dst, P.k_pages + row * kHeadDim, kKVBytes, &full[s], policy);
-                bulk_load_hint(dst + kKVBytes, P.v_pages + row * kHeadDim, kKVBytes, &full[s], policy);
-            } else {
+                if (lane == 0) {
+                    stage_ok[s] = 1;
+                    mbar_arrive_expect_tx(&full[s], kStageBytes);
+                }
+                bulk_load_hint(smem + s * kStageBytes + lane * kKVBytes, (lane ? P.v_pages : P.k_pages) + row * kHeadDim,
+                               kKVBytes, &full[s], policy);
+            } else if (lane == 0) {
+                stage_ok[s] = 0;
                 mbar_arrive(&full[s]);  // nothing to load: the consumer skips this tile
             }
         }
