@@ -163,6 +163,17 @@ class GpuBatch:
         self.sa.spec_verify_greedy(self.logits, self.cand, self.ncand, self.acc, self.nxt,
                                    self.vws, window=self.window, err_flag=self.err)
 
+    def prepare_defrag(self):
+        """Compaction plan of this batch's pool (host, not timed); its moves on the device."""
+        new, moves, n_live = self.sa.defrag_moves(self.dims, self.w.block_table, self.w.seq_lens)
+        self.moves = self.T(moves.reshape(-1, 2))
+        self.n_moves, self.n_live = len(moves), n_live
+        return new
+
+    def defrag(self):
+        # the moves copy pages (sources stay), so repeating them copies the same bytes again
+        self.sa.defrag_apply(self.dims, self.kp, self.vp, self.moves, self.n_moves, err_flag=self.err)
+
     def launches_per_step(self):
         return 1 + self.kernels_attn + (1 if self.verify else 0)
 
@@ -172,7 +183,7 @@ def timed_steps(batch: GpuBatch, steps: int, warmup: int, flush, parts):
     CUDA events on the launching stream, flushing L2 before every step."""
     torch = batch.torch
     stream = torch.cuda.current_stream()
-    fns = {"append": batch.append, "attend": batch.attend, "accept": batch.accept}
+    fns = {"append": batch.append, "attend": batch.attend, "accept": batch.accept, "defrag": batch.defrag}
     for _ in range(warmup):
         flush()
         for p in parts:
@@ -201,8 +212,8 @@ def timed_steps(batch: GpuBatch, steps: int, warmup: int, flush, parts):
 
 # DRAM bytes of one split_attn_kernel<4> launch on the decode batch, from the
 # ncu capture summarised in profiles/split_attn_kernel_R4_llama3_8b_decode.md
-# (200.35 MB read + 3.79 MB written). Set to None when the kernel changes.
-SPLIT_TRAFFIC_BYTES = 204_076_288
+# (200.35 MB read + 3.78 MB written). Set to None when the kernel changes.
+SPLIT_TRAFFIC_BYTES = 204_129_280
 
 
 def timed_sequence(batch: GpuBatch, steps: int, warmup: int, flush, parts):
@@ -211,7 +222,7 @@ def timed_sequence(batch: GpuBatch, steps: int, warmup: int, flush, parts):
     step one pair of CUDA events around all of them, L2 flushed before."""
     torch = batch.torch
     stream = torch.cuda.current_stream()
-    fns = {"append": batch.append, "attend": batch.attend, "accept": batch.accept}
+    fns = {"append": batch.append, "attend": batch.attend, "accept": batch.accept, "defrag": batch.defrag}
     for _ in range(warmup):
         flush()
         for p in parts:
@@ -374,8 +385,21 @@ def run_ours(args):
             dedup["plan"] = db.plan.stats()
         del db
 
+    # ---- fourth block: compaction of the spec-verify batch's fragmented pool
+    # (512 pages, 8 KV heads): the host plan once, the page copies timed
+    vb.prepare_defrag()
+    fparts, _ = timed_steps(vb, vsteps, args.warmup, flush, ["defrag"])
+    tf = max_over_ranks(statistics.mean(fparts["defrag"]))
+    moved = vb.n_moves * 2 * wv.num_kv_heads * wl.PAGE_SIZE * 128 * 2  # K and V bytes of the moved pages
+    defrag = {"workload": f"{wv.name} pool ({wv.num_pages} pages)", "live_pages": vb.n_live,
+              "moved_pages": vb.n_moves, "moved_bytes": moved, "ms": round(tf, 5),
+              "GBps": round(2 * moved / (tf * 1e-3) / 1e9, 1),
+              "counts": "bytes read + bytes written / device time of sa_defrag_apply"}
+    del vb
+
     peak, peak_kind = hbm_peak()
     achieved = cbytes / (t_attn_max * 1e-3) / 1e9
+    defrag["frac_of_hbm_peak"] = round(defrag["GBps"] / peak, 4)
     line = {
         "metric": METRIC,
         "value": round(world * sbytes / (t_step_max * 1e-3) / 1e9, 2),
@@ -429,6 +453,7 @@ def run_ours(args):
             "note": "per attention layer: one layer's attention + one greedy accept",
         },
         "dedup": dedup,
+        "defrag": defrag,
         "e2e": {"value": round(world * cbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 5)},

@@ -230,6 +230,50 @@ SA_API int sa_spec_verify_greedy(const float *logits, const int32_t *candidates,
                           int32_t *next_tok, int32_t *window, void *workspace,
                           size_t workspace_bytes, int32_t *err_flag, void *stream);
 
+/*
+ * sa_defrag_moves -- compaction plan for a fragmented cache (host only, no
+ * CUDA call).
+ *
+ * ExLlamaV2 "Dynamic Generator" page, section "Continuous batching": freeing
+ * a finished job's pages leaves holes, the block table need not be
+ * contiguous, and the cache can be defragmented (the generator does it only
+ * when its job queue is empty). The page gives no procedure; this call's
+ * reading: a page is live when a table names it within its sequence's
+ * length (the first ceil(seq_lens[b] / 256) entries). With L live pages,
+ * every live page whose id is L or more moves into a free id below L, the
+ * k-th such page (by increasing id) into the k-th free id (by increasing id);
+ * live pages below L stay. Tables are rewritten through the same map, so a
+ * page shared by several sequences stays shared.
+ *   block_table  host int32 [num_seqs, max_pages_per_seq]
+ *   seq_lens     host int32 [num_seqs]
+ *   new_table    host int32 [num_seqs, max_pages_per_seq] (output): the
+ *                remapped table; entries past a sequence's length are -1
+ *   moves        host int32 [num_pages][2] (output): (from, to) page pairs,
+ *                *n_moves of them, by increasing from; no page is both a
+ *                from and a to, and no to repeats
+ *   n_moves, n_live  host int32 (outputs)
+ * Uses num_seqs, num_pages and max_pages_per_seq of dims. Errors:
+ * SA_ERR_ARG (a NULL pointer, a negative length, a length that needs more
+ * than max_pages_per_seq pages), SA_ERR_PAGE_OOB (a used entry outside
+ * [0, num_pages)); outputs are then unspecified.
+ */
+SA_API int sa_defrag_moves(const sa_dims *dims, const int32_t *block_table, const int32_t *seq_lens,
+                           int32_t *new_table, int32_t *moves, int32_t *n_moves, int32_t *n_live);
+
+/*
+ * sa_defrag_apply -- make the moves of a compaction plan: for every (from,
+ * to) pair, page `to` of k_pages and of v_pages gets page `from`'s rows
+ * (every KV head). Same page and section as sa_defrag_moves.
+ *   k_pages, v_pages  device bf16 [num_pages, num_kv_heads, 256, 128]
+ *   moves        device int32 [n_moves][2]; no page may be both read and
+ *                written and no page written twice (as sa_defrag_moves
+ *                gives them); otherwise the result is unspecified
+ * A pair naming a page outside [0, num_pages) sets SA_ERR_PAGE_OOB in
+ * *err_flag and is skipped. One kernel; n_moves = 0 launches nothing.
+ */
+SA_API int sa_defrag_apply(const sa_dims *dims, uint16_t *k_pages, uint16_t *v_pages,
+                           const int32_t *moves, int32_t n_moves, int32_t *err_flag, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -61,6 +61,10 @@ def _load():
         lib.oracle_argmax.restype = I64
         lib.oracle_verify_greedy.argtypes = [P, P, P, I, I, I64, P, P, P]
         lib.oracle_verify_greedy.restype = I
+        lib.oracle_defrag_plan.argtypes = [I] * 4 + [P] * 6
+        lib.oracle_defrag_plan.restype = I
+        lib.oracle_defrag_move.argtypes = [I, I64, P, P, P, I]
+        lib.oracle_defrag_move.restype = I
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = I
         _lib = lib
@@ -152,3 +156,27 @@ def verify_greedy(logits, candidates, n_cand, window=None):
     _check(rc, "verify_greedy")
     return acc, nxt, win
 
+
+def defrag_plan(block_table, seq_lens, num_pages, page_size=256):
+    """Compaction of the cache: (new_table, moves [n, 2] as (from, to), n_live)."""
+    bt, sl = _c(block_table, np.int32), _c(seq_lens, np.int32)
+    B, max_pages = bt.shape
+    new = np.empty_like(bt)
+    moves = np.empty((max(num_pages, 1), 2), np.int32)
+    n_moves, n_live = ctypes.c_int32(0), ctypes.c_int32(0)
+    rc = _load().oracle_defrag_plan(B, page_size, num_pages, max_pages, _ptr(bt), _ptr(sl),
+                                    _ptr(new), _ptr(moves), ctypes.byref(n_moves),
+                                    ctypes.byref(n_live))
+    _check(rc, "defrag_plan")
+    return new, moves[:n_moves.value].copy(), int(n_live.value)
+
+
+def defrag_move(k_pages, v_pages, moves):
+    """Return copies of k_pages/v_pages with every move (from, to) made."""
+    kp, vp = _c(k_pages, np.uint16).copy(), _c(v_pages, np.uint16).copy()
+    mv = _c(moves, np.int32).reshape(-1, 2)
+    num_pages = kp.shape[0]
+    rc = _load().oracle_defrag_move(num_pages, int(np.prod(kp.shape[1:])), _ptr(kp), _ptr(vp),
+                                    _ptr(mv), len(mv))
+    _check(rc, "defrag_move")
+    return kp, vp

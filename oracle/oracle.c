@@ -42,6 +42,18 @@
  *    window grows; NaN never wins an argmax and an all-NaN row gives 0;
  *    -0.0 and +0.0 compare equal (a tie).
  *
+ *  - defragmentation: releasing pages leaves holes in the cache; the block
+ *    table need not be contiguous, and the cache can be defragmented (the
+ *    generator does it only when its job queue is empty).  ExLlamaV2
+ *    "Dynamic Generator" page, section "Continuous batching".  Reading (the
+ *    page gives no procedure): a page is live when some sequence's table
+ *    names it within that sequence's length; with L live pages, every live
+ *    page whose id is L or more moves into a free id below L, the k-th such
+ *    page (in increasing id) into the k-th free id (in increasing id); live
+ *    pages below L stay.  Tables are rewritten through the same map, so
+ *    shared pages stay shared; entries past a sequence's length become -1.
+ *    Moving copies each moved page's K and V rows for every KV head.
+ *
  * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (no fast-math, so
  * the arithmetic is the order written here on every machine).
  */
@@ -291,6 +303,81 @@ int oracle_verify_greedy(const float *logits, const int32_t *candidates, const i
         next_tok[b] = (int32_t)oracle_argmax(rows + (int64_t)a * V, V);
         /* step 5: +2 when everything matched, -1 otherwise (never below 1) */
         if (window) window[b] = (a == n) ? window[b] + 2 : (window[b] - 1 > 1 ? window[b] - 1 : 1);
+    }
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------- defragmentation */
+
+/* block_table [num_seqs][max_pages]; seq_lens [num_seqs].  Outputs:
+ * new_table [num_seqs][max_pages]; moves [num_pages][2] as (from, to) pairs,
+ * *n_moves of them; *n_live live pages.  The moves read only pages no move
+ * writes, so they may be made in any order. */
+int oracle_defrag_plan(int num_seqs, int page_size, int num_pages, int max_pages,
+                       const int32_t *block_table, const int32_t *seq_lens, int32_t *new_table,
+                       int32_t *moves, int32_t *n_moves, int32_t *n_live) {
+    if (num_seqs < 0 || page_size <= 0 || num_pages < 0 || max_pages < 0) return ORACLE_ERR_ARG;
+    char *live = calloc((size_t)num_pages + 1, 1);
+    int32_t *map = malloc(((size_t)num_pages + 1) * sizeof(int32_t));
+    if (!live || !map) {
+        free(live);
+        free(map);
+        return ORACLE_ERR_NOMEM;
+    }
+    int rc = ORACLE_OK;
+    /* 1. live pages: named by a table within its sequence's length */
+    for (int b = 0; b < num_seqs && rc == ORACLE_OK; ++b) {
+        if (seq_lens[b] < 0) rc = ORACLE_ERR_ARG;
+        int64_t used = ((int64_t)seq_lens[b] + page_size - 1) / page_size;
+        if (used > max_pages) rc = ORACLE_ERR_ARG;
+        for (int64_t j = 0; j < used && rc == ORACLE_OK; ++j) {
+            int32_t id = block_table[(int64_t)b * max_pages + j];
+            if (id < 0 || id >= num_pages) rc = ORACLE_ERR_PAGE_OOB;
+            else live[id] = 1;
+        }
+    }
+    if (rc == ORACLE_OK) {
+        int32_t L = 0;
+        for (int p = 0; p < num_pages; ++p) L += live[p];
+        /* 2. the k-th live page at or above L goes to the k-th free id below L */
+        int32_t hole = 0, m = 0;
+        for (int p = 0; p < num_pages; ++p) {
+            map[p] = p;
+            if (!live[p] || p < L) continue;
+            while (live[hole]) ++hole; /* a free id below L exists for every page above it */
+            map[p] = hole;
+            moves[2 * m] = p;
+            moves[2 * m + 1] = hole;
+            ++m;
+            ++hole;
+        }
+        /* 3. the tables through the map */
+        for (int b = 0; b < num_seqs; ++b) {
+            int64_t used = ((int64_t)seq_lens[b] + page_size - 1) / page_size;
+            for (int64_t j = 0; j < max_pages; ++j) {
+                int64_t i = (int64_t)b * max_pages + j;
+                new_table[i] = j < used ? map[block_table[i]] : -1;
+            }
+        }
+        *n_moves = m;
+        *n_live = L;
+    }
+    free(live);
+    free(map);
+    return rc;
+}
+
+/* k_pages, v_pages [num_pages][page_elems]: copy page `from` to page `to`
+ * for every move. */
+int oracle_defrag_move(int num_pages, int64_t page_elems, uint16_t *k_pages, uint16_t *v_pages,
+                       const int32_t *moves, int n_moves) {
+    for (int m = 0; m < n_moves; ++m) {
+        int32_t from = moves[2 * m], to = moves[2 * m + 1];
+        if (from < 0 || from >= num_pages || to < 0 || to >= num_pages) return ORACLE_ERR_PAGE_OOB;
+        memcpy(k_pages + (int64_t)to * page_elems, k_pages + (int64_t)from * page_elems,
+               (size_t)page_elems * sizeof(uint16_t));
+        memcpy(v_pages + (int64_t)to * page_elems, v_pages + (int64_t)from * page_elems,
+               (size_t)page_elems * sizeof(uint16_t));
     }
     return ORACLE_OK;
 }

@@ -11,6 +11,8 @@ from ._lib import (  # noqa: F401
     Plan,
     SpecAttnError,
     STATUS,
+    defrag_apply,
+    defrag_moves,
     dims_for,
     kv_append,
     library_path,

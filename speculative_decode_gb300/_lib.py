@@ -66,6 +66,8 @@ def load_library() -> ctypes.CDLL:
         "sa_paged_attn_noalloc": ([DP, P, P, P, P, P, P, F, P, P, P], ctypes.c_int),
         "sa_spec_verify_workspace_size": ([I32, I32, I32], SZ),
         "sa_spec_verify_greedy": ([P, P, P, I32, I32, I32, P, P, P, P, SZ, P, P], ctypes.c_int),
+        "sa_defrag_moves": ([DP, P, P, P, P, P, P], ctypes.c_int),
+        "sa_defrag_apply": ([DP, P, P, P, I32, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -217,3 +219,25 @@ def spec_verify_greedy(logits, candidates, n_cand, accepted, next_tok, workspace
                                               _ptr(window), _ptr(workspace), nbytes,
                                               _ptr(err_flag), _stream(stream))
     _check(rc, "sa_spec_verify_greedy")
+
+
+def defrag_moves(dims: Dims, block_table_host, seq_lens_host):
+    """Host compaction plan: (new_table, moves [n, 2] as (from, to), n_live)."""
+    import numpy as np
+    bt = np.ascontiguousarray(block_table_host, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+    new = np.empty_like(bt)
+    moves = np.empty((max(dims.num_pages, 1), 2), np.int32)
+    n_moves, n_live = ctypes.c_int32(), ctypes.c_int32()
+    rc = load_library().sa_defrag_moves(ctypes.byref(dims), bt.ctypes.data, sl.ctypes.data,
+                                        new.ctypes.data, moves.ctypes.data, ctypes.byref(n_moves),
+                                        ctypes.byref(n_live))
+    _check(rc, "sa_defrag_moves")
+    return new, moves[:n_moves.value].copy(), n_live.value
+
+
+def defrag_apply(dims: Dims, k_pages, v_pages, moves, n_moves: int, err_flag=None, stream=None) -> None:
+    """Make the moves (a device int32 [n, 2] tensor) on both page pools."""
+    rc = load_library().sa_defrag_apply(ctypes.byref(dims), _ptr(k_pages), _ptr(v_pages), _ptr(moves),
+                                        int(n_moves), _ptr(err_flag), _stream(stream))
+    _check(rc, "sa_defrag_apply")

@@ -353,6 +353,33 @@ int sa_spec_verify_greedy(const float *logits, const int32_t *candidates, const 
     return finish(s, err_flag);
 }
 
+int sa_defrag_moves(const sa_dims *dims, const int32_t *block_table, const int32_t *seq_lens,
+                    int32_t *new_table, int32_t *moves, int32_t *n_moves, int32_t *n_live) {
+    if (dims == nullptr || n_moves == nullptr || n_live == nullptr) return SA_ERR_ARG;
+    if (dims->num_seqs < 0 || dims->num_pages < 0 || dims->max_pages_per_seq < 0) return SA_ERR_ARG;
+    if (dims->num_seqs > 0 && (!block_table || !seq_lens || !new_table)) return SA_ERR_ARG;
+    if (dims->num_pages > 0 && !moves) return SA_ERR_ARG;
+    return defrag_plan_host(dims->num_seqs, dims->num_pages, dims->max_pages_per_seq, block_table,
+                            seq_lens, new_table, moves, n_moves, n_live);
+}
+
+int sa_defrag_apply(const sa_dims *dims, uint16_t *k_pages, uint16_t *v_pages, const int32_t *moves,
+                    int32_t n_moves, int32_t *err_flag, void *stream) {
+    int rc = check_dims(dims);
+    if (rc) return rc;
+    if (n_moves < 0) return SA_ERR_ARG;
+    if (n_moves == 0) return SA_OK;
+    if (!k_pages || !v_pages || !moves) return SA_ERR_ARG;
+    if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(moves, 4)) return SA_ERR_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return SA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_defrag(k_pages, v_pages, moves, n_moves, dims->num_pages, dims->num_kv_heads, err_flag, sms,
+                      s) != cudaSuccess)
+        return SA_ERR_CUDA;
+    return finish(s, err_flag);
+}
+
 // ---------------------------------------------------------------------------
 // Paged attention without any allocation by the caller or the library.
 //

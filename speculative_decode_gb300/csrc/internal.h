@@ -72,6 +72,13 @@ int split_tile_tokens();  // tokens per K/V tile of the split kernel
 int split_units_per_tile();  // balancing units of one tile and of a segment start
 int split_segment_cost();
 
+// Cache compaction (defrag.cu): the host planner and the page-copy kernel.
+int defrag_plan_host(int num_seqs, int num_pages, int max_pages, const int32_t *block_table,
+                     const int32_t *seq_lens, int32_t *new_table, int32_t *moves, int32_t *n_moves,
+                     int32_t *n_live);
+cudaError_t launch_defrag(uint16_t *k_pages, uint16_t *v_pages, const int32_t *moves, int n_moves,
+                          int num_pages, int num_kv_heads, int32_t *err, int sms, cudaStream_t stream);
+
 cudaError_t launch_kv_append(const sa_dims &d, const uint16_t *k_new, const uint16_t *v_new,
                              uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,
                              const int32_t *seq_lens, const int32_t *q_lens, int32_t *err,

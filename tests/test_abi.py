@@ -123,3 +123,28 @@ def test_planner_keeps_small_groups_on_the_split_path(sa):
     skip, _, runs, tiles = sa.plan_analyze(d, bt, np.array([P + 3, P + 9], np.int32),
                                            np.ones(2, np.int32), 148)
     assert runs == 0 and tiles == 0 and (skip == 0).all()
+
+
+@needs_nvcc
+@pytest.mark.parametrize("seed,shared", [(0, 0), (1, 3), (2, 1)])
+def test_defrag_planner_matches_oracle_without_gpu(sa, seed, shared):
+    """The library's host planner gives exactly the oracle's compaction."""
+    import oracle
+    w = wl.random_case(900 + seed, num_seqs=7, Hq=4, Hkv=2, max_ctx=2000, q_len_choices=(1, 6),
+                       num_pages=80, shared_prefix_pages=shared)
+    d = sa.dims_for(w.num_seqs, 4, 2, w.num_pages, w.max_pages_per_seq, w.total_q, 6)
+    new, moves, L = sa.defrag_moves(d, w.block_table, w.seq_lens)
+    new_o, moves_o, L_o = oracle.defrag_plan(w.block_table, w.seq_lens, w.num_pages)
+    assert L == L_o and np.array_equal(new, new_o) and np.array_equal(moves, moves_o)
+
+
+@needs_nvcc
+def test_defrag_planner_rejects_bad_tables(sa):
+    d = sa.dims_for(1, 4, 2, 4, 2, 1, 1)
+    with pytest.raises(sa.SpecAttnError):
+        sa.defrag_moves(d, np.array([[0, 5]], np.int32), np.array([300], np.int32))
+    with pytest.raises(sa.SpecAttnError):
+        sa.defrag_moves(d, np.array([[0, 1]], np.int32), np.array([513], np.int32))
+    lib = sa.load_library()
+    assert lib.sa_defrag_apply(ctypes.byref(d), None, None, None, -1, None, None) == 1
+    assert lib.sa_defrag_apply(ctypes.byref(d), None, None, None, 0, None, None) == 0

@@ -379,3 +379,52 @@ def test_verify_rejects_n_cand_above_k_max():
     with pytest.raises(oracle.OracleError, match="code 1"):
         oracle.verify_greedy(np.zeros((1, 3, 4), np.float32), np.zeros((1, 2), np.int32),
                              np.array([3], np.int32))
+
+
+# ------------------------------------------------------------ defragmentation
+DEFRAG = os.path.join(os.path.dirname(__file__), "golden", "defrag_cases.json")
+
+
+def test_defrag_hand_worked_cases():
+    for c in json.load(open(DEFRAG))["cases"]:
+        new, moves, n_live = oracle.defrag_plan(np.array(c["block_table"], np.int32),
+                                                np.array(c["seq_lens"], np.int32), c["num_pages"])
+        e = c["expect"]
+        assert n_live == e["n_live"], c["note"]
+        assert moves.tolist() == e["moves"], c["note"]
+        assert new.tolist() == e["new_table"], c["note"]
+
+
+@pytest.mark.parametrize("seed,shared", [(0, 0), (1, 2), (2, 0), (3, 3)])
+def test_defrag_compacts_and_keeps_attention_bitwise(seed, shared):
+    """Live pages end up exactly at ids 0..L-1 through one map (shared pages
+    stay shared), the moves are independent, and attention read through the
+    new tables over the moved pools equals attention before, bit for bit."""
+    w = wl.random_case(700 + seed, num_seqs=5, Hq=4, Hkv=2, max_ctx=1300, q_len_choices=(1, 2, 6),
+                       num_pages=64, shared_prefix_pages=shared)
+    used = [(b, j) for b, T in enumerate(w.seq_lens) for j in range(-(-int(T) // P))]
+    new, moves, L = oracle.defrag_plan(w.block_table, w.seq_lens, w.num_pages)
+    pairs = {(int(w.block_table[b, j]), int(new[b, j])) for b, j in used}
+    assert L == len({o for o, _ in pairs})
+    assert {n for _, n in pairs} == set(range(L))
+    assert len({n for _, n in pairs}) == len(pairs)          # one-to-one: shared stays shared
+    assert all(o == n for o, n in pairs if o < L)             # pages below L stay
+    f, t = moves[:, 0], moves[:, 1]
+    assert np.all(f >= L) and np.all(t < L) and len(set(t.tolist())) == len(t)
+    assert sorted(zip(f.tolist(), t.tolist())) == sorted((o, n) for o, n in pairs if o != n)
+    kp, vp = oracle.defrag_move(w.k_pages, w.v_pages, moves)
+    args = (w.seq_lens, w.q_lens, w.scale)
+    before = oracle.paged_attention(w.q, w.k_pages, w.v_pages, w.block_table, *args)
+    assert np.array_equal(before, oracle.paged_attention(w.q, kp, vp, new, *args))
+    if len(moves):  # the new tables without the moves read other pages
+        assert not np.array_equal(before, oracle.paged_attention(w.q, w.k_pages, w.v_pages, new, *args))
+
+
+def test_defrag_rejects_bad_tables():
+    bt = np.array([[0, 1]], np.int32)
+    with pytest.raises(oracle.OracleError):
+        oracle.defrag_plan(np.array([[0, 5]], np.int32), np.array([300], np.int32), 4)  # page 5 of 4
+    with pytest.raises(oracle.OracleError):
+        oracle.defrag_plan(bt, np.array([513], np.int32), 4)  # needs 3 entries, table has 2
+    new, moves, L = oracle.defrag_plan(bt, np.array([0], np.int32), 4)
+    assert L == 0 and len(moves) == 0 and new.tolist() == [[-1, -1]]
