@@ -67,7 +67,8 @@ typedef struct {
     int32_t num_pages;         /* physical pages in the pool */
     int32_t max_pages_per_seq; /* row stride of block_table */
     int32_t total_q;           /* sum of q_lens: rows of q and out */
-    int32_t max_q_len;         /* upper bound on every q_lens[b] (1 for decode, k+1 to verify), <= 16 */
+    int32_t max_q_len;         /* upper bound on every q_lens[b] (1 for decode, k+1 to verify, a prefill
+                                  chunk's length), <= 512 (<= 16 with a plan) */
 } sa_dims;
 
 typedef struct sa_plan sa_plan;
@@ -119,6 +120,7 @@ SA_API int sa_kv_append(const sa_dims *dims, const uint16_t *k_new, const uint16
  * The plan allocates one device buffer (its work lists) with cudaMalloc and
  * frees it in sa_plan_destroy. Make a new plan whenever the block tables or
  * lengths change. A plan with no shared runs is valid and costs nothing.
+ * Plans take max_q_len <= 16 (else SA_ERR_UNSUPPORTED).
  * On success *out receives the plan.
  */
 SA_API int sa_plan_create(const sa_dims *dims, const int32_t *block_table_host,

@@ -13,7 +13,8 @@ namespace sa {
 
 constexpr int kHeadDim = 128;
 constexpr int kPageSize = 256;
-constexpr int kMaxQLen = 16;
+constexpr int kMaxQLen = 512;     // new tokens per sequence in one call (decode 1, verify k+1, prefill chunks)
+constexpr int kPlanMaxQLen = 16;  // with a shared-prefix plan
 constexpr int kMaxKMax = 15;
 
 constexpr int32_t kErrBitPageOOB = 1 << SA_ERR_PAGE_OOB;

@@ -218,7 +218,7 @@ int check_plan_args(const sa_dims *d, const int32_t *bt, const int32_t *sl, cons
     if (d == nullptr || d->num_seqs < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 ||
         d->num_q_heads % d->num_kv_heads != 0 || d->max_pages_per_seq < 0 || d->total_q < 0)
         return SA_ERR_ARG;
-    if (d->head_dim != kHeadDim || d->page_size != kPageSize || d->max_q_len > kMaxQLen)
+    if (d->head_dim != kHeadDim || d->page_size != kPageSize || d->max_q_len > kPlanMaxQLen)
         return SA_ERR_UNSUPPORTED;
     if (d->num_seqs > 0 && (bt == nullptr || sl == nullptr || ql == nullptr)) return SA_ERR_ARG;
     int64_t tq = 0;

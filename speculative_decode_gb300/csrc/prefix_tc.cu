@@ -715,7 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (P.seq_mode && i > 0) {
                     // the softmax warps load this piece's query rows when the previous
                     // piece ends; bring them into L2 now, while that piece still runs
-                    for (int k = 0; k < pc.seq_n; ++k)
+                    const int k_hi = min(pc.seq_n, (pc.row0 + kM + P.G - 1) / P.G);
+                    for (int k = pc.row0 / P.G; k < k_hi; ++k)
                         bulk_prefetch_l2(P.q + (static_cast<int64_t>(pc.qstart + k) * P.Hq + pc.g * P.G) * kHeadDim,
                                          P.G * kHeadDim * 2);
                 }

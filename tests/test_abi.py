@@ -57,8 +57,12 @@ def test_host_side_argument_checks_need_no_gpu(sa):
     assert lib.sa_paged_attn(ctypes.byref(d), *([None] * 6), 0.1, None, None, None, 0, None, None) == 2
     d = sa.dims_for(4, 8, 3, 16, 4, 4, 1)      # Hq not a multiple of Hkv
     assert lib.sa_kv_append(ctypes.byref(d), *([None] * 9)) == 1
-    d = sa.dims_for(4, 8, 2, 16, 4, 4, 17)     # max_q_len above 16
+    d = sa.dims_for(4, 8, 2, 16, 4, 4, 513)    # max_q_len above 512
     assert lib.sa_paged_attn(ctypes.byref(d), *([None] * 6), 0.1, None, None, None, 0, None, None) == 2
+    d = sa.dims_for(1, 8, 2, 16, 4, 17, 17)     # plans take max_q_len <= 16
+    bt, sl, ql = np.zeros((1, 4), np.int32), np.array([17], np.int32), np.array([17], np.int32)
+    assert lib.sa_plan_analyze(ctypes.byref(d), bt.ctypes.data, sl.ctypes.data, ql.ctypes.data, 148,
+                               None, None, None, None) == 2
     d = sa.dims_for(4, 8, 2, 16, 4, 4, 1)
     assert lib.sa_paged_attn(ctypes.byref(d), *([None] * 6), 0.1, None, None, None, 0, None, None) == 1
     assert lib.sa_spec_verify_greedy(None, None, None, 2, 16, 100, *([None] * 4), 0, None, None) == 2

@@ -46,6 +46,36 @@ def test_random_small_cases(seed):
     assert_attention_close(out, oracle_attention(w), f"seed {seed}")
 
 
+@pytest.mark.parametrize("seed,G,q_choices", [(0, 4, (64, 200)), (1, 1, (17, 300)), (2, 8, (33, 128)),
+                                              (3, 4, (1, 6, 512))])
+def test_prefill_chunks(seed, G, q_choices):
+    """Long blocks of new tokens (prefill chunks through the pages, causal
+    inside the chunk; the tensor cores take them), appended then attended,
+    every row against the oracle; the last case mixes decode, verify and
+    prefill rows in one call."""
+    Hkv = 2
+    w = wl.random_case(1500 + seed, num_seqs=3, Hq=G * Hkv, Hkv=Hkv, max_ctx=1400, q_len_choices=q_choices)
+    out, err, _, _ = run_attention(w)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), f"seed {seed}")
+
+
+def test_prefill_chunk_workload_sampled_rows():
+    """The chunked-prefill workload the benchmark times, at full size (8
+    sequences, 3584 cached + 512 new tokens, 32q/8kv): every chunk's first and
+    last rows and 512 random rows against the oracle."""
+    w = wl.prefill_chunk()
+    out, err, _, _ = run_attention(w)
+    assert err == 0
+    rng = np.random.default_rng(5)
+    starts = np.concatenate([[0], np.cumsum(w.q_lens)[:-1]])
+    tok = np.concatenate([rng.integers(0, w.total_q, 512), starts, starts + w.q_lens - 1]).astype(np.int64)
+    hd = rng.integers(0, w.num_q_heads, len(tok)).astype(np.int32)
+    kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table, w.pos_start, w.q_lens)
+    ref = oracle.attention_rows(w.q, kp, vp, w.block_table, w.seq_lens, w.q_lens, w.scale, tok, hd)
+    assert_attention_close(out[tok, hd], ref, "prefill chunk")
+
+
 def test_kv_append_bit_exact():
     w = wl.random_case(31, num_seqs=5, Hq=8, Hkv=4, max_ctx=900, q_len_choices=(0, 1, 5, 16))
     _, err, kp, vp = run_attention(w)

@@ -83,6 +83,7 @@ def test_bf16_conversion_is_exact_for_every_pattern():
     (2, [257, 6, 1024], [6, 6, 1], 4, 4),
     (3, [40, 513], [0, 3], 6, 2),
     (4, [256, 255, 2], [2, 1, 2], 8, 1),
+    (5, [700, 300], [300, 120], 4, 2),   # prefill chunks: long causal blocks of new tokens
 ])
 def test_attention_matches_dense_sdpa(seed, seq_lens, q_lens, Hq, Hkv):
     case, dk, dv = dense_case(seed, seq_lens, q_lens, Hq, Hkv)

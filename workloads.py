@@ -243,6 +243,22 @@ def config(idx: int, seed: Optional[int] = None) -> Workload:
     raise ValueError(f"no config {idx}")
 
 
+def prefill_chunk(seed: int = 1100, num_seqs: int = 8, cached: int = 3584, chunk: int = 512,
+                  Hq: int = 32, Hkv: int = 8) -> Workload:
+    """Chunked prefill through the pages: every sequence has `cached` tokens
+    in the cache and appends a `chunk`-token block of new tokens (causal
+    inside the block), Llama3-8B-shaped heads, tables on a shuffled pool with
+    spare pages."""
+    rng = np.random.default_rng(seed)
+    P = PAGE_SIZE
+    T = cached + chunk
+    per_seq = -(-T // P)
+    alloc = PageAllocator(num_seqs * per_seq + 32, rng)
+    tables = [alloc.alloc(per_seq) for _ in range(num_seqs)]
+    return _finish(f"prefill-chunk-{num_seqs}seq-{cached}+{chunk}-{Hq}q{Hkv}kv", rng, Hq, Hkv,
+                   num_seqs * per_seq + 32, tables, [T] * num_seqs, [chunk] * num_seqs, max_pages=per_seq)
+
+
 def random_case(seed: int, num_seqs: int = 3, Hq: int = 4, Hkv: int = 2, max_ctx: int = 700,
                 q_len_choices=(0, 1, 2, 6), num_pages: Optional[int] = None,
                 shared_prefix_pages: int = 0) -> Workload:
