@@ -100,6 +100,12 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only); completes at a later
+// cp.async.wait_all of the same thread.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
 // The same with an L2 cache-policy hint (createpolicy).
 __device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
                                                uint64_t policy) {

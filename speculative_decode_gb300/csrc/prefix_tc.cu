@@ -455,21 +455,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // the piece's Q rows -> shared memory, 128-byte swizzled K-major (two
         // 64-column blocks), one copy per row group; every Q K^T of the
-        // previous piece has completed. The 128 threads read the rows together,
-        // 16 bytes each (16 threads per row), and write every copy. Lanes past
-        // the piece's rows keep whatever they hold: their S, P and O lanes are
-        // never read for output.
+        // previous piece has completed. The 128 threads copy the rows together
+        // with 16-byte asynchronous copies (16 threads per row: thread t takes
+        // column chunk t % 16 of rows t / 16 + 8k, for every copy of the row),
+        // all of a thread's copies in flight at once, then wait for them. Lanes
+        // past the piece's rows keep whatever they hold: their S, P and O lanes
+        // are never read for output.
         auto write_q = [&](const TcPiece &pc, const RowMap &m) {
             const int nrow = min(m.rpc, pc.row_count - pc.row0);
-            for (int idx = t; idx < nrow * 16; idx += kM) {
-                const int rr = idx >> 4, c = idx & 15;
+            const int c = t & 15;
+            for (int rr = t >> 4; rr < nrow; rr += 8) {
                 int32_t tk, hh, lim, sl;
                 row_of(pc, pc.row0 + rr, tk, hh, lim, sl);
-                const uint4 w = *reinterpret_cast<const uint4 *>(
-                    P.q + (static_cast<int64_t>(tk) * P.Hq + pc.g * P.G + hh) * kHeadDim + c * 8);
+                const uint16_t *src = P.q + (static_cast<int64_t>(tk) * P.Hq + pc.g * P.G + hh) * kHeadDim + c * 8;
                 for (int cp = 0; cp < m.rf; ++cp)
-                    *reinterpret_cast<uint4 *>(smem + kOffQ + (c >> 3) * kRowBlk + sw128_offset(cp * m.rpc + rr, c & 7)) = w;
+                    cp_async16(smem + kOffQ + (c >> 3) * kRowBlk + sw128_offset(cp * m.rpc + rr, c & 7), src);
             }
+            asm volatile("cp.async.wait_all;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(q_full);
         };
