@@ -291,18 +291,32 @@ def rank_seed(cfg: int, rank: int) -> int:
 def e2e_steps(batch: GpuBatch, steps: int, warmup: int):
     """The same decode step through the public API with host buffers: every
     step copies its inputs host->device from pinned memory and reads the
-    attention output back device->host; timed with events around all of it."""
+    attention output back device->host; timed with events around all of it.
+    The inputs (q, k_new, v_new, tables, lengths) sit in one pinned staging
+    buffer and go over in one copy into one device buffer, of which the
+    kernels read 256-byte-aligned views, as a serving loop would stage them."""
     torch = batch.torch
     stream = torch.cuda.current_stream()
-    host_in = [batch.q, batch.k_new, batch.v_new, batch.bt, batch.sl, batch.ql]
-    pinned = [t.cpu().pin_memory() for t in host_in]
+    names = ["q", "k_new", "v_new", "bt", "sl", "ql"]
+    srcs = [getattr(batch, n) for n in names]
+    sizes = [t.numel() * t.element_size() for t in srcs]
+    offs, total = [], 0
+    for n in sizes:
+        offs.append(total)
+        total += (n + 255) // 256 * 256
+    host_buf = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=srcs[0].device)
+    saved = {}
+    for name, t, o, n in zip(names, srcs, offs, sizes):
+        host_buf[o:o + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+        saved[name] = t
+        setattr(batch, name, dev_buf[o:o + n].view(t.dtype).view(t.shape))
     out_host = torch.empty(batch.out.shape, dtype=batch.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    h2d = sum(sizes)
     d2h = out_host.numel() * out_host.element_size()
 
     def step():
-        for dst, src in zip(host_in, pinned):
-            dst.copy_(src, non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         batch.append()
         batch.attend()
         out_host.copy_(batch.out, non_blocking=True)
@@ -318,6 +332,8 @@ def e2e_steps(batch: GpuBatch, steps: int, warmup: int):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
+    for name, t in saved.items():
+        setattr(batch, name, t)
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
@@ -490,7 +506,7 @@ def run_ours(args):
         "dedup": dedup,
         "defrag": defrag,
         "prefill": prefill,
-        "e2e": {"value": round(world * cbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(world * sbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": int(args.steps * batch.launches_per_step()),
