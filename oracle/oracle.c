@@ -42,6 +42,13 @@
  *    window grows; NaN never wins an argmax and an all-NaN row gives 0;
  *    -0.0 and +0.0 compare equal (a tie).
  *
+ *  - int8 pages: the ExLlamaV2 "Dynamic Generator" page, in its setup of the
+ *    model and cache, names quantised cache modes (Q4 now, Q8 planned) but
+ *    defines no format. Reading: every (page, KV head, token) row of 128 values
+ *    is stored as 128 int8 codes and one binary32 scale, scale = amax / 127,
+ *    code = round-to-nearest-even(x / scale) in binary32; a cached value is
+ *    code * scale, and attention is the plain definition over those values.
+ *
  *  - defragmentation: releasing pages leaves holes in the cache; the block
  *    table need not be contiguous, and the cache can be defragmented (the
  *    generator does it only when its job queue is empty).  ExLlamaV2
@@ -123,6 +130,9 @@ typedef struct {
     const uint16_t *q, *k_pages, *v_pages;
     const int32_t *block_table, *seq_lens, *q_lens;
     double scale;
+    /* int8 pages (NULL for bf16 pages): value = code * the row's scale */
+    const int8_t *k_codes, *v_codes;
+    const float *k_scales, *v_scales;
 } attn_args;
 
 /* One output row: new token i of sequence b, query head h. `kbuf`/`vbuf`
@@ -141,10 +151,19 @@ static int attention_row(const attn_args *a, const int64_t *q_row_of_seq, int b,
     for (int64_t t = 0; t < nkeys; ++t) {
         int64_t pg = page_of(a->block_table, a->max_pages_per_seq, a->num_pages, a->page_size, b, t);
         if (pg < 0) return ORACLE_ERR_PAGE_OOB;
-        int64_t base = ((pg * a->num_kv_heads + g) * a->page_size + t % a->page_size) * d;
-        for (int c = 0; c < d; ++c) {
-            kbuf[t * d + c] = oracle_bf16_to_f64(a->k_pages[base + c]);
-            vbuf[t * d + c] = oracle_bf16_to_f64(a->v_pages[base + c]);
+        int64_t srow = (pg * a->num_kv_heads + g) * a->page_size + t % a->page_size;
+        int64_t base = srow * d;
+        if (a->k_codes) { /* int8 pages: exact in double (an 8-bit integer times an fp32 scale) */
+            double ks = a->k_scales[srow], vs = a->v_scales[srow];
+            for (int c = 0; c < d; ++c) {
+                kbuf[t * d + c] = (double)a->k_codes[base + c] * ks;
+                vbuf[t * d + c] = (double)a->v_codes[base + c] * vs;
+            }
+        } else {
+            for (int c = 0; c < d; ++c) {
+                kbuf[t * d + c] = oracle_bf16_to_f64(a->k_pages[base + c]);
+                vbuf[t * d + c] = oracle_bf16_to_f64(a->v_pages[base + c]);
+            }
         }
     }
     /* 2. scores s_t = scale * q . k_t */
@@ -190,15 +209,10 @@ static int64_t *q_row_offsets(const attn_args *a) {
 
 /* Rows to compute are given as (packed query token, head) pairs; out is
  * [n_rows, head_dim]. n_threads <= 0 uses the OpenMP default. */
-int oracle_attention_rows(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                          int page_size, int num_pages, int max_pages_per_seq,
-                          const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
-                          const int32_t *block_table, const int32_t *seq_lens,
-                          const int32_t *q_lens, double scale,
-                          const int64_t *row_token, const int32_t *row_head, int64_t n_rows,
-                          double *out, int n_threads) {
-    attn_args a = {num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
-                   max_pages_per_seq, q, k_pages, v_pages, block_table, seq_lens, q_lens, scale};
+static int attention_rows_impl(attn_args a, const int64_t *row_token, const int32_t *row_head,
+                               int64_t n_rows, double *out, int n_threads) {
+    const int num_seqs = a.num_seqs, num_q_heads = a.num_q_heads, head_dim = a.head_dim;
+    const int32_t *seq_lens = a.seq_lens;
     int rc = check_attn_args(&a);
     if (rc) return rc;
     int64_t *off = q_row_offsets(&a);
@@ -243,6 +257,19 @@ int oracle_attention_rows(int num_seqs, int num_q_heads, int num_kv_heads, int h
     return status;
 }
 
+int oracle_attention_rows(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int page_size, int num_pages, int max_pages_per_seq,
+                          const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
+                          const int32_t *block_table, const int32_t *seq_lens,
+                          const int32_t *q_lens, double scale,
+                          const int64_t *row_token, const int32_t *row_head, int64_t n_rows,
+                          double *out, int n_threads) {
+    attn_args a = {num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                   max_pages_per_seq, q, k_pages, v_pages, block_table, seq_lens, q_lens, scale,
+                   NULL, NULL, NULL, NULL};
+    return attention_rows_impl(a, row_token, row_head, n_rows, out, n_threads);
+}
+
 /* Every row: out is [total_q, num_q_heads, head_dim]. */
 int oracle_paged_attention(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                            int page_size, int num_pages, int max_pages_per_seq,
@@ -269,6 +296,74 @@ int oracle_paged_attention(int num_seqs, int num_q_heads, int num_kv_heads, int 
     free(tok);
     free(head);
     return rc;
+}
+
+/* ------------------------------------------------------------- int8 pages */
+
+/* One row of d bf16 values -> d int8 codes and one scale: scale = amax / 127
+ * and code = round-to-nearest-even(x / scale), both in binary32 (the width
+ * the GPU path decides the codes in); a row of zeros gets scale 0 and codes
+ * 0. Inputs are finite. */
+int oracle_quantize_q8(const uint16_t *x, int64_t n_rows, int d, int8_t *codes, float *scales) {
+    for (int64_t r = 0; r < n_rows; ++r) {
+        float amax = 0.f;
+        for (int c = 0; c < d; ++c) {
+            float v = (float)oracle_bf16_to_f64(x[r * d + c]);
+            float av = v < 0.f ? -v : v;
+            if (av > amax) amax = av;
+        }
+        float sc = amax / 127.0f;
+        scales[r] = sc;
+        for (int c = 0; c < d; ++c) {
+            float v = (float)oracle_bf16_to_f64(x[r * d + c]);
+            float qv = sc > 0.f ? rintf(v / sc) : 0.f;
+            if (qv > 127.f) qv = 127.f;
+            if (qv < -127.f) qv = -127.f;
+            codes[r * d + c] = (int8_t)qv;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* kv_append for int8 pages: each new (token, KV head) row is quantized as
+ * above and written, codes and scale, where the block table puts it. */
+int oracle_kv_append_q8(int num_seqs, int num_kv_heads, int head_dim, int page_size,
+                        int num_pages, int max_pages_per_seq,
+                        const uint16_t *k_new, const uint16_t *v_new,
+                        int8_t *k_codes, int8_t *v_codes, float *k_scales, float *v_scales,
+                        const int32_t *block_table, const int32_t *pos_start,
+                        const int32_t *new_lens) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || page_size <= 0) return ORACLE_ERR_ARG;
+    int64_t row = 0;
+    for (int b = 0; b < num_seqs; ++b) {
+        for (int i = 0; i < new_lens[b]; ++i, ++row) {
+            int64_t pos = (int64_t)pos_start[b] + i;
+            int64_t pg = page_of(block_table, max_pages_per_seq, num_pages, page_size, b, pos);
+            if (pg < 0) return ORACLE_ERR_PAGE_OOB;
+            for (int g = 0; g < num_kv_heads; ++g) {
+                int64_t drow = (pg * num_kv_heads + g) * page_size + pos % page_size;
+                int64_t src = (row * num_kv_heads + g) * head_dim;
+                oracle_quantize_q8(k_new + src, 1, head_dim, k_codes + drow * head_dim, k_scales + drow);
+                oracle_quantize_q8(v_new + src, 1, head_dim, v_codes + drow * head_dim, v_scales + drow);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Attention over int8 pages: as oracle_attention_rows with every cached value
+ * replaced by code * scale (exact in double). */
+int oracle_attention_rows_q8(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int page_size, int num_pages, int max_pages_per_seq, const uint16_t *q,
+                             const int8_t *k_codes, const int8_t *v_codes, const float *k_scales,
+                             const float *v_scales, const int32_t *block_table,
+                             const int32_t *seq_lens, const int32_t *q_lens, double scale,
+                             const int64_t *row_token, const int32_t *row_head, int64_t n_rows,
+                             double *out, int n_threads) {
+    attn_args a = {num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                   max_pages_per_seq, q, NULL, NULL, block_table, seq_lens, q_lens, scale,
+                   k_codes, v_codes, k_scales, v_scales};
+    return attention_rows_impl(a, row_token, row_head, n_rows, out, n_threads);
 }
 
 /* ------------------------------------------------------- greedy verification */

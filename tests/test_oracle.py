@@ -429,3 +429,63 @@ def test_defrag_rejects_bad_tables():
         oracle.defrag_plan(bt, np.array([513], np.int32), 4)  # needs 3 entries, table has 2
     new, moves, L = oracle.defrag_plan(bt, np.array([0], np.int32), 4)
     assert L == 0 and len(moves) == 0 and new.tolist() == [[-1, -1]]
+
+
+# ------------------------------------------------------------------ int8 pages
+Q8 = os.path.join(os.path.dirname(__file__), "golden", "q8_cases.json")
+
+
+def test_q8_hand_worked_rows():
+    for c in json.load(open(Q8))["cases"]:
+        bits = np.array([c["bits"]], np.uint16)
+        assert np.array_equal(wl.bf16_to_f32(bits)[0], np.array(c["values"], np.float32)), c["note"]
+        codes, scales = oracle.quantize_q8(bits)
+        assert codes[0].tolist() == c["expect"]["codes"], c["note"]
+        assert abs(float(scales[0]) * 127 - c["expect"]["scale_times_127"]) <= 1e-6 * max(1.0, c["expect"]["scale_times_127"])
+
+
+def test_q8_error_within_half_a_step():
+    """Every value is recovered within half a quantisation step, and the
+    largest magnitude of a non-zero row maps to +-127."""
+    rng = np.random.default_rng(3)
+    x = wl.normal_bf16(rng, (500, 128))
+    x[7] = 0
+    codes, scales = oracle.quantize_q8(x)
+    xf = wl.bf16_to_f32(x).astype(np.float64)
+    rec = codes.astype(np.float64) * scales.astype(np.float64)[:, None]
+    # half a step, plus the binary32 rounding of x / scale (|x / scale| <= 127,
+    # so that quotient is off by at most 127 * 2^-23 steps)
+    assert np.all(np.abs(rec - xf) <= scales.astype(np.float64)[:, None] * (0.5 + 127 * 2.0 ** -23))
+    nz = np.abs(xf).max(axis=1) > 0
+    assert np.all(np.abs(codes[nz]).max(axis=1) == 127)
+    assert scales[7] == 0 and not codes[7].any()
+
+
+def test_q8_attention_is_exact_on_representable_rows():
+    """Rows of integers in [-127, 127] that contain 127 quantise exactly
+    (scale 1), so attention over the int8 pages equals attention over the
+    bf16 pages, bit for bit."""
+    rng = np.random.default_rng(11)
+    w = wl.random_case(41, num_seqs=3, Hq=8, Hkv=2, max_ctx=600, q_len_choices=(1, 2))
+    for pool in (w.k_pages, w.v_pages):
+        ints = rng.integers(-127, 128, size=pool.shape).astype(np.float32)
+        ints[..., 5] = 127
+        pool[...] = (ints.view(np.uint32) >> 16).astype(np.uint16)  # integers <= 127 are exact in bf16
+    kc, ks = oracle.quantize_q8(w.k_pages)
+    vc, vs = oracle.quantize_q8(w.v_pages)
+    assert np.all(ks == 1) and np.all(vs == 1)
+    args = (w.block_table, w.seq_lens, w.q_lens, w.scale)
+    ref = oracle.paged_attention(w.q, w.k_pages, w.v_pages, *args)
+    assert np.array_equal(oracle.attention_rows_q8(w.q, kc, vc, ks, vs, *args), ref)
+
+
+def test_kv_append_q8_quantises_the_rows_kv_append_writes():
+    w = wl.random_case(42, num_seqs=4, Hq=4, Hkv=2, max_ctx=700, q_len_choices=(1, 3, 6))
+    kc, ks = oracle.quantize_q8(w.k_pages)
+    vc, vs = oracle.quantize_q8(w.v_pages)
+    kc2, vc2, ks2, vs2 = oracle.kv_append_q8(kc, vc, ks, vs, w.k_new, w.v_new, w.block_table,
+                                             w.pos_start, w.q_lens)
+    kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table, w.pos_start, w.q_lens)
+    for got, pages in (((kc2, ks2), kp), ((vc2, vs2), vp)):
+        c, s = oracle.quantize_q8(pages)
+        assert np.array_equal(got[0], c) and np.array_equal(got[1], s)
