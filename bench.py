@@ -288,6 +288,47 @@ def rank_seed(cfg: int, rank: int) -> int:
     return 1000 + cfg + 1 + 7919 * rank
 
 
+def q8_block(batch: GpuBatch, w: wl.Workload, dev, steps: int, warmup: int, flush):
+    """paged_attn over int8 pages for the decode batch: codes uniform in
+    [-127, 127] and per-row scales near those of N(0,1) rows (synthetic, seeded);
+    counted bytes = distinct cached tokens x heads x (128 codes + 4-byte scale)
+    x 2, plus q, out and the tables."""
+    torch, sa = batch.torch, batch.sa
+    rng = np.random.default_rng(2024)
+    shape = w.k_pages.shape
+    kc = torch.from_numpy(rng.integers(-127, 128, size=shape, dtype=np.int8)).to(dev)
+    vc = torch.from_numpy(rng.integers(-127, 128, size=shape, dtype=np.int8)).to(dev)
+    ks = torch.from_numpy((rng.uniform(2.5, 3.5, size=shape[:-1]) / 127).astype(np.float32)).to(dev)
+    vs = torch.from_numpy((rng.uniform(2.5, 3.5, size=shape[:-1]) / 127).astype(np.float32)).to(dev)
+    ws = torch.zeros(sa.paged_attn_workspace_size(batch.dims), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        sa.paged_attn_q8(batch.dims, batch.q, kc, vc, ks, vs, batch.bt, batch.sl, batch.ql, w.scale,
+                         batch.out, ws, err_flag=batch.err)
+
+    for _ in range(warmup):
+        flush()
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for e0, e1 in ev:
+        flush()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    assert int(batch.err.item()) == 0, "device error flag set"
+    t = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev))
+    tokens_heads = sum(int(T) for T in w.seq_lens) * w.num_kv_heads
+    q8_bytes = (tokens_heads * (128 + 4) * 2 + 2 * w.q.nbytes + w.block_table.nbytes + w.seq_lens.nbytes
+                + w.q_lens.nbytes)
+    return {"workload": w.name + " int8 pages", "paged_attn_ms": round(t, 5), "counted_bytes": int(q8_bytes),
+            "GBps": round(q8_bytes / (t * 1e-3) / 1e9, 1),
+            "cached_tokens_per_s": round(sum(int(T) for T in w.seq_lens) / (t * 1e-3), 1)}
+
+
 def e2e_steps(batch: GpuBatch, steps: int, warmup: int):
     """The same decode step through the public API with host buffers: every
     step copies its inputs host->device from pinned memory and reads the
@@ -448,6 +489,11 @@ def run_ours(args):
                "counts": "4 x 128 x visible keys per (new token, query head) row / paged_attn device time"}
     del pb
 
+    # ---- sixth block: the decode batch over int8 pages (synthetic seeded codes
+    # and per-row scales of the same shapes), attention only
+    q8 = q8_block(batch, w, dev, vsteps, args.warmup, flush)
+    q8["bf16_paged_attn_ms"] = round(t_attn_max, 5)
+
     peak, peak_kind = hbm_peak()
     achieved = cbytes / (t_attn_max * 1e-3) / 1e9
     defrag["frac_of_hbm_peak"] = round(defrag["GBps"] / peak, 4)
@@ -506,6 +552,7 @@ def run_ours(args):
         "dedup": dedup,
         "defrag": defrag,
         "prefill": prefill,
+        "q8": q8,
         "e2e": {"value": round(world * sbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 5)},

@@ -177,6 +177,42 @@ SA_API int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t 
                   const sa_plan *plan, void *workspace, size_t workspace_bytes,
                   int32_t *err_flag, void *stream);
 
+/*
+ * int8 K/V pages -- sa_kv_append_q8 and sa_paged_attn_q8.
+ *
+ * The ExLlamaV2 "Dynamic Generator" page, in its setup of the model and the
+ * cache, names quantised cache modes (Q4 now, a Q8 mode planned) but gives no
+ * format. This library's int8 format: for every (page, KV head, token) row of
+ * 128 values, 128 int8 codes and one fp32 scale, with
+ *   scale = amax / 127,  code = round-half-even(x / scale)
+ * both computed in fp32 (IEEE division); a row of zeros has scale 0 and codes
+ * 0. A cached value is code * scale. Pools:
+ *   k_codes, v_codes    device int8 [num_pages, num_kv_heads, 256, 128]
+ *   k_scales, v_scales  device fp32 [num_pages, num_kv_heads, 256]
+ * (code pools 16-byte aligned, scale pools 16-byte aligned for attention and
+ * 4-byte aligned for the append).
+ *
+ * sa_kv_append_q8: sa_kv_append for int8 pages: every new (token, KV head)
+ * row is quantised as above and written, codes and scale, where the block
+ * table puts it. Same arguments and errors as sa_kv_append.
+ *
+ * sa_paged_attn_q8: sa_paged_attn over int8 pages (same definition with every
+ * cached value code * scale; fp32 accumulation, bf16 output). No plan, and
+ * fewer than 16 query rows per KV head (num_q_heads / num_kv_heads *
+ * max_q_len < 16: decode, and short verification blocks with few heads per KV
+ * head), else SA_ERR_UNSUPPORTED. The workspace is that of
+ * sa_paged_attn_workspace_size(dims, NULL).
+ */
+SA_API int sa_kv_append_q8(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_new,
+                           int8_t *k_codes, int8_t *v_codes, float *k_scales, float *v_scales,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           const int32_t *q_lens, int32_t *err_flag, void *stream);
+SA_API int sa_paged_attn_q8(const sa_dims *dims, const uint16_t *q, const int8_t *k_codes,
+                            const int8_t *v_codes, const float *k_scales, const float *v_scales,
+                            const int32_t *block_table, const int32_t *seq_lens,
+                            const int32_t *q_lens, float scale, uint16_t *out, void *workspace,
+                            size_t workspace_bytes, int32_t *err_flag, void *stream);
+
 /* Number of kernels one sa_paged_attn call with these shapes launches
  * (diagnostics; the same decomposition the call itself uses). Needs a device. */
 SA_API int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan);

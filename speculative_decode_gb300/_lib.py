@@ -66,6 +66,8 @@ def load_library() -> ctypes.CDLL:
         "sa_paged_attn_noalloc": ([DP, P, P, P, P, P, P, F, P, P, P], ctypes.c_int),
         "sa_spec_verify_workspace_size": ([I32, I32, I32], SZ),
         "sa_spec_verify_greedy": ([P, P, P, I32, I32, I32, P, P, P, P, SZ, P, P], ctypes.c_int),
+        "sa_kv_append_q8": ([DP] + [P] * 11, ctypes.c_int),
+        "sa_paged_attn_q8": ([DP, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P], ctypes.c_int),
         "sa_defrag_moves": ([DP, P, P, P, P, P, P], ctypes.c_int),
         "sa_defrag_apply": ([DP, P, P, P, I32, P, P], ctypes.c_int),
     }
@@ -241,3 +243,23 @@ def defrag_apply(dims: Dims, k_pages, v_pages, moves, n_moves: int, err_flag=Non
     rc = load_library().sa_defrag_apply(ctypes.byref(dims), _ptr(k_pages), _ptr(v_pages), _ptr(moves),
                                         int(n_moves), _ptr(err_flag), _stream(stream))
     _check(rc, "sa_defrag_apply")
+
+
+def kv_append_q8(dims: Dims, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_table,
+                 seq_lens, q_lens, err_flag=None, stream=None) -> None:
+    """kv_append into int8 pages (codes int8 [pages, Hkv, 256, 128], scales fp32 [pages, Hkv, 256])."""
+    rc = load_library().sa_kv_append_q8(ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(k_codes),
+                                        _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_table),
+                                        _ptr(seq_lens), _ptr(q_lens), _ptr(err_flag), _stream(stream))
+    _check(rc, "sa_kv_append_q8")
+
+
+def paged_attn_q8(dims: Dims, q, k_codes, v_codes, k_scales, v_scales, block_table, seq_lens, q_lens,
+                  scale: float, out, workspace, err_flag=None, stream=None) -> None:
+    """paged_attn over int8 pages; the workspace is paged_attn_workspace_size(dims)."""
+    rc = load_library().sa_paged_attn_q8(ctypes.byref(dims), _ptr(q), _ptr(k_codes), _ptr(v_codes),
+                                         _ptr(k_scales), _ptr(v_scales), _ptr(block_table),
+                                         _ptr(seq_lens), _ptr(q_lens), float(scale), _ptr(out),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _ptr(err_flag), _stream(stream))
+    _check(rc, "sa_paged_attn_q8")

@@ -53,6 +53,12 @@ constexpr int kTile = SA_SPLIT_TILE;          // tokens per stage (16 or 32)
 constexpr int kRowBytes = kHeadDim * 2;       // one K or V row: 256 bytes
 constexpr int kKVBytes = kTile * kRowBytes;   // K (or V) rows of one tile, contiguous in a page
 constexpr int kStageBytes = 2 * kKVBytes;     // K tile, then V tile
+// int8 pages: a stage holds the tile's K codes, V codes, K scales, V scales
+constexpr int kQ8CodeBytes = kTile * kHeadDim;            // 2 KiB
+constexpr int kQ8ScaleBytes = kTile * 4;                  // 64 bytes
+constexpr int kQ8VCodes = kQ8CodeBytes, kQ8KScales = 2 * kQ8CodeBytes, kQ8VScales = kQ8KScales + kQ8ScaleBytes;
+constexpr int kQ8StageBytes = kQ8VScales + kQ8ScaleBytes;
+static_assert(kQ8StageBytes <= kStageBytes, "int8 tiles use the bf16 stage");
 #ifndef SA_SPLIT_STAGES
 #define SA_SPLIT_STAGES 2
 #endif
@@ -132,6 +138,36 @@ __device__ __forceinline__ void load_tile_row(const uint8_t *tile, int t, int j,
     } else {
         const uint2 a = *reinterpret_cast<const uint2 *>(row + j * 8);
         w[0] = a.x; w[1] = a.y;
+    }
+}
+
+// The same dims of row t of a tile of int8 codes (128-byte rows), as pairs of
+// floats (pair k holds this lane's dims of bf16 word k); the codes' scale is
+// applied by the caller, per token.
+// Codes are converted exactly without the (slow) integer-to-float unit: u =
+// code + 128 (the word xor 0x80808080) put in the low byte of the binary32
+// 2^23 is 2^23 + u, and one paired subtraction of 2^23 + 128 leaves the code.
+__device__ __forceinline__ float2 codes_pair(uint32_t w, int hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float a = __uint_as_float(__byte_perm(u, 0x4B000000u, hi ? 0x7442u : 0x7440u));
+    const float b = __uint_as_float(__byte_perm(u, 0x4B000000u, hi ? 0x7443u : 0x7441u));
+    return ffma2(make_float2(a, b), make_float2(1.f, 1.f), make_float2(-8388736.f, -8388736.f));
+}
+
+template <int L>
+__device__ __forceinline__ void load_tile_row_q8(const uint8_t *tile, int t, int j, float2 (&f)[64 / L]) {
+    const uint8_t *row = tile + t * kHeadDim;
+    if constexpr (L == 8) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(row + j * 8);
+        const uint2 b = *reinterpret_cast<const uint2 *>(row + 64 + j * 8);
+        f[0] = codes_pair(a.x, 0); f[1] = codes_pair(a.x, 1); f[2] = codes_pair(a.y, 0); f[3] = codes_pair(a.y, 1);
+        f[4] = codes_pair(b.x, 0); f[5] = codes_pair(b.x, 1); f[6] = codes_pair(b.y, 0); f[7] = codes_pair(b.y, 1);
+    } else if constexpr (L == 16) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(row + j * 8);
+        f[0] = codes_pair(a.x, 0); f[1] = codes_pair(a.x, 1); f[2] = codes_pair(a.y, 0); f[3] = codes_pair(a.y, 1);
+    } else {
+        const uint32_t a = *reinterpret_cast<const uint32_t *>(row + j * 4);
+        f[0] = codes_pair(a, 0); f[1] = codes_pair(a, 1);
     }
 }
 
@@ -433,7 +469,7 @@ __device__ __forceinline__ void locate_seq(const SplitParams &P, int lane, bool 
 }
 
 
-template <int R>
+template <int R, bool Q8>
 __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(const SplitParams P) {
     using Gm = Geo<R>;
     using Lay = Layout<R>;
@@ -620,19 +656,30 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         const int pid = page_id(ib, t0 / kPageSize, (isi.T + kPageSize - 1) / kPageSize);
         const bool ok = static_cast<unsigned>(pid) < static_cast<unsigned>(P.num_pages);
         if (!ok && lane == 0) flag_error(P.err, kErrBitPageOOB);
-        if (lane < 2) {
+        if (lane < (Q8 ? 4 : 2)) {
             if (ok) {
                 // The tile's K rows and V rows are each one contiguous run in the
                 // page: lane 0 copies the K rows, lane 1 the V rows, in one
                 // instruction (the copy instruction's issue is slow; two lanes
-                // take the time of one).
+                // take the time of one). int8 pages: lanes 2 and 3 copy the rows'
+                // K and V scales (also contiguous) in the same instruction.
                 const int64_t row = static_cast<int64_t>(pid * P.Hkv + kvh) * kPageSize + (t0 % kPageSize);
                 if (lane == 0) {
                     stage_ok[s] = 1;
-                    mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    mbar_arrive_expect_tx(&full[s], Q8 ? kQ8StageBytes : kStageBytes);
                 }
-                bulk_load_hint(smem + s * kStageBytes + lane * kKVBytes, (lane ? P.v_pages : P.k_pages) + row * kHeadDim,
-                               kKVBytes, &full[s], policy);
+                if constexpr (Q8) {
+                    const void *src = lane == 0 ? static_cast<const void *>(P.k_codes + row * kHeadDim)
+                                    : lane == 1 ? static_cast<const void *>(P.v_codes + row * kHeadDim)
+                                    : lane == 2 ? static_cast<const void *>(P.k_scales + row)
+                                                : static_cast<const void *>(P.v_scales + row);
+                    const int off = lane == 0 ? 0 : lane == 1 ? kQ8VCodes : lane == 2 ? kQ8KScales : kQ8VScales;
+                    bulk_load_hint(smem + s * kStageBytes + off, src, lane < 2 ? kQ8CodeBytes : kQ8ScaleBytes,
+                                   &full[s], policy);
+                } else {
+                    bulk_load_hint(smem + s * kStageBytes + lane * kKVBytes, (lane ? P.v_pages : P.k_pages) + row * kHeadDim,
+                                   kKVBytes, &full[s], policy);
+                }
             } else if (lane == 0) {
                 stage_ok[s] = 0;
                 mbar_arrive(&full[s]);  // nothing to load: the consumer skips this tile
@@ -718,13 +765,15 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                     for (int bi = 0; bi < NB; ++bi) {
                         const int t = (b0 + bi) * TG + tg;
                         uint32_t kw[NW];
-                        load_tile_row<L>(st, t, j, kw);
+                        float2 kq[NW];
+                        if constexpr (Q8) load_tile_row_q8<L>(st, t, j, kq);
+                        else load_tile_row<L>(st, t, j, kw);
                         float2 a2[R];
 #pragma unroll
                         for (int r = 0; r < R; ++r) a2[r] = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int k = 0; k < NW; ++k) {
-                            const float2 kf = unpack_bf16x2(kw[k]);
+                            const float2 kf = Q8 ? kq[k] : unpack_bf16x2(kw[k]);
 #pragma unroll
                             for (int r = 0; r < R; ++r) a2[r] = ffma2(q2[r][k], kf, a2[r]);
                         }
@@ -755,7 +804,9 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
 #pragma unroll
                     for (int bi = 0; bi < NB; ++bi) {
                         const int t = (b0 + bi) * TG + tg;
-                        sv[b0 + bi] = t0 + t <= lim ? v[bi][0] : -INFINITY;
+                        // int8 pages: the dot was over codes; the key row's scale completes it
+                        const float ks = Q8 ? reinterpret_cast<const float *>(st + kQ8KScales)[t] : 1.f;
+                        sv[b0 + bi] = t0 + t <= lim ? v[bi][0] * ks : -INFINITY;
                     }
                 }
 
@@ -778,7 +829,9 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                 for (int step = 0; step < NS; ++step) {
                     const float p = exp2f(sv[step] - m_use);
                     lsum += p;
-                    if (row_writer) pbuf[step * TG + tg][rj] = p;
+                    // int8 pages: p times the value row's scale, so that P V runs on codes
+                    if (row_writer)
+                        pbuf[step * TG + tg][rj] = Q8 ? p * reinterpret_cast<const float *>(st + kQ8VScales)[step * TG + tg] : p;
                 }
                 if (__any_sync(0xffffffffu, grow)) {
                     if (tg == 0 && row_writer) rowx[rj] = alpha;
@@ -799,7 +852,9 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                     const int t = step * TG + tg;
                     if (t < nvalid) {
                         uint32_t vw[NW];
-                        load_tile_row<L>(st + kKVBytes, t, j, vw);
+                        float2 vq[NW];
+                        if constexpr (Q8) load_tile_row_q8<L>(st + kQ8VCodes, t, j, vq);
+                        else load_tile_row<L>(st + kKVBytes, t, j, vw);
                         float pr[R];
 #pragma unroll
                         for (int r4 = 0; r4 < R / 4; ++r4) {
@@ -811,7 +866,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                         }
 #pragma unroll
                         for (int k = 0; k < NW; ++k) {
-                            const float2 vf = unpack_bf16x2(vw[k]);
+                            const float2 vf = Q8 ? vq[k] : unpack_bf16x2(vw[k]);
 #pragma unroll
                             for (int r = 0; r < R; ++r) acc[r][k] = ffma2(make_float2(pr[r], pr[r]), vf, acc[r][k]);
                         }
@@ -983,9 +1038,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32, SA_COMBINE_MIN_CTAS) combi
 template <int R>
 constexpr size_t smem_bytes() { return Layout<R>::kBytes + 1024; }
 
-template <int R>
+template <int R, bool Q8>
 cudaError_t prepare() {
-    static cudaError_t err = cudaFuncSetAttribute(split_attn_kernel<R>,
+    static cudaError_t err = cudaFuncSetAttribute(split_attn_kernel<R, Q8>,
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                   static_cast<int>(smem_bytes<R>()));
     return err;
@@ -1011,11 +1066,11 @@ cudaError_t launch_dependent(Kernel kernel, int grid, int threads, size_t smem, 
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int R>
+template <int R, bool Q8>
 cudaError_t launch_r(const SplitParams &p, cudaStream_t stream) {
-    cudaError_t e = prepare<R>();
+    cudaError_t e = prepare<R, Q8>();
     if (e != cudaSuccess) return e;
-    e = launch_dependent(split_attn_kernel<R>, p.split_ctas, 32, smem_bytes<R>(), stream, p);
+    e = launch_dependent(split_attn_kernel<R, Q8>, p.split_ctas, 32, smem_bytes<R>(), stream, p);
     if (e != cudaSuccess) return e;
     // the combine pass: its scan runs while the split kernel finishes
     const int64_t units = static_cast<int64_t>(p.B) * p.Hkv * p.n_row_blocks * (R / 4);
@@ -1023,11 +1078,11 @@ cudaError_t launch_r(const SplitParams &p, cudaStream_t stream) {
                             kCombineWarps * 32, 0, stream, p);
 }
 
-template <int R>
+template <int R, bool Q8>
 cudaError_t occupancy_r(int *ctas_per_sm) {
-    cudaError_t e = prepare<R>();
+    cudaError_t e = prepare<R, Q8>();
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, split_attn_kernel<R>, 32,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, split_attn_kernel<R, Q8>, 32,
                                                          smem_bytes<R>());
 }
 
@@ -1037,20 +1092,27 @@ int split_tile_tokens() { return kTile; }
 int split_units_per_tile() { return kUnitsPerTile; }
 int split_segment_cost() { return kSegmentCost; }
 
-cudaError_t split_occupancy(int R, int, int *ctas_per_sm) {
-    switch (R) {
-        case 4: return occupancy_r<4>(ctas_per_sm);
-        case 8: return occupancy_r<8>(ctas_per_sm);
-        case 16: return occupancy_r<16>(ctas_per_sm);
+cudaError_t split_occupancy(int R, bool q8, int *ctas_per_sm) {
+    switch (R * 2 + (q8 ? 1 : 0)) {
+        case 8: return occupancy_r<4, false>(ctas_per_sm);
+        case 16: return occupancy_r<8, false>(ctas_per_sm);
+        case 32: return occupancy_r<16, false>(ctas_per_sm);
+        case 9: return occupancy_r<4, true>(ctas_per_sm);
+        case 17: return occupancy_r<8, true>(ctas_per_sm);
+        case 33: return occupancy_r<16, true>(ctas_per_sm);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_split_attn(const SplitParams &p, cudaStream_t stream) {
-    switch (p.rows_per_block) {
-        case 4: return launch_r<4>(p, stream);
-        case 8: return launch_r<8>(p, stream);
-        case 16: return launch_r<16>(p, stream);
+    const bool q8 = p.k_codes != nullptr;
+    switch (p.rows_per_block * 2 + (q8 ? 1 : 0)) {
+        case 8: return launch_r<4, false>(p, stream);
+        case 16: return launch_r<8, false>(p, stream);
+        case 32: return launch_r<16, false>(p, stream);
+        case 9: return launch_r<4, true>(p, stream);
+        case 17: return launch_r<8, true>(p, stream);
+        case 33: return launch_r<16, true>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

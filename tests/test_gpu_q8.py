@@ -1,0 +1,82 @@
+"""int8 K/V pages on the GPU against the oracle: the append's codes and
+scales bit-exact, attention over int8 pages within the attention tolerance
+(the oracle attends the same code * scale values in fp64)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decode_gb300 as sa
+import workloads as wl
+from gpu_path import assert_attention_close, dev_tensor, dims_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from speculative_decode_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+def q8_pools(w):
+    kc, ks = oracle.quantize_q8(w.k_pages)
+    vc, vs = oracle.quantize_q8(w.v_pages)
+    return kc, vc, ks, vs
+
+
+def run_q8(w, append=True):
+    """kv_append_q8 (optional) then paged_attn_q8 on the GPU from pools the
+    oracle quantised; returns (out bits, err, pools after the call)."""
+    d = dims_of(w)
+    kc, vc, ks, vs = (dev_tensor(a) for a in q8_pools(w))
+    bt, sl, ql = dev_tensor(w.block_table), dev_tensor(w.seq_lens), dev_tensor(w.q_lens)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if append:
+        sa.kv_append_q8(d, dev_tensor(w.k_new), dev_tensor(w.v_new), kc, vc, ks, vs, bt, sl, ql, err_flag=err)
+    ws = torch.zeros(sa.paged_attn_workspace_size(d), dtype=torch.uint8, device="cuda")
+    q = dev_tensor(w.q)
+    out = torch.zeros_like(q)
+    sa.paged_attn_q8(d, q, kc, vc, ks, vs, bt, sl, ql, w.scale, out, ws, err_flag=err)
+    torch.cuda.synchronize()
+    return (out.cpu().numpy().view(np.uint16), int(err.item()),
+            tuple(t.cpu().numpy() for t in (kc, vc, ks, vs)))
+
+
+def oracle_q8(w, append=True):
+    pools = q8_pools(w)
+    if append:
+        pools = oracle.kv_append_q8(*pools, w.k_new, w.v_new, w.block_table, w.pos_start, w.q_lens)
+    kc, vc, ks, vs = pools
+    return oracle.attention_rows_q8(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens, w.q_lens, w.scale), pools
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_q8_random_small_cases(seed):
+    rng = np.random.default_rng(seed)
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4]))
+    w = wl.random_case(300 + seed, num_seqs=int(rng.integers(1, 6)), Hq=G * Hkv, Hkv=Hkv,
+                       max_ctx=int(rng.choice([40, 300, 1300])), q_len_choices=(0, 1, 2, 3))
+    out, err, pools = run_q8(w)
+    ref, ref_pools = oracle_q8(w)
+    assert err == 0
+    for got, exp in zip(pools, ref_pools):  # the append's codes and scales, bit for bit
+        assert np.array_equal(got.view(exp.dtype) if got.dtype != exp.dtype else got, exp)
+    assert_attention_close(out, ref, f"seed {seed}")
+
+
+def test_q8_llama3_decode_batch_all_rows():
+    """The Llama3-8B-shaped decode batch (64 sequences, 32q/8kv) over int8 pages."""
+    w = wl.config(1)
+    out, err, _ = run_q8(w)
+    ref, _ = oracle_q8(w)
+    assert err == 0
+    assert_attention_close(out, ref, "decode q8")
+
+
+def test_q8_rejects_tensor_core_shapes():
+    w = wl.random_case(310, num_seqs=2, Hq=8, Hkv=2, max_ctx=300, q_len_choices=(6,))  # 24 rows per KV head
+    with pytest.raises(sa.SpecAttnError):
+        run_q8(w, append=False)
