@@ -230,8 +230,8 @@ def timed_steps(batch: GpuBatch, steps: int, warmup: int, flush, parts):
 
 # DRAM bytes of one split_attn_kernel<4> launch on the decode batch, from the
 # ncu capture summarised in profiles/split_attn_kernel_R4_llama3_8b_decode.md
-# (200.35 MB read + 3.83 MB written). Set to None when the kernel changes.
-SPLIT_TRAFFIC_BYTES = 204_171_264
+# (200.35 MB read + 3.74 MB written). Set to None when the kernel changes.
+SPLIT_TRAFFIC_BYTES = 204_091_392
 
 
 def timed_sequence(batch: GpuBatch, steps: int, warmup: int, flush, parts):
