@@ -312,6 +312,17 @@ SA_API int sa_defrag_moves(const sa_dims *dims, const int32_t *block_table, cons
 SA_API int sa_defrag_apply(const sa_dims *dims, uint16_t *k_pages, uint16_t *v_pages,
                            const int32_t *moves, int32_t n_moves, int32_t *err_flag, void *stream);
 
+/*
+ * sa_defrag_apply_bytes -- the same moves on any two pools paged alike:
+ * page p of a pool is the page_bytes bytes at p * page_bytes. For int8 pages
+ * (sa_kv_append_q8), call it once for the code pools (page_bytes =
+ * num_kv_heads * 256 * 128) and once for the scale pools (num_kv_heads * 256
+ * * 4). page_bytes a multiple of 16, pools 16-byte aligned (else SA_ERR_ARG);
+ * moves and errors as in sa_defrag_apply.
+ */
+SA_API int sa_defrag_apply_bytes(int32_t num_pages, int64_t page_bytes, void *pool_a, void *pool_b,
+                                 const int32_t *moves, int32_t n_moves, int32_t *err_flag, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

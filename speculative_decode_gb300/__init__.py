@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     SpecAttnError,
     STATUS,
     defrag_apply,
+    defrag_apply_bytes,
     defrag_moves,
     dims_for,
     kv_append,

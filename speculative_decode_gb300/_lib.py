@@ -70,6 +70,7 @@ def load_library() -> ctypes.CDLL:
         "sa_paged_attn_q8": ([DP, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P], ctypes.c_int),
         "sa_defrag_moves": ([DP, P, P, P, P, P, P], ctypes.c_int),
         "sa_defrag_apply": ([DP, P, P, P, I32, P, P], ctypes.c_int),
+        "sa_defrag_apply_bytes": ([I32, ctypes.c_int64, P, P, P, I32, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -263,3 +264,11 @@ def paged_attn_q8(dims: Dims, q, k_codes, v_codes, k_scales, v_scales, block_tab
                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                                          _ptr(err_flag), _stream(stream))
     _check(rc, "sa_paged_attn_q8")
+
+
+def defrag_apply_bytes(num_pages: int, page_bytes: int, pool_a, pool_b, moves, n_moves: int,
+                       err_flag=None, stream=None) -> None:
+    """Make the moves on two pools paged alike (page p = bytes [p * page_bytes, (p + 1) * page_bytes))."""
+    rc = load_library().sa_defrag_apply_bytes(int(num_pages), int(page_bytes), _ptr(pool_a), _ptr(pool_b),
+                                              _ptr(moves), int(n_moves), _ptr(err_flag), _stream(stream))
+    _check(rc, "sa_defrag_apply_bytes")

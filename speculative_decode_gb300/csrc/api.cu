@@ -433,8 +433,23 @@ int sa_defrag_apply(const sa_dims *dims, uint16_t *k_pages, uint16_t *v_pages, c
     const int sms = device_sm_count();
     if (sms <= 0) return SA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (launch_defrag(k_pages, v_pages, moves, n_moves, dims->num_pages, dims->num_kv_heads, err_flag, sms,
-                      s) != cudaSuccess)
+    const int64_t page_bytes = static_cast<int64_t>(dims->num_kv_heads) * kPageSize * kHeadDim * 2;
+    if (launch_defrag(k_pages, v_pages, moves, n_moves, dims->num_pages, page_bytes, err_flag, sms, s) !=
+        cudaSuccess)
+        return SA_ERR_CUDA;
+    return finish(s, err_flag);
+}
+
+int sa_defrag_apply_bytes(int32_t num_pages, int64_t page_bytes, void *pool_a, void *pool_b,
+                          const int32_t *moves, int32_t n_moves, int32_t *err_flag, void *stream) {
+    if (num_pages < 0 || page_bytes <= 0 || page_bytes % 16 != 0 || n_moves < 0) return SA_ERR_ARG;
+    if (n_moves == 0) return SA_OK;
+    if (!pool_a || !pool_b || !moves) return SA_ERR_ARG;
+    if (!aligned(pool_a, 16) || !aligned(pool_b, 16) || !aligned(moves, 4)) return SA_ERR_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return SA_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_defrag(pool_a, pool_b, moves, n_moves, num_pages, page_bytes, err_flag, sms, s) != cudaSuccess)
         return SA_ERR_CUDA;
     return finish(s, err_flag);
 }

@@ -17,10 +17,14 @@
 //    of work that is cut into equal contiguous ranges, one per warp
 //    (stream-K): perfectly balanced whatever the context lengths, with at
 //    most two partial pieces per warp and no scheduling atomics.
-//  * One warp owns its range. Lane 0 streams each tile's K rows and V rows
-//    (each one contiguous run inside a page) with two 1-D bulk copies into
-//    the warp's private ring of S stages, and bulk-copies each piece's query
-//    rows ahead of use; all 32 lanes compute.
+//  * One warp owns its range. It streams each tile's K rows and V rows (each
+//    one contiguous run inside a page) into its private ring of S stages with
+//    two 1-D bulk copies issued by lanes 0 and 1 in one instruction, and
+//    bulk-copies each piece's query rows ahead of use; all 32 lanes compute.
+//  * int8 pages (Q8 instances): the same kernel over int8 codes with one fp32
+//    scale per (page, head, token) row; lanes 2 and 3 also copy the tile's K
+//    and V scales, the loops run on codes converted exactly to floats, and
+//    the row scales multiply the scores (K) and the probabilities (V).
 //  * Lane mapping: a token is handled by L = 2R lanes (8, 16 or 32), each
 //    owning 128/L head dims, so pre-scaled queries and output accumulators
 //    live in registers. Q.K partial dots are combined with a shuffle

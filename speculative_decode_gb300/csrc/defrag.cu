@@ -34,11 +34,13 @@ __device__ __forceinline__ uint4 load_stream(const uint4 *p) {
     return v;
 }
 
+// Two pools of pages of page_vecs 16-byte vectors each (the K and V pools,
+// or any pair of pools paged alike); a page's last chunk may be partial.
 __global__ void __launch_bounds__(kCopyThreads) defrag_kernel(uint4 *k_pages, uint4 *v_pages,
                                                                const int32_t *__restrict__ moves,
                                                                int n_moves, int num_pages,
                                                                int64_t page_vecs, int32_t *err) {
-    const int64_t chunks = page_vecs / kChunkVecs;  // per page and pool
+    const int64_t chunks = (page_vecs + kChunkVecs - 1) / kChunkVecs;  // per page and pool
     const int64_t units = static_cast<int64_t>(n_moves) * 2 * chunks;
     for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
         const int m = static_cast<int>(u / (2 * chunks));
@@ -54,9 +56,11 @@ __global__ void __launch_bounds__(kCopyThreads) defrag_kernel(uint4 *k_pages, ui
         uint4 *dst = pool + static_cast<int64_t>(to) * page_vecs + off;
         uint4 x[kVecPerThread];
 #pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i) x[i] = load_stream(src + i * kCopyThreads);
+        for (int i = 0; i < kVecPerThread; ++i)
+            if (off + i * kCopyThreads < page_vecs) x[i] = load_stream(src + i * kCopyThreads);
 #pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i) __stcs(dst + i * kCopyThreads, x[i]);
+        for (int i = 0; i < kVecPerThread; ++i)
+            if (off + i * kCopyThreads < page_vecs) __stcs(dst + i * kCopyThreads, x[i]);
     }
 }
 
@@ -105,10 +109,10 @@ int defrag_plan_host(int num_seqs, int num_pages, int max_pages, const int32_t *
     return SA_OK;
 }
 
-cudaError_t launch_defrag(uint16_t *k_pages, uint16_t *v_pages, const int32_t *moves, int n_moves,
-                          int num_pages, int num_kv_heads, int32_t *err, int sms, cudaStream_t stream) {
-    const int64_t page_vecs = static_cast<int64_t>(num_kv_heads) * kPageSize * kHeadDim * 2 / 16;
-    const int64_t units = static_cast<int64_t>(n_moves) * 2 * (page_vecs / kChunkVecs);
+cudaError_t launch_defrag(void *k_pages, void *v_pages, const int32_t *moves, int n_moves,
+                          int num_pages, int64_t page_bytes, int32_t *err, int sms, cudaStream_t stream) {
+    const int64_t page_vecs = page_bytes / 16;
+    const int64_t units = static_cast<int64_t>(n_moves) * 2 * ((page_vecs + kChunkVecs - 1) / kChunkVecs);
     const int grid = static_cast<int>(std::min<int64_t>(units, static_cast<int64_t>(sms) * 8));
     defrag_kernel<<<grid, kCopyThreads, 0, stream>>>(reinterpret_cast<uint4 *>(k_pages),
                                                      reinterpret_cast<uint4 *>(v_pages), moves, n_moves,

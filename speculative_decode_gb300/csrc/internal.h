@@ -81,8 +81,8 @@ int split_segment_cost();
 int defrag_plan_host(int num_seqs, int num_pages, int max_pages, const int32_t *block_table,
                      const int32_t *seq_lens, int32_t *new_table, int32_t *moves, int32_t *n_moves,
                      int32_t *n_live);
-cudaError_t launch_defrag(uint16_t *k_pages, uint16_t *v_pages, const int32_t *moves, int n_moves,
-                          int num_pages, int num_kv_heads, int32_t *err, int sms, cudaStream_t stream);
+cudaError_t launch_defrag(void *k_pages, void *v_pages, const int32_t *moves, int n_moves,
+                          int num_pages, int64_t page_bytes, int32_t *err, int sms, cudaStream_t stream);
 
 cudaError_t launch_kv_append_q8(const sa_dims &d, const uint16_t *k_new, const uint16_t *v_new,
                                 int8_t *k_codes, int8_t *v_codes, float *k_scales, float *v_scales,

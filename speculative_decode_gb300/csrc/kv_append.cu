@@ -7,6 +7,9 @@
 //
 // One CTA per (query token slot, sequence); one warp per KV head copies the
 // 256-byte K row and V row with 8-byte coalesced accesses. Pure bandwidth.
+// For int8 pages (the page names quantised cache modes and gives no format)
+// the warp quantises each row instead: scale = amax / 127, codes rounded
+// half to even, in fp32, and writes 128 codes and the scale.
 #include "common.cuh"
 
 namespace sa {

@@ -152,3 +152,8 @@ def test_defrag_planner_rejects_bad_tables(sa):
     lib = sa.load_library()
     assert lib.sa_defrag_apply(ctypes.byref(d), None, None, None, -1, None, None) == 1
     assert lib.sa_defrag_apply(ctypes.byref(d), None, None, None, 0, None, None) == 0
+    # byte pools: page size must be a positive multiple of 16
+    assert lib.sa_defrag_apply_bytes(4, 24, None, None, None, 1, None, None) == 1
+    assert lib.sa_defrag_apply_bytes(4, 0, None, None, None, 0, None, None) == 1
+    assert lib.sa_defrag_apply_bytes(4, 2048, None, None, None, 0, None, None) == 0
+    assert lib.sa_defrag_apply_bytes(4, 2048, None, None, None, 1, None, None) == 1

@@ -80,3 +80,42 @@ def test_q8_rejects_tensor_core_shapes():
     w = wl.random_case(310, num_seqs=2, Hq=8, Hkv=2, max_ctx=300, q_len_choices=(6,))  # 24 rows per KV head
     with pytest.raises(sa.SpecAttnError):
         run_q8(w, append=False)
+
+
+@pytest.mark.parametrize("seed,Hkv", [(0, 2), (1, 8)])
+def test_q8_defrag_codes_and_scales(seed, Hkv):
+    """Compaction of int8 pools: the code pools and the scale pools (pages of
+    Hkv*256*128 and Hkv*256*4 bytes, the latter not a whole 32 KiB chunk) move
+    by one plan; pools bit-exact against the oracle's page moves, attention
+    through the new tables bit-identical to attention before."""
+    w = wl.random_case(1300 + seed, num_seqs=5, Hq=4 * Hkv, Hkv=Hkv, max_ctx=1500, q_len_choices=(1, 2),
+                       num_pages=80, shared_prefix_pages=2 * seed)
+    d = dims_of(w)
+    new, moves, _ = sa.defrag_moves(d, w.block_table, w.seq_lens)
+    assert len(moves) > 0
+    kc, vc, ks, vs = q8_pools(w)
+    g = [dev_tensor(a) for a in (kc, vc, ks, vs)]
+    mv = torch.from_numpy(np.ascontiguousarray(moves, np.int32).reshape(-1, 2)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    npg = kc.shape[0]
+    sa.defrag_apply_bytes(npg, kc[0].nbytes, g[0], g[1], mv, len(moves), err_flag=err)
+    sa.defrag_apply_bytes(npg, ks[0].nbytes, g[2], g[3], mv, len(moves), err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = [t.cpu().numpy() for t in g]
+    u16 = lambda a: a.view(np.uint16).reshape(npg, -1)  # the oracle moves pages of 16-bit words
+    kc2, vc2 = oracle.defrag_move(u16(kc), u16(vc), moves)
+    ks2, vs2 = oracle.defrag_move(u16(ks), u16(vs), moves)
+    for a, b in zip(got, (kc2, vc2, ks2, vs2)):
+        assert np.array_equal(u16(a), b)
+    before, e0, _ = run_q8(w, append=False)
+
+    # attention from the moved pools through the new tables
+    bt, sl, ql = dev_tensor(new), dev_tensor(w.seq_lens), dev_tensor(w.q_lens)
+    ws = torch.zeros(sa.paged_attn_workspace_size(d), dtype=torch.uint8, device="cuda")
+    q = dev_tensor(w.q)
+    out = torch.zeros_like(q)
+    sa.paged_attn_q8(d, q, g[0], g[1], g[2], g[3], bt, sl, ql, w.scale, out, ws, err_flag=err)
+    torch.cuda.synchronize()
+    assert e0 == 0 and int(err.item()) == 0
+    assert np.array_equal(before, out.cpu().numpy().view(np.uint16))
