@@ -67,6 +67,12 @@ def _load():
         lib.oracle_kv_append_q8.restype = I
         lib.oracle_attention_rows_q8.argtypes = [I] * 7 + [P] * 8 + [D, P, P, I64, P, I]
         lib.oracle_attention_rows_q8.restype = I
+        lib.oracle_quantize_q4.argtypes = [P, I64, I, P, P]
+        lib.oracle_quantize_q4.restype = I
+        lib.oracle_kv_append_q4.argtypes = [I] * 6 + [P] * 9
+        lib.oracle_kv_append_q4.restype = I
+        lib.oracle_attention_rows_q4.argtypes = [I] * 7 + [P] * 8 + [D, P, P, I64, P, I]
+        lib.oracle_attention_rows_q4.restype = I
         lib.oracle_defrag_plan.argtypes = [I] * 4 + [P] * 6
         lib.oracle_defrag_plan.restype = I
         lib.oracle_defrag_move.argtypes = [I, I64, P, P, P, I]
@@ -236,4 +242,57 @@ def attention_rows_q8(q, k_codes, v_codes, k_scales, v_scales, block_table, seq_
                                           _ptr(ql), float(scale), _ptr(tok), _ptr(hd), len(tok),
                                           _ptr(out), int(n_threads))
     _check(rc, "attention_rows_q8")
+    return out.reshape(qb.shape[0], hq, d) if full else out
+
+
+def quantize_q4(x):
+    """bf16 rows [..., d] -> (packed nibbles uint8 [..., d / 2], float32 scales [...])."""
+    xb = _c(x, np.uint16)
+    d = xb.shape[-1]
+    n = xb.size // d
+    packed = np.empty(xb.shape[:-1] + (d // 2,), np.uint8)
+    scales = np.empty(xb.shape[:-1], np.float32)
+    _check(_load().oracle_quantize_q4(_ptr(xb), n, d, _ptr(packed), _ptr(scales)), "quantize_q4")
+    return packed, scales
+
+
+def kv_append_q4(k_nib, v_nib, k_scales, v_scales, k_new, v_new, block_table, pos_start,
+                 new_lens, page_size=256):
+    """Return copies of the int4 pools with the new tokens' rows quantized and written."""
+    kc, vc = _c(k_nib, np.uint8).copy(), _c(v_nib, np.uint8).copy()
+    ks, vs = _c(k_scales, np.float32).copy(), _c(v_scales, np.float32).copy()
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    bt, ps, nl = _c(block_table, np.int32), _c(pos_start, np.int32), _c(new_lens, np.int32)
+    num_pages, hkv, P, dh = kc.shape
+    rc = _load().oracle_kv_append_q4(len(nl), hkv, 2 * dh, P, num_pages, bt.shape[1], _ptr(kn), _ptr(vn),
+                                     _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(ps),
+                                     _ptr(nl))
+    _check(rc, "kv_append_q4")
+    return kc, vc, ks, vs
+
+
+def attention_rows_q4(q, k_nib, v_nib, k_scales, v_scales, block_table, seq_lens, q_lens,
+                      scale, tokens=None, heads=None, n_threads: int = 0) -> np.ndarray:
+    """fp64 attention over int4 pages (nibbles [num_pages, Hkv, P, d / 2]);
+    every row ([total_q, Hq, d]) or the selected (packed query token, q head)
+    rows ([n, d])."""
+    qb = _c(q, np.uint16)
+    kc, vc = _c(k_nib, np.uint8), _c(v_nib, np.uint8)
+    ks, vs = _c(k_scales, np.float32), _c(v_scales, np.float32)
+    bt, sl, ql = _c(block_table, np.int32), _c(seq_lens, np.int32), _c(q_lens, np.int32)
+    num_pages, hkv, P, dh = kc.shape
+    d = 2 * dh
+    hq = qb.shape[1]
+    full = tokens is None
+    if full:
+        tok = np.repeat(np.arange(qb.shape[0], dtype=np.int64), hq)
+        hd = np.tile(np.arange(hq, dtype=np.int32), qb.shape[0])
+    else:
+        tok, hd = _c(tokens, np.int64), _c(heads, np.int32)
+    out = np.empty((len(tok), d), dtype=np.float64)
+    rc = _load().oracle_attention_rows_q4(len(sl), hq, hkv, d, P, num_pages, bt.shape[1], _ptr(qb),
+                                          _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl),
+                                          _ptr(ql), float(scale), _ptr(tok), _ptr(hd), len(tok),
+                                          _ptr(out), int(n_threads))
+    _check(rc, "attention_rows_q4")
     return out.reshape(qb.shape[0], hq, d) if full else out

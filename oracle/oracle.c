@@ -49,6 +49,11 @@
  *    code = round-to-nearest-even(x / scale) in binary32; a cached value is
  *    code * scale, and attention is the plain definition over those values.
  *
+ *  - int4 pages (the Q4 mode that page names): the same reading with 4-bit
+ *    codes, scale = amax / 7, code = round-to-nearest-even(x / scale) clamped
+ *    to [-7, 7], stored as the nibble code + 8; the row's byte c holds value
+ *    2c in its low nibble and value 2c + 1 in its high nibble.
+ *
  *  - defragmentation: releasing pages leaves holes in the cache; the block
  *    table need not be contiguous, and the cache can be defragmented (the
  *    generator does it only when its job queue is empty).  ExLlamaV2
@@ -133,6 +138,8 @@ typedef struct {
     /* int8 pages (NULL for bf16 pages): value = code * the row's scale */
     const int8_t *k_codes, *v_codes;
     const float *k_scales, *v_scales;
+    /* int4 pages (NULL otherwise): packed nibbles, value = (nibble - 8) * scale */
+    const uint8_t *k_nib, *v_nib;
 } attn_args;
 
 /* One output row: new token i of sequence b, query head h. `kbuf`/`vbuf`
@@ -153,7 +160,16 @@ static int attention_row(const attn_args *a, const int64_t *q_row_of_seq, int b,
         if (pg < 0) return ORACLE_ERR_PAGE_OOB;
         int64_t srow = (pg * a->num_kv_heads + g) * a->page_size + t % a->page_size;
         int64_t base = srow * d;
-        if (a->k_codes) { /* int8 pages: exact in double (an 8-bit integer times an fp32 scale) */
+        if (a->k_nib) { /* int4 pages: row srow is d / 2 bytes, value c in nibble c % 2 of byte c / 2 */
+            double ks = a->k_scales[srow], vs = a->v_scales[srow];
+            const uint8_t *kr = a->k_nib + srow * (d / 2), *vr = a->v_nib + srow * (d / 2);
+            for (int c = 0; c < d; ++c) {
+                int kn = (c % 2 == 0) ? (kr[c / 2] & 15) : (kr[c / 2] >> 4);
+                int vn = (c % 2 == 0) ? (vr[c / 2] & 15) : (vr[c / 2] >> 4);
+                kbuf[t * d + c] = (double)(kn - 8) * ks;
+                vbuf[t * d + c] = (double)(vn - 8) * vs;
+            }
+        } else if (a->k_codes) { /* int8 pages: exact in double (an 8-bit integer times an fp32 scale) */
             double ks = a->k_scales[srow], vs = a->v_scales[srow];
             for (int c = 0; c < d; ++c) {
                 kbuf[t * d + c] = (double)a->k_codes[base + c] * ks;
@@ -266,7 +282,7 @@ int oracle_attention_rows(int num_seqs, int num_q_heads, int num_kv_heads, int h
                           double *out, int n_threads) {
     attn_args a = {num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                    max_pages_per_seq, q, k_pages, v_pages, block_table, seq_lens, q_lens, scale,
-                   NULL, NULL, NULL, NULL};
+                   NULL, NULL, NULL, NULL, NULL, NULL};
     return attention_rows_impl(a, row_token, row_head, n_rows, out, n_threads);
 }
 
@@ -362,7 +378,82 @@ int oracle_attention_rows_q8(int num_seqs, int num_q_heads, int num_kv_heads, in
                              double *out, int n_threads) {
     attn_args a = {num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
                    max_pages_per_seq, q, NULL, NULL, block_table, seq_lens, q_lens, scale,
-                   k_codes, v_codes, k_scales, v_scales};
+                   k_codes, v_codes, k_scales, v_scales, NULL, NULL};
+    return attention_rows_impl(a, row_token, row_head, n_rows, out, n_threads);
+}
+
+/* ------------------------------------------------------------- int4 pages */
+
+/* One row of d (even) bf16 values -> d/2 bytes of nibbles and one scale:
+ * scale = amax / 7, code = round-to-nearest-even(x / scale) in binary32,
+ * clamped to [-7, 7], nibble = code + 8; byte c = nibble(2c) | nibble(2c+1) << 4.
+ * A row of zeros gets scale 0 and every nibble 8. Inputs are finite. */
+int oracle_quantize_q4(const uint16_t *x, int64_t n_rows, int d, uint8_t *packed, float *scales) {
+    if (d <= 0 || d % 2 != 0) return ORACLE_ERR_ARG;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        float amax = 0.f;
+        for (int c = 0; c < d; ++c) {
+            float v = (float)oracle_bf16_to_f64(x[r * d + c]);
+            float av = v < 0.f ? -v : v;
+            if (av > amax) amax = av;
+        }
+        float sc = amax / 7.0f;
+        scales[r] = sc;
+        for (int c = 0; c < d; c += 2) {
+            int nib[2];
+            for (int e = 0; e < 2; ++e) {
+                float v = (float)oracle_bf16_to_f64(x[r * d + c + e]);
+                float qv = sc > 0.f ? rintf(v / sc) : 0.f;
+                if (qv > 7.f) qv = 7.f;
+                if (qv < -7.f) qv = -7.f;
+                nib[e] = (int)qv + 8;
+            }
+            packed[r * (d / 2) + c / 2] = (uint8_t)(nib[0] | (nib[1] << 4));
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* kv_append for int4 pages: each new (token, KV head) row is quantized as
+ * above and written, nibbles and scale, where the block table puts it. */
+int oracle_kv_append_q4(int num_seqs, int num_kv_heads, int head_dim, int page_size,
+                        int num_pages, int max_pages_per_seq,
+                        const uint16_t *k_new, const uint16_t *v_new,
+                        uint8_t *k_nib, uint8_t *v_nib, float *k_scales, float *v_scales,
+                        const int32_t *block_table, const int32_t *pos_start,
+                        const int32_t *new_lens) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 2 != 0 || page_size <= 0)
+        return ORACLE_ERR_ARG;
+    int64_t row = 0;
+    for (int b = 0; b < num_seqs; ++b) {
+        for (int i = 0; i < new_lens[b]; ++i, ++row) {
+            int64_t pos = (int64_t)pos_start[b] + i;
+            int64_t pg = page_of(block_table, max_pages_per_seq, num_pages, page_size, b, pos);
+            if (pg < 0) return ORACLE_ERR_PAGE_OOB;
+            for (int g = 0; g < num_kv_heads; ++g) {
+                int64_t drow = (pg * num_kv_heads + g) * page_size + pos % page_size;
+                int64_t src = (row * num_kv_heads + g) * head_dim;
+                oracle_quantize_q4(k_new + src, 1, head_dim, k_nib + drow * (head_dim / 2), k_scales + drow);
+                oracle_quantize_q4(v_new + src, 1, head_dim, v_nib + drow * (head_dim / 2), v_scales + drow);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* Attention over int4 pages: as oracle_attention_rows with every cached value
+ * replaced by (nibble - 8) * scale (exact in double). */
+int oracle_attention_rows_q4(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int page_size, int num_pages, int max_pages_per_seq, const uint16_t *q,
+                             const uint8_t *k_nib, const uint8_t *v_nib, const float *k_scales,
+                             const float *v_scales, const int32_t *block_table,
+                             const int32_t *seq_lens, const int32_t *q_lens, double scale,
+                             const int64_t *row_token, const int32_t *row_head, int64_t n_rows,
+                             double *out, int n_threads) {
+    if (head_dim % 2 != 0) return ORACLE_ERR_ARG;
+    attn_args a = {num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                   max_pages_per_seq, q, NULL, NULL, block_table, seq_lens, q_lens, scale,
+                   NULL, NULL, k_scales, v_scales, k_nib, v_nib};
     return attention_rows_impl(a, row_token, row_head, n_rows, out, n_threads);
 }
 

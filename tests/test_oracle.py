@@ -489,3 +489,92 @@ def test_kv_append_q8_quantises_the_rows_kv_append_writes():
     for got, pages in (((kc2, ks2), kp), ((vc2, vs2), vp)):
         c, s = oracle.quantize_q8(pages)
         assert np.array_equal(got[0], c) and np.array_equal(got[1], s)
+
+
+# ------------------------------------------------------------------ int4 pages
+Q4 = os.path.join(os.path.dirname(__file__), "golden", "q4_cases.json")
+
+
+def q4_values(packed, scales):
+    """Decode packed int4 rows by the stated layout: value 2c is the low nibble
+    of byte c, value 2c + 1 the high one, each nibble minus 8 times the scale."""
+    b = np.asarray(packed, np.uint8)
+    nib = np.stack([b & 15, b >> 4], axis=-1).reshape(b.shape[:-1] + (2 * b.shape[-1],))
+    return (nib.astype(np.float64) - 8.0) * np.asarray(scales, np.float64)[..., None]
+
+
+def test_q4_hand_worked_rows():
+    for c in json.load(open(Q4))["cases"]:
+        bits = np.array([c["bits"]], np.uint16)
+        assert np.array_equal(wl.bf16_to_f32(bits)[0], np.array(c["values"], np.float32)), c["note"]
+        packed, scales = oracle.quantize_q4(bits)
+        assert packed[0].tolist() == c["expect"]["bytes"], c["note"]
+        assert abs(float(scales[0]) * 7 - c["expect"]["scale_times_7"]) <= 1e-6 * max(1.0, c["expect"]["scale_times_7"])
+
+
+def test_q4_error_within_half_a_step():
+    """Every value is recovered within half a quantisation step, the largest
+    magnitude of a non-zero row maps to +-7, and nibble 0 (code -8) is never
+    written."""
+    rng = np.random.default_rng(4)
+    x = wl.normal_bf16(rng, (500, 128))
+    x[9] = 0
+    packed, scales = oracle.quantize_q4(x)
+    assert packed.shape == (500, 64)
+    xf = wl.bf16_to_f32(x).astype(np.float64)
+    rec = q4_values(packed, scales)
+    # half a step, plus the binary32 rounding of x / scale (|x / scale| <= 7)
+    assert np.all(np.abs(rec - xf) <= scales.astype(np.float64)[:, None] * (0.5 + 7 * 2.0 ** -23))
+    codes = np.rint(rec / np.where(scales > 0, scales, 1)[:, None])
+    nz = np.abs(xf).max(axis=1) > 0
+    assert np.all(np.abs(codes[nz]).max(axis=1) == 7)
+    assert np.all((packed & 15) != 0) and np.all((packed >> 4) != 0)
+    assert scales[9] == 0 and np.all(packed[9] == 0x88)
+
+
+def test_q4_attention_is_exact_on_representable_rows():
+    """Rows of quarter-integers in [-1.75, 1.75] that contain 1.75 quantise
+    exactly (scale 0.25), so attention over the int4 pages equals attention
+    over the bf16 pages, bit for bit."""
+    rng = np.random.default_rng(12)
+    w = wl.random_case(43, num_seqs=3, Hq=8, Hkv=2, max_ctx=600, q_len_choices=(1, 2))
+    for pool in (w.k_pages, w.v_pages):
+        v = rng.integers(-7, 8, size=pool.shape).astype(np.float32) * np.float32(0.25)
+        v[..., 9] = -1.75
+        pool[...] = (v.view(np.uint32) >> 16).astype(np.uint16)  # quarter-integers are exact in bf16
+    kc, ks = oracle.quantize_q4(w.k_pages)
+    vc, vs = oracle.quantize_q4(w.v_pages)
+    assert np.all(ks == 0.25) and np.all(vs == 0.25)
+    args = (w.block_table, w.seq_lens, w.q_lens, w.scale)
+    ref = oracle.paged_attention(w.q, w.k_pages, w.v_pages, *args)
+    assert np.array_equal(oracle.attention_rows_q4(w.q, kc, vc, ks, vs, *args), ref)
+
+
+def test_q4_attention_equals_attention_over_decoded_values():
+    """On random rows the int4 attention is the bf16-page attention applied to
+    the decoded values wherever those are bf16-exact: rescale every row so its
+    scale is a power of two (values then have at most 4 significant bits)."""
+    rng = np.random.default_rng(13)
+    w = wl.random_case(44, num_seqs=2, Hq=4, Hkv=1, max_ctx=400, q_len_choices=(1, 3))
+    kc, ks = oracle.quantize_q4(w.k_pages)
+    vc, vs = oracle.quantize_q4(w.v_pages)
+    ks[...] = 2.0 ** rng.integers(-3, 2, size=ks.shape)
+    vs[...] = 2.0 ** rng.integers(-3, 2, size=vs.shape)
+    to_bf16 = lambda f: (f.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    kp, vp = to_bf16(q4_values(kc, ks)), to_bf16(q4_values(vc, vs))
+    assert np.array_equal(wl.bf16_to_f32(kp), q4_values(kc, ks).astype(np.float32))
+    args = (w.block_table, w.seq_lens, w.q_lens, w.scale)
+    assert np.array_equal(oracle.attention_rows_q4(w.q, kc, vc, ks, vs, *args),
+                          oracle.paged_attention(w.q, kp, vp, *args))
+
+
+def test_kv_append_q4_quantises_the_rows_kv_append_writes():
+    w = wl.random_case(45, num_seqs=4, Hq=4, Hkv=2, max_ctx=700, q_len_choices=(1, 3, 6))
+    kc, ks = oracle.quantize_q4(w.k_pages)
+    vc, vs = oracle.quantize_q4(w.v_pages)
+    kc2, vc2, ks2, vs2 = oracle.kv_append_q4(kc, vc, ks, vs, w.k_new, w.v_new, w.block_table,
+                                             w.pos_start, w.q_lens)
+    kp, vp = oracle.kv_append(w.k_pages, w.v_pages, w.k_new, w.v_new, w.block_table, w.pos_start, w.q_lens)
+    for got, pages in (((kc2, ks2), kp), ((vc2, vs2), vp)):
+        c, s = oracle.quantize_q4(pages)
+        assert np.array_equal(got[0], c) and np.array_equal(got[1], s)
