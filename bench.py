@@ -288,24 +288,32 @@ def rank_seed(cfg: int, rank: int) -> int:
     return 1000 + cfg + 1 + 7919 * rank
 
 
-def q8_block(batch: GpuBatch, w: wl.Workload, dev, steps: int, warmup: int, flush):
-    """paged_attn over int8 pages for the decode batch: codes uniform in
-    [-127, 127] and per-row scales near those of N(0,1) rows (synthetic, seeded);
-    counted bytes = distinct cached tokens x heads x (128 codes + 4-byte scale)
-    x 2, plus q, out and the tables."""
+def quant_block(batch: GpuBatch, w: wl.Workload, dev, steps: int, warmup: int, flush, bits: int):
+    """paged_attn over int8 (bits 8) or int4 (bits 4) pages for the decode
+    batch: codes uniform over [-127, 127] (int8) or [-7, 7] (int4, as nibbles
+    1..15) and per-row scales near those of N(0,1) rows (synthetic, seeded);
+    counted bytes = distinct cached tokens x heads x (128 codes of `bits` bits
+    + 4-byte scale) x 2, plus q, out and the tables."""
     torch, sa = batch.torch, batch.sa
-    rng = np.random.default_rng(2024)
+    rng = np.random.default_rng(2024 + bits)
     shape = w.k_pages.shape
-    kc = torch.from_numpy(rng.integers(-127, 128, size=shape, dtype=np.int8)).to(dev)
-    vc = torch.from_numpy(rng.integers(-127, 128, size=shape, dtype=np.int8)).to(dev)
-    ks = torch.from_numpy((rng.uniform(2.5, 3.5, size=shape[:-1]) / 127).astype(np.float32)).to(dev)
-    vs = torch.from_numpy((rng.uniform(2.5, 3.5, size=shape[:-1]) / 127).astype(np.float32)).to(dev)
+    cmax = 127 if bits == 8 else 7
+    if bits == 8:
+        codes = lambda: rng.integers(-127, 128, size=shape, dtype=np.int8)
+    else:
+        codes = lambda: (rng.integers(1, 16, size=shape[:-1] + (64,), dtype=np.uint8)
+                         | (rng.integers(1, 16, size=shape[:-1] + (64,), dtype=np.uint8) << 4))
+    kc = torch.from_numpy(codes()).to(dev)
+    vc = torch.from_numpy(codes()).to(dev)
+    ks = torch.from_numpy((rng.uniform(2.5, 3.5, size=shape[:-1]) / cmax).astype(np.float32)).to(dev)
+    vs = torch.from_numpy((rng.uniform(2.5, 3.5, size=shape[:-1]) / cmax).astype(np.float32)).to(dev)
     ws = torch.zeros(sa.paged_attn_workspace_size(batch.dims), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    attn = sa.paged_attn_q8 if bits == 8 else sa.paged_attn_q4
 
     def call():
-        sa.paged_attn_q8(batch.dims, batch.q, kc, vc, ks, vs, batch.bt, batch.sl, batch.ql, w.scale,
-                         batch.out, ws, err_flag=batch.err)
+        attn(batch.dims, batch.q, kc, vc, ks, vs, batch.bt, batch.sl, batch.ql, w.scale,
+             batch.out, ws, err_flag=batch.err)
 
     for _ in range(warmup):
         flush()
@@ -322,10 +330,10 @@ def q8_block(batch: GpuBatch, w: wl.Workload, dev, steps: int, warmup: int, flus
     assert int(batch.err.item()) == 0, "device error flag set"
     t = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev))
     tokens_heads = sum(int(T) for T in w.seq_lens) * w.num_kv_heads
-    q8_bytes = (tokens_heads * (128 + 4) * 2 + 2 * w.q.nbytes + w.block_table.nbytes + w.seq_lens.nbytes
-                + w.q_lens.nbytes)
-    return {"workload": w.name + " int8 pages", "paged_attn_ms": round(t, 5), "counted_bytes": int(q8_bytes),
-            "GBps": round(q8_bytes / (t * 1e-3) / 1e9, 1),
+    q_bytes = (tokens_heads * (128 * bits // 8 + 4) * 2 + 2 * w.q.nbytes + w.block_table.nbytes
+               + w.seq_lens.nbytes + w.q_lens.nbytes)
+    return {"workload": w.name + (" int8 pages" if bits == 8 else " int4 pages"), "paged_attn_ms": round(t, 5),
+            "counted_bytes": int(q_bytes), "GBps": round(q_bytes / (t * 1e-3) / 1e9, 1),
             "cached_tokens_per_s": round(sum(int(T) for T in w.seq_lens) / (t * 1e-3), 1)}
 
 
@@ -489,10 +497,11 @@ def run_ours(args):
                "counts": "4 x 128 x visible keys per (new token, query head) row / paged_attn device time"}
     del pb
 
-    # ---- sixth block: the decode batch over int8 pages (synthetic seeded codes
-    # and per-row scales of the same shapes), attention only
-    q8 = q8_block(batch, w, dev, vsteps, args.warmup, flush)
-    q8["bf16_paged_attn_ms"] = round(t_attn_max, 5)
+    # ---- sixth block: the decode batch over int8 and int4 pages (synthetic
+    # seeded codes and per-row scales of the same shapes), attention only
+    q8 = quant_block(batch, w, dev, vsteps, args.warmup, flush, 8)
+    q4 = quant_block(batch, w, dev, vsteps, args.warmup, flush, 4)
+    q8["bf16_paged_attn_ms"] = q4["bf16_paged_attn_ms"] = round(t_attn_max, 5)
 
     peak, peak_kind = hbm_peak()
     achieved = cbytes / (t_attn_max * 1e-3) / 1e9
@@ -553,6 +562,7 @@ def run_ours(args):
         "defrag": defrag,
         "prefill": prefill,
         "q8": q8,
+        "q4": q4,
         "e2e": {"value": round(world * sbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_ms, 5)},

@@ -213,6 +213,36 @@ SA_API int sa_paged_attn_q8(const sa_dims *dims, const uint16_t *q, const int8_t
                             const int32_t *q_lens, float scale, uint16_t *out, void *workspace,
                             size_t workspace_bytes, int32_t *err_flag, void *stream);
 
+/*
+ * int4 K/V pages -- sa_kv_append_q4 and sa_paged_attn_q4.
+ *
+ * The Q4 cache mode that the same page names (it is the quantised mode the
+ * dynamic generator takes; the page gives no format). This library's int4
+ * format: for every (page, KV head, token) row of 128 values, 64 bytes of
+ * 4-bit codes and one fp32 scale, with
+ *   scale = amax / 7,  code = round-half-even(x / scale) clamped to [-7, 7]
+ * both computed in fp32 (IEEE division), stored as the nibble code + 8; byte
+ * c of the row holds value 2c in its low nibble and value 2c + 1 in its high
+ * nibble. A row of zeros has scale 0 and every nibble 8. A cached value is
+ * (nibble - 8) * scale. Pools:
+ *   k_codes, v_codes    device uint8 [num_pages, num_kv_heads, 256, 64]
+ *   k_scales, v_scales  device fp32 [num_pages, num_kv_heads, 256]
+ * (alignment as for int8 pages).
+ *
+ * sa_kv_append_q4 and sa_paged_attn_q4: as the int8 calls above, over int4
+ * pages; same arguments, restrictions and errors. sa_defrag_apply_bytes
+ * moves int4 pools too (code pages of num_kv_heads * 256 * 64 bytes).
+ */
+SA_API int sa_kv_append_q4(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_new,
+                           uint8_t *k_codes, uint8_t *v_codes, float *k_scales, float *v_scales,
+                           const int32_t *block_table, const int32_t *seq_lens,
+                           const int32_t *q_lens, int32_t *err_flag, void *stream);
+SA_API int sa_paged_attn_q4(const sa_dims *dims, const uint16_t *q, const uint8_t *k_codes,
+                            const uint8_t *v_codes, const float *k_scales, const float *v_scales,
+                            const int32_t *block_table, const int32_t *seq_lens,
+                            const int32_t *q_lens, float scale, uint16_t *out, void *workspace,
+                            size_t workspace_bytes, int32_t *err_flag, void *stream);
+
 /* Number of kernels one sa_paged_attn call with these shapes launches
  * (diagnostics; the same decomposition the call itself uses). Needs a device. */
 SA_API int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan);

@@ -16,10 +16,12 @@ from ._lib import (  # noqa: F401
     defrag_moves,
     dims_for,
     kv_append,
+    kv_append_q4,
     kv_append_q8,
     library_path,
     load_library,
     paged_attn,
+    paged_attn_q4,
     paged_attn_q8,
     paged_attn_kernel_count,
     paged_attn_noalloc,

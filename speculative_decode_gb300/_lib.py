@@ -68,6 +68,8 @@ def load_library() -> ctypes.CDLL:
         "sa_spec_verify_greedy": ([P, P, P, I32, I32, I32, P, P, P, P, SZ, P, P], ctypes.c_int),
         "sa_kv_append_q8": ([DP] + [P] * 11, ctypes.c_int),
         "sa_paged_attn_q8": ([DP, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P], ctypes.c_int),
+        "sa_kv_append_q4": ([DP] + [P] * 11, ctypes.c_int),
+        "sa_paged_attn_q4": ([DP, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P], ctypes.c_int),
         "sa_defrag_moves": ([DP, P, P, P, P, P, P], ctypes.c_int),
         "sa_defrag_apply": ([DP, P, P, P, I32, P, P], ctypes.c_int),
         "sa_defrag_apply_bytes": ([I32, ctypes.c_int64, P, P, P, I32, P, P], ctypes.c_int),
@@ -264,6 +266,26 @@ def paged_attn_q8(dims: Dims, q, k_codes, v_codes, k_scales, v_scales, block_tab
                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
                                          _ptr(err_flag), _stream(stream))
     _check(rc, "sa_paged_attn_q8")
+
+
+def kv_append_q4(dims: Dims, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_table,
+                 seq_lens, q_lens, err_flag=None, stream=None) -> None:
+    """kv_append into int4 pages (nibbles uint8 [pages, Hkv, 256, 64], scales fp32 [pages, Hkv, 256])."""
+    rc = load_library().sa_kv_append_q4(ctypes.byref(dims), _ptr(k_new), _ptr(v_new), _ptr(k_codes),
+                                        _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), _ptr(block_table),
+                                        _ptr(seq_lens), _ptr(q_lens), _ptr(err_flag), _stream(stream))
+    _check(rc, "sa_kv_append_q4")
+
+
+def paged_attn_q4(dims: Dims, q, k_codes, v_codes, k_scales, v_scales, block_table, seq_lens, q_lens,
+                  scale: float, out, workspace, err_flag=None, stream=None) -> None:
+    """paged_attn over int4 pages; the workspace is paged_attn_workspace_size(dims)."""
+    rc = load_library().sa_paged_attn_q4(ctypes.byref(dims), _ptr(q), _ptr(k_codes), _ptr(v_codes),
+                                         _ptr(k_scales), _ptr(v_scales), _ptr(block_table),
+                                         _ptr(seq_lens), _ptr(q_lens), float(scale), _ptr(out),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _ptr(err_flag), _stream(stream))
+    _check(rc, "sa_paged_attn_q4")
 
 
 def defrag_apply_bytes(num_pages: int, page_bytes: int, pool_a, pool_b, moves, n_moves: int,

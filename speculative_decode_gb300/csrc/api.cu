@@ -196,14 +196,15 @@ size_t sa_paged_attn_workspace_size(const sa_dims *dims, const sa_plan *plan) {
     return attn_ws_layout(*dims, plan).total;
 }
 
-// int8 pools of sa_paged_attn_q8 (all NULL for bf16 pages)
-struct Q8Pools {
-    const int8_t *k_codes, *v_codes;
+// quantised pools of sa_paged_attn_q8 / _q4 (all NULL for bf16 pages)
+struct QuantPools {
+    const uint8_t *k_codes, *v_codes;
     const float *k_scales, *v_scales;
+    int bits;  // 8 or 4
 };
 
 static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_t *k_pages,
-                           const uint16_t *v_pages, const Q8Pools &q8, const int32_t *block_table,
+                           const uint16_t *v_pages, const QuantPools &q8, const int32_t *block_table,
                            const int32_t *seq_lens, const int32_t *q_lens, float scale, uint16_t *out,
                            const sa_plan *plan, void *workspace, size_t workspace_bytes,
                            int32_t *err_flag, void *stream) {
@@ -220,8 +221,8 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
                  !aligned(q8.v_scales, 16))
               : (!aligned(k_pages, 16) || !aligned(v_pages, 16)))
         return SA_ERR_ARG;
-    // int8 pages are attended on the CUDA cores only: no plan, fewer than
-    // kTcMinRows query rows per KV head
+    // quantised pages are attended on the CUDA cores only: no plan, fewer
+    // than kTcMinRows query rows per KV head
     if (is_q8 && (plan != nullptr || d.num_q_heads / d.num_kv_heads * std::max(1, d.max_q_len) >= kTcMinRows))
         return SA_ERR_UNSUPPORTED;
     if (plan && !plan_matches(plan, d)) return SA_ERR_ARG;
@@ -272,6 +273,7 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
     p.v_codes = q8.v_codes;
     p.k_scales = q8.k_scales;
     p.v_scales = q8.v_scales;
+    p.code_bits = q8.bits;
     p.v_pages = v_pages;
     p.out = out;
     p.block_table = block_table;
@@ -301,7 +303,7 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
     p.evict_first = c.nrb == 1;
 
     int per_sm = 0;
-    if (split_occupancy(c.R, is_q8, &per_sm) != cudaSuccess || per_sm <= 0) return SA_ERR_CUDA;
+    if (split_occupancy(c.R, is_q8 ? q8.bits : 16, &per_sm) != cudaSuccess || per_sm <= 0) return SA_ERR_CUDA;
     p.split_ctas = sms * per_sm;  // one warp per CTA, all resident
     p.pages_ready = ((pd && pd->num_tiles > 0) || c.tc.min_rows > 0) ? 1 : 0;
     if (launch_split_attn(p, s) != cudaSuccess)
@@ -313,7 +315,7 @@ int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t *k_page
                   const uint16_t *v_pages, const int32_t *block_table, const int32_t *seq_lens,
                   const int32_t *q_lens, float scale, uint16_t *out, const sa_plan *plan,
                   void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream) {
-    return paged_attn_impl(dims, q, k_pages, v_pages, Q8Pools{nullptr, nullptr, nullptr, nullptr},
+    return paged_attn_impl(dims, q, k_pages, v_pages, QuantPools{nullptr, nullptr, nullptr, nullptr, 16},
                            block_table, seq_lens, q_lens, scale, out, plan, workspace, workspace_bytes,
                            err_flag, stream);
 }
@@ -324,15 +326,28 @@ int sa_paged_attn_q8(const sa_dims *dims, const uint16_t *q, const int8_t *k_cod
                      float scale, uint16_t *out, void *workspace, size_t workspace_bytes,
                      int32_t *err_flag, void *stream) {
     if (k_codes == nullptr) return SA_ERR_ARG;
-    return paged_attn_impl(dims, q, nullptr, nullptr, Q8Pools{k_codes, v_codes, k_scales, v_scales},
+    return paged_attn_impl(dims, q, nullptr, nullptr,
+                           QuantPools{reinterpret_cast<const uint8_t *>(k_codes),
+                                      reinterpret_cast<const uint8_t *>(v_codes), k_scales, v_scales, 8},
                            block_table, seq_lens, q_lens, scale, out, nullptr, workspace,
                            workspace_bytes, err_flag, stream);
 }
 
-int sa_kv_append_q8(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_new,
-                    int8_t *k_codes, int8_t *v_codes, float *k_scales, float *v_scales,
-                    const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens,
-                    int32_t *err_flag, void *stream) {
+int sa_paged_attn_q4(const sa_dims *dims, const uint16_t *q, const uint8_t *k_codes,
+                     const uint8_t *v_codes, const float *k_scales, const float *v_scales,
+                     const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens,
+                     float scale, uint16_t *out, void *workspace, size_t workspace_bytes,
+                     int32_t *err_flag, void *stream) {
+    if (k_codes == nullptr) return SA_ERR_ARG;
+    return paged_attn_impl(dims, q, nullptr, nullptr, QuantPools{k_codes, v_codes, k_scales, v_scales, 4},
+                           block_table, seq_lens, q_lens, scale, out, nullptr, workspace,
+                           workspace_bytes, err_flag, stream);
+}
+
+static int kv_append_quant(const sa_dims *dims, int bits, const uint16_t *k_new, const uint16_t *v_new,
+                           uint8_t *k_codes, uint8_t *v_codes, float *k_scales, float *v_scales,
+                           const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens,
+                           int32_t *err_flag, void *stream) {
     int rc = check_dims(dims);
     if (rc) return rc;
     if (dims->num_seqs == 0 || dims->total_q == 0) return SA_OK;
@@ -343,10 +358,27 @@ int sa_kv_append_q8(const sa_dims *dims, const uint16_t *k_new, const uint16_t *
         !aligned(k_scales, 4) || !aligned(v_scales, 4))
         return SA_ERR_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (launch_kv_append_q8(*dims, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_table,
-                            seq_lens, q_lens, err_flag, s) != cudaSuccess)
+    if (launch_kv_append_quant(*dims, bits, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_table,
+                               seq_lens, q_lens, err_flag, s) != cudaSuccess)
         return SA_ERR_CUDA;
     return finish(s, err_flag);
+}
+
+int sa_kv_append_q8(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_new,
+                    int8_t *k_codes, int8_t *v_codes, float *k_scales, float *v_scales,
+                    const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens,
+                    int32_t *err_flag, void *stream) {
+    return kv_append_quant(dims, 8, k_new, v_new, reinterpret_cast<uint8_t *>(k_codes),
+                           reinterpret_cast<uint8_t *>(v_codes), k_scales, v_scales, block_table, seq_lens,
+                           q_lens, err_flag, stream);
+}
+
+int sa_kv_append_q4(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_new,
+                    uint8_t *k_codes, uint8_t *v_codes, float *k_scales, float *v_scales,
+                    const int32_t *block_table, const int32_t *seq_lens, const int32_t *q_lens,
+                    int32_t *err_flag, void *stream) {
+    return kv_append_quant(dims, 4, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_table,
+                           seq_lens, q_lens, err_flag, stream);
 }
 
 int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan) {

@@ -21,10 +21,11 @@
 //    one contiguous run inside a page) into its private ring of S stages with
 //    two 1-D bulk copies issued by lanes 0 and 1 in one instruction, and
 //    bulk-copies each piece's query rows ahead of use; all 32 lanes compute.
-//  * int8 pages (Q8 instances): the same kernel over int8 codes with one fp32
-//    scale per (page, head, token) row; lanes 2 and 3 also copy the tile's K
-//    and V scales, the loops run on codes converted exactly to floats, and
-//    the row scales multiply the scores (K) and the probabilities (V).
+//  * int8 and int4 pages (KB = 8 and 4 instances): the same kernel over codes
+//    with one fp32 scale per (page, head, token) row; lanes 2 and 3 also copy
+//    the tile's K and V scales, the loops run on codes converted exactly to
+//    floats, and the row scales multiply the scores (K) and the
+//    probabilities (V).
 //  * Lane mapping: a token is handled by L = 2R lanes (8, 16 or 32), each
 //    owning 128/L head dims, so pre-scaled queries and output accumulators
 //    live in registers. Q.K partial dots are combined with a shuffle
@@ -57,12 +58,17 @@ constexpr int kTile = SA_SPLIT_TILE;          // tokens per stage (16 or 32)
 constexpr int kRowBytes = kHeadDim * 2;       // one K or V row: 256 bytes
 constexpr int kKVBytes = kTile * kRowBytes;   // K (or V) rows of one tile, contiguous in a page
 constexpr int kStageBytes = 2 * kKVBytes;     // K tile, then V tile
-// int8 pages: a stage holds the tile's K codes, V codes, K scales, V scales
-constexpr int kQ8CodeBytes = kTile * kHeadDim;            // 2 KiB
-constexpr int kQ8ScaleBytes = kTile * 4;                  // 64 bytes
-constexpr int kQ8VCodes = kQ8CodeBytes, kQ8KScales = 2 * kQ8CodeBytes, kQ8VScales = kQ8KScales + kQ8ScaleBytes;
-constexpr int kQ8StageBytes = kQ8VScales + kQ8ScaleBytes;
-static_assert(kQ8StageBytes <= kStageBytes, "int8 tiles use the bf16 stage");
+// Quantised pages (KB-bit codes, KB = 8 or 4): a stage holds the tile's K
+// codes, V codes, K scales and V scales, in that order.
+template <int KB>
+struct QTile {
+    static constexpr int kCodeRow = kHeadDim * KB / 8;         // bytes of one row's codes
+    static constexpr int kCodeBytes = kTile * kCodeRow;        // 2 KiB (int8), 1 KiB (int4)
+    static constexpr int kScaleBytes = kTile * 4;              // 64 bytes
+    static constexpr int kVCodes = kCodeBytes, kKScales = 2 * kCodeBytes, kVScales = kKScales + kScaleBytes;
+    static constexpr int kBytes = kVScales + kScaleBytes;
+};
+static_assert(QTile<8>::kBytes <= kStageBytes && QTile<4>::kBytes <= kStageBytes, "quantised tiles use the bf16 stage");
 #ifndef SA_SPLIT_STAGES
 #define SA_SPLIT_STAGES 2
 #endif
@@ -172,6 +178,36 @@ __device__ __forceinline__ void load_tile_row_q8(const uint8_t *tile, int t, int
     } else {
         const uint32_t a = *reinterpret_cast<const uint32_t *>(row + j * 4);
         f[0] = codes_pair(a, 0); f[1] = codes_pair(a, 1);
+    }
+}
+
+// The same dims of row t of a tile of int4 codes (64-byte rows; value 2c is
+// the low nibble of byte c, stored as code + 8), as pairs of floats. The
+// nibbles of a word are split into bytes (low nibbles, high nibbles) and
+// converted like int8 codes: byte n in the low byte of 2^23 is 2^23 + n, and
+// one paired subtraction of 2^23 + 8 leaves the code, exactly.
+__device__ __forceinline__ void nibbles_pairs(uint32_t w, int npairs, float2 *f) {
+    const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (k < npairs) {
+            const float a = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u + k));
+            const float b = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u + k));
+            f[k] = ffma2(make_float2(a, b), make_float2(1.f, 1.f), make_float2(-8388616.f, -8388616.f));
+        }
+    }
+}
+
+template <int L>
+__device__ __forceinline__ void load_tile_row_q4(const uint8_t *tile, int t, int j, float2 (&f)[64 / L]) {
+    const uint8_t *row = tile + t * (kHeadDim / 2);
+    if constexpr (L == 8) {  // dims 8j..8j+7 and 64+8j..64+8j+7: bytes 4j.. and 32+4j..
+        nibbles_pairs(*reinterpret_cast<const uint32_t *>(row + j * 4), 4, f);
+        nibbles_pairs(*reinterpret_cast<const uint32_t *>(row + 32 + j * 4), 4, f + 4);
+    } else if constexpr (L == 16) {  // dims 8j..8j+7: bytes 4j..4j+3
+        nibbles_pairs(*reinterpret_cast<const uint32_t *>(row + j * 4), 4, f);
+    } else {  // dims 4j..4j+3: bytes 2j, 2j+1
+        nibbles_pairs(*reinterpret_cast<const uint16_t *>(row + j * 2), 2, f);
     }
 }
 
@@ -473,10 +509,13 @@ __device__ __forceinline__ void locate_seq(const SplitParams &P, int lane, bool 
 }
 
 
-template <int R, bool Q8>
+// KB: 16 for bf16 pages, 8 for int8 pages, 4 for int4 pages.
+template <int R, int KB>
 __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(const SplitParams P) {
     using Gm = Geo<R>;
     using Lay = Layout<R>;
+    using QT = QTile<KB < 16 ? KB : 8>;
+    constexpr bool Q = KB < 16;
     constexpr int L = Gm::L, TG = Gm::TG, NS = Gm::NS, NW = Gm::NW, DUP = Gm::DUP;
     constexpr int S = kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -660,25 +699,25 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
         const int pid = page_id(ib, t0 / kPageSize, (isi.T + kPageSize - 1) / kPageSize);
         const bool ok = static_cast<unsigned>(pid) < static_cast<unsigned>(P.num_pages);
         if (!ok && lane == 0) flag_error(P.err, kErrBitPageOOB);
-        if (lane < (Q8 ? 4 : 2)) {
+        if (lane < (Q ? 4 : 2)) {
             if (ok) {
                 // The tile's K rows and V rows are each one contiguous run in the
                 // page: lane 0 copies the K rows, lane 1 the V rows, in one
                 // instruction (the copy instruction's issue is slow; two lanes
-                // take the time of one). int8 pages: lanes 2 and 3 copy the rows'
-                // K and V scales (also contiguous) in the same instruction.
+                // take the time of one). Quantised pages: lanes 2 and 3 copy the
+                // rows' K and V scales (also contiguous) in the same instruction.
                 const int64_t row = static_cast<int64_t>(pid * P.Hkv + kvh) * kPageSize + (t0 % kPageSize);
                 if (lane == 0) {
                     stage_ok[s] = 1;
-                    mbar_arrive_expect_tx(&full[s], Q8 ? kQ8StageBytes : kStageBytes);
+                    mbar_arrive_expect_tx(&full[s], Q ? QT::kBytes : kStageBytes);
                 }
-                if constexpr (Q8) {
-                    const void *src = lane == 0 ? static_cast<const void *>(P.k_codes + row * kHeadDim)
-                                    : lane == 1 ? static_cast<const void *>(P.v_codes + row * kHeadDim)
+                if constexpr (Q) {
+                    const void *src = lane == 0 ? static_cast<const void *>(P.k_codes + row * QT::kCodeRow)
+                                    : lane == 1 ? static_cast<const void *>(P.v_codes + row * QT::kCodeRow)
                                     : lane == 2 ? static_cast<const void *>(P.k_scales + row)
                                                 : static_cast<const void *>(P.v_scales + row);
-                    const int off = lane == 0 ? 0 : lane == 1 ? kQ8VCodes : lane == 2 ? kQ8KScales : kQ8VScales;
-                    bulk_load_hint(smem + s * kStageBytes + off, src, lane < 2 ? kQ8CodeBytes : kQ8ScaleBytes,
+                    const int off = lane == 0 ? 0 : lane == 1 ? QT::kVCodes : lane == 2 ? QT::kKScales : QT::kVScales;
+                    bulk_load_hint(smem + s * kStageBytes + off, src, lane < 2 ? QT::kCodeBytes : QT::kScaleBytes,
                                    &full[s], policy);
                 } else {
                     bulk_load_hint(smem + s * kStageBytes + lane * kKVBytes, (lane ? P.v_pages : P.k_pages) + row * kHeadDim,
@@ -770,14 +809,15 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                         const int t = (b0 + bi) * TG + tg;
                         uint32_t kw[NW];
                         float2 kq[NW];
-                        if constexpr (Q8) load_tile_row_q8<L>(st, t, j, kq);
+                        if constexpr (KB == 8) load_tile_row_q8<L>(st, t, j, kq);
+                        else if constexpr (KB == 4) load_tile_row_q4<L>(st, t, j, kq);
                         else load_tile_row<L>(st, t, j, kw);
                         float2 a2[R];
 #pragma unroll
                         for (int r = 0; r < R; ++r) a2[r] = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int k = 0; k < NW; ++k) {
-                            const float2 kf = Q8 ? kq[k] : unpack_bf16x2(kw[k]);
+                            const float2 kf = Q ? kq[k] : unpack_bf16x2(kw[k]);
 #pragma unroll
                             for (int r = 0; r < R; ++r) a2[r] = ffma2(q2[r][k], kf, a2[r]);
                         }
@@ -808,8 +848,8 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
 #pragma unroll
                     for (int bi = 0; bi < NB; ++bi) {
                         const int t = (b0 + bi) * TG + tg;
-                        // int8 pages: the dot was over codes; the key row's scale completes it
-                        const float ks = Q8 ? reinterpret_cast<const float *>(st + kQ8KScales)[t] : 1.f;
+                        // quantised pages: the dot was over codes; the key row's scale completes it
+                        const float ks = Q ? reinterpret_cast<const float *>(st + QT::kKScales)[t] : 1.f;
                         sv[b0 + bi] = t0 + t <= lim ? v[bi][0] * ks : -INFINITY;
                     }
                 }
@@ -833,9 +873,9 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                 for (int step = 0; step < NS; ++step) {
                     const float p = exp2f(sv[step] - m_use);
                     lsum += p;
-                    // int8 pages: p times the value row's scale, so that P V runs on codes
+                    // quantised pages: p times the value row's scale, so that P V runs on codes
                     if (row_writer)
-                        pbuf[step * TG + tg][rj] = Q8 ? p * reinterpret_cast<const float *>(st + kQ8VScales)[step * TG + tg] : p;
+                        pbuf[step * TG + tg][rj] = Q ? p * reinterpret_cast<const float *>(st + QT::kVScales)[step * TG + tg] : p;
                 }
                 if (__any_sync(0xffffffffu, grow)) {
                     if (tg == 0 && row_writer) rowx[rj] = alpha;
@@ -857,7 +897,8 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                     if (t < nvalid) {
                         uint32_t vw[NW];
                         float2 vq[NW];
-                        if constexpr (Q8) load_tile_row_q8<L>(st + kQ8VCodes, t, j, vq);
+                        if constexpr (KB == 8) load_tile_row_q8<L>(st + QT::kVCodes, t, j, vq);
+                        else if constexpr (KB == 4) load_tile_row_q4<L>(st + QT::kVCodes, t, j, vq);
                         else load_tile_row<L>(st + kKVBytes, t, j, vw);
                         float pr[R];
 #pragma unroll
@@ -870,7 +911,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                         }
 #pragma unroll
                         for (int k = 0; k < NW; ++k) {
-                            const float2 vf = Q8 ? vq[k] : unpack_bf16x2(vw[k]);
+                            const float2 vf = Q ? vq[k] : unpack_bf16x2(vw[k]);
 #pragma unroll
                             for (int r = 0; r < R; ++r) acc[r][k] = ffma2(make_float2(pr[r], pr[r]), vf, acc[r][k]);
                         }
@@ -1042,9 +1083,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32, SA_COMBINE_MIN_CTAS) combi
 template <int R>
 constexpr size_t smem_bytes() { return Layout<R>::kBytes + 1024; }
 
-template <int R, bool Q8>
+template <int R, int KB>
 cudaError_t prepare() {
-    static cudaError_t err = cudaFuncSetAttribute(split_attn_kernel<R, Q8>,
+    static cudaError_t err = cudaFuncSetAttribute(split_attn_kernel<R, KB>,
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                   static_cast<int>(smem_bytes<R>()));
     return err;
@@ -1070,11 +1111,11 @@ cudaError_t launch_dependent(Kernel kernel, int grid, int threads, size_t smem, 
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-template <int R, bool Q8>
+template <int R, int KB>
 cudaError_t launch_r(const SplitParams &p, cudaStream_t stream) {
-    cudaError_t e = prepare<R, Q8>();
+    cudaError_t e = prepare<R, KB>();
     if (e != cudaSuccess) return e;
-    e = launch_dependent(split_attn_kernel<R, Q8>, p.split_ctas, 32, smem_bytes<R>(), stream, p);
+    e = launch_dependent(split_attn_kernel<R, KB>, p.split_ctas, 32, smem_bytes<R>(), stream, p);
     if (e != cudaSuccess) return e;
     // the combine pass: its scan runs while the split kernel finishes
     const int64_t units = static_cast<int64_t>(p.B) * p.Hkv * p.n_row_blocks * (R / 4);
@@ -1082,11 +1123,11 @@ cudaError_t launch_r(const SplitParams &p, cudaStream_t stream) {
                             kCombineWarps * 32, 0, stream, p);
 }
 
-template <int R, bool Q8>
+template <int R, int KB>
 cudaError_t occupancy_r(int *ctas_per_sm) {
-    cudaError_t e = prepare<R, Q8>();
+    cudaError_t e = prepare<R, KB>();
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, split_attn_kernel<R, Q8>, 32,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, split_attn_kernel<R, KB>, 32,
                                                          smem_bytes<R>());
 }
 
@@ -1096,29 +1137,29 @@ int split_tile_tokens() { return kTile; }
 int split_units_per_tile() { return kUnitsPerTile; }
 int split_segment_cost() { return kSegmentCost; }
 
-cudaError_t split_occupancy(int R, bool q8, int *ctas_per_sm) {
-    switch (R * 2 + (q8 ? 1 : 0)) {
-        case 8: return occupancy_r<4, false>(ctas_per_sm);
-        case 16: return occupancy_r<8, false>(ctas_per_sm);
-        case 32: return occupancy_r<16, false>(ctas_per_sm);
-        case 9: return occupancy_r<4, true>(ctas_per_sm);
-        case 17: return occupancy_r<8, true>(ctas_per_sm);
-        case 33: return occupancy_r<16, true>(ctas_per_sm);
-        default: return cudaErrorInvalidValue;
+#define SA_SPLIT_CASES(F, ...)                                                                      \
+    switch (R * 100 + KB) {                                                                          \
+        case 416: return F<4, 16>(__VA_ARGS__);                                                       \
+        case 816: return F<8, 16>(__VA_ARGS__);                                                       \
+        case 1616: return F<16, 16>(__VA_ARGS__);                                                     \
+        case 408: return F<4, 8>(__VA_ARGS__);                                                        \
+        case 808: return F<8, 8>(__VA_ARGS__);                                                        \
+        case 1608: return F<16, 8>(__VA_ARGS__);                                                      \
+        case 404: return F<4, 4>(__VA_ARGS__);                                                        \
+        case 804: return F<8, 4>(__VA_ARGS__);                                                        \
+        case 1604: return F<16, 4>(__VA_ARGS__);                                                      \
+        default: return cudaErrorInvalidValue;                                                       \
     }
+
+cudaError_t split_occupancy(int R, int code_bits, int *ctas_per_sm) {
+    const int KB = code_bits;
+    SA_SPLIT_CASES(occupancy_r, ctas_per_sm)
 }
 
 cudaError_t launch_split_attn(const SplitParams &p, cudaStream_t stream) {
-    const bool q8 = p.k_codes != nullptr;
-    switch (p.rows_per_block * 2 + (q8 ? 1 : 0)) {
-        case 8: return launch_r<4, false>(p, stream);
-        case 16: return launch_r<8, false>(p, stream);
-        case 32: return launch_r<16, false>(p, stream);
-        case 9: return launch_r<4, true>(p, stream);
-        case 17: return launch_r<8, true>(p, stream);
-        case 33: return launch_r<16, true>(p, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    const int R = p.rows_per_block, KB = p.k_codes != nullptr ? p.code_bits : 16;
+    SA_SPLIT_CASES(launch_r, p, stream)
 }
+#undef SA_SPLIT_CASES
 
 }  // namespace sa

@@ -61,10 +61,13 @@ struct SplitParams {
     int32_t evict_first;
     int32_t split_ctas;         // grid of the split kernel (one warp each); the combine
                                 // pass recomputes the same cut of the work
-    // int8 pages (NULL for bf16 pages): codes [num_pages, Hkv, 256, 128], one
-    // scale per (page, head, token) row [num_pages, Hkv, 256]; value = code * scale
-    const int8_t *k_codes, *v_codes;
+    // quantised pages (NULL for bf16 pages): codes [num_pages, Hkv, 256, 128 *
+    // code_bits / 8] (int8 codes, or int4 as nibble = code + 8 with value 2c in
+    // the low nibble of byte c), one scale per (page, head, token) row
+    // [num_pages, Hkv, 256]; value = code * scale
+    const uint8_t *k_codes, *v_codes;
     const float *k_scales, *v_scales;
+    int32_t code_bits;          // 8 or 4 when k_codes is set
     int32_t pages_ready;        // 1: a kernel of this call that started after the pages were
                                 // written ran first, so pages are read without waiting for it
 };
@@ -72,7 +75,7 @@ struct SplitParams {
 // Split kernel over p.split_ctas one-warp CTAs, then the combine pass that
 // merges the partials of segments cut into pieces (two kernels).
 cudaError_t launch_split_attn(const SplitParams &p, cudaStream_t stream);
-cudaError_t split_occupancy(int R, bool q8, int *ctas_per_sm);
+cudaError_t split_occupancy(int R, int code_bits, int *ctas_per_sm);  // code_bits 16: bf16 pages
 int split_tile_tokens();  // tokens per K/V tile of the split kernel
 int split_units_per_tile();  // balancing units of one tile and of a segment start
 int split_segment_cost();
@@ -84,10 +87,12 @@ int defrag_plan_host(int num_seqs, int num_pages, int max_pages, const int32_t *
 cudaError_t launch_defrag(void *k_pages, void *v_pages, const int32_t *moves, int n_moves,
                           int num_pages, int64_t page_bytes, int32_t *err, int sms, cudaStream_t stream);
 
-cudaError_t launch_kv_append_q8(const sa_dims &d, const uint16_t *k_new, const uint16_t *v_new,
-                                int8_t *k_codes, int8_t *v_codes, float *k_scales, float *v_scales,
-                                const int32_t *block_table, const int32_t *seq_lens,
-                                const int32_t *q_lens, int32_t *err, cudaStream_t stream);
+// kv_append for quantised pages: code_bits 8 (int8) or 4 (int4 nibbles)
+cudaError_t launch_kv_append_quant(const sa_dims &d, int code_bits, const uint16_t *k_new,
+                                   const uint16_t *v_new, uint8_t *k_codes, uint8_t *v_codes,
+                                   float *k_scales, float *v_scales, const int32_t *block_table,
+                                   const int32_t *seq_lens, const int32_t *q_lens, int32_t *err,
+                                   cudaStream_t stream);
 cudaError_t launch_kv_append(const sa_dims &d, const uint16_t *k_new, const uint16_t *v_new,
                              uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,
                              const int32_t *seq_lens, const int32_t *q_lens, int32_t *err,

@@ -1,0 +1,123 @@
+"""int4 K/V pages on the GPU against the oracle: the append's nibbles and
+scales bit-exact, attention over int4 pages within the attention tolerance
+(the oracle attends the same (nibble - 8) * scale values in fp64)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decode_gb300 as sa
+import workloads as wl
+from gpu_path import assert_attention_close, dev_tensor, dims_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from speculative_decode_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+def q4_pools(w):
+    kc, ks = oracle.quantize_q4(w.k_pages)
+    vc, vs = oracle.quantize_q4(w.v_pages)
+    return kc, vc, ks, vs
+
+
+def attend_q4(w, pools, block_table=None):
+    """paged_attn_q4 on the GPU over device pools; returns (out bits, err)."""
+    d = dims_of(w)
+    bt = dev_tensor(w.block_table if block_table is None else block_table)
+    sl, ql = dev_tensor(w.seq_lens), dev_tensor(w.q_lens)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(sa.paged_attn_workspace_size(d), dtype=torch.uint8, device="cuda")
+    q = dev_tensor(w.q)
+    out = torch.zeros_like(q)
+    sa.paged_attn_q4(d, q, *pools, bt, sl, ql, w.scale, out, ws, err_flag=err)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().view(np.uint16), int(err.item())
+
+
+def run_q4(w, append=True):
+    """kv_append_q4 (optional) then paged_attn_q4 on the GPU from pools the
+    oracle quantised; returns (out bits, err, pools after the call)."""
+    d = dims_of(w)
+    pools = [dev_tensor(a) for a in q4_pools(w)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if append:
+        sa.kv_append_q4(d, dev_tensor(w.k_new), dev_tensor(w.v_new), *pools, dev_tensor(w.block_table),
+                        dev_tensor(w.seq_lens), dev_tensor(w.q_lens), err_flag=err)
+    out, e = attend_q4(w, pools)
+    torch.cuda.synchronize()
+    return out, int(err.item()) | e, tuple(t.cpu().numpy() for t in pools)
+
+
+def oracle_q4(w, append=True):
+    pools = q4_pools(w)
+    if append:
+        pools = oracle.kv_append_q4(*pools, w.k_new, w.v_new, w.block_table, w.pos_start, w.q_lens)
+    kc, vc, ks, vs = pools
+    return oracle.attention_rows_q4(w.q, kc, vc, ks, vs, w.block_table, w.seq_lens, w.q_lens, w.scale), pools
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_q4_random_small_cases(seed):
+    """Random GQA ratios (1, 2, 4 query heads per KV head), context lengths
+    from a few tokens to several pages and q_len 0-3: every row block size of
+    the CUDA-core kernel (4, 8 and 16 rows) over int4 pages."""
+    rng = np.random.default_rng(100 + seed)
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4]))
+    w = wl.random_case(320 + seed, num_seqs=int(rng.integers(1, 6)), Hq=G * Hkv, Hkv=Hkv,
+                       max_ctx=int(rng.choice([40, 300, 1300])), q_len_choices=(0, 1, 2, 3))
+    out, err, pools = run_q4(w)
+    ref, ref_pools = oracle_q4(w)
+    assert err == 0
+    for got, exp in zip(pools, ref_pools):  # the append's nibbles and scales, bit for bit
+        assert np.array_equal(got.view(exp.dtype) if got.dtype != exp.dtype else got, exp)
+    assert_attention_close(out, ref, f"seed {seed}")
+
+
+def test_q4_llama3_decode_batch_all_rows():
+    """The Llama3-8B-shaped decode batch (64 sequences, 32q/8kv) over int4 pages."""
+    w = wl.config(1)
+    out, err, _ = run_q4(w)
+    ref, _ = oracle_q4(w)
+    assert err == 0
+    assert_attention_close(out, ref, "decode q4")
+
+
+def test_q4_rejects_tensor_core_shapes():
+    w = wl.random_case(311, num_seqs=2, Hq=8, Hkv=2, max_ctx=300, q_len_choices=(6,))  # 24 rows per KV head
+    with pytest.raises(sa.SpecAttnError):
+        run_q4(w, append=False)
+
+
+def test_q4_defrag_codes_and_scales():
+    """Compaction of int4 pools (code pages of Hkv*256*64 bytes, scale pages
+    of Hkv*256*4): pools bit-exact against the oracle's page moves, attention
+    through the new tables bit-identical to attention before."""
+    w = wl.random_case(1310, num_seqs=5, Hq=16, Hkv=4, max_ctx=1500, q_len_choices=(1, 2),
+                       num_pages=80, shared_prefix_pages=2)
+    d = dims_of(w)
+    new, moves, _ = sa.defrag_moves(d, w.block_table, w.seq_lens)
+    assert len(moves) > 0
+    host = q4_pools(w)
+    g = [dev_tensor(a) for a in host]
+    before, e0 = attend_q4(w, g)
+    mv = torch.from_numpy(np.ascontiguousarray(moves, np.int32).reshape(-1, 2)).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    npg = host[0].shape[0]
+    sa.defrag_apply_bytes(npg, host[0][0].nbytes, g[0], g[1], mv, len(moves), err_flag=err)
+    sa.defrag_apply_bytes(npg, host[2][0].nbytes, g[2], g[3], mv, len(moves), err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    u16 = lambda a: a.view(np.uint16).reshape(npg, -1)  # the oracle moves pages of 16-bit words
+    exp = oracle.defrag_move(u16(host[0]), u16(host[1]), moves) + oracle.defrag_move(u16(host[2]), u16(host[3]), moves)
+    for t, e in zip(g, exp):
+        assert np.array_equal(u16(t.cpu().numpy()), e)
+    after, e1 = attend_q4(w, g, block_table=new)
+    assert e0 == 0 and e1 == 0
+    assert np.array_equal(before, after)
