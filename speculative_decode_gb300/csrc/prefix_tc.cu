@@ -98,6 +98,25 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// Paired fp32 fused multiply-add: (a.x * b.x + c.x, a.y * b.y + c.y), one instruction.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long ra = *reinterpret_cast<unsigned long long *>(&a);
+    unsigned long long rb = *reinterpret_cast<unsigned long long *>(&b);
+    unsigned long long rc = *reinterpret_cast<unsigned long long *>(&c);
+    unsigned long long rd;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    return *reinterpret_cast<float2 *>(&rd);
+}
+
+// 2^x by the special-function unit's approximation, results below the
+// smallest normal flushed to zero (a probability that small adds nothing
+// to a row sum of at least 1).
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // 32 consecutive 32-bit columns of this thread's tensor-memory lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
@@ -486,6 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         int i = 0;  // tile index over all pieces of this CTA
         int p = 0;  // piece index
+        const bool pos_scale = P.qscale > 0.f;
+        const float qs = pos_scale ? P.qscale : 1.f;  // the scale applied in the exponent
         TcCursor cur;
         TcPiece pc;
         bool more = first_piece(cur, pc);
@@ -532,18 +553,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_cols<KPC>(tmem + (i % kSBufs) * kN + koff + lane_base, x);
                     tc_fence_before();
                     mbar_arrive(&s_free[i % kSBufs]);  // Q K^T of tile i + kSBufs may overwrite it
-                    const bool whole = pos0 + kN - 1 <= rm.limit;  // no key of this tile is masked for this row
+                    // Scores stay unscaled: with a positive scale the row max of the
+                    // raw scores, scaled once, is the max of the scaled scores, and
+                    // the scale enters each probability's exponent through one paired
+                    // FMA. Any other scale multiplies the scores first (qs = 1).
+                    if (!pos_scale) {
 #pragma unroll
-                    for (int k = 0; k < KPC; ++k)
-                        x[k] = (whole || pos0 + koff + k <= rm.limit) ? x[k] * P.qscale : -INFINITY;
+                        for (int k = 0; k < KPC; ++k) x[k] *= P.qscale;
+                    }
+                    if (pos0 + kN - 1 > rm.limit) {  // a diagonal tile: keys past the row's limit are masked
+#pragma unroll
+                        for (int k = 0; k < KPC; ++k)
+                            if (pos0 + koff + k > rm.limit) x[k] = -INFINITY;
+                    }
                     // row max as a tree (independent partial maxima, short dependency chains)
                     float mx[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) mx[k] = x[k];
 #pragma unroll
                     for (int k = 8; k < KPC; ++k) mx[k & 7] = fmaxf(mx[k & 7], x[k]);
-                    const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    const float tmax = qs * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                     // move the reference max only when it grows by more than 2^8, so
                     // that tensor-memory O is rarely rescaled (p stays below 256)
                     const bool grow = tmax > m_ref + 8.f;
@@ -552,16 +582,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float m_use = m_new == -INFINITY ? 0.f : m_new;
                     // probabilities, packed to bf16 pairs while the tensor cores run P V
                     uint32_t pw[KPC / 2];
-                    float ps[8];
+                    float2 ps[4];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+                    for (int k = 0; k < 4; ++k) ps[k] = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int k = 0; k < KPC / 2; ++k) {
-                        const float a = exp2f(x[2 * k] - m_use), b = exp2f(x[2 * k + 1] - m_use);
-                        ps[k & 7] += a + b;
-                        pw[k] = pack_bf16x2(a, b);
+                        const float2 e = fma2(make_float2(x[2 * k], x[2 * k + 1]), make_float2(qs, qs),
+                                              make_float2(-m_use, -m_use));
+                        const float2 ab = make_float2(ex2_ftz(e.x), ex2_ftz(e.y));
+                        ps[k & 3] = fma2(ab, make_float2(1.f, 1.f), ps[k & 3]);
+                        pw[k] = pack_bf16x2(ab.x, ab.y);
                     }
-                    const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                    const float psum = ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
                     if (i >= 2) {  // P V of tile i - 2 must be done before its P buffer is rewritten
                         ok = wait_pv(i - 2);
                         if (!ok) break;
