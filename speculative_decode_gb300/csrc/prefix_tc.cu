@@ -108,6 +108,13 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     return *reinterpret_cast<float2 *>(&rd);
 }
 
+// max(a, b, c) in one instruction (exact, like two fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // 2^x by the special-function unit's approximation, results below the
 // smallest normal flushed to zero (a probability that small adds nothing
 // to a row sum of at least 1).
@@ -566,14 +573,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < KPC; ++k)
                             if (pos0 + koff + k > rm.limit) x[k] = -INFINITY;
                     }
-                    // row max as a tree (independent partial maxima, short dependency chains)
+                    // row max as a tree of three-input maxima (independent partial
+                    // maxima, short dependency chains)
                     float mx[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) mx[k] = x[k];
 #pragma unroll
-                    for (int k = 8; k < KPC; ++k) mx[k & 7] = fmaxf(mx[k & 7], x[k]);
-                    const float tmax = qs * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    for (int k = 8; k < KPC; k += 16)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) mx[c] = fmax3(mx[c], x[k + c], k + 8 + c < KPC ? x[k + 8 + c] : x[k + c]);
+                    const float tmax = qs * fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], fmax3(mx[4], mx[5], mx[6]), mx[7]));
                     // move the reference max only when it grows by more than 2^8, so
                     // that tensor-memory O is rarely rescaled (p stays below 256)
                     const bool grow = tmax > m_ref + 8.f;
