@@ -204,7 +204,7 @@ struct QuantPools {
 };
 
 static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_t *k_pages,
-                           const uint16_t *v_pages, const QuantPools &q8, const int32_t *block_table,
+                           const uint16_t *v_pages, const QuantPools &qp, const int32_t *block_table,
                            const int32_t *seq_lens, const int32_t *q_lens, float scale, uint16_t *out,
                            const sa_plan *plan, void *workspace, size_t workspace_bytes,
                            int32_t *err_flag, void *stream) {
@@ -212,18 +212,18 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
     if (rc) return rc;
     const sa_dims &d = *dims;
     if (d.num_seqs == 0 || d.total_q == 0) return SA_OK;
-    const bool is_q8 = q8.k_codes != nullptr;
+    const bool quant = qp.k_codes != nullptr;
     if (!q || !block_table || !seq_lens || !q_lens || !out) return SA_ERR_ARG;
-    if (is_q8 ? (!q8.v_codes || !q8.k_scales || !q8.v_scales) : (!k_pages || !v_pages)) return SA_ERR_ARG;
+    if (quant ? (!qp.v_codes || !qp.k_scales || !qp.v_scales) : (!k_pages || !v_pages)) return SA_ERR_ARG;
     if (d.num_pages == 0 || d.max_pages_per_seq == 0) return SA_ERR_ARG;
     if (!aligned(q, 16) || !aligned(out, 16)) return SA_ERR_ARG;
-    if (is_q8 ? (!aligned(q8.k_codes, 16) || !aligned(q8.v_codes, 16) || !aligned(q8.k_scales, 16) ||
-                 !aligned(q8.v_scales, 16))
+    if (quant ? (!aligned(qp.k_codes, 16) || !aligned(qp.v_codes, 16) || !aligned(qp.k_scales, 16) ||
+                 !aligned(qp.v_scales, 16))
               : (!aligned(k_pages, 16) || !aligned(v_pages, 16)))
         return SA_ERR_ARG;
     // quantised pages are attended on the CUDA cores only: no plan, fewer
     // than kTcMinRows query rows per KV head
-    if (is_q8 && (plan != nullptr || d.num_q_heads / d.num_kv_heads * std::max(1, d.max_q_len) >= kTcMinRows))
+    if (quant && (plan != nullptr || d.num_q_heads / d.num_kv_heads * std::max(1, d.max_q_len) >= kTcMinRows))
         return SA_ERR_UNSUPPORTED;
     if (plan && !plan_matches(plan, d)) return SA_ERR_ARG;
     const WsLayout wl = attn_ws_layout(d, plan);
@@ -269,11 +269,11 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
     SplitParams p{};
     p.q = q;
     p.k_pages = k_pages;
-    p.k_codes = q8.k_codes;
-    p.v_codes = q8.v_codes;
-    p.k_scales = q8.k_scales;
-    p.v_scales = q8.v_scales;
-    p.code_bits = q8.bits;
+    p.k_codes = qp.k_codes;
+    p.v_codes = qp.v_codes;
+    p.k_scales = qp.k_scales;
+    p.v_scales = qp.v_scales;
+    p.code_bits = qp.bits;
     p.v_pages = v_pages;
     p.out = out;
     p.block_table = block_table;
@@ -303,7 +303,7 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
     p.evict_first = c.nrb == 1;
 
     int per_sm = 0;
-    if (split_occupancy(c.R, is_q8 ? q8.bits : 16, &per_sm) != cudaSuccess || per_sm <= 0) return SA_ERR_CUDA;
+    if (split_occupancy(c.R, quant ? qp.bits : 16, &per_sm) != cudaSuccess || per_sm <= 0) return SA_ERR_CUDA;
     p.split_ctas = sms * per_sm;  // one warp per CTA, all resident
     p.pages_ready = ((pd && pd->num_tiles > 0) || c.tc.min_rows > 0) ? 1 : 0;
     if (launch_split_attn(p, s) != cudaSuccess)

@@ -514,8 +514,8 @@ template <int R, int KB>
 __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(const SplitParams P) {
     using Gm = Geo<R>;
     using Lay = Layout<R>;
-    using QT = QTile<KB < 16 ? KB : 8>;
-    constexpr bool Q = KB < 16;
+    constexpr bool Q = KB < 16;             // quantised pages
+    using QT = QTile<Q ? KB : 8>;           // their stage layout (unused for bf16 pages)
     constexpr int L = Gm::L, TG = Gm::TG, NS = Gm::NS, NW = Gm::NW, DUP = Gm::DUP;
     constexpr int S = kStages;
     extern __shared__ uint8_t smem_raw[];

@@ -128,6 +128,7 @@ cudaError_t launch_kv_append_quant(const sa_dims &d, int code_bits, const uint16
     if (d.num_seqs == 0 || d.max_q_len == 0) return cudaSuccess;
     const int threads = 32 * (d.num_kv_heads < 8 ? d.num_kv_heads : 8);
     dim3 grid(d.max_q_len, d.num_seqs);
+    if (code_bits != 8 && code_bits != 4) return cudaErrorInvalidValue;
     auto kernel = code_bits == 8 ? kv_append_kernel<8> : kv_append_kernel<4>;
     kernel<<<grid, threads, 0, stream>>>(k_new, v_new, nullptr, nullptr,
                                                          QPages{k_codes, v_codes, k_scales, v_scales},
