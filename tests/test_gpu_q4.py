@@ -121,3 +121,22 @@ def test_q4_defrag_codes_and_scales():
     after, e1 = attend_q4(w, g, block_table=new)
     assert e0 == 0 and e1 == 0
     assert np.array_equal(before, after)
+
+
+def test_q4_out_of_range_page_sets_the_flag():
+    w = wl.random_case(351, num_seqs=3, Hq=4, Hkv=2, max_ctx=600, q_len_choices=(1,))
+    w.block_table = w.block_table.copy()
+    w.block_table[1, 0] = w.num_pages + 5
+    _, err, _ = run_q4(w, append=False)
+    assert err & (1 << 3)
+
+
+def test_q4_repeated_calls_identical():
+    """The cut of the work and every summation order are fixed: the same call
+    twice gives the same bits."""
+    w = wl.random_case(352, num_seqs=5, Hq=8, Hkv=2, max_ctx=1500, q_len_choices=(1, 2))
+    pools = [dev_tensor(a) for a in q4_pools(w)]
+    a, e0 = attend_q4(w, pools)
+    b, e1 = attend_q4(w, pools)
+    assert e0 == 0 and e1 == 0
+    assert np.array_equal(a, b)

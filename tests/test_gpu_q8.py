@@ -119,3 +119,11 @@ def test_q8_defrag_codes_and_scales(seed, Hkv):
     torch.cuda.synchronize()
     assert e0 == 0 and int(err.item()) == 0
     assert np.array_equal(before, out.cpu().numpy().view(np.uint16))
+
+
+def test_q8_out_of_range_page_sets_the_flag():
+    w = wl.random_case(341, num_seqs=3, Hq=4, Hkv=2, max_ctx=600, q_len_choices=(1,))
+    w.block_table = w.block_table.copy()
+    w.block_table[1, 0] = w.num_pages + 5
+    _, err, _ = run_q8(w, append=False)
+    assert err & (1 << 3)
