@@ -228,10 +228,10 @@ def timed_steps(batch: GpuBatch, steps: int, warmup: int, flush, parts):
     return per_part, wall
 
 
-# DRAM bytes of one split_attn_kernel<4> launch on the decode batch, from the
-# ncu capture summarised in profiles/split_attn_kernel_R4_llama3_8b_decode.md
-# (200.35 MB read + 3.74 MB written). Set to None when the kernel changes.
-SPLIT_TRAFFIC_BYTES = 204_091_392
+# DRAM bytes (read + written) of one decode-batch launch of the attention
+# kernel, from one ncu capture of the build that bench.py times; None until
+# that capture is taken again after a change to the kernel.
+DECODE_TRAFFIC_BYTES = None
 
 
 def timed_sequence(batch: GpuBatch, steps: int, warmup: int, flush, parts):
@@ -539,10 +539,10 @@ def run_ours(args):
         "frac_of_hbm_peak": round(achieved / peak, 4),
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": SPLIT_TRAFFIC_BYTES,
-            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of split_attn_kernel<4>, "
-                              "one capture of this build (profiles/split_attn_kernel_R4_llama3_8b_decode.md)",
-            "kernel": "paged_attn call (split_attn_kernel + combine_kernel)",
+            "frac": round(achieved / peak, 4), "traffic": DECODE_TRAFFIC_BYTES,
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of stream_attn_kernel<4>, "
+                              "one capture of this build",
+            "kernel": "paged_attn call (stream_attn_kernel<4>, one launch)",
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback 6.8 TB/s",
         },

@@ -21,11 +21,14 @@
  *     caller clears the flag and reads it when it chooses. err_flag may be
  *     NULL, in which case such errors are dropped silently.
  *   - Workspaces are caller-owned device buffers of at least the size the
- *     matching *_workspace_size call returns, 256-byte aligned. The
- *     sa_paged_attn workspace needs no initialisation; the sa_spec_verify_greedy
- *     workspace must be ZERO-FILLED BEFORE ITS FIRST USE, and every call leaves
- *     its counters at zero again. A workspace can be reused call after call on
- *     one stream; two calls in flight at once need two workspaces.
+ *     matching *_workspace_size call returns, 256-byte aligned. Both the
+ *     sa_paged_attn and the sa_spec_verify_greedy workspace must be
+ *     ZERO-FILLED BEFORE THEIR FIRST USE (they hold counters), and every call
+ *     that completes without a device error leaves those counters at zero
+ *     again; after a call that set a device error flag, zero the workspace
+ *     again. A workspace can be reused call after call on one stream, for any
+ *     shapes it is large enough for; two calls in flight at once need two
+ *     workspaces.
  */
 #ifndef SPECATTN_H
 #define SPECATTN_H
@@ -261,9 +264,11 @@ SA_API int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan);
  *     above 16 MiB are rejected with SA_ERR_WORKSPACE before any GPU work.
  *   - The first call on a device looks up the array's device address with that
  *     device current; make that first call before any stream capture.
- *   - Every call reuses the same array (partial accumulators, no counters):
- *     two calls that overlap on the GPU (different streams, or different host
- *     threads on one device) race and give wrong results.
+ *   - Every call reuses the same array (partial accumulators and counters,
+ *     zero when the library is loaded and left at zero by every call that
+ *     completes without a device error): two calls that overlap on the GPU
+ *     (different streams, or different host threads on one device) race and
+ *     give wrong results.
  *   - No cudaMalloc, cudaFree or other allocating routine is called.
  */
 SA_API int sa_paged_attn_noalloc(const sa_dims *dims, const uint16_t *q, const uint16_t *k_pages,

@@ -35,9 +35,8 @@ _lib = None
 
 
 def library_path() -> str:
-    """The library this process loads: the in-tree build, or the file named by
-    SA_LIBRARY_PATH (a build of the same sources with other tuning constants)."""
-    return os.environ.get("SA_LIBRARY_PATH") or LIB
+    """The library this process loads: the in-tree build."""
+    return LIB
 
 
 def load_library() -> ctypes.CDLL:

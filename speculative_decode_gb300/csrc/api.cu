@@ -90,26 +90,55 @@ constexpr int kMaxMergeSlotsHost = 16;
 bool merge_fits(const SplitConfig &c) { return c.n_slots <= kMaxMergeSlotsHost;
 }
 
-// Workspace layout: fp32 accumulators [n_slots][total_q * Hq][128], then
-// (max, sum) pairs [n_slots][total_q * Hq][2]. Every slot a call reads was
-// written earlier in the same call, so the workspace needs no initialisation.
-// It is sized for the finest split any device could choose, so sizing needs
-// no device.
+// Workspace layout. The first kCounterBytes hold the persistent kernel's
+// counters (one per cut segment; zero between calls: every call leaves them at
+// zero, so the workspace must be zero-filled once before its first use); no
+// other kernel touches them, so one workspace serves calls of any shape. Then
+// the partials: for the persistent kernel, fp32 accumulators [slots][R][128]
+// and (max, sum) pairs [slots][R][2] (two slots per CTA); for the split kernel,
+// accumulators [n_slots][total_q * Hq][128] and pairs [n_slots][total_q * Hq]
+// [2]. Every partial a call reads was written earlier in the same call. The
+// sizes are for the finest split any device could choose, so sizing needs no
+// device.
+constexpr size_t kCounterBytes = 4096;
+static_assert(kStreamMaxCtas * 4 <= static_cast<int>(kCounterBytes), "counters fit their region");
+
 struct WsLayout {
-    int64_t slots_cap;
-    size_t ml_offset, total;
+    size_t acc_offset, ml_offset, total;
 };
 
-WsLayout attn_ws_layout(const sa_dims &d, const sa_plan *plan) {
+// Calls with bf16 pages, no plan and fewer than kTcMinRows query rows per KV
+// head go to the persistent page-streaming kernel.
+bool use_stream(const sa_dims &d, const sa_plan *plan, bool quant) {
+    return !quant && plan == nullptr && d.num_q_heads / d.num_kv_heads * std::max(1, d.max_q_len) < kTcMinRows;
+}
+
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+WsLayout attn_ws_layout(const sa_dims &d, const sa_plan *plan, bool quant) {
     WsLayout w{};
     const SplitConfig c = split_config(d, plan);
-    w.slots_cap = c.n_slots;
+    w.acc_offset = kCounterBytes;
+    if (use_stream(d, plan, quant)) {
+        const size_t rows = static_cast<size_t>(kStreamSlots) * c.R;
+        w.ml_offset = w.acc_offset + align256(rows * kHeadDim * 4);
+        w.total = w.ml_offset + align256(rows * 2 * 4);
+        return w;
+    }
     const int64_t rows = static_cast<int64_t>(d.total_q) * d.num_q_heads;
-    const size_t acc = static_cast<size_t>(w.slots_cap * rows * kHeadDim * 4);
-    const size_t ml = static_cast<size_t>(w.slots_cap * rows * 2 * 4);
-    w.ml_offset = (acc + 255) / 256 * 256;
-    w.total = w.ml_offset + (ml + 255) / 256 * 256;
+    const size_t acc = static_cast<size_t>(c.n_slots * rows * kHeadDim * 4);
+    const size_t ml = static_cast<size_t>(c.n_slots * rows * 2 * 4);
+    w.ml_offset = w.acc_offset + align256(acc);
+    w.total = w.ml_offset + align256(ml);
     return w;
+}
+
+// The size sa_paged_attn_workspace_size reports: without a plan it covers
+// both bf16 and quantised pages (the quantised calls take the same size).
+size_t attn_ws_bytes(const sa_dims &d, const sa_plan *plan) {
+    size_t n = attn_ws_layout(d, plan, false).total;
+    if (plan == nullptr) n = std::max(n, attn_ws_layout(d, plan, true).total);
+    return n;
 }
 
 using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -143,6 +172,32 @@ CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void 
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, dtype, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// Tensor maps of the persistent kernel for one pair of pools. A decode loop
+// calls with the same pools every step, so the last pair's maps are kept
+// (per host thread; a map holds only the pool's address and shape).
+const StreamMaps *stream_maps(const uint16_t *k_pages, const uint16_t *v_pages, uint64_t rows) {
+    struct Entry {
+        const void *k = nullptr, *v = nullptr;
+        uint64_t rows = 0;
+        StreamMaps maps;
+    };
+    thread_local Entry e;
+    if (e.k == k_pages && e.v == v_pages && e.rows == rows) return &e.maps;
+    e.k = nullptr;
+    for (int i = 0; i < kStreamBoxKinds; ++i) {
+        const uint32_t box_rows = static_cast<uint32_t>(stream_tile_tokens()) << i;
+        if (encode_tensor_map_2d(&e.maps.k[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(k_pages),
+                                 kHeadDim, rows, kHeadDim * 2, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+            encode_tensor_map_2d(&e.maps.v[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(v_pages),
+                                 kHeadDim, rows, kHeadDim * 2, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return nullptr;
+    }
+    e.k = k_pages;
+    e.v = v_pages;
+    e.rows = rows;
+    return &e.maps;
 }
 
 int device_sm_count() {
@@ -193,7 +248,7 @@ int sa_kv_append(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_n
 
 size_t sa_paged_attn_workspace_size(const sa_dims *dims, const sa_plan *plan) {
     if (check_dims(dims) != SA_OK) return 0;
-    return attn_ws_layout(*dims, plan).total;
+    return attn_ws_bytes(*dims, plan);
 }
 
 // quantised pools of sa_paged_attn_q8 / _q4 (all NULL for bf16 pages)
@@ -226,14 +281,51 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
     if (quant && (plan != nullptr || d.num_q_heads / d.num_kv_heads * std::max(1, d.max_q_len) >= kTcMinRows))
         return SA_ERR_UNSUPPORTED;
     if (plan && !plan_matches(plan, d)) return SA_ERR_ARG;
-    const WsLayout wl = attn_ws_layout(d, plan);
+    const WsLayout wl = attn_ws_layout(d, plan, quant);
     if (workspace == nullptr || workspace_bytes < wl.total || !aligned(workspace, 256))
         return SA_ERR_WORKSPACE;
     const int sms = device_sm_count();
     if (sms <= 0) return SA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
 
     const SplitConfig c = split_config(d, plan);
+    if (use_stream(d, plan, quant)) {
+        // the work is counted in 32-bit balancing units
+        const int64_t max_units = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.nrb *
+                                  (static_cast<int64_t>(d.max_pages_per_seq) * (kPageSize / stream_tile_tokens()) *
+                                       stream_units_per_tile() + stream_segment_cost());
+        if (max_units > INT32_MAX / 2) return SA_ERR_UNSUPPORTED;
+        StreamParams p{};
+        p.q = q;
+        p.k_pages = k_pages;
+        p.v_pages = v_pages;
+        p.out = out;
+        p.block_table = block_table;
+        p.seq_lens = seq_lens;
+        p.q_lens = q_lens;
+        p.part_acc = reinterpret_cast<float *>(ws + wl.acc_offset);
+        p.part_ml = reinterpret_cast<float *>(ws + wl.ml_offset);
+        p.counters = reinterpret_cast<int32_t *>(ws);
+        p.err = err_flag;
+        p.B = d.num_seqs;
+        p.Hq = d.num_q_heads;
+        p.Hkv = d.num_kv_heads;
+        p.G = d.num_q_heads / d.num_kv_heads;
+        p.num_pages = d.num_pages;
+        p.max_pages = d.max_pages_per_seq;
+        p.total_q = d.total_q;
+        p.max_q_len = d.max_q_len;
+        p.R = c.R;
+        p.qscale = scale * 1.4426950408889634f;
+        p.n_ctas = std::min(sms, kStreamMaxCtas);
+        p.evict_first = c.nrb == 1;
+        const uint64_t rows = static_cast<uint64_t>(d.num_pages) * d.num_kv_heads * kPageSize;
+        const StreamMaps *maps = stream_maps(k_pages, v_pages, rows);
+        if (maps == nullptr) return SA_ERR_CUDA;
+        if (launch_stream_attn(p, *maps, s) != cudaSuccess) return SA_ERR_CUDA;
+        return finish(s, err_flag);
+    }
     if (!merge_fits(c)) return SA_ERR_UNSUPPORTED;  // too many partials per row to merge
     // the split kernel counts work in 32-bit balancing units
     const int64_t max_work = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.nrb *
@@ -241,8 +333,8 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
                                   split_units_per_tile() + split_segment_cost());
     if (max_work > INT32_MAX) return SA_ERR_UNSUPPORTED;
     const int64_t rows_total = static_cast<int64_t>(d.total_q) * d.num_q_heads;
-    float *ws_acc = static_cast<float *>(workspace);
-    float *ws_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + wl.ml_offset);
+    float *ws_acc = reinterpret_cast<float *>(ws + wl.acc_offset);
+    float *ws_ml = reinterpret_cast<float *>(ws + wl.ml_offset);
 
     const uint64_t pool_rows = static_cast<uint64_t>(d.num_pages) * d.num_kv_heads * kPageSize;
     const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
@@ -386,6 +478,7 @@ int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan) {
     const int sms = device_sm_count();
     if (sms <= 0) return -1;
     const PlanDevice *pd = plan ? plan_device(plan) : nullptr;
+    if (use_stream(*dims, plan, false)) return 1;
     const SplitConfig c = split_config(*dims, plan);
     return 2 + ((pd && pd->num_tiles > 0) ? 1 : 0) + (c.tc.min_rows > 0 ? 1 : 0);
 }
@@ -530,8 +623,7 @@ int sa_paged_attn_noalloc(const sa_dims *dims, const uint16_t *q, const uint16_t
                           uint16_t *out, int32_t *err_flag, void *stream) {
     int rc = check_dims(dims);
     if (rc) return rc;
-    const WsLayout wl = attn_ws_layout(*dims, nullptr);
-    if (wl.total > kStaticScratchBytes) return SA_ERR_WORKSPACE;  // shapes exceed the fixed scratch
+    if (attn_ws_bytes(*dims, nullptr) > kStaticScratchBytes) return SA_ERR_WORKSPACE;  // shapes exceed the fixed scratch
     void *ws = nullptr;
     rc = static_scratch_address(&ws);
     if (rc) return rc;

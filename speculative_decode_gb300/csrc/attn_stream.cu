@@ -1,0 +1,981 @@
+// attn_stream.cu -- page-streamed attention with one persistent CTA per SM:
+// decode (q_len = 1) and short causal multi-query blocks (fewer than 16 query
+// rows per KV head), bf16 pages.
+//
+// What it computes: for each sequence b, new query token i and query head h,
+// softmax(scale * q . K_b^T) V_b over the keys at positions
+// 0 .. seq_len - q_len + i, with K_b/V_b gathered through the block table
+// (ExLlamaV2 "Dynamic Generator" page, "Continuous batching"; causal rows as
+// in the Hugging Face "Assisted Generation" page, "How Assisted Generation
+// works"). The softmax is evaluated online; partial (max, sum, accumulator)
+// states are merged exactly with max-shifted rescaling.
+//
+// Design (sm_103a):
+//  * Segment = (sequence, KV head, block of R <= 16 query rows): the G query
+//    heads of the KV head times the sequence's new tokens, so every K/V byte
+//    read serves all of them. The segments' 16-token sub-tiles, plus a small
+//    cost per segment start, form one sequence of work units that is cut into
+//    one equal contiguous range per CTA (one CTA per SM).
+//  * Warp 0 produces: it walks the CTA's range and streams the tokens of one
+//    KV head up to the next multiple of 64 per stage (so a stage lies in one
+//    page) into a ring of six 32 KiB stages with 2-D TMA copies (128-byte
+//    swizzle; at most three boxes of 64, 32 or 16 rows per half of K or V,
+//    all issued by one instruction, since every box costs the TMA unit tens
+//    of cycles to issue), and bulk-copies each piece's query rows. Six stages
+//    keep about 160 KiB per SM in flight.
+//  * Warps 4-7 consume: warp c takes tokens 16c .. 16c + 15 of every stage, a
+//    16-token sub-tile. Each sub-tile is two tensor-core contractions of
+//    one warp (mma.sync m16n8k16, bf16 in, fp32 accumulate): S = Q K^T with
+//    the segment's query rows as M (padded to 16), eight tokens per N and the
+//    head dimension as K, then O += P V with the probabilities as the A
+//    operand straight from the S accumulators. K and V fragments come from
+//    the swizzled stage with ldmatrix (transposed for V), free of bank
+//    conflicts. Each warp keeps its own online-softmax state (lazy rescaling:
+//    the reference maximum only moves when a tile beats it by 2^8).
+//  * Warp 1 merges: at the end of a piece each consumer warp writes its
+//    state over its own rows of the stage and hands the piece over through a
+//    four-deep ring; the merge warp combines the four states, writes bf16
+//    output (or an fp32 partial when the segment is cut between CTAs) and
+//    releases the stage, so the consumers never wait for global memory.
+//  * A CTA first streams the head of the segment it shares with the next CTA,
+//    then the tail of the one it shares with the previous CTA, then its whole
+//    segments, so that every CTA ends on segments it writes directly. Warp 2
+//    counts the partials: the last CTA to finish a piece of a cut segment (one
+//    atomic counter per cut, reset by that CTA) merges all of the segment's
+//    partials; no CTA waits for another, and neither the consumers nor the
+//    merge warp wait for these round trips to L2.
+//  * Every wait is bounded (common.cuh). On timeout a warp flags
+//    SA_ERR_TIMEOUT and leaves; the producer first waits (bounded) for its
+//    copies in flight.
+#include "common.cuh"
+
+namespace sa {
+
+namespace {
+
+constexpr int kStages = 6;                       // ring depth
+constexpr int kStageTok = 64;                    // tokens per stage
+constexpr int kSub = 16;                         // tokens per sub-tile (and per TMA box)
+constexpr int kConsumers = 4;                    // consumer warps (warps 4-7)
+constexpr int kWarpTok = kStageTok / kConsumers; // 16 tokens of a stage per consumer warp
+static_assert(kWarpTok == kSub, "one sub-tile per consumer warp and stage");
+constexpr int kThreads = 8 * 32;                 // warp 0 produces, 1 merges, 2 counts, 3 idle
+constexpr int kHalf = kStageTok * 128;           // 64 columns x 64 rows of bf16: 8 KiB
+constexpr int kStageBytes = 4 * kHalf;           // K (two halves), then V (two halves): 32 KiB
+constexpr int kBoxBytes = kSub * 128;            // one 16-row x 64-column box: 2 KiB
+constexpr int kUnitsPerSub = 4;                  // balancing units of a 16-token sub-tile
+constexpr int kSegCost = 12;                     // units of a segment start (about a stage: its
+                                                 // merge and its partly filled last stage)
+constexpr int kMinUnits = kUnitsPerSub * kStageTok / kSub;  // smallest range: one full stage
+constexpr int kPieceInts = 16;
+constexpr int kQRow = kHeadDim + 8;              // query row stride in shared memory (bf16):
+                                                 // 272 bytes, so that eight rows fall on
+                                                 // different banks
+constexpr int kMergeSlots = 4;
+constexpr int kMslotInts = 8;
+
+// stage descriptor flags
+constexpr int kFirst = 1;  // first stage of a piece
+constexpr int kLast = 2;   // last stage of a piece
+constexpr int kEnd = 4;    // no more stages
+constexpr int kSkip = 8;   // page id out of range: nothing was loaded
+
+struct Lay {
+    static constexpr int kQ = kStages * kStageBytes;                 // bf16 [2][16][kQRow]
+    static constexpr int kMl = kQ + 2 * 16 * kQRow * 2;              // float2 [kStages][warp][16]
+    static constexpr int kPiece = kMl + kStages * kConsumers * 16 * 8;  // int32 [2][16]
+    static constexpr int kDesc = kPiece + 2 * kPieceInts * 4;        // int32 [kStages][4]
+    static constexpr int kMslot = kDesc + kStages * 16;              // int32 [4][8]
+    static constexpr int kXslot = kMslot + kMergeSlots * kMslotInts * 4;  // int32 [4][8]
+    static constexpr int kBar = kXslot + kMergeSlots * kMslotInts * 4;
+    // full[3] empty[3] qfull[2] qempty[2] mfull[4] mempty[4] xfull[4] xempty[4]
+    static constexpr int kNumBars = 2 * kStages + 4 + 4 * kMergeSlots;
+    static constexpr int kBytes = kBar + kNumBars * 8;
+};
+
+// Shape of one sequence's work; tiles = 0 when it has none.
+struct Seq {
+    int T, n, tiles, nrb;
+};
+
+template <int R>
+__device__ __forceinline__ Seq seq_from(const StreamParams &P, int T, int n, bool flag) {
+    Seq s{T, n, 0, 0};
+    if (n <= 0) return s;
+    const int npages = (T + kPageSize - 1) / kPageSize;
+    if (n > T || n > P.max_q_len || npages > P.max_pages) {
+        if (flag) flag_error(P.err, kErrBitQlen);
+        return s;
+    }
+    s.tiles = (T + kSub - 1) / kSub;
+    s.nrb = (P.G * n + R - 1) / R;
+    return s;
+}
+
+template <int R>
+__device__ __forceinline__ Seq seq_at(const StreamParams &P, int b) {
+    if (b >= P.B) return Seq{0, 0, 0, 0};
+    return seq_from<R>(P, P.seq_lens[b], P.q_lens[b], false);
+}
+
+__device__ __forceinline__ int seg_units(const Seq &s) {
+    return s.tiles > 0 ? kSegCost + kUnitsPerSub * s.tiles : 0;
+}
+
+__device__ __forceinline__ int seq_units(const StreamParams &P, const Seq &s) {
+    return seg_units(s) * P.Hkv * s.nrb;
+}
+
+// The cut of the units [0, total) into one contiguous range per CTA: C or
+// C + 1 units each (the first `rem` get C + 1), or ranges of kMinUnits units
+// (one stage) when there is less work than that, the last CTAs then staying
+// idle, so that a piece is never so short that its merge costs more than its
+// stream. A range of at least kUnitsPerSub units inside a segment holds a
+// sub-tile start, so every CTA between a cut segment's first and last holds a
+// piece.
+struct Ranges {
+    int C, rem;
+    __device__ __forceinline__ int begin(int c) const { return c * C + min(c, rem); }
+    __device__ __forceinline__ int range_of(int u) const {
+        const int big = rem * (C + 1);
+        return u < big ? u / (C + 1) : rem + (u - big) / C;
+    }
+};
+
+__device__ __forceinline__ Ranges make_ranges(int total, int n) {
+    const int even = total / n;
+    if (even >= kMinUnits) return Ranges{even, total - even * n};
+    return Ranges{kMinUnits, 0};
+}
+
+__device__ __forceinline__ int ceil_units(int x) { return x <= 0 ? 0 : (x + kUnitsPerSub - 1) / kUnitsPerSub; }
+
+// Warp-wide pass over the lengths: total units and total query tokens. For
+// batches of up to 512 sequences it also pulls the first line of every
+// block-table row into L1, so that the windows read after the cut is known
+// do not wait for DRAM.
+template <int R>
+__device__ void scan_work(const StreamParams &P, int lane, int &total, int &q_total) {
+    total = 0;
+    q_total = 0;
+    if (P.B <= 512)
+        for (int b = lane; b < P.B; b += 32)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(P.block_table + static_cast<int64_t>(b) * P.max_pages));
+    int T = lane < P.B ? P.seq_lens[lane] : 0, n = lane < P.B ? P.q_lens[lane] : 0;
+#pragma unroll 1
+    for (int base = 0; base < P.B; base += 32) {
+        const int cT = T, cn = n;
+        if (base + 32 < P.B) {  // the next round's lengths are in flight while this one is reduced
+            const int b = base + 32 + lane;
+            T = b < P.B ? P.seq_lens[b] : 0;
+            n = b < P.B ? P.q_lens[b] : 0;
+        }
+        const Seq s = seq_from<R>(P, cT, cn, true);
+        total += static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(seq_units(P, s))));
+        q_total += static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(max(0, cn))));
+    }
+}
+
+// Where a unit falls: the sequence whose units hold it, that sequence's unit
+// and query-row offsets and its shape (b = B past the work).
+struct Loc {
+    int b, ws, qs;
+    Seq s;
+};
+
+// One pass over the lengths locating units g0 and g1 (g0 <= g1), the same on
+// every lane.
+template <int R>
+__device__ void locate2(const StreamParams &P, int lane, int g0, int g1, Loc &l0, Loc &l1) {
+    l0 = Loc{P.B, 0, 0, Seq{0, 0, 0, 0}};
+    l1 = l0;
+    bool f0 = false, f1 = false;
+    int w_base = 0, q_base = 0;
+#pragma unroll 1
+    for (int base = 0; base < P.B && !f1; base += 32) {
+        const int b = base + lane;
+        const Seq s = seq_at<R>(P, b);
+        const int w = seq_units(P, s), qn = b < P.B ? max(0, s.n) : 0;
+        int wi = w, qi = qn;  // inclusive prefix sums over the lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, wi, o), c = __shfl_up_sync(0xffffffffu, qi, o);
+            if (lane >= o) {
+                wi += a;
+                qi += c;
+            }
+        }
+        const int wx = w_base + wi - w, qx = q_base + qi - qn;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const int g = which ? g1 : g0;
+            const unsigned hit = __ballot_sync(0xffffffffu, w > 0 && wx <= g && g < wx + w);
+            if (hit && !(which ? f1 : f0)) {
+                const int src = __ffs(hit) - 1;
+                Loc l;
+                l.b = base + src;
+                l.ws = __shfl_sync(0xffffffffu, wx, src);
+                l.qs = __shfl_sync(0xffffffffu, qx, src);
+                l.s.T = __shfl_sync(0xffffffffu, s.T, src);
+                l.s.n = __shfl_sync(0xffffffffu, s.n, src);
+                l.s.tiles = __shfl_sync(0xffffffffu, s.tiles, src);
+                l.s.nrb = __shfl_sync(0xffffffffu, s.nrb, src);
+                if (which) {
+                    l1 = l;
+                    f1 = true;
+                } else {
+                    l0 = l;
+                    f0 = true;
+                }
+            }
+        }
+        w_base += __shfl_sync(0xffffffffu, wi, 31);
+        q_base += __shfl_sync(0xffffffffu, qi, 31);
+    }
+}
+
+// Bounded wait by a whole warp: true on every lane when the phase completed.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t n) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+// D += A B for one m16n8k16 tile: A 16x16 bf16 (four registers), B 16x8 bf16
+// (two registers), D 16x8 fp32.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte address of 16-byte chunk j of row r inside a swizzled 64-column half.
+__device__ __forceinline__ uint32_t sw_addr(uint32_t half, int r, int j) {
+    return half + r * 128 + (((j ^ r) & 7) << 4);
+}
+
+// Consumer warp c's state inside a stage: row r of O (512 bytes) over the
+// warp's own 16 rows of the four halves (2 KiB each), four O rows per half,
+// word w of row r stored at w ^ 4 (r % 8) (so that the eight rows a store
+// instruction touches fall on different banks); its (max, sum) pairs in the
+// stage's slot of the pair array.
+__device__ __forceinline__ float *state_row(uint8_t *stage, int c, int r) {
+    return reinterpret_cast<float *>(stage + (r >> 2) * kHalf + c * (kSub * 128) + (r & 3) * 512);
+}
+__device__ __forceinline__ float2 *state_ml(float2 *ml, int st, int c) {
+    return ml + (st * kConsumers + c) * 16;
+}
+
+template <int R>
+__device__ __forceinline__ int64_t part_row(int sl, int r) {
+    return static_cast<int64_t>(sl) * R + r;
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 1)
+    stream_attn_kernel(const StreamParams P, const __grid_constant__ StreamMaps maps) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint16_t *qbuf = reinterpret_cast<uint16_t *>(smem + Lay::kQ);
+    int32_t *ring = reinterpret_cast<int32_t *>(smem + Lay::kPiece);
+    float2 *mlbuf = reinterpret_cast<float2 *>(smem + Lay::kMl);
+    int32_t *desc = reinterpret_cast<int32_t *>(smem + Lay::kDesc);
+    int32_t *mslot = reinterpret_cast<int32_t *>(smem + Lay::kMslot);
+    int32_t *xslot = reinterpret_cast<int32_t *>(smem + Lay::kXslot);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::kBar);
+    uint64_t *empty = full + kStages;
+    uint64_t *qfull = empty + kStages;
+    uint64_t *qempty = qfull + 2;
+    uint64_t *mfull = qempty + 2;
+    uint64_t *mempty = mfull + kMergeSlots;
+    uint64_t *xfull = mempty + kMergeSlots;
+    uint64_t *xempty = xfull + kMergeSlots;
+    const int cta = blockIdx.x;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumers);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&qfull[s], 1);
+            mbar_init(&qempty[s], kConsumers);
+        }
+        for (int s = 0; s < kMergeSlots; ++s) {
+            mbar_init(&mfull[s], kConsumers);
+            mbar_init(&mempty[s], 1);
+            mbar_init(&xfull[s], 1);
+            mbar_init(&xempty[s], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ================================================================ producer
+        if (lane < 2 * kStreamBoxKinds)
+            prefetch_tensormap(lane < kStreamBoxKinds ? &maps.k[lane] : &maps.v[lane - kStreamBoxKinds]);
+        int total = 0, q_total = 0;
+        scan_work<R>(P, lane, total, q_total);
+        uint32_t k = 0;   // stages issued
+        uint32_t pc = 0;  // pieces issued
+        auto finish = [&]() {  // the end marker, after the last stage
+            const int s = k % kStages;
+            if (!warp_wait(&empty[s], ((k / kStages) & 1) ^ 1)) return false;
+            if (lane == 0) {
+                desc[s * 4 + 2] = kEnd;
+                mbar_arrive(&full[s]);
+            }
+            return true;
+        };
+        auto drain = [&]() {  // timeout: wait (bounded) for the copies still in flight
+            if (lane == 0) flag_error(P.err, kErrBitTimeout);
+            for (uint32_t c = k > kStages ? k - kStages : 0; c < k; ++c)
+                (void)mbar_wait(&full[c % kStages], (c / kStages) & 1);
+            for (uint32_t c = pc > 2 ? pc - 2 : 0; c < pc; ++c) (void)mbar_wait(&qfull[c % 2], (c / 2) & 1);
+        };
+        if (q_total > P.total_q) {  // q_lens disagree with dims.total_q: reject the whole call
+            if (lane == 0) flag_error(P.err, kErrBitQlen);
+            if (!finish()) drain();
+            return;
+        }
+        const Ranges rg = make_ranges(total, P.n_ctas);
+        const int gb = min(total, rg.begin(cta));
+        const int ge = min(total, rg.begin(cta + 1));
+        Loc L0{P.B, 0, 0, Seq{0, 0, 0, 0}}, L1 = L0;
+        if (gb < ge) locate2<R>(P, lane, gb, ge - 1, L0, L1);
+        const int iseg0 = L0.b < P.B ? (gb - L0.ws) / seg_units(L0.s) : 0;
+        const int iseg1 = L1.b < P.B ? (ge - 1 - L1.ws) / seg_units(L1.s) : 0;
+
+        // Block-table entries: two cached windows of 32 consecutive entries of
+        // one sequence (lane i holds entry 32w + i); entry A is the one in use.
+        int ab = -1, aw = 0, ap = -1, bb = -1, bw = 0, bp = -1;
+        auto load_win = [&](int b, int w) -> int {
+            const int jj = (w << 5) + lane;
+            return (b >= 0 && b < P.B && jj < P.max_pages)
+                       ? P.block_table[static_cast<int64_t>(b) * P.max_pages + jj] : -1;
+        };
+        auto pid_of = [&](int b, int jp) -> int {
+            const int w = jp >> 5;
+            if (b != ab || w != aw) {
+                const int tb = ab, tw = aw, tp = ap;
+                if (b == bb && w == bw) {
+                    ab = bb; aw = bw; ap = bp;
+                } else {
+                    ab = b; aw = w; ap = load_win(b, w);
+                }
+                bb = tb; bw = tw; bp = tp;
+            }
+            return __shfl_sync(0xffffffffu, ap, jp & 31);
+        };
+        auto prefetch = [&](int b, int w) {
+            if ((b == ab && w == aw) || (b == bb && w == bw)) return;
+            bb = b; bw = w; bp = load_win(b, w);
+        };
+        if (gb < ge) {  // the first windows this CTA needs, in flight before the dependency wait
+            const int u1 = L1.ws + iseg1 * seg_units(L1.s);
+            const int t1 = ceil_units(gb - u1 - kSegCost) * kSub;
+            ab = L1.b; aw = (t1 / kPageSize) >> 5; ap = load_win(ab, aw);
+            const int u0 = L0.ws + iseg0 * seg_units(L0.s);
+            const int t0 = ceil_units(gb - u0 - kSegCost) * kSub;
+            prefetch(L0.b, (t0 / kPageSize) >> 5);
+        }
+        const uint64_t policy = P.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+        // queries and pages may be written by the kernel before this one
+        grid_dependency_wait();
+
+        int last_b = -1;
+        // One piece: tokens [tok_lo, tok_hi) of segment (b, kvh, rb); its
+        // partial goes to `slot` and counts at counter f when pieces > 1.
+        auto issue_piece = [&](int b, int kvh, int rb, const Seq &s, int qs, int tok_lo, int tok_hi, int pieces,
+                               int slot, int f) -> bool {
+            if (b != last_b) {  // next sequence's first window, while this one streams
+                last_b = b;
+                prefetch(b + 1, 0);
+            }
+            const int nvr = min(R, P.G * s.n - rb * R);
+            // the piece's descriptor and query rows
+            const int qslot = pc & 1;
+            if (!warp_wait(&qempty[qslot], ((pc >> 1) & 1) ^ 1)) return false;
+            if (lane == 0) {
+                int32_t *d = ring + qslot * kPieceInts;
+                d[0] = b; d[1] = kvh; d[2] = rb; d[3] = s.T; d[4] = s.n; d[5] = qs; d[6] = nvr;
+                d[7] = pieces; d[8] = slot; d[9] = f;
+                mbar_arrive_expect_tx(&qfull[qslot], nvr * 256);
+            }
+            __syncwarp();
+            if (lane < nvr) {  // query row r = rb R + lane: token r / G, head kvh G + r % G
+                const int r = rb * R + lane;
+                const uint16_t *src = P.q + (static_cast<int64_t>(qs + r / P.G) * P.Hq + kvh * P.G + r % P.G) * kHeadDim;
+                bulk_load(qbuf + (qslot * 16 + lane) * kQRow, src, 256, &qfull[qslot]);
+            }
+            ++pc;
+            // the stages: tokens up to the next multiple of 64, so a stage lies in
+            // one page; its rows go in at most three boxes per half of K or V
+            // (64, 32 and 16 rows: the binary digits of its 16-row count)
+            for (int t = tok_lo; t < tok_hi;) {
+                const int e = min(tok_hi, (t / kStageTok + 1) * kStageTok);
+                const int st = k % kStages;
+                const int pid = pid_of(b, t / kPageSize);
+                if (!warp_wait(&empty[st], ((k / kStages) & 1) ^ 1)) return false;
+                const bool ok = static_cast<unsigned>(pid) < static_cast<unsigned>(P.num_pages);
+                const int n16 = (e - t + kSub - 1) / kSub;  // 16-row chunks per half
+                if (lane == 0) {
+                    desc[st * 4 + 0] = t;
+                    desc[st * 4 + 1] = e - t;
+                    desc[st * 4 + 2] = (t == tok_lo ? kFirst : 0) | (e == tok_hi ? kLast : 0) | (ok ? 0 : kSkip);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&full[st], n16 * 4 * kBoxBytes);
+                    } else {
+                        flag_error(P.err, kErrBitPageOOB);
+                        mbar_arrive(&full[st]);
+                    }
+                }
+                __syncwarp();
+                // lane: box (lane & 7) of half-tensor (lane >> 3): K low and high
+                // 64 columns, then V low and high, all in one instruction
+                int sel = -1, off = 0;
+                {
+                    int at = 0, idx = 0;
+#pragma unroll
+                    for (int m = kStreamBoxKinds - 1; m >= 0; --m) {
+                        if (n16 & (1 << m)) {
+                            if (idx == (lane & 7)) {
+                                sel = m;
+                                off = at;
+                            }
+                            at += 1 << m;
+                            ++idx;
+                        }
+                    }
+                }
+                if (ok && sel >= 0) {
+                    const int qh = lane >> 3;  // 0, 1: K halves; 2, 3: V halves
+                    const int row = (pid * P.Hkv + kvh) * kPageSize + (t % kPageSize) + off * kSub;
+                    tma_load_2d(smem + st * kStageBytes + qh * kHalf + off * kBoxBytes,
+                                qh < 2 ? &maps.k[sel] : &maps.v[sel], &full[st], 64 * (qh & 1), row, policy);
+                }
+                ++k;
+                t = e;
+            }
+            return true;
+        };
+        // One piece of the static range: the part of segment iseg of sequence
+        // b (units from ws, query rows from qs) inside [gb, ge).
+        auto emit = [&](int b, int iseg, const Seq &s, int ws, int qs) -> bool {
+            const int u0 = ws + iseg * seg_units(s);
+            const int t_lo = min(s.tiles, ceil_units(gb - u0 - kSegCost));
+            const int t_hi = min(s.tiles, ceil_units(ge - u0 - kSegCost));
+            if (t_lo >= t_hi) return true;
+            const int f = rg.range_of(u0 + kSegCost);
+            const int pieces = rg.range_of(u0 + kSegCost + kUnitsPerSub * (s.tiles - 1)) - f + 1;
+            const bool head = t_lo == 0 && t_hi < s.tiles;
+            return issue_piece(b, iseg / s.nrb, iseg % s.nrb, s, qs, t_lo * kSub, min(s.T, t_hi * kSub), pieces,
+                               2 * cta + (head ? 1 : 0), f);
+        };
+
+        bool ok = true;
+        if (gb < ge) {
+            // 1. the head of the segment shared with the next CTA
+            bool rotated = false;
+            if (L1.b < P.B && !(L1.b == L0.b && iseg1 == iseg0)) {
+                const int u1 = L1.ws + iseg1 * seg_units(L1.s);
+                const int t_lo = ceil_units(gb - u1 - kSegCost), t_hi = min(L1.s.tiles, ceil_units(ge - u1 - kSegCost));
+                if (t_lo == 0 && t_hi > 0 && t_hi < L1.s.tiles) {
+                    rotated = true;
+                    ok = emit(L1.b, iseg1, L1.s, L1.ws, L1.qs);
+                }
+            }
+            // 2. everything else, in order
+            int b = L0.b, iseg = iseg0, ws = L0.ws, qs = L0.qs;
+            Seq s = L0.s;
+#pragma unroll 1
+            while (ok && b < P.B) {
+                if (ws + iseg * seg_units(s) >= ge) break;
+                if (!(rotated && b == L1.b && iseg == iseg1)) ok = emit(b, iseg, s, ws, qs);
+                if (++iseg == P.Hkv * s.nrb) {
+                    iseg = 0;
+                    do {
+                        ws += seq_units(P, s);
+                        qs += max(0, s.n);
+                        if (++b >= P.B) break;
+                        s = seq_at<R>(P, b);
+                    } while (seq_units(P, s) == 0);
+                }
+            }
+        }
+        if (!ok || !finish()) drain();
+        return;
+    }
+
+    if (warp == 1) {
+        // ================================================================ merge warp
+        // outputs are written after the kernel before this one has completed
+        grid_dependency_wait();
+        uint32_t xp = 0;  // partials handed to the counting warp
+        auto hand_over = [&](int nvr, int qs, int kvh, int rb, int pieces, int f) -> bool {
+            const int xs = xp % kMergeSlots;
+            if (!warp_wait(&xempty[xs], ((xp / kMergeSlots) & 1) ^ 1)) return false;
+            if (lane == 0) {
+                int32_t *x = xslot + xs * kMslotInts;
+                x[0] = nvr; x[1] = qs; x[2] = kvh; x[3] = rb; x[4] = pieces; x[5] = f;
+            }
+            __syncwarp();  // the partial writes of every lane precede the hand-over
+            if (lane == 0) mbar_arrive(&xfull[xs]);
+            ++xp;
+            return true;
+        };
+#pragma unroll 1
+        for (uint32_t hp = 0;; ++hp) {
+            const int ms = hp % kMergeSlots;
+            if (!warp_wait(&mfull[ms], (hp / kMergeSlots) & 1)) {
+                if (lane == 0) flag_error(P.err, kErrBitTimeout);
+                return;
+            }
+            const int32_t *m = mslot + ms * kMslotInts;
+            const int st = m[0], nvr = m[1], qs = m[2], kvh = m[3], rb = m[4], pieces = m[5], slot = m[6], f = m[7];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mempty[ms]);
+            if (st < 0) {  // the consumers are done: so is the counting warp, after the partials before
+                if (!hand_over(-1, 0, 0, 0, 0, 0) && lane == 0) flag_error(P.err, kErrBitTimeout);
+                return;
+            }
+            uint8_t *stage = smem + st * kStageBytes;
+            const bool direct = pieces == 1;
+            // each lane owns head dims 4 lane .. 4 lane + 3 of every row; the
+            // rows' shared-memory loads are all independent
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                if (r < nvr) {
+                    float2 x[kConsumers];
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < kConsumers; ++c) {
+                        x[c] = state_ml(mlbuf, st, c)[r];
+                        if (x[c].y > 0.f) M = fmaxf(M, x[c].x);
+                    }
+                    float Ls = 0.f;
+                    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int c = 0; c < kConsumers; ++c) {
+                        const float wt = x[c].y > 0.f ? exp2f(x[c].x - M) : 0.f;
+                        Ls += x[c].y * wt;
+                        const float4 a = reinterpret_cast<const float4 *>(state_row(stage, c, r))[lane ^ (r & 7)];
+                        o.x += a.x * wt;
+                        o.y += a.y * wt;
+                        o.z += a.z * wt;
+                        o.w += a.w * wt;
+                    }
+                    const int rr = rb * R + r;
+                    const int64_t orow = static_cast<int64_t>(qs + rr / P.G) * P.Hq + kvh * P.G + rr % P.G;
+                    if (direct) {
+                        const float inv = Ls > 0.f ? __frcp_rn(Ls) : 0.f;
+                        reinterpret_cast<uint2 *>(P.out + orow * kHeadDim)[lane] =
+                            make_uint2(pack_bf16x2(o.x * inv, o.y * inv), pack_bf16x2(o.z * inv, o.w * inv));
+                    } else {
+                        reinterpret_cast<float4 *>(P.part_acc + part_row<R>(slot, r) * kHeadDim)[lane] = o;
+                        if (lane == 0) reinterpret_cast<float2 *>(P.part_ml)[part_row<R>(slot, r)] = make_float2(M, Ls);
+                    }
+                }
+            }
+            // the states are read: the stage may be refilled (the next writes
+            // to it are the TMA's)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive_n(&empty[st], kConsumers);
+            if (!direct && !hand_over(nvr, qs, kvh, rb, pieces, f)) {
+                if (lane == 0) flag_error(P.err, kErrBitTimeout);
+                return;
+            }
+        }
+    }
+
+    if (warp == 2) {
+        // ============================================================= counting warp
+        // Counts the partials of cut segments; the last piece of a segment to
+        // finish merges all of them. Its loads go to L2 under a full HBM
+        // stream, so they are issued together: every piece's (max, sum) pairs
+        // at once, then each piece's accumulator rows at once.
+        grid_dependency_wait();
+#pragma unroll 1
+        for (uint32_t xp = 0;; ++xp) {
+            const int xs = xp % kMergeSlots;
+            if (!warp_wait(&xfull[xs], (xp / kMergeSlots) & 1)) {
+                if (lane == 0) flag_error(P.err, kErrBitTimeout);
+                return;
+            }
+            const int32_t *x = xslot + xs * kMslotInts;
+            const int nvr = x[0], qs = x[1], kvh = x[2], rb = x[3], pieces = x[4], f = x[5];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xempty[xs]);
+            if (nvr < 0) return;
+            // The release orders the merge warp's partial writes (which this
+            // warp synchronised with) before the count; the acquire lets the
+            // merge below see the other CTAs' partials.
+            int old = 0;
+            if (lane == 0)
+                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(P.counters + f) : "memory");
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old != pieces - 1) continue;
+            // the head in its first CTA's second slot, the rest in their CTAs' first slots
+            auto piece_slot = [&](int kk) { return kk == 0 ? 2 * f + 1 : 2 * (f + kk); };
+            constexpr int RG = 4;  // rows merged together
+#pragma unroll 1
+            for (int r0 = 0; r0 < nvr; r0 += RG) {
+                float M[RG], Ls[RG];
+                float4 o[RG];
+#pragma unroll
+                for (int i = 0; i < RG; ++i) {
+                    M[i] = -INFINITY;
+                    Ls[i] = 0.f;
+                    o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                for (int k0 = 0; k0 < pieces; k0 += 32) {  // lane kk: piece k0 + kk
+                    const int kk = k0 + lane;
+#pragma unroll
+                    for (int i = 0; i < RG; ++i) {
+                        if (kk < pieces && r0 + i < nvr) {
+                            const float2 v = __ldcg(reinterpret_cast<const float2 *>(P.part_ml) + part_row<R>(piece_slot(kk), r0 + i));
+                            if (v.y > 0.f) M[i] = fmaxf(M[i], v.x);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < RG; ++i)
+#pragma unroll
+                    for (int sh = 16; sh >= 1; sh >>= 1) M[i] = fmaxf(M[i], __shfl_xor_sync(0xffffffffu, M[i], sh));
+                for (int k0 = 0; k0 < pieces; k0 += 32) {
+                    const int kk = k0 + lane;
+                    float wt[RG];
+#pragma unroll
+                    for (int i = 0; i < RG; ++i) {
+                        wt[i] = 0.f;
+                        float lw = 0.f;
+                        if (kk < pieces && r0 + i < nvr) {
+                            const float2 v = __ldcg(reinterpret_cast<const float2 *>(P.part_ml) + part_row<R>(piece_slot(kk), r0 + i));
+                            if (v.y > 0.f) {
+                                wt[i] = exp2f(v.x - M[i]);
+                                lw = v.y * wt[i];
+                            }
+                        }
+#pragma unroll
+                        for (int sh = 16; sh >= 1; sh >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, sh);
+                        Ls[i] += lw;
+                    }
+                    const int cnt = min(32, pieces - k0);
+                    constexpr int PJ = 4;  // pieces whose rows are loaded together
+                    for (int j0 = 0; j0 < cnt; j0 += PJ) {
+                        float4 a[PJ][RG];
+                        float w[PJ][RG];
+#pragma unroll
+                        for (int jj = 0; jj < PJ; ++jj)
+#pragma unroll
+                            for (int i = 0; i < RG; ++i) {
+                                const int j = min(j0 + jj, 31);
+                                w[jj][i] = j0 + jj < cnt ? __shfl_sync(0xffffffffu, wt[i], j) : 0.f;
+                                a[jj][i] = (r0 + i < nvr && w[jj][i] != 0.f)
+                                               ? __ldcg(reinterpret_cast<const float4 *>(
+                                                            P.part_acc + part_row<R>(piece_slot(k0 + j), r0 + i) * kHeadDim) + lane)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+#pragma unroll
+                        for (int jj = 0; jj < PJ; ++jj)
+#pragma unroll
+                            for (int i = 0; i < RG; ++i) {
+                                o[i].x += a[jj][i].x * w[jj][i];
+                                o[i].y += a[jj][i].y * w[jj][i];
+                                o[i].z += a[jj][i].z * w[jj][i];
+                                o[i].w += a[jj][i].w * w[jj][i];
+                            }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < RG; ++i) {
+                    if (r0 + i < nvr) {
+                        const int rr = rb * R + r0 + i;
+                        const int64_t orow = static_cast<int64_t>(qs + rr / P.G) * P.Hq + kvh * P.G + rr % P.G;
+                        const float inv = Ls[i] > 0.f ? __frcp_rn(Ls[i]) : 0.f;
+                        reinterpret_cast<uint2 *>(P.out + orow * kHeadDim)[lane] =
+                            make_uint2(pack_bf16x2(o[i].x * inv, o[i].y * inv), pack_bf16x2(o[i].z * inv, o[i].w * inv));
+                    }
+                }
+            }
+            if (lane == 0) P.counters[f] = 0;  // ready for the next call
+        }
+    }
+    if (warp < kConsumers) return;  // warp 3 has no role
+
+    // ==================================================================== consumers
+    const int cw = warp - 4;
+    const int g = lane >> 2, cq = lane & 3;  // mma fragment row group and column pair
+    // Lane address parts for ldmatrix: matrix index and row within it
+    const int lm = lane >> 3, lr = lane & 7;
+    const uint32_t smem_base = smem_u32(smem);
+
+    uint32_t qa[8][4];   // Q as the A operand, one 16-dim K-step per entry (rows g, g + 8)
+    float o[16][4];      // O accumulators: 16 eight-dim N tiles (rows g, g + 8)
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows g and g + 8
+    int lim0 = -1, lim1 = -1;
+    int pT = 0, pn = 0, prb = 0, pnvr = 0, pqs = 0, pkvh = 0, ppieces = 1, pslot = 0, pf = 0;
+    const float qscale = P.qscale;
+    uint32_t k = 0, pc = 0;
+#pragma unroll 1
+    while (true) {
+        const int st = k % kStages;
+        if (!warp_wait(&full[st], (k / kStages) & 1)) {
+            if (lane == 0) flag_error(P.err, kErrBitTimeout);
+            return;
+        }
+        uint8_t *stage = smem + st * kStageBytes;
+        const int t0 = desc[st * 4 + 0], ntok = desc[st * 4 + 1], flags = desc[st * 4 + 2];
+        if (flags & kEnd) {
+            // hand the end over to the merge warp
+            const int ms = pc % kMergeSlots;
+            if (!warp_wait(&mempty[ms], ((pc / kMergeSlots) & 1) ^ 1)) {
+                if (lane == 0) flag_error(P.err, kErrBitTimeout);
+                return;
+            }
+            if (cw == 0 && lane == 0) mslot[ms * kMslotInts] = -1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mfull[ms]);
+            return;
+        }
+        if (flags & kFirst) {
+            // a new piece: its descriptor, then its queries as A fragments
+            const int qslot = pc & 1;
+            const int32_t *d = ring + qslot * kPieceInts;
+            pkvh = d[1]; prb = d[2]; pT = d[3]; pn = d[4]; pqs = d[5]; pnvr = d[6];
+            ppieces = d[7]; pslot = d[8]; pf = d[9];
+            if (!warp_wait(&qfull[qslot], (pc >> 1) & 1)) {
+                if (lane == 0) flag_error(P.err, kErrBitTimeout);
+                return;
+            }
+            const uint32_t *qw = reinterpret_cast<const uint32_t *>(qbuf + qslot * 16 * kQRow);
+            constexpr int kQW = kQRow / 2;  // words per query row
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                // rows past nvr hold stale data; their scores are masked
+                qa[s][0] = qw[g * kQW + 8 * s + cq];
+                qa[s][2] = qw[g * kQW + 8 * s + 4 + cq];
+                if constexpr (R == 16) {
+                    qa[s][1] = qw[(g + 8) * kQW + 8 * s + cq];
+                    qa[s][3] = qw[(g + 8) * kQW + 8 * s + 4 + cq];
+                } else {
+                    qa[s][1] = 0u;
+                    qa[s][3] = 0u;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&qempty[qslot]);
+#pragma unroll
+            for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+            lim0 = g < pnvr ? pT - pn + (prb * R + g) / P.G : -1;  // last key of each row
+            lim1 = (R == 16 && g + 8 < pnvr) ? pT - pn + (prb * R + g + 8) / P.G : -1;
+        }
+        if (!(flags & kSkip)) {
+            const uint32_t kh0 = smem_base + st * kStageBytes, kh1 = kh0 + kHalf;
+            const uint32_t vh0 = kh0 + 2 * kHalf, vh1 = kh0 + 3 * kHalf;
+            do {  // this warp's sub-tile of the stage
+                const int tb = kSub * cw;              // its first stage row
+                const int nv = min(kSub, ntok - tb);   // its valid tokens
+                if (nv <= 0) break;
+                if (nv < kSub) {
+                    // rows past the valid tokens hold whatever the page held: zero
+                    // their V so that 0 x (stale) cannot be NaN
+                    for (int i = lane; i < (kSub - nv) * 16; i += 32) {
+                        const int rr = tb + nv + i / 16, ch = i % 16;
+                        *reinterpret_cast<uint4 *>(stage + 2 * kHalf + (ch >> 3) * kHalf + rr * 128 + (ch & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    __syncwarp();
+                }
+                // ---- S = Q K^T over the sub-tile's 16 tokens (two N tiles of 8),
+                // even and odd K-steps in two chains of accumulators (half the
+                // dependent latency), added at the end
+                float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float sodd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t half = s < 4 ? kh0 : kh1;
+                    const int row = tb + 8 * (lm >> 1) + lr;
+                    uint32_t b00, b01, b10, b11;
+                    ldsm_x4(sw_addr(half, row, 2 * (s & 3) + (lm & 1)), b00, b01, b10, b11);
+                    mma_bf16((s & 1) ? sodd[0] : sacc[0], qa[s], b00, b01);
+                    mma_bf16((s & 1) ? sodd[1] : sacc[1], qa[s], b10, b11);
+                }
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[n][e] += sodd[n][e];
+                // ---- online softmax on rows g (and g + 8), log2 units
+                const int kabs = t0 + tb + 2 * cq;  // key of sacc[n][0] is kabs + 8 n
+                float x[2][4];
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int kl = 8 * n + 2 * cq + (e & 1);  // key within the sub-tile
+                        const int lim = e < 2 ? lim0 : lim1;
+                        x[n][e] = (kl < nv && kabs + 8 * n + (e & 1) <= lim) ? sacc[n][e] * qscale : -INFINITY;
+                    }
+                float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                float mx1 = -INFINITY;
+                if constexpr (R == 16) {
+                    mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                }
+                // the reference max only moves when the tile max beats it by 2^8
+                const bool grow0 = mx0 > m0 + 8.f, grow1 = mx1 > m1 + 8.f;
+                if (__any_sync(0xffffffffu, grow0 || grow1)) {
+                    const float a0 = grow0 ? exp2f(m0 - mx0) : 1.f;  // 0 when m was -inf
+                    const float a1 = grow1 ? exp2f(m1 - mx1) : 1.f;
+                    if (grow0) m0 = mx0;
+                    if (grow1) m1 = mx1;
+                    l0 *= a0;
+                    l1 *= a1;
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        o[n][0] *= a0;
+                        o[n][1] *= a0;
+                        o[n][2] *= a1;
+                        o[n][3] *= a1;
+                    }
+                }
+                const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+                float p[2][4];
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    p[n][0] = exp2f(x[n][0] - mu0);
+                    p[n][1] = exp2f(x[n][1] - mu0);
+                    l0 += p[n][0] + p[n][1];
+                    if constexpr (R == 16) {
+                        p[n][2] = exp2f(x[n][2] - mu1);
+                        p[n][3] = exp2f(x[n][3] - mu1);
+                        l1 += p[n][2] + p[n][3];
+                    } else {
+                        p[n][2] = p[n][3] = 0.f;
+                    }
+                }
+                // P as the A operand (16 rows x 16 keys) of O += P V
+                const uint32_t pa[4] = {pack_bf16x2(p[0][0], p[0][1]), pack_bf16x2(p[0][2], p[0][3]),
+                                        pack_bf16x2(p[1][0], p[1][1]), pack_bf16x2(p[1][2], p[1][3])};
+#pragma unroll
+                for (int n = 0; n < 16; n += 2) {
+                    const uint32_t half = n < 8 ? vh0 : vh1;
+                    const int row = tb + 8 * (lm & 1) + lr;
+                    uint32_t v00, v01, v10, v11;
+                    ldsm_x4_t(sw_addr(half, row, (n & 7) + (lm >> 1)), v00, v01, v10, v11);
+                    mma_bf16(o[n], pa, v00, v01);
+                    mma_bf16(o[n + 1], pa, v10, v11);
+                }
+            } while (false);
+        }
+        if (flags & kLast) {
+            // ---- end of the piece: hand the state to the merge warp
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+            const int ms = pc % kMergeSlots;
+            if (!warp_wait(&mempty[ms], ((pc / kMergeSlots) & 1) ^ 1)) {
+                if (lane == 0) flag_error(P.err, kErrBitTimeout);
+                return;
+            }
+            __syncwarp();  // every lane of this warp is done reading its rows of the stage
+            if (g < pnvr) {
+                float *dst = state_row(stage, cw, g);
+#pragma unroll
+                for (int n = 0; n < 16; ++n)
+                    *reinterpret_cast<float2 *>(dst + ((8 * n + 2 * cq) ^ (4 * g))) = make_float2(o[n][0], o[n][1]);
+                if (cq == 0) state_ml(mlbuf, st, cw)[g] = make_float2(m0, l0);
+            }
+            if (R == 16 && g + 8 < pnvr) {
+                float *dst = state_row(stage, cw, g + 8);
+#pragma unroll
+                for (int n = 0; n < 16; ++n)
+                    *reinterpret_cast<float2 *>(dst + ((8 * n + 2 * cq) ^ (4 * g))) = make_float2(o[n][2], o[n][3]);
+                if (cq == 0) state_ml(mlbuf, st, cw)[g + 8] = make_float2(m1, l1);
+            }
+            // the state was written by this (generic) proxy; the next writes to
+            // the stage, after the merge warp releases it, are the TMA's
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (cw == 0 && lane == 0) {
+                int32_t *m = mslot + ms * kMslotInts;
+                m[0] = st; m[1] = pnvr; m[2] = pqs; m[3] = pkvh; m[4] = prb; m[5] = ppieces; m[6] = pslot; m[7] = pf;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mfull[ms]);
+            ++pc;
+        } else {
+            // the zeroed V rows were written by this (generic) proxy; the next
+            // writes to the stage are the TMA's
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        ++k;
+    }
+}
+
+constexpr size_t smem_bytes() { return Lay::kBytes + 1024; }
+
+template <int R>
+cudaError_t launch_r(const StreamParams &p, const StreamMaps &maps, cudaStream_t stream) {
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        stream_attn_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes()));
+    if (attr != cudaSuccess) return attr;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.n_ctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes();
+    cfg.stream = stream;
+    // a programmatic dependent of the kernel before it: the work scan and the
+    // first block-table reads overlap that kernel's end (sa_kv_append allows
+    // it); queries and pages are read, and outputs written, after the
+    // dependency wait
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, stream_attn_kernel<R>, p, maps);
+}
+
+}  // namespace
+
+int stream_units_per_tile() { return kUnitsPerSub; }
+int stream_segment_cost() { return kSegCost; }
+int stream_tile_tokens() { return kSub; }
+
+cudaError_t launch_stream_attn(const StreamParams &p, const StreamMaps &maps, cudaStream_t stream) {
+    switch (p.R) {
+        case 4: return launch_r<4>(p, maps, stream);
+        case 8: return launch_r<8>(p, maps, stream);
+        case 16: return launch_r<16>(p, maps, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace sa

@@ -72,6 +72,43 @@ struct SplitParams {
                                 // written ran first, so pages are read without waiting for it
 };
 
+// Parameters of the persistent page-streaming kernel (attn_stream.cu): bf16
+// pages, no plan, fewer than 16 query rows per KV head.
+constexpr int kStreamMaxCtas = 256;   // grid cap (one CTA per SM); workspace is sized for it
+// partial slots: two per CTA (the pieces it shares with its neighbours)
+constexpr int kStreamSlots = 2 * kStreamMaxCtas;
+struct StreamParams {
+    const uint16_t *q;
+    const uint16_t *k_pages;    // [num_pages, Hkv, 256, 128]
+    const uint16_t *v_pages;
+    uint16_t *out;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    const int32_t *q_lens;
+    float *part_acc;            // [kStreamSlots][R][128] fp32 partials of cut segments
+    float *part_ml;             // [kStreamSlots][R][2] (max in log2 units, sum)
+    int32_t *counters;          // [kStreamMaxCtas] pieces finished per cut segment, zero
+                                // between calls
+    int32_t *err;
+    int32_t B, Hq, Hkv, G, num_pages, max_pages, total_q, max_q_len;
+    int32_t R;                  // rows per segment (4, 8 or 16)
+    float qscale;               // scale * log2(e)
+    int32_t n_ctas;             // grid: one CTA per SM, at most kStreamMaxCtas
+    int32_t evict_first;
+};
+// Tensor maps of the K and V pools, each viewed as [num_pages * Hkv * 256
+// rows][128] bf16 with 128-byte swizzle: box kind i is 64 columns x (16 << i)
+// rows.
+constexpr int kStreamBoxKinds = 3;
+struct StreamMaps {
+    CUtensorMap k[kStreamBoxKinds];
+    CUtensorMap v[kStreamBoxKinds];
+};
+cudaError_t launch_stream_attn(const StreamParams &p, const StreamMaps &maps, cudaStream_t stream);
+int stream_units_per_tile();
+int stream_segment_cost();
+int stream_tile_tokens();
+
 // Split kernel over p.split_ctas one-warp CTAs, then the combine pass that
 // merges the partials of segments cut into pieces (two kernels).
 cudaError_t launch_split_attn(const SplitParams &p, cudaStream_t stream);
