@@ -27,8 +27,9 @@
 //    16-token sub-tile. Each sub-tile is two tensor-core contractions of
 //    one warp (mma.sync m16n8k16, bf16 in, fp32 accumulate): S = Q K^T with
 //    the segment's query rows as M (padded to 16), eight tokens per N and the
-//    head dimension as K, then O += P V with the probabilities as the A
-//    operand straight from the S accumulators. K and V fragments come from
+//    head dimension as K, then O^T += V^T P^T with the head dimension as M, so
+//    that the probabilities are the B operand straight from the S accumulators
+//    and the R <= 8 query rows fill N = 8 without padding. K and V fragments come from
 //    the swizzled stage with ldmatrix (transposed for V), free of bank
 //    conflicts. Each warp keeps its own online-softmax state (lazy rescaling:
 //    the reference maximum only moves when a tile beats it by 2^8).
@@ -71,6 +72,7 @@ constexpr int kPieceInts = 16;
 constexpr int kQRow = kHeadDim + 8;              // query row stride in shared memory (bf16):
                                                  // 272 bytes, so that eight rows fall on
                                                  // different banks
+constexpr int kQSlots = 4;                       // pieces whose queries are loaded ahead
 constexpr int kMergeSlots = 4;
 constexpr int kMslotInts = 8;
 
@@ -81,15 +83,15 @@ constexpr int kEnd = 4;    // no more stages
 constexpr int kSkip = 8;   // page id out of range: nothing was loaded
 
 struct Lay {
-    static constexpr int kQ = kStages * kStageBytes;                 // bf16 [2][16][kQRow]
-    static constexpr int kMl = kQ + 2 * 16 * kQRow * 2;              // float2 [kStages][warp][16]
-    static constexpr int kPiece = kMl + kStages * kConsumers * 16 * 8;  // int32 [2][16]
-    static constexpr int kDesc = kPiece + 2 * kPieceInts * 4;        // int32 [kStages][4]
+    static constexpr int kQ = kStages * kStageBytes;                 // bf16 [kQSlots][16][kQRow]
+    static constexpr int kMl = kQ + kQSlots * 16 * kQRow * 2;        // float2 [kStages][warp][16]
+    static constexpr int kPiece = kMl + kStages * kConsumers * 16 * 8;  // int32 [kQSlots][16]
+    static constexpr int kDesc = kPiece + kQSlots * kPieceInts * 4;  // int32 [kStages][4]
     static constexpr int kMslot = kDesc + kStages * 16;              // int32 [4][8]
     static constexpr int kXslot = kMslot + kMergeSlots * kMslotInts * 4;  // int32 [4][8]
     static constexpr int kBar = kXslot + kMergeSlots * kMslotInts * 4;
-    // full[3] empty[3] qfull[2] qempty[2] mfull[4] mempty[4] xfull[4] xempty[4]
-    static constexpr int kNumBars = 2 * kStages + 4 + 4 * kMergeSlots;
+    // full, empty [kStages]; qfull, qempty [kQSlots]; mfull, mempty, xfull, xempty [kMergeSlots]
+    static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 4 * kMergeSlots;
     static constexpr int kBytes = kBar + kNumBars * 8;
 };
 
@@ -302,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::kBar);
     uint64_t *empty = full + kStages;
     uint64_t *qfull = empty + kStages;
-    uint64_t *qempty = qfull + 2;
-    uint64_t *mfull = qempty + 2;
+    uint64_t *qempty = qfull + kQSlots;
+    uint64_t *mfull = qempty + kQSlots;
     uint64_t *mempty = mfull + kMergeSlots;
     uint64_t *xfull = mempty + kMergeSlots;
     uint64_t *xempty = xfull + kMergeSlots;
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumers);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kQSlots; ++s) {
             mbar_init(&qfull[s], 1);
             mbar_init(&qempty[s], kConsumers);
         }
@@ -349,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) flag_error(P.err, kErrBitTimeout);
             for (uint32_t c = k > kStages ? k - kStages : 0; c < k; ++c)
                 (void)mbar_wait(&full[c % kStages], (c / kStages) & 1);
-            for (uint32_t c = pc > 2 ? pc - 2 : 0; c < pc; ++c) (void)mbar_wait(&qfull[c % 2], (c / 2) & 1);
+            for (uint32_t c = pc > kQSlots ? pc - kQSlots : 0; c < pc; ++c)
+                (void)mbar_wait(&qfull[c % kQSlots], (c / kQSlots) & 1);
         };
         if (q_total > P.total_q) {  // q_lens disagree with dims.total_q: reject the whole call
             if (lane == 0) flag_error(P.err, kErrBitQlen);
@@ -412,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int nvr = min(R, P.G * s.n - rb * R);
             // the piece's descriptor and query rows
-            const int qslot = pc & 1;
-            if (!warp_wait(&qempty[qslot], ((pc >> 1) & 1) ^ 1)) return false;
+            const int qslot = pc % kQSlots;
+            if (!warp_wait(&qempty[qslot], ((pc / kQSlots) & 1) ^ 1)) return false;
             if (lane == 0) {
                 int32_t *d = ring + qslot * kPieceInts;
                 d[0] = b; d[1] = kvh; d[2] = rb; d[3] = s.T; d[4] = s.n; d[5] = qs; d[6] = nvr;
@@ -729,8 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lm = lane >> 3, lr = lane & 7;
     const uint32_t smem_base = smem_u32(smem);
 
+    constexpr int NR = R == 16 ? 2 : 1;  // eight-row tiles of the query rows
     uint32_t qa[8][4];   // Q as the A operand, one 16-dim K-step per entry (rows g, g + 8)
-    float o[16][4];      // O accumulators: 16 eight-dim N tiles (rows g, g + 8)
+    // O transposed: ot[m][nr] is the 16-dim x 8-row tile (dims 16 m .., rows
+    // 8 nr ..); lane (g, cq) holds dims 16 m + g (+ 8) of rows 8 nr + 2 cq (+ 1)
+    float ot[8][NR][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows g and g + 8
     int lim0 = -1, lim1 = -1;
     int pT = 0, pn = 0, prb = 0, pnvr = 0, pqs = 0, pkvh = 0, ppieces = 1, pslot = 0, pf = 0;
@@ -759,11 +765,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (flags & kFirst) {
             // a new piece: its descriptor, then its queries as A fragments
-            const int qslot = pc & 1;
+            const int qslot = pc % kQSlots;
             const int32_t *d = ring + qslot * kPieceInts;
             pkvh = d[1]; prb = d[2]; pT = d[3]; pn = d[4]; pqs = d[5]; pnvr = d[6];
             ppieces = d[7]; pslot = d[8]; pf = d[9];
-            if (!warp_wait(&qfull[qslot], (pc >> 1) & 1)) {
+            if (!warp_wait(&qfull[qslot], (pc / kQSlots) & 1)) {
                 if (lane == 0) flag_error(P.err, kErrBitTimeout);
                 return;
             }
@@ -785,7 +791,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&qempty[qslot]);
 #pragma unroll
-            for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+            for (int m = 0; m < 8; ++m)
+#pragma unroll
+                for (int nr = 0; nr < NR; ++nr) ot[m][nr][0] = ot[m][nr][1] = ot[m][nr][2] = ot[m][nr][3] = 0.f;
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
             lim0 = g < pnvr ? pT - pn + (prb * R + g) / P.G : -1;  // last key of each row
@@ -855,12 +863,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (grow1) m1 = mx1;
                     l0 *= a0;
                     l1 *= a1;
+                    // this lane's O rows are 2 cq and 2 cq + 1 (of each row tile),
+                    // whose factors the lanes of row groups 2 cq and 2 cq + 1 hold
+                    const float r0a = __shfl_sync(0xffffffffu, a0, 8 * cq), r1a = __shfl_sync(0xffffffffu, a0, 8 * cq + 4);
+                    const float r0b = __shfl_sync(0xffffffffu, a1, 8 * cq), r1b = __shfl_sync(0xffffffffu, a1, 8 * cq + 4);
 #pragma unroll
-                    for (int n = 0; n < 16; ++n) {
-                        o[n][0] *= a0;
-                        o[n][1] *= a0;
-                        o[n][2] *= a1;
-                        o[n][3] *= a1;
+                    for (int m = 0; m < 8; ++m) {
+                        ot[m][0][0] *= r0a;
+                        ot[m][0][1] *= r1a;
+                        ot[m][0][2] *= r0a;
+                        ot[m][0][3] *= r1a;
+                        if constexpr (NR == 2) {
+                            ot[m][1][0] *= r0b;
+                            ot[m][1][1] *= r1b;
+                            ot[m][1][2] *= r0b;
+                            ot[m][1][3] *= r1b;
+                        }
                     }
                 }
                 const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
@@ -878,17 +896,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p[n][2] = p[n][3] = 0.f;
                     }
                 }
-                // P as the A operand (16 rows x 16 keys) of O += P V
-                const uint32_t pa[4] = {pack_bf16x2(p[0][0], p[0][1]), pack_bf16x2(p[0][2], p[0][3]),
-                                        pack_bf16x2(p[1][0], p[1][1]), pack_bf16x2(p[1][2], p[1][3])};
+                // O^T += V^T P^T: P (bf16) is the B operand (16 keys x 8 rows)
+                // straight from the S accumulators; V^T the A operand (16 dims x
+                // 16 keys) by transposing loads
+                uint32_t pb[NR][2];
+                pb[0][0] = pack_bf16x2(p[0][0], p[0][1]);
+                pb[0][1] = pack_bf16x2(p[1][0], p[1][1]);
+                if constexpr (NR == 2) {
+                    pb[1][0] = pack_bf16x2(p[0][2], p[0][3]);
+                    pb[1][1] = pack_bf16x2(p[1][2], p[1][3]);
+                }
 #pragma unroll
-                for (int n = 0; n < 16; n += 2) {
-                    const uint32_t half = n < 8 ? vh0 : vh1;
-                    const int row = tb + 8 * (lm & 1) + lr;
-                    uint32_t v00, v01, v10, v11;
-                    ldsm_x4_t(sw_addr(half, row, (n & 7) + (lm >> 1)), v00, v01, v10, v11);
-                    mma_bf16(o[n], pa, v00, v01);
-                    mma_bf16(o[n + 1], pa, v10, v11);
+                for (int m = 0; m < 8; ++m) {
+                    const uint32_t half = m < 4 ? vh0 : vh1;
+                    const int row = tb + 8 * (lm >> 1) + lr;
+                    uint32_t va[4];
+                    ldsm_x4_t(sw_addr(half, row, 2 * (m & 3) + (lm & 1)), va[0], va[1], va[2], va[3]);
+#pragma unroll
+                    for (int nr = 0; nr < NR; ++nr) mma_bf16(ot[m][nr], va, pb[nr][0], pb[nr][1]);
                 }
             } while (false);
         }
@@ -904,20 +929,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return;
             }
             __syncwarp();  // every lane of this warp is done reading its rows of the stage
-            if (g < pnvr) {
-                float *dst = state_row(stage, cw, g);
 #pragma unroll
-                for (int n = 0; n < 16; ++n)
-                    *reinterpret_cast<float2 *>(dst + ((8 * n + 2 * cq) ^ (4 * g))) = make_float2(o[n][0], o[n][1]);
-                if (cq == 0) state_ml(mlbuf, st, cw)[g] = make_float2(m0, l0);
-            }
-            if (R == 16 && g + 8 < pnvr) {
-                float *dst = state_row(stage, cw, g + 8);
+            for (int nr = 0; nr < NR; ++nr)
 #pragma unroll
-                for (int n = 0; n < 16; ++n)
-                    *reinterpret_cast<float2 *>(dst + ((8 * n + 2 * cq) ^ (4 * g))) = make_float2(o[n][2], o[n][3]);
-                if (cq == 0) state_ml(mlbuf, st, cw)[g + 8] = make_float2(m1, l1);
-            }
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int row = 8 * nr + 2 * cq + e2;
+                    if (row < pnvr) {
+                        float *dst = state_row(stage, cw, row);
+#pragma unroll
+                        for (int m = 0; m < 8; ++m) {
+                            dst[(16 * m + g) ^ (4 * (row & 7))] = ot[m][nr][e2];
+                            dst[(16 * m + g + 8) ^ (4 * (row & 7))] = ot[m][nr][2 + e2];
+                        }
+                    }
+                }
+            if (g < pnvr && cq == 0) state_ml(mlbuf, st, cw)[g] = make_float2(m0, l0);
+            if (R == 16 && g + 8 < pnvr && cq == 0) state_ml(mlbuf, st, cw)[g + 8] = make_float2(m1, l1);
             // the state was written by this (generic) proxy; the next writes to
             // the stage, after the merge warp releases it, are the TMA's
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -929,9 +956,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&mfull[ms]);
             ++pc;
         } else {
-            // the zeroed V rows were written by this (generic) proxy; the next
+            // zeroed V rows were written by this (generic) proxy; the next
             // writes to the stage are the TMA's
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (ntok < kSub * (cw + 1)) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
