@@ -61,6 +61,8 @@ def _load():
         lib.oracle_argmax.restype = I64
         lib.oracle_verify_greedy.argtypes = [P, P, P, I, I, I64, P, P, P]
         lib.oracle_verify_greedy.restype = I
+        lib.oracle_spec_advance.argtypes = [I, I, P, P, P, P, P, P]
+        lib.oracle_spec_advance.restype = I
         lib.oracle_quantize_q8.argtypes = [P, I64, I, P, P]
         lib.oracle_quantize_q8.restype = I
         lib.oracle_kv_append_q8.argtypes = [I] * 6 + [P] * 9
@@ -167,6 +169,20 @@ def verify_greedy(logits, candidates, n_cand, window=None):
                                       _ptr(nxt), _ptr(win))
     _check(rc, "verify_greedy")
     return acc, nxt, win
+
+
+def spec_advance(k_max, n_cand, accepted, window, seq_lens, q_lens):
+    """Shapes of the next verify call after a greedy accept (the assisted
+    generation loop returning to its drafting step): returns (seq_lens,
+    q_lens, n_cand) of that call, from this call's n_cand, accepted counts,
+    windows after the adjustment, seq_lens and q_lens."""
+    nc, acc, win = _c(n_cand, np.int32), _c(accepted, np.int32), _c(window, np.int32)
+    sl, ql = _c(seq_lens, np.int32).copy(), _c(q_lens, np.int32).copy()
+    out = np.zeros_like(nc)
+    rc = _load().oracle_spec_advance(len(nc), int(k_max), _ptr(nc), _ptr(acc), _ptr(win), _ptr(sl), _ptr(ql),
+                                     _ptr(out))
+    _check(rc, "spec_advance")
+    return sl, ql, out
 
 
 def defrag_plan(block_table, seq_lens, num_pages, page_size=256):

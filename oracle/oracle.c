@@ -42,6 +42,17 @@
  *    window grows; NaN never wins an argmax and an all-NaN row gives 0;
  *    -0.0 and +0.0 compare equal (a tie).
  *
+ *  - the next step of the loop: the same page's loop returns to step 1
+ *    after step 5, the assistant drafting as many tokens as the adjusted
+ *    window says. Reading of the cache (the page speaks of tokens, not of a
+ *    cache): the verify call's new tokens are [the last token of the previous
+ *    step, candidate 0 .. candidate n-1], so after step 4 the sequence holds
+ *    the tokens before the call, that first token and the accepted
+ *    candidates (seq_len - q_len + accepted + 1 tokens); the correction
+ *    token opens the next call, followed by min(window, k_max) candidates
+ *    (k_max being the most the caller's buffers take), so the next call has
+ *    q_len = that count + 1 and seq_len = the kept tokens + q_len.
+ *
  *  - int8 pages: the ExLlamaV2 "Dynamic Generator" page, in its setup of the
  *    model and cache, names quantised cache modes (Q4 now, Q8 planned) but
  *    defines no format. Reading: every (page, KV head, token) row of 128 values
@@ -489,6 +500,26 @@ int oracle_verify_greedy(const float *logits, const int32_t *candidates, const i
         next_tok[b] = (int32_t)oracle_argmax(rows + (int64_t)a * V, V);
         /* step 5: +2 when everything matched, -1 otherwise (never below 1) */
         if (window) window[b] = (a == n) ? window[b] + 2 : (window[b] - 1 > 1 ? window[b] - 1 : 1);
+    }
+    return ORACLE_OK;
+}
+
+/* The shapes of the next verify call (see the header): window holds the
+ * windows after step 5. A sequence whose q_lens < n_cand + 1 or whose
+ * seq_lens < q_lens has no consistent cache: ORACLE_ERR_ARG. */
+int oracle_spec_advance(int B, int k_max, const int32_t *n_cand, const int32_t *accepted,
+                        const int32_t *window, int32_t *seq_lens, int32_t *q_lens, int32_t *n_cand_next) {
+    if (B < 0 || k_max < 0) return ORACLE_ERR_ARG;
+    for (int b = 0; b < B; ++b) {
+        if (q_lens[b] < n_cand[b] + 1 || seq_lens[b] < q_lens[b] || accepted[b] < 0 || accepted[b] > n_cand[b])
+            return ORACLE_ERR_ARG;
+        /* kept: everything before the call, its first token, the accepted candidates */
+        const int32_t kept = seq_lens[b] - q_lens[b] + 1 + accepted[b];
+        /* step 1 again: as many candidates as the window says, at most k_max */
+        const int32_t n = window[b] < k_max ? window[b] : k_max;
+        n_cand_next[b] = n;
+        q_lens[b] = n + 1;  /* the correction token, then the candidates */
+        seq_lens[b] = kept + n + 1;
     }
     return ORACLE_OK;
 }

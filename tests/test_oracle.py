@@ -578,3 +578,46 @@ def test_kv_append_q4_quantises_the_rows_kv_append_writes():
     for got, pages in (((kc2, ks2), kp), ((vc2, vs2), vp)):
         c, s = oracle.quantize_q4(pages)
         assert np.array_equal(got[0], c) and np.array_equal(got[1], s)
+
+
+ADVANCE = os.path.join(os.path.dirname(__file__), "golden", "advance_cases.json")
+
+
+def test_golden_advance_cases():
+    """The next call's shapes after a greedy accept, hand-worked from the
+    Assisted Generation loop (step 5, then step 1 again)."""
+    for case in json.load(open(ADVANCE))["cases"]:
+        sl, ql, nc = oracle.spec_advance(case["k_max"], [case["n_cand"]], [case["accepted"]],
+                                         [case["window_after"]], [case["seq_len"]], [case["q_len"]])
+        want = case["expect"]
+        assert (int(sl[0]), int(ql[0]), int(nc[0])) == (want["seq_len"], want["q_len"], want["n_cand"]), case["note"]
+
+
+def test_advance_rejects_inconsistent_lengths():
+    for n_cand, acc, sl, ql in ((3, 1, 10, 3), (2, 3, 10, 3), (1, 0, 2, 3), (1, -1, 10, 2)):
+        with pytest.raises(Exception):
+            oracle.spec_advance(4, [n_cand], [acc], [2], [sl], [ql])
+
+
+def test_advance_chain_keeps_every_accepted_token():
+    """Invariant over a chain of steps: the kept length grows by accepted + 1
+    each step, the next call carries min(window, k_max) candidates, and the
+    window follows the golden window sequence when the outcomes do."""
+    seq = json.load(open(GOLDEN))["window_sequence"]
+    k_max, L = 6, 777
+    w = np.array([seq["start"]], np.int32)
+    n = np.array([min(seq["start"], k_max)], np.int32)
+    sl, ql = np.array([L + n[0] + 1], np.int32), n + 1
+    V = 16
+    for outcome, want_w in zip(seq["outcomes"], seq["windows"]):
+        rows = np.zeros((1, k_max + 1, V), np.float32)
+        rows[0, :, 5] = 1.0                                   # the verifier says 5 everywhere
+        cand = np.full((1, k_max), 5, np.int32)
+        if outcome == "miss":
+            cand[0, n[0] - 1] = 6                             # the last candidate misses
+        acc, _, w = oracle.verify_greedy(rows, cand, n, w)
+        assert int(w[0]) == want_w
+        assert int(acc[0]) == (n[0] if outcome == "all" else n[0] - 1)
+        kept = int(sl[0]) - int(ql[0]) + 1 + int(acc[0])
+        sl, ql, n = oracle.spec_advance(k_max, n, acc, w, sl, ql)
+        assert int(n[0]) == min(want_w, k_max) and int(ql[0]) == n[0] + 1 and int(sl[0]) == kept + ql[0]
