@@ -304,6 +304,38 @@ SA_API int sa_spec_verify_greedy(const float *logits, const int32_t *candidates,
                           size_t workspace_bytes, int32_t *err_flag, void *stream);
 
 /*
+ * sa_spec_verify_greedy_advance -- sa_spec_verify_greedy, then the shapes of
+ * the next verify call, in the same launch.
+ *
+ * Hugging Face "Assisted Generation" page, section "Assisted Generation
+ * loop": after step 5 adjusts the window the loop returns to step 1, the
+ * assistant drafting as many tokens as the window says. Reading (the page
+ * speaks of tokens, not of a cache): this call's new tokens are the previous
+ * step's last token followed by the n_cand[b] candidates, so the sequence
+ * keeps seq_lens[b] - q_lens[b] + 1 + accepted[b] tokens (the cache rows of
+ * the rejected candidates are simply overwritten by the next append); the
+ * next call opens with next_tok[b] followed by min(window, k_max) candidates.
+ * Everything sa_spec_verify_greedy does, plus, per sequence b:
+ *   window[b]       <- the adjusted window (as there; required here)
+ *   n_cand_next[b]  <- n = min(window[b], k_max)   (device int32 [num_seqs])
+ *   q_lens[b]       <- n + 1                       (device int32, in/out)
+ *   seq_lens[b]     <- seq_lens[b] - q_lens[b] + 1 + accepted[b] + n + 1
+ *                                                  (device int32, in/out)
+ * so the next step's kv_append, paged_attn and verify read their lengths
+ * straight from these buffers with no host round trip. n_cand_next may be
+ * the n_cand buffer itself (every read of n_cand[b] precedes the write). A
+ * sequence with q_lens[b] < n_cand[b] + 1 or seq_lens[b] < q_lens[b] gets
+ * SA_ERR_QLEN in *err_flag and its window and lengths are left unchanged.
+ * Other arguments, the workspace and the errors as in sa_spec_verify_greedy.
+ */
+SA_API int sa_spec_verify_greedy_advance(const float *logits, const int32_t *candidates,
+                                         const int32_t *n_cand, int32_t num_seqs, int32_t k_max,
+                                         int32_t vocab, int32_t *accepted, int32_t *next_tok,
+                                         int32_t *window, int32_t *seq_lens, int32_t *q_lens,
+                                         int32_t *n_cand_next, void *workspace, size_t workspace_bytes,
+                                         int32_t *err_flag, void *stream);
+
+/*
  * sa_defrag_moves -- compaction plan for a fragmented cache (host only, no
  * CUDA call).
  *

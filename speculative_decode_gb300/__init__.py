@@ -29,6 +29,7 @@ from ._lib import (  # noqa: F401
     plan_analyze,
     sm_count,
     spec_verify_greedy,
+    spec_verify_greedy_advance,
     spec_verify_workspace_size,
     status_string,
 )

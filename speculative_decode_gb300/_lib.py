@@ -65,6 +65,7 @@ def load_library() -> ctypes.CDLL:
         "sa_paged_attn_noalloc": ([DP, P, P, P, P, P, P, F, P, P, P], ctypes.c_int),
         "sa_spec_verify_workspace_size": ([I32, I32, I32], SZ),
         "sa_spec_verify_greedy": ([P, P, P, I32, I32, I32, P, P, P, P, SZ, P, P], ctypes.c_int),
+        "sa_spec_verify_greedy_advance": ([P, P, P, I32, I32, I32, P, P, P, P, P, P, P, SZ, P, P], ctypes.c_int),
         "sa_kv_append_q8": ([DP] + [P] * 11, ctypes.c_int),
         "sa_paged_attn_q8": ([DP, P, P, P, P, P, P, P, P, F, P, P, SZ, P, P], ctypes.c_int),
         "sa_kv_append_q4": ([DP] + [P] * 11, ctypes.c_int),
@@ -223,6 +224,19 @@ def spec_verify_greedy(logits, candidates, n_cand, accepted, next_tok, workspace
                                               _ptr(window), _ptr(workspace), nbytes,
                                               _ptr(err_flag), _stream(stream))
     _check(rc, "sa_spec_verify_greedy")
+
+
+def spec_verify_greedy_advance(logits, candidates, n_cand, accepted, next_tok, window, seq_lens, q_lens,
+                               n_cand_next, workspace, err_flag=None, stream=None) -> None:
+    """spec_verify_greedy plus the next verify call's lengths (window,
+    seq_lens and q_lens updated in place, n_cand_next written)."""
+    B, k1, V = logits.shape
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = load_library().sa_spec_verify_greedy_advance(
+        _ptr(logits), _ptr(candidates), _ptr(n_cand), B, k1 - 1, V, _ptr(accepted), _ptr(next_tok),
+        _ptr(window), _ptr(seq_lens), _ptr(q_lens), _ptr(n_cand_next), _ptr(workspace), nbytes,
+        _ptr(err_flag), _stream(stream))
+    _check(rc, "sa_spec_verify_greedy_advance")
 
 
 def defrag_moves(dims: Dims, block_table_host, seq_lens_host):

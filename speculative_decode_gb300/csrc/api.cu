@@ -492,10 +492,11 @@ size_t sa_spec_verify_workspace_size(int32_t num_seqs, int32_t k_max, int32_t vo
     return 2 * a + c;
 }
 
-int sa_spec_verify_greedy(const float *logits, const int32_t *candidates, const int32_t *n_cand,
-                          int32_t num_seqs, int32_t k_max, int32_t vocab, int32_t *accepted,
-                          int32_t *next_tok, int32_t *window, void *workspace,
-                          size_t workspace_bytes, int32_t *err_flag, void *stream) {
+static int verify_impl(const float *logits, const int32_t *candidates, const int32_t *n_cand,
+                       int32_t num_seqs, int32_t k_max, int32_t vocab, int32_t *accepted,
+                       int32_t *next_tok, int32_t *window, int32_t *seq_lens, int32_t *q_lens,
+                       int32_t *n_cand_next, void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                       void *stream) {
     if (num_seqs < 0 || k_max < 0 || vocab <= 0) return SA_ERR_ARG;
     if (k_max > kMaxKMax) return SA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return SA_OK;
@@ -523,6 +524,9 @@ int sa_spec_verify_greedy(const float *logits, const int32_t *candidates, const 
     p.accepted = accepted;
     p.next_tok = next_tok;
     p.window = window;
+    p.seq_lens = seq_lens;
+    p.q_lens = q_lens;
+    p.n_cand_next = n_cand_next;
     p.part_val = static_cast<float *>(workspace);
     p.part_idx = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + a);
     p.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + 2 * a);
@@ -535,6 +539,24 @@ int sa_spec_verify_greedy(const float *logits, const int32_t *candidates, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (launch_verify(p, s) != cudaSuccess) return SA_ERR_CUDA;
     return finish(s, err_flag);
+}
+
+int sa_spec_verify_greedy(const float *logits, const int32_t *candidates, const int32_t *n_cand,
+                          int32_t num_seqs, int32_t k_max, int32_t vocab, int32_t *accepted,
+                          int32_t *next_tok, int32_t *window, void *workspace,
+                          size_t workspace_bytes, int32_t *err_flag, void *stream) {
+    return verify_impl(logits, candidates, n_cand, num_seqs, k_max, vocab, accepted, next_tok, window,
+                       nullptr, nullptr, nullptr, workspace, workspace_bytes, err_flag, stream);
+}
+
+int sa_spec_verify_greedy_advance(const float *logits, const int32_t *candidates, const int32_t *n_cand,
+                                  int32_t num_seqs, int32_t k_max, int32_t vocab, int32_t *accepted,
+                                  int32_t *next_tok, int32_t *window, int32_t *seq_lens, int32_t *q_lens,
+                                  int32_t *n_cand_next, void *workspace, size_t workspace_bytes,
+                                  int32_t *err_flag, void *stream) {
+    if (num_seqs > 0 && (!window || !seq_lens || !q_lens || !n_cand_next)) return SA_ERR_ARG;
+    return verify_impl(logits, candidates, n_cand, num_seqs, k_max, vocab, accepted, next_tok, window,
+                       seq_lens, q_lens, n_cand_next, workspace, workspace_bytes, err_flag, stream);
 }
 
 int sa_defrag_moves(const sa_dims *dims, const int32_t *block_table, const int32_t *seq_lens,

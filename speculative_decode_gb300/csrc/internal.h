@@ -142,6 +142,9 @@ struct VerifyParams {
     int32_t *accepted;
     int32_t *next_tok;
     int32_t *window;
+    int32_t *seq_lens;    // nullable: in/out, the next call's lengths (with q_lens, n_cand_next)
+    int32_t *q_lens;
+    int32_t *n_cand_next;
     float *part_val;      // [B * (k_max + 1)][n_chunks]
     int32_t *part_idx;    // same shape
     int32_t *counters;    // [B], zero between calls

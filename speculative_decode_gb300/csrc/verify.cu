@@ -6,10 +6,13 @@
 // candidates from the left (step 3); at the first mismatch the verifier's
 // token is kept and the later candidates are dropped (step 4); the draft
 // window grows by 2 when every candidate matched and shrinks by 1 otherwise
-// (step 5). Readings: ties go to the lowest index, -0.0 == +0.0, NaN never
-// wins (an all-NaN row gives 0), the window never drops below 1, and with no
-// mismatch the correction token is the verifier's bonus token after the last
-// candidate.
+// (step 5), and the loop drafts again with that window (step 1). Readings:
+// ties go to the lowest index, -0.0 == +0.0, NaN never wins (an all-NaN row
+// gives 0), the window never drops below 1, with no mismatch the correction
+// token is the verifier's bonus token after the last candidate, and the
+// call's new tokens are the previous step's last token followed by the
+// candidates (so the next call keeps seq_len - q_len + 1 + accepted tokens and
+// opens with the correction token and min(window, k_max) candidates).
 //
 // Design: the logits rows (fp32, 128256 wide for a Llama-3 vocabulary) are the
 // only real traffic. Each row is cut into chunks; one CTA streams one chunk
@@ -155,7 +158,24 @@ __global__ void __launch_bounds__(256) argmax_accept_kernel(const VerifyParams P
         while (a < n && P.candidates[static_cast<int64_t>(b) * P.k_max + a] == s_tok[a]) ++a;
         P.accepted[b] = a;
         P.next_tok[b] = s_tok[a];
-        if (P.window) {
+        if (P.seq_lens) {
+            // the next call (the loop drafts again with the adjusted window):
+            // it keeps the tokens before this call, this call's first token
+            // and the accepted candidates, then opens with the correction
+            // token followed by min(window, k_max) candidates
+            const int ql = P.q_lens[b], T = P.seq_lens[b];
+            if (ql < n + 1 || T < ql) {
+                flag_error(P.err, kErrBitQlen);
+            } else {
+                const int w = P.window[b];
+                const int w2 = a == n ? w + 2 : (w - 1 > 1 ? w - 1 : 1);
+                const int nn = w2 < P.k_max ? w2 : P.k_max;
+                P.window[b] = w2;
+                P.n_cand_next[b] = nn;
+                P.q_lens[b] = nn + 1;
+                P.seq_lens[b] = T - ql + 1 + a + nn + 1;
+            }
+        } else if (P.window) {
             const int w = P.window[b];
             P.window[b] = a == n ? w + 2 : (w - 1 > 1 ? w - 1 : 1);
         }
