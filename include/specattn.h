@@ -200,10 +200,12 @@ SA_API int sa_paged_attn(const sa_dims *dims, const uint16_t *q, const uint16_t 
  * table puts it. Same arguments and errors as sa_kv_append.
  *
  * sa_paged_attn_q8: sa_paged_attn over int8 pages (same definition with every
- * cached value code * scale; fp32 accumulation, bf16 output). No plan, and
- * fewer than 16 query rows per KV head (num_q_heads / num_kv_heads *
- * max_q_len < 16: decode, and short verification blocks with few heads per KV
- * head), else SA_ERR_UNSUPPORTED. The workspace is that of
+ * cached value code * scale; fp32 accumulation, bf16 output). No plan, and at
+ * most 128 query rows per KV head (num_q_heads / num_kv_heads * max_q_len <=
+ * 128: decode and verification blocks, not prefill chunks), else
+ * SA_ERR_UNSUPPORTED. The dequantisation is fused into the CUDA-core kernel;
+ * above 16 rows per KV head the rows go in blocks of 16, each of which
+ * streams the pages. The workspace is that of
  * sa_paged_attn_workspace_size(dims, NULL).
  */
 SA_API int sa_kv_append_q8(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_new,

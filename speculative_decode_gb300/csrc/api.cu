@@ -69,7 +69,12 @@ constexpr int kPieceSlots = 8;
 // they go to the tensor cores (persistent CTAs over an even cut of their tiles).
 constexpr int kTcMinRows = 16;
 
-SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
+// Quantised pages are attended on the CUDA cores only: sequences with many
+// query rows per KV head take several 16-row blocks, each streaming the pages
+// again, up to this many rows (verification blocks; not prefill chunks).
+constexpr int kQuantMaxRows = 128;
+
+SplitConfig split_config(const sa_dims &d, const sa_plan *plan, bool quant = false) {
     SplitConfig c{};
     const int G = d.num_q_heads / d.num_kv_heads;
     const int rows = G * std::max(1, d.max_q_len);
@@ -78,7 +83,7 @@ SplitConfig split_config(const sa_dims &d, const sa_plan *plan) {
     const int max_tiles = std::max(1, d.max_pages_per_seq) * (kPageSize / split_tile_tokens());
     c.piece_slots = std::min(kPieceSlots, max_tiles);
     c.tc = SeqTcConfig{0, 0};  // grid is set at launch (one CTA per SM)
-    if (plan == nullptr && G * std::max(1, d.max_q_len) >= kTcMinRows) c.tc.min_rows = kTcMinRows;
+    if (!quant && plan == nullptr && G * std::max(1, d.max_q_len) >= kTcMinRows) c.tc.min_rows = kTcMinRows;
     c.run_slots = plan ? plan_run_slots(plan) : (c.tc.min_rows > 0 ? kTcMaxPieces : 0);
     c.n_slots = c.run_slots + c.piece_slots;
     return c;
@@ -117,7 +122,7 @@ size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
 WsLayout attn_ws_layout(const sa_dims &d, const sa_plan *plan, bool quant) {
     WsLayout w{};
-    const SplitConfig c = split_config(d, plan);
+    const SplitConfig c = split_config(d, plan, quant);
     w.acc_offset = kCounterBytes;
     if (use_stream(d, plan, quant)) {
         const size_t rows = static_cast<size_t>(kStreamSlots) * c.R;
@@ -276,9 +281,9 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
                  !aligned(qp.v_scales, 16))
               : (!aligned(k_pages, 16) || !aligned(v_pages, 16)))
         return SA_ERR_ARG;
-    // quantised pages are attended on the CUDA cores only: no plan, fewer
-    // than kTcMinRows query rows per KV head
-    if (quant && (plan != nullptr || d.num_q_heads / d.num_kv_heads * std::max(1, d.max_q_len) >= kTcMinRows))
+    // quantised pages are attended on the CUDA cores only: no plan, at most
+    // kQuantMaxRows query rows per KV head
+    if (quant && (plan != nullptr || d.num_q_heads / d.num_kv_heads * std::max(1, d.max_q_len) > kQuantMaxRows))
         return SA_ERR_UNSUPPORTED;
     if (plan && !plan_matches(plan, d)) return SA_ERR_ARG;
     const WsLayout wl = attn_ws_layout(d, plan, quant);
@@ -289,7 +294,7 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
 
-    const SplitConfig c = split_config(d, plan);
+    const SplitConfig c = split_config(d, plan, quant);
     if (use_stream(d, plan, quant)) {
         // the work is counted in 32-bit balancing units
         const int64_t max_units = static_cast<int64_t>(d.num_seqs) * d.num_kv_heads * c.nrb *

@@ -89,8 +89,35 @@ def test_q4_llama3_decode_batch_all_rows():
     assert_attention_close(out, ref, "decode q4")
 
 
-def test_q4_rejects_tensor_core_shapes():
-    w = wl.random_case(311, num_seqs=2, Hq=8, Hkv=2, max_ctx=300, q_len_choices=(6,))  # 24 rows per KV head
+def test_q4_verify_batch_all_rows():
+    """The speculative-verification batch (16 sequences, contexts 2048-8192,
+    q_len 6 causal, 32q/8kv: 24 query rows per KV head, two blocks of 16)
+    over int4 pages, every row against the oracle."""
+    w = wl.config(3)
+    out, err, _ = run_q4(w)
+    ref, _ = oracle_q4(w)
+    assert err == 0
+    assert_attention_close(out, ref, "verify q4")
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_q4_many_rows_per_kv_head(seed):
+    """Blocks of 16 query rows: G x q_len from 10 to 128 rows per KV head,
+    causal inside the new tokens, random lengths and tables."""
+    rng = np.random.default_rng(70 + seed)
+    G = int(rng.choice([2, 4, 8]))
+    Hkv = int(rng.choice([1, 2]))
+    q_choices = {2: (5, 16, 33), 4: (3, 6, 17), 8: (2, 6, 16)}[G]
+    w = wl.random_case(360 + seed, num_seqs=int(rng.integers(1, 5)), Hq=G * Hkv, Hkv=Hkv,
+                       max_ctx=int(rng.choice([300, 1300])), q_len_choices=(1,) + q_choices)
+    out, err, _ = run_q4(w)
+    ref, _ = oracle_q4(w)
+    assert err == 0
+    assert_attention_close(out, ref, f"seed {seed}")
+
+
+def test_q4_rejects_more_than_128_rows_per_kv_head():
+    w = wl.random_case(310, num_seqs=2, Hq=8, Hkv=2, max_ctx=300, q_len_choices=(33,))  # 132 rows per KV head
     with pytest.raises(sa.SpecAttnError):
         run_q4(w, append=False)
 
