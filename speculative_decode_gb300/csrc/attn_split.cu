@@ -48,13 +48,7 @@ namespace {
 
 // Tuning constants (measured on GB300: 16-token tiles, two stages per warp and
 // 2R lanes per token were fastest for the decode batch).
-#ifndef SA_SPLIT_TILE
-#define SA_SPLIT_TILE 16
-#endif
-#ifndef SA_SPLIT_MIN_WARPS
-#define SA_SPLIT_MIN_WARPS 1
-#endif
-constexpr int kTile = SA_SPLIT_TILE;          // tokens per stage (16 or 32)
+constexpr int kTile = 16;                     // tokens per stage
 constexpr int kRowBytes = kHeadDim * 2;       // one K or V row: 256 bytes
 constexpr int kKVBytes = kTile * kRowBytes;   // K (or V) rows of one tile, contiguous in a page
 constexpr int kStageBytes = 2 * kKVBytes;     // K tile, then V tile
@@ -69,19 +63,13 @@ struct QTile {
     static constexpr int kBytes = kVScales + kScaleBytes;
 };
 static_assert(QTile<8>::kBytes <= kStageBytes && QTile<4>::kBytes <= kStageBytes, "quantised tiles use the bf16 stage");
-#ifndef SA_SPLIT_STAGES
-#define SA_SPLIT_STAGES 2
-#endif
-constexpr int kStages = SA_SPLIT_STAGES;      // pipeline depth per warp
+constexpr int kStages = 2;                    // pipeline depth per warp
 constexpr int kRing = kStages + 2;            // piece descriptors in flight (>= kStages + 1)
 constexpr int kPieceInts = 16;
 
-#ifndef SA_SPLIT_LPT
-#define SA_SPLIT_LPT 2
-#endif
 template <int R>
 struct Geo {
-    static constexpr int L = SA_SPLIT_LPT * R < 32 ? SA_SPLIT_LPT * R : 32;  // lanes per token
+    static constexpr int L = 2 * R < 32 ? 2 * R : 32;                // lanes per token
     static constexpr int DUP = L / R;                          // lanes holding each row's score
     static constexpr int TG = 32 / L;                          // tokens per warp step
     static constexpr int NS = kTile / TG;                      // steps per tile
@@ -109,16 +97,9 @@ struct SeqInfo {
     int tc;  // attended on the tensor cores (runs are then per segment: tc_work.cuh)
 };
 
-#ifndef SA_SPLIT_SCALAR_FMA
-#define SA_SPLIT_SCALAR_FMA 0
-#endif
-#ifndef SA_SPLIT_QK_BATCH
-#define SA_SPLIT_QK_BATCH 32
-#endif
+constexpr int kQkBatch = 32;  // score values a lane reduces in one batch of steps
+
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-#if SA_SPLIT_SCALAR_FMA
-    return make_float2(fmaf(a.x, b.x, c.x), fmaf(a.y, b.y, c.y));
-#endif
     unsigned long long ra = *reinterpret_cast<unsigned long long *>(&a);
     unsigned long long rb = *reinterpret_cast<unsigned long long *>(&b);
     unsigned long long rc = *reinterpret_cast<unsigned long long *>(&c);
@@ -298,11 +279,8 @@ __device__ __forceinline__ Ranges make_ranges(int total, int W, int C_min) {
 // segment gets fewer tiles. Tile t of a segment that starts at unit u sits at
 // unit u + kSegmentCost + kUnitsPerTile * t and belongs to the warp whose range
 // holds that unit.
-#ifndef SA_SPLIT_SEG_COST
-#define SA_SPLIT_SEG_COST 8
-#endif
 constexpr int kUnitsPerTile = 4;
-constexpr int kSegmentCost = SA_SPLIT_SEG_COST;
+constexpr int kSegmentCost = 8;
 
 __device__ __forceinline__ int segment_units(const SeqInfo &s) {
     return s.tiles > 0 ? kSegmentCost + kUnitsPerTile * s.tiles : 0;
@@ -511,7 +489,7 @@ __device__ __forceinline__ void locate_seq(const SplitParams &P, int lane, bool 
 
 // KB: 16 for bf16 pages, 8 for int8 pages, 4 for int4 pages.
 template <int R, int KB>
-__global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(const SplitParams P) {
+__global__ void __launch_bounds__(32, 1) split_attn_kernel(const SplitParams P) {
     using Gm = Geo<R>;
     using Lay = Layout<R>;
     constexpr bool Q = KB < 16;             // quantised pages
@@ -799,7 +777,7 @@ __global__ void __launch_bounds__(32, SA_SPLIT_MIN_WARPS) split_attn_kernel(cons
                 // steps, then the reduce-scatter over L lanes level by level across
                 // the batch, so that independent shuffles overlap
                 float sv[NS];
-                constexpr int NB0 = (SA_SPLIT_QK_BATCH / R) < NS ? (SA_SPLIT_QK_BATCH / R) : NS;
+                constexpr int NB0 = (kQkBatch / R) < NS ? (kQkBatch / R) : NS;
                 constexpr int NB = NB0 > 0 ? NB0 : 1;  // steps per batch
 #pragma unroll
                 for (int b0 = 0; b0 < NS; b0 += NB) {
@@ -1021,16 +999,11 @@ __device__ int tc_pieces(const SplitParams &P, int lane, int bt, int kvh, int mt
 // grid dependency wait, so this overlaps the split kernel) to find the pieces.
 // One warp per CTA and at most 128 registers, so that a combine CTA fits beside
 // the eight resident split CTAs of an SM and can be scheduled early.
-#ifndef SA_COMBINE_WARPS
-#define SA_COMBINE_WARPS 1
-#endif
-#ifndef SA_COMBINE_MIN_CTAS
-#define SA_COMBINE_MIN_CTAS 16
-#endif
-constexpr int kCombineWarps = SA_COMBINE_WARPS;
+constexpr int kCombineWarps = 1;
+constexpr int kCombineMinCtas = 16;
 
 template <int R>
-__global__ void __launch_bounds__(kCombineWarps * 32, SA_COMBINE_MIN_CTAS) combine_kernel(const SplitParams P) {
+__global__ void __launch_bounds__(kCombineWarps * 32, kCombineMinCtas) combine_kernel(const SplitParams P) {
     const int lane = threadIdx.x & 31;
     constexpr int RG = R / 4;
     const int64_t unit = static_cast<int64_t>(blockIdx.x) * kCombineWarps + threadIdx.x / 32;

@@ -46,10 +46,7 @@ constexpr int kKVBlk = kN * 128;              // one 64-wide bf16 column block o
 constexpr int kQBytes = 2 * kRowBlk;          // Q [128 rows][128 d]
 constexpr int kPBytes = kRowBlk;              // P [128 rows][64 keys], double-buffered
 constexpr int kKVStage = 4 * kKVBlk;          // K (2 blocks) + V (2 blocks) = 32 KiB
-#ifndef SA_TC_STAGES
-#define SA_TC_STAGES 5
-#endif
-constexpr int kStagesTC = SA_TC_STAGES;
+constexpr int kStagesTC = 5;                  // K/V stages
 constexpr int kSBufs = 3;                     // S buffers: Q K^T runs up to two tiles ahead of the softmax
 constexpr int kTmemCols = 512;                // S buffers: columns 0 .. 3*64-1, two O buffers: the next 2*128
 constexpr int kThreads = 224;
