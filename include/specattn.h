@@ -260,12 +260,16 @@ SA_API int sa_paged_attn_kernel_count(const sa_dims *dims, const sa_plan *plan);
  * process whose memory pool owns the whole GPU, or a decode loop that may not
  * call cudaMalloc because it synchronises the device. It computes exactly what
  * sa_paged_attn computes (same arguments, no plan), but its scratch is a fixed
- * 16 MiB array inside the library, reserved on every GPU that loads the
- * library until the process exits. The caller still passes inputs and outputs.
+ * 16 MiB array inside the library. The caller still passes inputs and outputs.
  *   - Shapes whose workspace (sa_paged_attn_workspace_size with no plan) is
  *     above 16 MiB are rejected with SA_ERR_WORKSPACE before any GPU work.
  *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *     device current. That lookup makes the driver load the library's device
+ *     code on the device, which commits the 16 MiB there until the process
+ *     exits: make the first call on each device before a memory pool reserves
+ *     the rest of the device, and before any stream capture. The address is
+ *     kept per device and looked up again when the device's context changes
+ *     (after cudaDeviceReset).
  *   - Every call reuses the same array (partial accumulators and counters,
  *     zero when the library is loaded and left at zero by every call that
  *     completes without a device error): two calls that overlap on the GPU

@@ -612,9 +612,13 @@ int sa_defrag_apply_bytes(int32_t num_pages, int64_t page_bytes, void *pool_a, v
 // Some callers cannot allocate device memory at all: a plugin that runs inside
 // a serving process whose memory pool already owns every byte of the GPU, or a
 // decode loop that may not call cudaMalloc because it synchronises the whole
-// device. For them the split kernel's scratch (partial accumulators and their
-// maxima and sums) lives in one fixed array in this file, reserved on every GPU that
-// loads the library until the process exits.
+// device. For them the kernels' scratch (partial accumulators, their maxima
+// and sums, and the counters) lives in one fixed array in this file. The
+// array belongs to this file's module, which the driver loads on a device at
+// the first lookup of its address there (the first call of the entry point on
+// that device): from then on the 16 MiB stay reserved on that device until
+// the process exits. The array is zero when loaded and every call that
+// completes without a device error leaves its counters at zero.
 // ---------------------------------------------------------------------------
 constexpr size_t kStaticScratchBytes = size_t{16} << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
@@ -623,22 +627,46 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
-void *g_scratch_ptr[kMaxDevices];  // device address of g_static_scratch, per device
+struct ScratchEntry {
+    CUcontext ctx;  // the context the address belongs to (a device reset makes a new one)
+    void *ptr;      // device address of g_static_scratch in it
+};
+ScratchEntry g_scratch[kMaxDevices];
 
-// Device address of the fixed scratch on the current device. Looked up once per
-// device, with that device current; the host-side name of the array is not a
-// device address and is never passed to a kernel.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<CtxGetCurrentFn>(p);
+    }();
+    return fn;
+}
+
+// Device address of the fixed scratch on the current device, looked up with
+// that device current (the host-side name of the array is not a device address
+// and is never passed to a kernel) and kept until the device's context
+// changes.
 int static_scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return SA_ERR_UNSUPPORTED;
+    if (cudaFree(nullptr) != cudaSuccess) return SA_ERR_CUDA;  // makes the device's context current (frees nothing)
+    CUcontext ctx = nullptr;
+    CtxGetCurrentFn get = ctx_get_current_fn();
+    if (get == nullptr || get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return SA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    ScratchEntry &e = g_scratch[dev];
+    if (e.ptr == nullptr || e.ctx != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return SA_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+        e.ctx = ctx;
+        e.ptr = p;
     }
-    *out = g_scratch_ptr[dev];
+    *out = e.ptr;
     return SA_OK;
 }
 
