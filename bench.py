@@ -41,6 +41,8 @@ METRIC = "paged-attn KV GB/s (frac of HBM peak); verified tokens/s at 1 GB300"
 DECODE_CFG = 1   # Llama3-8B-shaped decode batch
 VERIFY_CFG = 3   # speculative verification batch
 DEDUP_CFG = 2    # 100 sequences sharing a 16-page prefix
+TINY_CFG = 0     # 4 sequences, 8 q / 2 KV heads
+FRAG_CFG = 4     # 8 x 8192-token contexts on a churned pool, q_len 1 or 6
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -328,7 +330,7 @@ def quant_block(batch: GpuBatch, w: wl.Workload, dev, steps: int, warmup: int, f
         e1.record(stream)
     torch.cuda.synchronize()
     assert int(batch.err.item()) == 0, "device error flag set"
-    t = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev))
+    t = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in ev))
     tokens_heads = sum(int(T) for T in w.seq_lens) * w.num_kv_heads
     q_bytes = (tokens_heads * (128 * bits // 8 + 4) * 2 + 2 * w.q.nbytes + w.block_table.nbytes
                + w.seq_lens.nbytes + w.q_lens.nbytes)
@@ -429,11 +431,11 @@ def run_ours(args):
         # each kernel call timed on its own (events between them) for the roofline
         parts, wall = timed_steps(batch, args.steps, args.warmup, flush, ["append", "attend"])
     clocks = clk.summary()
-    t_attn = statistics.mean(parts["attend"])      # ms
-    t_step = statistics.mean(steps_ms)
+    t_attn = statistics.median(parts["attend"])      # ms
+    t_step = statistics.median(steps_ms)
     t_attn_max = max_over_ranks(t_attn)
     t_step_max = max_over_ranks(t_step)
-    t_append_max = max_over_ranks(statistics.mean(parts["append"]))
+    t_append_max = max_over_ranks(statistics.median(parts["append"]))
     assert int(batch.err.item()) == 0, "device error flag set"
 
     e2e_ms, h2d, d2h = e2e_steps(batch, max(10, args.steps // 10), args.warmup)
@@ -444,9 +446,9 @@ def run_ours(args):
     vb = GpuBatch(wv, dev)
     vsteps = max(3, args.steps // 4)
     vparts, _ = timed_steps(vb, vsteps, args.warmup, flush, ["append", "attend", "accept"])
-    tv_attn = max_over_ranks(statistics.mean(vparts["attend"]))
-    tv_acc = max_over_ranks(statistics.mean(vparts["accept"]))
-    tv_step = max_over_ranks(statistics.mean(
+    tv_attn = max_over_ranks(statistics.median(vparts["attend"]))
+    tv_acc = max_over_ranks(statistics.median(vparts["accept"]))
+    tv_step = max_over_ranks(statistics.median(
         [a + b + c for a, b, c in zip(vparts["append"], vparts["attend"], vparts["accept"])]))
     torch.cuda.synchronize()
     emitted = int((vb.acc.cpu().numpy() + 1).sum())
@@ -461,7 +463,7 @@ def run_ours(args):
     for label, use_plan in (("with_plan", True), ("without_plan", False)):
         db = GpuBatch(wd, dev, use_plan=use_plan)
         dparts, _ = timed_steps(db, dsteps, args.warmup, flush, ["attend"])
-        t = max_over_ranks(statistics.mean(dparts["attend"]))
+        t = max_over_ranks(statistics.median(dparts["attend"]))
         dedup[label] = {"paged_attn_ms": round(t, 5),
                         "GBps_unique": round(dedup["unique_bytes"] / (t * 1e-3) / 1e9, 1)}
         if use_plan:
@@ -472,7 +474,7 @@ def run_ours(args):
     # (512 pages, 8 KV heads): the host plan once, the page copies timed
     vb.prepare_defrag()
     fparts, _ = timed_steps(vb, vsteps, args.warmup, flush, ["defrag"])
-    tf = max_over_ranks(statistics.mean(fparts["defrag"]))
+    tf = max_over_ranks(statistics.median(fparts["defrag"]))
     moved = vb.n_moves * 2 * wv.num_kv_heads * wl.PAGE_SIZE * 128 * 2  # K and V bytes of the moved pages
     defrag = {"workload": f"{wv.name} pool ({wv.num_pages} pages)", "live_pages": vb.n_live,
               "moved_pages": vb.n_moves, "moved_bytes": moved, "ms": round(tf, 5),
@@ -485,8 +487,8 @@ def run_ours(args):
     wp = wl.prefill_chunk(seed=1100 + rank)
     pb = GpuBatch(wp, dev)
     pparts, _ = timed_steps(pb, vsteps, args.warmup, flush, ["append", "attend"])
-    tp = max_over_ranks(statistics.mean(pparts["attend"]))
-    tpa = max_over_ranks(statistics.mean(pparts["append"]))
+    tp = max_over_ranks(statistics.median(pparts["attend"]))
+    tpa = max_over_ranks(statistics.median(pparts["append"]))
     pflops = attention_flops(wp)
     tpeak, tpeak_kind = bf16_peak()
     prefill = {"workload": wp.name, "paged_attn_ms": round(tp, 5), "kv_append_ms": round(tpa, 5),
@@ -497,6 +499,20 @@ def run_ours(args):
                "counts": "4 x 128 x visible keys per (new token, query head) row / paged_attn device time"}
     del pb
 
+    # ---- the tiny decode batch and the fragmented long-context batch,
+    # paged_attn only (KV bytes over device time, as for the headline)
+    extra = {}
+    for label, cfg in (("tiny", TINY_CFG), ("fragmented", FRAG_CFG)):
+        we = wl.config(cfg, seed=rank_seed(cfg, rank))
+        eb = GpuBatch(we, dev)
+        eparts, _ = timed_steps(eb, vsteps, args.warmup, flush, ["attend"])
+        t = max_over_ranks(statistics.median(eparts["attend"]))
+        eby = counted_bytes(we)
+        extra[label] = {"workload": we.name, "paged_attn_ms": round(t, 5), "bytes": eby,
+                        "GBps": round(eby / (t * 1e-3) / 1e9, 1), "kernels": eb.kernels_attn}
+        assert int(eb.err.item()) == 0, "device error flag set"
+        del eb
+
     # ---- sixth block: the decode batch over int8 and int4 pages (synthetic
     # seeded codes and per-row scales of the same shapes), attention only
     q8 = quant_block(batch, w, dev, vsteps, args.warmup, flush, 8)
@@ -506,6 +522,8 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     achieved = cbytes / (t_attn_max * 1e-3) / 1e9
     defrag["frac_of_hbm_peak"] = round(defrag["GBps"] / peak, 4)
+    for v in extra.values():
+        v["frac_of_hbm_peak"] = round(v["GBps"] / peak, 4)
     line = {
         "metric": METRIC,
         "value": round(world * sbytes / (t_step_max * 1e-3) / 1e9, 2),
@@ -530,6 +548,7 @@ def run_ours(args):
                             "+ q + out + tables; kv_append: new K/V rows read and written) / step device "
                             "time (one event pair around kv_append + paged_attn launched back to back)",
             "l2": "flushed before every step: 2x L2 written, then 2x L2 of other data read",
+            "timing": "median over the timed steps of each block's CUDA-event times",
             "parallelism": f"replicas x{world} (independent batches, no collective)",
         },
         "counted_bytes_per_step": sbytes,
@@ -558,6 +577,8 @@ def run_ours(args):
             "step_ms": round(tv_step, 5),
             "note": "per attention layer: one layer's attention + one greedy accept",
         },
+        "tiny": extra["tiny"],
+        "fragmented": extra["fragmented"],
         "dedup": dedup,
         "defrag": defrag,
         "prefill": prefill,
