@@ -64,9 +64,12 @@ struct SplitConfig {
 };
 
 constexpr int kPieceSlots = 8;
-// Sequences with at least this many query rows per KV head (G heads x new
-// tokens: q_len = k+1 verification) are a dense contraction: without a plan
-// they go to the tensor cores (persistent CTAs over an even cut of their tiles).
+// A batch whose largest sequence has at least this many query rows per KV
+// head (G heads x new tokens: q_len = k+1 verification, prefill chunks) is a
+// dense contraction: without a plan all of its sequences go to the tensor
+// cores (persistent CTAs over an even cut of their tiles), the ones with few
+// rows too, so that a mixed batch is one even cut of all its keys. Smaller
+// batches go to the persistent page-streaming kernel.
 constexpr int kTcMinRows = 16;
 
 // Quantised pages are attended on the CUDA cores only: sequences with many
@@ -83,7 +86,7 @@ SplitConfig split_config(const sa_dims &d, const sa_plan *plan, bool quant = fal
     const int max_tiles = std::max(1, d.max_pages_per_seq) * (kPageSize / split_tile_tokens());
     c.piece_slots = std::min(kPieceSlots, max_tiles);
     c.tc = SeqTcConfig{0, 0};  // grid is set at launch (one CTA per SM)
-    if (!quant && plan == nullptr && G * std::max(1, d.max_q_len) >= kTcMinRows) c.tc.min_rows = kTcMinRows;
+    if (!quant && plan == nullptr && G * std::max(1, d.max_q_len) >= kTcMinRows) c.tc.min_rows = 1;
     c.run_slots = plan ? plan_run_slots(plan) : (c.tc.min_rows > 0 ? kTcMaxPieces : 0);
     c.n_slots = c.run_slots + c.piece_slots;
     return c;
