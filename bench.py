@@ -231,9 +231,10 @@ def timed_steps(batch: GpuBatch, steps: int, warmup: int, flush, parts):
 
 
 # DRAM bytes (read + written) of one decode-batch launch of the attention
-# kernel, from one ncu capture of the build that bench.py times; None until
-# that capture is taken again after a change to the kernel.
-DECODE_TRAFFIC_BYTES = None
+# kernel (stream_attn_kernel<4>), from one ncu capture of this build
+# (dram__bytes_read.sum 200.362752 MB + dram__bytes_write.sum 4.123136 MB);
+# None whenever the kernel changes until it is captured again.
+DECODE_TRAFFIC_BYTES = 204485888
 
 
 def timed_sequence(batch: GpuBatch, steps: int, warmup: int, flush, parts):
