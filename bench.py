@@ -234,7 +234,7 @@ def timed_steps(batch: GpuBatch, steps: int, warmup: int, flush, parts):
 # kernel (stream_attn_kernel<4>), from one ncu capture of this build
 # (dram__bytes_read.sum 200.362752 MB + dram__bytes_write.sum 4.123136 MB);
 # None whenever the kernel changes until it is captured again.
-DECODE_TRAFFIC_BYTES = 204485888
+DECODE_TRAFFIC_BYTES = None
 
 
 def timed_sequence(batch: GpuBatch, steps: int, warmup: int, flush, parts):

@@ -195,7 +195,7 @@ const StreamMaps *stream_maps(const uint16_t *k_pages, const uint16_t *v_pages, 
     if (e.k == k_pages && e.v == v_pages && e.rows == rows) return &e.maps;
     e.k = nullptr;
     for (int i = 0; i < kStreamBoxKinds; ++i) {
-        const uint32_t box_rows = static_cast<uint32_t>(stream_tile_tokens()) << i;
+        const uint32_t box_rows = static_cast<uint32_t>(stream_box_rows()) << i;
         if (encode_tensor_map_2d(&e.maps.k[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(k_pages),
                                  kHeadDim, rows, kHeadDim * 2, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
             encode_tensor_map_2d(&e.maps.v[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(v_pages),

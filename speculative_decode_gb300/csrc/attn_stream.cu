@@ -64,10 +64,15 @@ constexpr int kThreads = 8 * 32;                 // warp 0 produces, 1 merges, 2
 constexpr int kHalf = kStageTok * 128;           // 64 columns x 64 rows of bf16: 8 KiB
 constexpr int kStageBytes = 4 * kHalf;           // K (two halves), then V (two halves): 32 KiB
 constexpr int kBoxBytes = kSub * 128;            // one 16-row x 64-column box: 2 KiB
-constexpr int kUnitsPerSub = 4;                  // balancing units of a 16-token sub-tile
-constexpr int kSegCost = 12;                     // units of a segment start (about a stage: its
-                                                 // merge and its partly filled last stage)
-constexpr int kMinUnits = kUnitsPerSub * kStageTok / kSub;  // smallest range: one full stage
+// The work is cut between CTAs at whole stages of a segment (64-token
+// tiles): under a saturated memory system every stage in flight takes about
+// one memory latency whatever its size, so a CTA's time follows its count of
+// stages, and a cut inside a stage would add a partly filled one on each side.
+constexpr int kCutTok = kStageTok;               // tokens per cut tile
+constexpr int kUnitsPerTile = 16;                // balancing units of a cut tile
+constexpr int kSegCost = 12;                     // units of a segment start (its queries, its
+                                                 // merge)
+constexpr int kMinUnits = kUnitsPerTile;         // smallest range: one full stage
 constexpr int kPieceInts = 16;
 constexpr int kQRow = kHeadDim + 8;              // query row stride in shared memory (bf16):
                                                  // 272 bytes, so that eight rows fall on
@@ -109,7 +114,7 @@ __device__ __forceinline__ Seq seq_from(const StreamParams &P, int T, int n, boo
         if (flag) flag_error(P.err, kErrBitQlen);
         return s;
     }
-    s.tiles = (T + kSub - 1) / kSub;
+    s.tiles = (T + kCutTok - 1) / kCutTok;
     s.nrb = (P.G * n + R - 1) / R;
     return s;
 }
@@ -121,7 +126,7 @@ __device__ __forceinline__ Seq seq_at(const StreamParams &P, int b) {
 }
 
 __device__ __forceinline__ int seg_units(const Seq &s) {
-    return s.tiles > 0 ? kSegCost + kUnitsPerSub * s.tiles : 0;
+    return s.tiles > 0 ? kSegCost + kUnitsPerTile * s.tiles : 0;
 }
 
 __device__ __forceinline__ int seq_units(const StreamParams &P, const Seq &s) {
@@ -132,8 +137,8 @@ __device__ __forceinline__ int seq_units(const StreamParams &P, const Seq &s) {
 // C + 1 units each (the first `rem` get C + 1), or ranges of kMinUnits units
 // (one stage) when there is less work than that, the last CTAs then staying
 // idle, so that a piece is never so short that its merge costs more than its
-// stream. A range of at least kUnitsPerSub units inside a segment holds a
-// sub-tile start, so every CTA between a cut segment's first and last holds a
+// stream. A range of at least kUnitsPerTile units inside a segment holds a
+// tile start, so every CTA between a cut segment's first and last holds a
 // piece.
 struct Ranges {
     int C, rem;
@@ -150,7 +155,7 @@ __device__ __forceinline__ Ranges make_ranges(int total, int n) {
     return Ranges{kMinUnits, 0};
 }
 
-__device__ __forceinline__ int ceil_units(int x) { return x <= 0 ? 0 : (x + kUnitsPerSub - 1) / kUnitsPerSub; }
+__device__ __forceinline__ int ceil_units(int x) { return x <= 0 ? 0 : (x + kUnitsPerTile - 1) / kUnitsPerTile; }
 
 // Warp-wide pass over the lengths: total units and total query tokens. For
 // batches of up to 512 sequences it also pulls the first line of every
@@ -338,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         scan_work<R>(P, lane, total, q_total);
         uint32_t k = 0;   // stages issued
         uint32_t pc = 0;  // pieces issued
+        uint32_t qi = 0;  // pieces whose query rows were requested
         auto finish = [&]() {  // the end marker, after the last stage
             const int s = k % kStages;
             if (!warp_wait(&empty[s], ((k / kStages) & 1) ^ 1)) return false;
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) flag_error(P.err, kErrBitTimeout);
             for (uint32_t c = k > kStages ? k - kStages : 0; c < k; ++c)
                 (void)mbar_wait(&full[c % kStages], (c / kStages) & 1);
-            for (uint32_t c = pc > kQSlots ? pc - kQSlots : 0; c < pc; ++c)
+            for (uint32_t c = qi > kQSlots ? qi - kQSlots : 0; c < qi; ++c)
                 (void)mbar_wait(&qfull[c % kQSlots], (c / kQSlots) & 1);
         };
         if (q_total > P.total_q) {  // q_lens disagree with dims.total_q: reject the whole call
@@ -394,10 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         if (gb < ge) {  // the first windows this CTA needs, in flight before the dependency wait
             const int u1 = L1.ws + iseg1 * seg_units(L1.s);
-            const int t1 = ceil_units(gb - u1 - kSegCost) * kSub;
+            const int t1 = ceil_units(gb - u1 - kSegCost) * kCutTok;
             ab = L1.b; aw = (t1 / kPageSize) >> 5; ap = load_win(ab, aw);
             const int u0 = L0.ws + iseg0 * seg_units(L0.s);
-            const int t0 = ceil_units(gb - u0 - kSegCost) * kSub;
+            const int t0 = ceil_units(gb - u0 - kSegCost) * kCutTok;
             prefetch(L0.b, (t0 / kPageSize) >> 5);
         }
         const uint64_t policy = P.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
@@ -405,30 +411,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         grid_dependency_wait();
 
         int last_b = -1;
+        bool keep_window = false;  // the next piece's window is already held
         // One piece: tokens [tok_lo, tok_hi) of segment (b, kvh, rb); its
         // partial goes to `slot` and counts at counter f when pieces > 1.
         auto issue_piece = [&](int b, int kvh, int rb, const Seq &s, int qs, int tok_lo, int tok_hi, int pieces,
                                int slot, int f) -> bool {
-            if (b != last_b) {  // next sequence's first window, while this one streams
-                last_b = b;
-                prefetch(b + 1, 0);
-            }
+            // next sequence's first window, while this one streams (after this
+            // piece's first stage is issued: the load may first wait for the
+            // one before it into the same registers)
+            bool want_window = b != last_b && !keep_window;
+            keep_window = false;
+            last_b = b;
             const int nvr = min(R, P.G * s.n - rb * R);
-            // the piece's descriptor and query rows
+            // the piece's descriptor now, its query rows after its first stage
             const int qslot = pc % kQSlots;
             if (!warp_wait(&qempty[qslot], ((pc / kQSlots) & 1) ^ 1)) return false;
             if (lane == 0) {
                 int32_t *d = ring + qslot * kPieceInts;
                 d[0] = b; d[1] = kvh; d[2] = rb; d[3] = s.T; d[4] = s.n; d[5] = qs; d[6] = nvr;
                 d[7] = pieces; d[8] = slot; d[9] = f;
-                mbar_arrive_expect_tx(&qfull[qslot], nvr * 256);
             }
             __syncwarp();
-            if (lane < nvr) {  // query row r = rb R + lane: token r / G, head kvh G + r % G
-                const int r = rb * R + lane;
-                const uint16_t *src = P.q + (static_cast<int64_t>(qs + r / P.G) * P.Hq + kvh * P.G + r % P.G) * kHeadDim;
-                bulk_load(qbuf + (qslot * 16 + lane) * kQRow, src, 256, &qfull[qslot]);
-            }
+            bool want_q = true;
+            auto issue_q = [&]() {
+                if (lane == 0) mbar_arrive_expect_tx(&qfull[qslot], nvr * 256);
+                __syncwarp();
+                if (lane < nvr) {  // query row r = rb R + lane: token r / G, head kvh G + r % G
+                    const int r = rb * R + lane;
+                    const uint16_t *src =
+                        P.q + (static_cast<int64_t>(qs + r / P.G) * P.Hq + kvh * P.G + r % P.G) * kHeadDim;
+                    bulk_load(qbuf + (qslot * 16 + lane) * kQRow, src, 256, &qfull[qslot]);
+                }
+                want_q = false;
+                ++qi;
+            };
             ++pc;
             // the stages: tokens up to the next multiple of 64, so a stage lies in
             // one page; its rows go in at most three boxes per half of K or V
@@ -477,7 +493,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++k;
                 t = e;
+                if (want_q) issue_q();
+                if (want_window) {
+                    prefetch(b + 1, 0);
+                    want_window = false;
+                }
             }
+            if (want_q) issue_q();  // (a piece has at least one stage)
             return true;
         };
         // One piece of the static range: the part of segment iseg of sequence
@@ -488,9 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t_hi = min(s.tiles, ceil_units(ge - u0 - kSegCost));
             if (t_lo >= t_hi) return true;
             const int f = rg.range_of(u0 + kSegCost);
-            const int pieces = rg.range_of(u0 + kSegCost + kUnitsPerSub * (s.tiles - 1)) - f + 1;
+            const int pieces = rg.range_of(u0 + kSegCost + kUnitsPerTile * (s.tiles - 1)) - f + 1;
             const bool head = t_lo == 0 && t_hi < s.tiles;
-            return issue_piece(b, iseg / s.nrb, iseg % s.nrb, s, qs, t_lo * kSub, min(s.T, t_hi * kSub), pieces,
+            return issue_piece(b, iseg / s.nrb, iseg % s.nrb, s, qs, t_lo * kCutTok, min(s.T, t_hi * kCutTok), pieces,
                                2 * cta + (head ? 1 : 0), f);
         };
 
@@ -503,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int t_lo = ceil_units(gb - u1 - kSegCost), t_hi = min(L1.s.tiles, ceil_units(ge - u1 - kSegCost));
                 if (t_lo == 0 && t_hi > 0 && t_hi < L1.s.tiles) {
                     rotated = true;
+                    keep_window = true;  // the window of L0's sequence, fetched above, comes next
                     ok = emit(L1.b, iseg1, L1.s, L1.ws, L1.qs);
                 }
             }
@@ -992,9 +1015,10 @@ cudaError_t launch_r(const StreamParams &p, const StreamMaps &maps, cudaStream_t
 
 }  // namespace
 
-int stream_units_per_tile() { return kUnitsPerSub; }
+int stream_units_per_tile() { return kUnitsPerTile; }
 int stream_segment_cost() { return kSegCost; }
-int stream_tile_tokens() { return kSub; }
+int stream_tile_tokens() { return kCutTok; }
+int stream_box_rows() { return kSub; }
 
 cudaError_t launch_stream_attn(const StreamParams &p, const StreamMaps &maps, cudaStream_t stream) {
     switch (p.R) {

@@ -107,7 +107,8 @@ struct StreamMaps {
 cudaError_t launch_stream_attn(const StreamParams &p, const StreamMaps &maps, cudaStream_t stream);
 int stream_units_per_tile();
 int stream_segment_cost();
-int stream_tile_tokens();
+int stream_tile_tokens();  // tokens per cut tile (the work is counted in these)
+int stream_box_rows();     // rows of the smallest TMA box
 
 // Split kernel over p.split_ctas one-warp CTAs, then the combine pass that
 // merges the partials of segments cut into pieces (two kernels).
