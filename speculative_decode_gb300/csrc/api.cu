@@ -115,10 +115,11 @@ struct WsLayout {
     size_t acc_offset, ml_offset, total;
 };
 
-// Calls with bf16 pages, no plan and fewer than kTcMinRows query rows per KV
-// head go to the persistent page-streaming kernel.
+// Calls with no plan and fewer than kTcMinRows query rows per KV head (over
+// bf16, int8 or int4 pages) go to the persistent page-streaming kernel.
 bool use_stream(const sa_dims &d, const sa_plan *plan, bool quant) {
-    return !quant && plan == nullptr && d.num_q_heads / d.num_kv_heads * std::max(1, d.max_q_len) < kTcMinRows;
+    (void)quant;
+    return plan == nullptr && d.num_q_heads / d.num_kv_heads * std::max(1, d.max_q_len) < kTcMinRows;
 }
 
 size_t align256(size_t n) { return (n + 255) / 256 * 256; }
@@ -182,29 +183,44 @@ CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void 
               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// Tensor maps of the persistent kernel for one pair of pools. A decode loop
-// calls with the same pools every step, so the last pair's maps are kept
-// (per host thread; a map holds only the pool's address and shape).
-const StreamMaps *stream_maps(const uint16_t *k_pages, const uint16_t *v_pages, uint64_t rows) {
+// Tensor maps of the persistent kernel for one pair of pools: bf16 pages
+// (bits 16: rows of 128 values, boxes of 64 columns with 128-byte swizzle),
+// int8 codes (bits 8: rows of 128 bytes, 128-byte swizzle) or int4 codes
+// (bits 4: rows of 64 bytes, 64-byte swizzle). A decode loop calls with the
+// same pools every step, so the last pair's maps are kept (per host thread;
+// a map holds only the pool's address and shape).
+const StreamMaps *stream_maps(const void *k_pool, const void *v_pool, uint64_t rows, int bits) {
     struct Entry {
         const void *k = nullptr, *v = nullptr;
         uint64_t rows = 0;
+        int bits = 0;
         StreamMaps maps;
     };
     thread_local Entry e;
-    if (e.k == k_pages && e.v == v_pages && e.rows == rows) return &e.maps;
+    if (e.k == k_pool && e.v == v_pool && e.rows == rows && e.bits == bits) return &e.maps;
     e.k = nullptr;
     for (int i = 0; i < kStreamBoxKinds; ++i) {
         const uint32_t box_rows = static_cast<uint32_t>(stream_box_rows()) << i;
-        if (encode_tensor_map_2d(&e.maps.k[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(k_pages),
-                                 kHeadDim, rows, kHeadDim * 2, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-            encode_tensor_map_2d(&e.maps.v[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(v_pages),
-                                 kHeadDim, rows, kHeadDim * 2, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-            return nullptr;
+        CUresult rk, rv;
+        if (bits == 16) {
+            rk = encode_tensor_map_2d(&e.maps.k[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(k_pool),
+                                      kHeadDim, rows, kHeadDim * 2, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+            rv = encode_tensor_map_2d(&e.maps.v[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void *>(v_pool),
+                                      kHeadDim, rows, kHeadDim * 2, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+        } else {
+            const uint32_t row_bytes = kHeadDim * bits / 8;
+            const CUtensorMapSwizzle sw = bits == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+            rk = encode_tensor_map_2d(&e.maps.k[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(k_pool),
+                                      row_bytes, rows, row_bytes, row_bytes, box_rows, sw);
+            rv = encode_tensor_map_2d(&e.maps.v[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, const_cast<void *>(v_pool),
+                                      row_bytes, rows, row_bytes, row_bytes, box_rows, sw);
+        }
+        if (rk != CUDA_SUCCESS || rv != CUDA_SUCCESS) return nullptr;
     }
-    e.k = k_pages;
-    e.v = v_pages;
+    e.k = k_pool;
+    e.v = v_pool;
     e.rows = rows;
+    e.bits = bits;
     return &e.maps;
 }
 
@@ -328,8 +344,12 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
         p.qscale = scale * 1.4426950408889634f;
         p.n_ctas = std::min(sms, kStreamMaxCtas);
         p.evict_first = c.nrb == 1;
+        p.code_bits = quant ? qp.bits : 16;
+        p.k_scales = qp.k_scales;
+        p.v_scales = qp.v_scales;
         const uint64_t rows = static_cast<uint64_t>(d.num_pages) * d.num_kv_heads * kPageSize;
-        const StreamMaps *maps = stream_maps(k_pages, v_pages, rows);
+        const StreamMaps *maps = quant ? stream_maps(qp.k_codes, qp.v_codes, rows, qp.bits)
+                                       : stream_maps(k_pages, v_pages, rows, 16);
         if (maps == nullptr) return SA_ERR_CUDA;
         if (launch_stream_attn(p, *maps, s) != cudaSuccess) return SA_ERR_CUDA;
         return finish(s, err_flag);

@@ -48,22 +48,22 @@
 //  * Every wait is bounded (common.cuh). On timeout a warp flags
 //    SA_ERR_TIMEOUT and leaves; the producer first waits (bounded) for its
 //    copies in flight.
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace sa {
 
 namespace {
 
-constexpr int kStages = 6;                       // ring depth
-constexpr int kStageTok = 64;                    // tokens per stage
-constexpr int kSub = 16;                         // tokens per sub-tile (and per TMA box)
+constexpr int kStageTok = 64;                    // tokens per stage of bf16 pages
+constexpr int kSub = 16;                         // tokens per sub-tile (and per smallest TMA box)
 constexpr int kConsumers = 4;                    // consumer warps (warps 4-7)
-constexpr int kWarpTok = kStageTok / kConsumers; // 16 tokens of a stage per consumer warp
-static_assert(kWarpTok == kSub, "one sub-tile per consumer warp and stage");
 constexpr int kThreads = 8 * 32;                 // warp 0 produces, 1 merges, 2 counts, 3 idle
-constexpr int kHalf = kStageTok * 128;           // 64 columns x 64 rows of bf16: 8 KiB
-constexpr int kStageBytes = 4 * kHalf;           // K (two halves), then V (two halves): 32 KiB
-constexpr int kBoxBytes = kSub * 128;            // one 16-row x 64-column box: 2 KiB
+constexpr int kHalf = kStageTok * 128;           // bf16 pages: 64 columns x 64 rows, 8 KiB
+constexpr int kBoxBytes = kSub * 128;            // bf16 pages: one 16-row x 64-column box, 2 KiB
 // The work is cut between CTAs at whole stages of a segment (64-token
 // tiles): under a saturated memory system every stage in flight takes about
 // one memory latency whatever its size, so a CTA's time follows its count of
@@ -80,6 +80,7 @@ constexpr int kQRow = kHeadDim + 8;              // query row stride in shared m
 constexpr int kQSlots = 4;                       // pieces whose queries are loaded ahead
 constexpr int kMergeSlots = 4;
 constexpr int kMslotInts = 8;
+constexpr int kSmemLimit = 232448;               // dynamic shared memory of one CTA (227 KiB)
 
 // stage descriptor flags
 constexpr int kFirst = 1;  // first stage of a piece
@@ -87,17 +88,59 @@ constexpr int kLast = 2;   // last stage of a piece
 constexpr int kEnd = 4;    // no more stages
 constexpr int kSkip = 8;   // page id out of range: nothing was loaded
 
+// A stage of one page format; KB = bits of a cached value: 16 (bf16 pages),
+// 8 (int8 codes) or 4 (int4 codes, two per byte). Every stage costs the
+// producer about the same few copies to issue, so stages of codes hold more
+// tokens: about 32 KiB each.
+//  * bf16: 64 tokens; K as two 64-column halves of 64 rows x 128 bytes
+//    (128-byte swizzle), then V alike: 32 KiB.
+//  * int8: 128 tokens; K codes, 128 rows x 128 bytes (128-byte swizzle), V
+//    codes alike, then 128 K scales and 128 V scales (fp32): 33 KiB.
+//  * int4: 256 tokens (a page); K codes, 256 rows x 64 bytes (64-byte
+//    swizzle), V codes alike, then the scales: 34 KiB.
+template <int KB>
+struct Fmt {
+    static constexpr bool kQuant = KB != 16;
+    static constexpr int kStageTok = KB == 16 ? 64 : KB == 8 ? 128 : 256;  // tokens per stage
+    static constexpr int kWarpTok = kStageTok / kConsumers;  // tokens of a stage per consumer warp
+    static constexpr int kRowBytes = KB * kHeadDim / 8;      // one cached row: 256, 128 or 64 bytes
+    static constexpr int kRegion = kStageTok * kRowBytes;    // K (or V) rows of a stage
+    static constexpr int kScaleOff = 2 * kRegion;            // K scales, then V scales
+    static constexpr int kScaleBytes = kStageTok * 4;        // one stage's scales of K (or V)
+    static constexpr int kStageBytes = 2 * kRegion + (kQuant ? 2 * kScaleBytes : 0);
+    static_assert(kStageBytes % 1024 == 0, "stages keep the swizzle atoms aligned");
+    static_assert(!kQuant || kScaleOff + 2 * kScaleBytes == kStageBytes, "the scales close a quantised stage");
+    static_assert(kPageSize % kStageTok == 0, "a stage lies in one page");
+    static_assert(kWarpTok % kSub == 0 && kStageTok / kSub < (1 << kStreamBoxKinds), "boxes of a stage");
+};
+
+// Shared memory of one CTA. Over quantised pages the consumers hand their
+// piece states to the merge warp in a buffer of their own (over bf16 pages
+// they write them over the stage they just used, which is large enough), and
+// the ring holds as many stages as fit.
+template <int R, int KB>
 struct Lay {
-    static constexpr int kQ = kStages * kStageBytes;                 // bf16 [kQSlots][16][kQRow]
-    static constexpr int kMl = kQ + kQSlots * 16 * kQRow * 2;        // float2 [kStages][warp][16]
-    static constexpr int kPiece = kMl + kStages * kConsumers * 16 * 8;  // int32 [kQSlots][16]
+    using F = Fmt<KB>;
+    static constexpr int kStateBytes = F::kQuant ? kConsumers * R * kHeadDim * 4 : 0;
+    static constexpr int kFixed = kQSlots * 16 * kQRow * 2 + kStateBytes + kConsumers * 16 * 8 +
+                                  kQSlots * kPieceInts * 4 + 2 * kMergeSlots * kMslotInts * 4 +
+                                  (2 * kQSlots + 4 * kMergeSlots + 1) * 8 + 1024;
+    static constexpr int kPerStage = F::kStageBytes + 16 + 16 + (F::kQuant ? 0 : kConsumers * 16 * 8);
+    static constexpr int kFit = (kSmemLimit - kFixed) / kPerStage;
+    static constexpr int kStages = F::kQuant ? (kFit < 24 ? kFit : 24) : 6;  // ring depth
+    static constexpr int kQ = kStages * F::kStageBytes;              // bf16 [kQSlots][16][kQRow]
+    static constexpr int kState = kQ + kQSlots * 16 * kQRow * 2;     // fp32 [warp][R][128] (quantised)
+    static constexpr int kMl = kState + kStateBytes;                 // float2 [stage or 1][warp][16]
+    static constexpr int kPiece = kMl + (F::kQuant ? 1 : kStages) * kConsumers * 16 * 8;  // int32 [kQSlots][16]
     static constexpr int kDesc = kPiece + kQSlots * kPieceInts * 4;  // int32 [kStages][4]
     static constexpr int kMslot = kDesc + kStages * 16;              // int32 [4][8]
     static constexpr int kXslot = kMslot + kMergeSlots * kMslotInts * 4;  // int32 [4][8]
     static constexpr int kBar = kXslot + kMergeSlots * kMslotInts * 4;
-    // full, empty [kStages]; qfull, qempty [kQSlots]; mfull, mempty, xfull, xempty [kMergeSlots]
-    static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 4 * kMergeSlots;
+    // full, empty [kStages]; qfull, qempty [kQSlots]; mfull, mempty, xfull,
+    // xempty [kMergeSlots]; sempty (quantised: the state buffer is free)
+    static constexpr int kNumBars = 2 * kStages + 2 * kQSlots + 4 * kMergeSlots + 1;
     static constexpr int kBytes = kBar + kNumBars * 8;
+    static_assert(kBytes + 1024 <= kSmemLimit, "shared memory of one CTA");
 };
 
 // Shape of one sequence's work; tiles = 0 when it has none.
@@ -275,6 +318,59 @@ __device__ __forceinline__ uint32_t sw_addr(uint32_t half, int r, int j) {
     return half + r * 128 + (((j ^ r) & 7) << 4);
 }
 
+// Byte address of 16-byte chunk j of row r of 64-byte rows with the 64-byte
+// swizzle (int4 codes).
+__device__ __forceinline__ uint32_t sw64_addr(uint32_t base, int r, int j) {
+    return base + r * 64 + (((j ^ (r >> 1)) & 3) << 4);
+}
+
+// Bytes of the scales of a stage's n rows: whole 16-byte chunks (the rows
+// past n in the chunk lie in the same page and are never used).
+__device__ __forceinline__ uint32_t scale_bytes(int n) { return static_cast<uint32_t>((n + 3) / 4 * 16); }
+
+// D += A B for one m16n8k16 tile in fp16 (fp32 accumulate).
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Codes to exact fp16 values. An integer u in [0, 1023] placed in the
+// mantissa of 1024 (bits 0x6400 | u) is the fp16 number 1024 + u, so one
+// fp16 subtraction leaves u minus the offset exactly.
+//  * int8: w holds four codes (two's complement); the sign flip makes them
+//    code + 128; lo/hi pick bytes (0, 2) and (1, 3) of w as two fp16 pairs.
+__device__ __forceinline__ void i8x4_pairs(uint32_t w, uint32_t sel_lo, uint32_t sel_hi, uint32_t &lo, uint32_t &hi) {
+    w ^= 0x80808080u;
+    lo = hsub2(prmt(w, 0x64646464u, sel_lo), 0x64806480u);  // - (1024 + 128)
+    hi = hsub2(prmt(w, 0x64646464u, sel_hi), 0x64806480u);
+}
+//  * int4: nibble i of w (code + 8) and nibble i + 4 become one fp16 pair,
+//    for i = 0..3.
+__device__ __forceinline__ uint32_t i4_pair(uint32_t w, int i) {
+    const uint32_t x = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+    return hsub2(x, 0x64086408u);  // - (1024 + 8)
+}
+
+__device__ __forceinline__ uint32_t half2_bits(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 // Consumer warp c's state inside a stage: row r of O (512 bytes) over the
 // warp's own 16 rows of the four halves (2 KiB each), four O rows per half,
 // word w of row r stored at w ^ 4 (r % 8) (so that the eight rows a store
@@ -287,26 +383,97 @@ __device__ __forceinline__ float2 *state_ml(float2 *ml, int st, int c) {
     return ml + (st * kConsumers + c) * 16;
 }
 
+// Query row fragments (fp16) for the products with codes: the row times the
+// softmax scale and a power of two that puts its largest magnitude in [2^13,
+// 2^14) (within fp16 range, at full fp16 precision). The head dimensions are
+// ordered as the code fragments deliver them: int8, k-step s pairs dims (16 s
+// + 4 cq, + 1) and (+ 2, + 3); int4, k-steps 2 c and 2 c + 1 pair dims 32 c +
+// 8 cq + (0, 4), (1, 5) and (2, 6), (3, 7). Row sel 0 fills a0/a2, 1 fills
+// a1/a3. Returns the factor that undoes the power of two on the scores.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int KB>
+__device__ __forceinline__ float quant_q_row(const uint16_t *qrow, int cq, float qscale, uint32_t (&qa)[8][4],
+                                             int sel) {
+    float amax = 0.f;
+    if constexpr (KB == 8) {
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(qrow + 16 * s + 4 * cq);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf_lo(w.x)), fabsf(bf_hi(w.x))),
+                                     fmaxf(fabsf(bf_lo(w.y)), fabsf(bf_hi(w.y)))));
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 32 * c + 8 * cq);
+            amax = fmaxf(amax, fmaxf(fmaxf(fmaxf(fabsf(bf_lo(w.x)), fabsf(bf_hi(w.x))),
+                                           fmaxf(fabsf(bf_lo(w.y)), fabsf(bf_hi(w.y)))),
+                                     fmaxf(fmaxf(fabsf(bf_lo(w.z)), fabsf(bf_hi(w.z))),
+                                           fmaxf(fabsf(bf_lo(w.w)), fabsf(bf_hi(w.w))))));
+        }
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float m = amax * fabsf(qscale);
+    int ex = m > 0.f ? ((__float_as_int(m) >> 23) & 0xff) - 127 : 0;
+    ex = min(max(ex, -100), 127);
+    const float up = qscale * __int_as_float((127 + 13 - ex) << 23);
+    if constexpr (KB == 8) {
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(qrow + 16 * s + 4 * cq);
+            qa[s][sel] = half2_bits(bf_lo(w.x) * up, bf_hi(w.x) * up);
+            qa[s][2 + sel] = half2_bits(bf_lo(w.y) * up, bf_hi(w.y) * up);
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 32 * c + 8 * cq);
+            // dims 0..7 of the lane's eight: w.x = (0, 1), w.y = (2, 3), w.z = (4, 5), w.w = (6, 7)
+            qa[2 * c][sel] = half2_bits(bf_lo(w.x) * up, bf_lo(w.z) * up);
+            qa[2 * c][2 + sel] = half2_bits(bf_hi(w.x) * up, bf_hi(w.z) * up);
+            qa[2 * c + 1][sel] = half2_bits(bf_lo(w.y) * up, bf_lo(w.w) * up);
+            qa[2 * c + 1][2 + sel] = half2_bits(bf_hi(w.y) * up, bf_hi(w.w) * up);
+        }
+    }
+    return __int_as_float((127 + ex - 13) << 23);
+}
+
+// Head dimension of O^T row g (hi = 0) or g + 8 (hi = 1) of 16-dim block m,
+// as the products deliver them.
+template <int KB>
+__device__ __forceinline__ int o_dim(int m, int g, int hi) {
+    if constexpr (KB == 16) return 16 * m + g + 8 * hi;
+    else if constexpr (KB == 8) return 16 * m + 2 * g + hi;
+    else return 32 * (m >> 1) + 4 * g + 2 * (m & 1) + hi;
+}
+
 template <int R>
 __device__ __forceinline__ int64_t part_row(int sl, int r) {
     return static_cast<int64_t>(sl) * R + r;
 }
 
-template <int R>
+template <int R, int KB>
 __global__ void __launch_bounds__(kThreads, 1)
     stream_attn_kernel(const StreamParams P, const __grid_constant__ StreamMaps maps) {
+    using L = Lay<R, KB>;
+    using F = Fmt<KB>;
+    constexpr int kStages = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    uint16_t *qbuf = reinterpret_cast<uint16_t *>(smem + Lay::kQ);
-    int32_t *ring = reinterpret_cast<int32_t *>(smem + Lay::kPiece);
-    float2 *mlbuf = reinterpret_cast<float2 *>(smem + Lay::kMl);
-    int32_t *desc = reinterpret_cast<int32_t *>(smem + Lay::kDesc);
-    int32_t *mslot = reinterpret_cast<int32_t *>(smem + Lay::kMslot);
-    int32_t *xslot = reinterpret_cast<int32_t *>(smem + Lay::kXslot);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::kBar);
+    uint16_t *qbuf = reinterpret_cast<uint16_t *>(smem + L::kQ);
+    float *sbuf = reinterpret_cast<float *>(smem + L::kState);  // quantised: the consumers' piece states
+    int32_t *ring = reinterpret_cast<int32_t *>(smem + L::kPiece);
+    float2 *mlbuf = reinterpret_cast<float2 *>(smem + L::kMl);
+    int32_t *desc = reinterpret_cast<int32_t *>(smem + L::kDesc);
+    int32_t *mslot = reinterpret_cast<int32_t *>(smem + L::kMslot);
+    int32_t *xslot = reinterpret_cast<int32_t *>(smem + L::kXslot);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kBar);
     uint64_t *empty = full + kStages;
     uint64_t *qfull = empty + kStages;
     uint64_t *qempty = qfull + kQSlots;
@@ -314,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *mempty = mfull + kMergeSlots;
     uint64_t *xfull = mempty + kMergeSlots;
     uint64_t *xempty = xfull + kMergeSlots;
+    uint64_t *sempty = xempty + kMergeSlots;
     const int cta = blockIdx.x;
 
     if (threadIdx.x == 0) {
@@ -331,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&xfull[s], 1);
             mbar_init(&xempty[s], 1);
         }
+        mbar_init(sempty, 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -450,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // one page; its rows go in at most three boxes per half of K or V
             // (64, 32 and 16 rows: the binary digits of its 16-row count)
             for (int t = tok_lo; t < tok_hi;) {
-                const int e = min(tok_hi, (t / kStageTok + 1) * kStageTok);
+                const int e = min(tok_hi, (t / F::kStageTok + 1) * F::kStageTok);
                 const int st = k % kStages;
                 const int pid = pid_of(b, t / kPageSize);
                 if (!warp_wait(&empty[st], ((k / kStages) & 1) ^ 1)) return false;
@@ -461,7 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     desc[st * 4 + 1] = e - t;
                     desc[st * 4 + 2] = (t == tok_lo ? kFirst : 0) | (e == tok_hi ? kLast : 0) | (ok ? 0 : kSkip);
                     if (ok) {
-                        mbar_arrive_expect_tx(&full[st], n16 * 4 * kBoxBytes);
+                        if constexpr (F::kQuant)  // codes of K and V, and their scales
+                            mbar_arrive_expect_tx(&full[st], n16 * kSub * 2 * F::kRowBytes + 2 * scale_bytes(e - t));
+                        else
+                            mbar_arrive_expect_tx(&full[st], n16 * 4 * kBoxBytes);
                     } else {
                         flag_error(P.err, kErrBitPageOOB);
                         mbar_arrive(&full[st]);
@@ -485,10 +657,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (ok && sel >= 0) {
+                if constexpr (F::kQuant) {
+                    // lanes 0-2: boxes of K codes, 8-10: of V codes; lanes 16, 17:
+                    // the K and V scales of the stage's rows (one bulk copy each)
+                    const int row = (pid * P.Hkv + kvh) * kPageSize + (t % kPageSize);
+                    if (ok && sel >= 0 && lane < 16) {
+                        const int qh = lane >> 3;
+                        tma_load_2d(smem + st * F::kStageBytes + qh * F::kRegion + off * kSub * F::kRowBytes,
+                                    qh == 0 ? &maps.k[sel] : &maps.v[sel], &full[st], 0, row + off * kSub, policy);
+                    }
+                    if (ok && (lane == 16 || lane == 17))
+                        bulk_load(smem + st * F::kStageBytes + F::kScaleOff + (lane - 16) * F::kScaleBytes,
+                                  (lane == 16 ? P.k_scales : P.v_scales) + row, scale_bytes(e - t), &full[st]);
+                } else if (ok && sel >= 0) {
                     const int qh = lane >> 3;  // 0, 1: K halves; 2, 3: V halves
                     const int row = (pid * P.Hkv + kvh) * kPageSize + (t % kPageSize) + off * kSub;
-                    tma_load_2d(smem + st * kStageBytes + qh * kHalf + off * kBoxBytes,
+                    tma_load_2d(smem + st * F::kStageBytes + qh * kHalf + off * kBoxBytes,
                                 qh < 2 ? &maps.k[sel] : &maps.v[sel], &full[st], 64 * (qh & 1), row, policy);
                 }
                 ++k;
@@ -583,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!hand_over(-1, 0, 0, 0, 0, 0) && lane == 0) flag_error(P.err, kErrBitTimeout);
                 return;
             }
-            uint8_t *stage = smem + st * kStageBytes;
+            uint8_t *stage = smem + st * F::kStageBytes;
             const bool direct = pieces == 1;
             // each lane owns head dims 4 lane .. 4 lane + 3 of every row; the
             // rows' shared-memory loads are all independent
@@ -594,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float M = -INFINITY;
 #pragma unroll
                     for (int c = 0; c < kConsumers; ++c) {
-                        x[c] = state_ml(mlbuf, st, c)[r];
+                        x[c] = state_ml(mlbuf, F::kQuant ? 0 : st, c)[r];
                         if (x[c].y > 0.f) M = fmaxf(M, x[c].x);
                     }
                     float Ls = 0.f;
@@ -603,7 +787,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < kConsumers; ++c) {
                         const float wt = x[c].y > 0.f ? exp2f(x[c].x - M) : 0.f;
                         Ls += x[c].y * wt;
-                        const float4 a = reinterpret_cast<const float4 *>(state_row(stage, c, r))[lane ^ (r & 7)];
+                        const float *srow = F::kQuant ? sbuf + (c * R + r) * kHeadDim : state_row(stage, c, r);
+                        const float4 a = reinterpret_cast<const float4 *>(srow)[lane ^ (r & 7)];
                         o.x += a.x * wt;
                         o.y += a.y * wt;
                         o.z += a.z * wt;
@@ -621,11 +806,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // the states are read: the stage may be refilled (the next writes
-            // to it are the TMA's)
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive_n(&empty[st], kConsumers);
+            if constexpr (F::kQuant) {
+                // the states are read: the consumers may write the next ones
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sempty);
+            } else {
+                // the states are read: the stage may be refilled (the next
+                // writes to it are the TMA's)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive_n(&empty[st], kConsumers);
+            }
             if (!direct && !hand_over(nvr, qs, kvh, rb, pieces, f)) {
                 if (lane == 0) flag_error(P.err, kErrBitTimeout);
                 return;
@@ -761,9 +952,261 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 8 nr ..); lane (g, cq) holds dims 16 m + g (+ 8) of rows 8 nr + 2 cq (+ 1)
     float ot[8][NR][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows g and g + 8
+    float qf0 = 1.f, qf1 = 1.f;  // quantised pages: factors that undo the query rows' powers of two
     int lim0 = -1, lim1 = -1;
     int pT = 0, pn = 0, prb = 0, pnvr = 0, pqs = 0, pkvh = 0, ppieces = 1, pslot = 0, pf = 0;
     const float qscale = P.qscale;
+    // One step of this warp: NS 16-token sub-tiles (stage st_u, first row
+    // tb_u, keys t0_u + tb_u .., of which the first nv_u are valid), as one
+    // tile of 16 NS keys with one online-softmax update. Over quantised pages
+    // a warp's 32 or 64 tokens of a stage go two sub-tiles at a time, so that
+    // their products and conversions overlap (one consumer warp per
+    // scheduler leaves nothing else to hide their latency).
+    auto consume = [&](auto ns_tag, int stA, int stB, int tbA, int tbB, int t0A, int t0B, int nvA, int nvB) {
+        constexpr int NS = decltype(ns_tag)::value;
+        constexpr int NT = 2 * NS;  // eight-key tiles
+        const int st_u[2] = {stA, stB}, tb_u[2] = {tbA, tbB}, t0_u[2] = {t0A, t0B}, nv_u[2] = {nvA, nvB};
+        // ---- S = Q K^T over the 16 NS keys (2 NS N tiles of 8), even and odd
+        // K-steps in two chains of accumulators (half the dependent latency),
+        // added at the end
+        float sacc[NT][4], sodd[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] = sodd[nt][e] = 0.f;
+        // quantised pages: matrix j of a four-matrix load is tokens 8 (j & 1)
+        // .. + 7 of 16-byte column (j >> 1) of the pair being read
+#pragma unroll
+        for (int u = 0; u < NS; ++u) {
+            const int tb = tb_u[u];
+            const int qrow = tb + 8 * (lm & 1) + lr;
+            (void)qrow;
+            uint8_t *stage = smem + st_u[u] * F::kStageBytes;
+            const uint32_t kh0 = smem_base + st_u[u] * F::kStageBytes, kh1 = kh0 + kHalf;
+            (void)kh1;
+            if (!F::kQuant && nv_u[u] < kSub) {
+                // rows past the valid tokens hold whatever the page held: zero
+                // their V so that 0 x (stale) cannot be NaN (codes are
+                // integers, and their probabilities are zeroed before the V
+                // scales multiply them)
+                for (int i = lane; i < (kSub - nv_u[u]) * 16; i += 32) {
+                    const int rr = tb + nv_u[u] + i / 16, ch = i % 16;
+                    *reinterpret_cast<uint4 *>(stage + 2 * kHalf + (ch >> 3) * kHalf + rr * 128 + (ch & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            if constexpr (KB == 8) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {  // k-steps 2 i, 2 i + 1 (one column each)
+                    uint32_t r[4];
+                    ldsm_x4(sw_addr(kh0, qrow, 2 * i + (lm >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t b0, b1;
+                        i8x4_pairs(r[j], 0x4140u, 0x4342u, b0, b1);
+                        mma_f16((j >> 1) ? sodd[2 * u + (j & 1)] : sacc[2 * u + (j & 1)], qa[2 * i + (j >> 1)], b0, b1);
+                    }
+                }
+            } else if constexpr (KB == 4) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {  // columns 2 i, 2 i + 1: k-steps 4 i .. 4 i + 3
+                    uint32_t r[4];
+                    ldsm_x4(sw64_addr(kh0, qrow, 2 * i + (lm >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int c = 2 * i + (j >> 1);
+                        mma_f16(sacc[2 * u + (j & 1)], qa[2 * c], i4_pair(r[j], 0), i4_pair(r[j], 1));
+                        mma_f16(sodd[2 * u + (j & 1)], qa[2 * c + 1], i4_pair(r[j], 2), i4_pair(r[j], 3));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t half = s < 4 ? kh0 : kh1;
+                    const int row = tb + 8 * (lm >> 1) + lr;
+                    uint32_t b00, b01, b10, b11;
+                    ldsm_x4(sw_addr(half, row, 2 * (s & 3) + (lm & 1)), b00, b01, b10, b11);
+                    mma_bf16((s & 1) ? sodd[2 * u] : sacc[2 * u], qa[s], b00, b01);
+                    mma_bf16((s & 1) ? sodd[2 * u + 1] : sacc[2 * u + 1], qa[s], b10, b11);
+                }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] += sodd[nt][e];
+        // quantised pages: the scales of this lane's keys (tb + 8 n + 2 cq, + 1),
+        // K's at the stage's scale area, V's after them
+        float2 ks[NT], vs[NT];
+        (void)ks;
+        (void)vs;
+        if constexpr (F::kQuant) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float *scl = reinterpret_cast<const float *>(smem + st_u[nt >> 1] * F::kStageBytes + F::kScaleOff);
+                const int key = tb_u[nt >> 1] + 8 * (nt & 1) + 2 * cq;
+                ks[nt] = *reinterpret_cast<const float2 *>(scl + key);
+                vs[nt] = *reinterpret_cast<const float2 *>(scl + F::kStageTok + key);
+            }
+        }
+        // ---- online softmax on rows g (and g + 8), log2 units
+        float x[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kl = 8 * (nt & 1) + 2 * cq + (e & 1);  // key within the sub-tile
+                const int lim = e < 2 ? lim0 : lim1;
+                float sc = qscale;
+                if constexpr (F::kQuant) sc = ((e & 1) ? ks[nt].y : ks[nt].x) * (e < 2 ? qf0 : qf1);
+                x[nt][e] = (kl < nv_u[nt >> 1] && t0_u[nt >> 1] + tb_u[nt >> 1] + kl <= lim) ? sacc[nt][e] * sc : -INFINITY;
+            }
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mx0 = fmaxf(mx0, fmaxf(x[nt][0], x[nt][1]));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        if constexpr (R == 16) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mx1 = fmaxf(mx1, fmaxf(x[nt][2], x[nt][3]));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        }
+        // the reference max only moves when the tile max beats it by 2^8
+        const bool grow0 = mx0 > m0 + 8.f, grow1 = mx1 > m1 + 8.f;
+        if (__any_sync(0xffffffffu, grow0 || grow1)) {
+            const float a0 = grow0 ? exp2f(m0 - mx0) : 1.f;  // 0 when m was -inf
+            const float a1 = grow1 ? exp2f(m1 - mx1) : 1.f;
+            if (grow0) m0 = mx0;
+            if (grow1) m1 = mx1;
+            l0 *= a0;
+            l1 *= a1;
+            // this lane's O rows are 2 cq and 2 cq + 1 (of each row tile),
+            // whose factors the lanes of row groups 2 cq and 2 cq + 1 hold
+            const float r0a = __shfl_sync(0xffffffffu, a0, 8 * cq), r1a = __shfl_sync(0xffffffffu, a0, 8 * cq + 4);
+            const float r0b = __shfl_sync(0xffffffffu, a1, 8 * cq), r1b = __shfl_sync(0xffffffffu, a1, 8 * cq + 4);
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                ot[m][0][0] *= r0a;
+                ot[m][0][1] *= r1a;
+                ot[m][0][2] *= r0a;
+                ot[m][0][3] *= r1a;
+                if constexpr (NR == 2) {
+                    ot[m][1][0] *= r0b;
+                    ot[m][1][1] *= r1b;
+                    ot[m][1][2] *= r0b;
+                    ot[m][1][3] *= r1b;
+                }
+            }
+        }
+        const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+        (void)mu1;
+        float p[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            p[nt][0] = exp2f(x[nt][0] - mu0);
+            p[nt][1] = exp2f(x[nt][1] - mu0);
+            l0 += p[nt][0] + p[nt][1];
+            if constexpr (R == 16) {
+                p[nt][2] = exp2f(x[nt][2] - mu1);
+                p[nt][3] = exp2f(x[nt][3] - mu1);
+                l1 += p[nt][2] + p[nt][3];
+            } else {
+                p[nt][2] = p[nt][3] = 0.f;
+            }
+        }
+        // O^T += V^T P^T: P is the B operand (16 keys x 8 rows) straight from
+        // the S accumulators, per sub-tile; V^T the A operand (16 dims x 16
+        // keys) by transposing loads
+        uint32_t pb[NS][NR][2];
+#pragma unroll
+        for (int u = 0; u < NS; ++u) {
+            if constexpr (F::kQuant) {
+                // P times the V scales (fp16); a zero probability stays zero
+                // whatever the scale of its row
+                float pv[2][4];
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 v = vs[2 * u + n];
+                        pv[n][e] = p[2 * u + n][e] > 0.f ? p[2 * u + n][e] * ((e & 1) ? v.y : v.x) : 0.f;
+                    }
+                pb[u][0][0] = half2_bits(pv[0][0], pv[0][1]);
+                pb[u][0][1] = half2_bits(pv[1][0], pv[1][1]);
+                if constexpr (NR == 2) {
+                    pb[u][1][0] = half2_bits(pv[0][2], pv[0][3]);
+                    pb[u][1][1] = half2_bits(pv[1][2], pv[1][3]);
+                }
+            } else {
+                pb[u][0][0] = pack_bf16x2(p[2 * u][0], p[2 * u][1]);
+                pb[u][0][1] = pack_bf16x2(p[2 * u + 1][0], p[2 * u + 1][1]);
+                if constexpr (NR == 2) {
+                    pb[u][1][0] = pack_bf16x2(p[2 * u][2], p[2 * u][3]);
+                    pb[u][1][1] = pack_bf16x2(p[2 * u + 1][2], p[2 * u + 1][3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NS; ++u) {
+            const uint32_t kh0 = smem_base + st_u[u] * F::kStageBytes;
+            const int qrow = tb_u[u] + 8 * (lm & 1) + lr;
+            (void)qrow;
+            if constexpr (KB == 8) {
+                // V codes by transposing loads: matrix j holds tokens 8 (j & 1) ..
+                // of 16-dim block 2 i + (j >> 1); a lane's word is two tokens x
+                // dims (2 g, 2 g + 1), so O^T row g is dim 2 g, row g + 8 dim 2 g + 1
+                const uint32_t vq = kh0 + F::kRegion;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t r[4];
+                    ldsm_x4_t(sw_addr(vq, qrow, 2 * i + (lm >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t va[4];
+                        i8x4_pairs(r[2 * h], 0x4240u, 0x4341u, va[0], va[1]);
+                        i8x4_pairs(r[2 * h + 1], 0x4240u, 0x4341u, va[2], va[3]);
+#pragma unroll
+                        for (int nr = 0; nr < NR; ++nr) mma_f16(ot[2 * i + h][nr], va, pb[u][nr][0], pb[u][nr][1]);
+                    }
+                }
+            } else if constexpr (KB == 4) {
+                // int4: a lane's word is two tokens x dims 4 g .. 4 g + 3 of a
+                // 32-dim column; block 2 c takes dims 4 g, 4 g + 1, block 2 c + 1
+                // dims 4 g + 2, 4 g + 3
+                const uint32_t vq = kh0 + F::kRegion;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    uint32_t r[4];
+                    ldsm_x4_t(sw64_addr(vq, qrow, 2 * i + (lm >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = 2 * i + h;
+                        const uint32_t ra = r[2 * h], rb = r[2 * h + 1];
+                        const uint32_t va[4] = {i4_pair(ra, 0), i4_pair(ra, 1), i4_pair(rb, 0), i4_pair(rb, 1)};
+                        const uint32_t vb[4] = {i4_pair(ra, 2), i4_pair(ra, 3), i4_pair(rb, 2), i4_pair(rb, 3)};
+#pragma unroll
+                        for (int nr = 0; nr < NR; ++nr) {
+                            mma_f16(ot[2 * c][nr], va, pb[u][nr][0], pb[u][nr][1]);
+                            mma_f16(ot[2 * c + 1][nr], vb, pb[u][nr][0], pb[u][nr][1]);
+                        }
+                    }
+                }
+            } else {
+                const uint32_t vh0 = kh0 + 2 * kHalf, vh1 = kh0 + 3 * kHalf;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const uint32_t half = m < 4 ? vh0 : vh1;
+                    const int row = tb_u[u] + 8 * (lm >> 1) + lr;
+                    uint32_t va[4];
+                    ldsm_x4_t(sw_addr(half, row, 2 * (m & 3) + (lm & 1)), va[0], va[1], va[2], va[3]);
+#pragma unroll
+                    for (int nr = 0; nr < NR; ++nr) mma_bf16(ot[m][nr], va, pb[u][nr][0], pb[u][nr][1]);
+                }
+            }
+        }
+    };
     uint32_t k = 0, pc = 0;
 #pragma unroll 1
     while (true) {
@@ -772,7 +1215,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) flag_error(P.err, kErrBitTimeout);
             return;
         }
-        uint8_t *stage = smem + st * kStageBytes;
         const int t0 = desc[st * 4 + 0], ntok = desc[st * 4 + 1], flags = desc[st * 4 + 2];
         if (flags & kEnd) {
             // hand the end over to the merge warp
@@ -796,19 +1238,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) flag_error(P.err, kErrBitTimeout);
                 return;
             }
-            const uint32_t *qw = reinterpret_cast<const uint32_t *>(qbuf + qslot * 16 * kQRow);
-            constexpr int kQW = kQRow / 2;  // words per query row
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                // rows past nvr hold stale data; their scores are masked
-                qa[s][0] = qw[g * kQW + 8 * s + cq];
-                qa[s][2] = qw[g * kQW + 8 * s + 4 + cq];
+            // rows past nvr hold stale data; their scores are masked
+            if constexpr (F::kQuant) {
+                const uint16_t *qrows = qbuf + qslot * 16 * kQRow;
+                qf0 = quant_q_row<KB>(qrows + g * kQRow, cq, qscale, qa, 0);
                 if constexpr (R == 16) {
-                    qa[s][1] = qw[(g + 8) * kQW + 8 * s + cq];
-                    qa[s][3] = qw[(g + 8) * kQW + 8 * s + 4 + cq];
+                    qf1 = quant_q_row<KB>(qrows + (g + 8) * kQRow, cq, qscale, qa, 1);
                 } else {
-                    qa[s][1] = 0u;
-                    qa[s][3] = 0u;
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) qa[s][1] = qa[s][3] = 0u;
+                }
+            } else {
+                const uint32_t *qw = reinterpret_cast<const uint32_t *>(qbuf + qslot * 16 * kQRow);
+                constexpr int kQW = kQRow / 2;  // words per query row
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    qa[s][0] = qw[g * kQW + 8 * s + cq];
+                    qa[s][2] = qw[g * kQW + 8 * s + 4 + cq];
+                    if constexpr (R == 16) {
+                        qa[s][1] = qw[(g + 8) * kQW + 8 * s + cq];
+                        qa[s][3] = qw[(g + 8) * kQW + 8 * s + 4 + cq];
+                    } else {
+                        qa[s][1] = 0u;
+                        qa[s][3] = 0u;
+                    }
                 }
             }
             __syncwarp();
@@ -822,124 +1275,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             lim0 = g < pnvr ? pT - pn + (prb * R + g) / P.G : -1;  // last key of each row
             lim1 = (R == 16 && g + 8 < pnvr) ? pT - pn + (prb * R + g + 8) / P.G : -1;
         }
-        if (!(flags & kSkip)) {
-            const uint32_t kh0 = smem_base + st * kStageBytes, kh1 = kh0 + kHalf;
-            const uint32_t vh0 = kh0 + 2 * kHalf, vh1 = kh0 + 3 * kHalf;
-            do {  // this warp's sub-tile of the stage
-                const int tb = kSub * cw;              // its first stage row
-                const int nv = min(kSub, ntok - tb);   // its valid tokens
-                if (nv <= 0) break;
-                if (nv < kSub) {
-                    // rows past the valid tokens hold whatever the page held: zero
-                    // their V so that 0 x (stale) cannot be NaN
-                    for (int i = lane; i < (kSub - nv) * 16; i += 32) {
-                        const int rr = tb + nv + i / 16, ch = i % 16;
-                        *reinterpret_cast<uint4 *>(stage + 2 * kHalf + (ch >> 3) * kHalf + rr * 128 + (ch & 7) * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    __syncwarp();
-                }
-                // ---- S = Q K^T over the sub-tile's 16 tokens (two N tiles of 8),
-                // even and odd K-steps in two chains of accumulators (half the
-                // dependent latency), added at the end
-                float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                float sodd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t half = s < 4 ? kh0 : kh1;
-                    const int row = tb + 8 * (lm >> 1) + lr;
-                    uint32_t b00, b01, b10, b11;
-                    ldsm_x4(sw_addr(half, row, 2 * (s & 3) + (lm & 1)), b00, b01, b10, b11);
-                    mma_bf16((s & 1) ? sodd[0] : sacc[0], qa[s], b00, b01);
-                    mma_bf16((s & 1) ? sodd[1] : sacc[1], qa[s], b10, b11);
-                }
-#pragma unroll
-                for (int n = 0; n < 2; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sacc[n][e] += sodd[n][e];
-                // ---- online softmax on rows g (and g + 8), log2 units
-                const int kabs = t0 + tb + 2 * cq;  // key of sacc[n][0] is kabs + 8 n
-                float x[2][4];
-#pragma unroll
-                for (int n = 0; n < 2; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int kl = 8 * n + 2 * cq + (e & 1);  // key within the sub-tile
-                        const int lim = e < 2 ? lim0 : lim1;
-                        x[n][e] = (kl < nv && kabs + 8 * n + (e & 1) <= lim) ? sacc[n][e] * qscale : -INFINITY;
-                    }
-                float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                float mx1 = -INFINITY;
-                if constexpr (R == 16) {
-                    mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                }
-                // the reference max only moves when the tile max beats it by 2^8
-                const bool grow0 = mx0 > m0 + 8.f, grow1 = mx1 > m1 + 8.f;
-                if (__any_sync(0xffffffffu, grow0 || grow1)) {
-                    const float a0 = grow0 ? exp2f(m0 - mx0) : 1.f;  // 0 when m was -inf
-                    const float a1 = grow1 ? exp2f(m1 - mx1) : 1.f;
-                    if (grow0) m0 = mx0;
-                    if (grow1) m1 = mx1;
-                    l0 *= a0;
-                    l1 *= a1;
-                    // this lane's O rows are 2 cq and 2 cq + 1 (of each row tile),
-                    // whose factors the lanes of row groups 2 cq and 2 cq + 1 hold
-                    const float r0a = __shfl_sync(0xffffffffu, a0, 8 * cq), r1a = __shfl_sync(0xffffffffu, a0, 8 * cq + 4);
-                    const float r0b = __shfl_sync(0xffffffffu, a1, 8 * cq), r1b = __shfl_sync(0xffffffffu, a1, 8 * cq + 4);
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        ot[m][0][0] *= r0a;
-                        ot[m][0][1] *= r1a;
-                        ot[m][0][2] *= r0a;
-                        ot[m][0][3] *= r1a;
-                        if constexpr (NR == 2) {
-                            ot[m][1][0] *= r0b;
-                            ot[m][1][1] *= r1b;
-                            ot[m][1][2] *= r0b;
-                            ot[m][1][3] *= r1b;
-                        }
-                    }
-                }
-                const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
-                float p[2][4];
-#pragma unroll
-                for (int n = 0; n < 2; ++n) {
-                    p[n][0] = exp2f(x[n][0] - mu0);
-                    p[n][1] = exp2f(x[n][1] - mu0);
-                    l0 += p[n][0] + p[n][1];
-                    if constexpr (R == 16) {
-                        p[n][2] = exp2f(x[n][2] - mu1);
-                        p[n][3] = exp2f(x[n][3] - mu1);
-                        l1 += p[n][2] + p[n][3];
-                    } else {
-                        p[n][2] = p[n][3] = 0.f;
-                    }
-                }
-                // O^T += V^T P^T: P (bf16) is the B operand (16 keys x 8 rows)
-                // straight from the S accumulators; V^T the A operand (16 dims x
-                // 16 keys) by transposing loads
-                uint32_t pb[NR][2];
-                pb[0][0] = pack_bf16x2(p[0][0], p[0][1]);
-                pb[0][1] = pack_bf16x2(p[1][0], p[1][1]);
-                if constexpr (NR == 2) {
-                    pb[1][0] = pack_bf16x2(p[0][2], p[0][3]);
-                    pb[1][1] = pack_bf16x2(p[1][2], p[1][3]);
-                }
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const uint32_t half = m < 4 ? vh0 : vh1;
-                    const int row = tb + 8 * (lm >> 1) + lr;
-                    uint32_t va[4];
-                    ldsm_x4_t(sw_addr(half, row, 2 * (m & 3) + (lm & 1)), va[0], va[1], va[2], va[3]);
-#pragma unroll
-                    for (int nr = 0; nr < NR; ++nr) mma_bf16(ot[m][nr], va, pb[nr][0], pb[nr][1]);
-                }
-            } while (false);
+        // this warp's sub-tiles of the stage: rows cw W .. cw W + W - 1, two at a
+        // time over quantised pages (16 query rows: one, no registers to spare)
+        constexpr int kNS = (F::kQuant && R < 16) ? 2 : 1;
+        const int nvw = (flags & kSkip) ? 0 : ntok - cw * F::kWarpTok;  // its valid tokens
+#pragma unroll 1
+        for (int j = 0; j < F::kWarpTok && j < nvw; j += kNS * kSub) {
+            const int tb = cw * F::kWarpTok + j;
+            const int nvA = min(kSub, nvw - j);
+            if constexpr (kNS == 2)
+                consume(std::integral_constant<int, 2>{}, st, st, tb, tb + kSub, t0, t0, nvA, max(0, min(kSub, nvw - j - kSub)));
+            else
+                consume(std::integral_constant<int, 1>{}, st, st, tb, tb, t0, t0, nvA, 0);
         }
+        uint8_t *stage = smem + st * F::kStageBytes;
         if (flags & kLast) {
             // ---- end of the piece: hand the state to the merge warp
             l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -951,6 +1300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) flag_error(P.err, kErrBitTimeout);
                 return;
             }
+            // quantised pages: the state buffer, once the merge warp has read
+            // the previous piece's states from it
+            if (F::kQuant && !warp_wait(sempty, (pc & 1) ^ 1)) {
+                if (lane == 0) flag_error(P.err, kErrBitTimeout);
+                return;
+            }
             __syncwarp();  // every lane of this warp is done reading its rows of the stage
 #pragma unroll
             for (int nr = 0; nr < NR; ++nr)
@@ -958,30 +1313,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e2 = 0; e2 < 2; ++e2) {
                     const int row = 8 * nr + 2 * cq + e2;
                     if (row < pnvr) {
-                        float *dst = state_row(stage, cw, row);
+                        float *dst = F::kQuant ? sbuf + (cw * R + row) * kHeadDim : state_row(stage, cw, row);
 #pragma unroll
                         for (int m = 0; m < 8; ++m) {
-                            dst[(16 * m + g) ^ (4 * (row & 7))] = ot[m][nr][e2];
-                            dst[(16 * m + g + 8) ^ (4 * (row & 7))] = ot[m][nr][2 + e2];
+                            dst[o_dim<KB>(m, g, 0) ^ (4 * (row & 7))] = ot[m][nr][e2];
+                            dst[o_dim<KB>(m, g, 1) ^ (4 * (row & 7))] = ot[m][nr][2 + e2];
                         }
                     }
                 }
-            if (g < pnvr && cq == 0) state_ml(mlbuf, st, cw)[g] = make_float2(m0, l0);
-            if (R == 16 && g + 8 < pnvr && cq == 0) state_ml(mlbuf, st, cw)[g + 8] = make_float2(m1, l1);
+            float2 *mlw = state_ml(mlbuf, F::kQuant ? 0 : st, cw);
+            if (g < pnvr && cq == 0) mlw[g] = make_float2(m0, l0);
+            if (R == 16 && g + 8 < pnvr && cq == 0) mlw[g + 8] = make_float2(m1, l1);
             // the state was written by this (generic) proxy; the next writes to
             // the stage, after the merge warp releases it, are the TMA's
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if constexpr (!F::kQuant) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             if (cw == 0 && lane == 0) {
                 int32_t *m = mslot + ms * kMslotInts;
                 m[0] = st; m[1] = pnvr; m[2] = pqs; m[3] = pkvh; m[4] = prb; m[5] = ppieces; m[6] = pslot; m[7] = pf;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&mfull[ms]);
+            if (F::kQuant && lane == 0) mbar_arrive(&empty[st]);  // the stage itself is free now
             ++pc;
         } else {
             // zeroed V rows were written by this (generic) proxy; the next
             // writes to the stage are the TMA's
-            if (ntok < kSub * (cw + 1)) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (!F::kQuant && nvw > 0 && nvw < kSub) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
@@ -989,17 +1346,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-constexpr size_t smem_bytes() { return Lay::kBytes + 1024; }
+template <int R, int KB>
+constexpr size_t smem_bytes() { return Lay<R, KB>::kBytes + 1024; }
 
-template <int R>
+template <int R, int KB>
 cudaError_t launch_r(const StreamParams &p, const StreamMaps &maps, cudaStream_t stream) {
     static const cudaError_t attr = cudaFuncSetAttribute(
-        stream_attn_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes()));
+        stream_attn_kernel<R, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes<R, KB>()));
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(p.n_ctas));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes();
+    cfg.dynamicSmemBytes = smem_bytes<R, KB>();
     cfg.stream = stream;
     // a programmatic dependent of the kernel before it: the work scan and the
     // first block-table reads overlap that kernel's end (sa_kv_append allows
@@ -1010,7 +1368,7 @@ cudaError_t launch_r(const StreamParams &p, const StreamMaps &maps, cudaStream_t
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, stream_attn_kernel<R>, p, maps);
+    return cudaLaunchKernelEx(&cfg, stream_attn_kernel<R, KB>, p, maps);
 }
 
 }  // namespace
@@ -1020,11 +1378,21 @@ int stream_segment_cost() { return kSegCost; }
 int stream_tile_tokens() { return kCutTok; }
 int stream_box_rows() { return kSub; }
 
-cudaError_t launch_stream_attn(const StreamParams &p, const StreamMaps &maps, cudaStream_t stream) {
+template <int KB>
+cudaError_t launch_kb(const StreamParams &p, const StreamMaps &maps, cudaStream_t stream) {
     switch (p.R) {
-        case 4: return launch_r<4>(p, maps, stream);
-        case 8: return launch_r<8>(p, maps, stream);
-        case 16: return launch_r<16>(p, maps, stream);
+        case 4: return launch_r<4, KB>(p, maps, stream);
+        case 8: return launch_r<8, KB>(p, maps, stream);
+        case 16: return launch_r<16, KB>(p, maps, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_stream_attn(const StreamParams &p, const StreamMaps &maps, cudaStream_t stream) {
+    switch (p.code_bits) {
+        case 16: return launch_kb<16>(p, maps, stream);
+        case 8: return launch_kb<8>(p, maps, stream);
+        case 4: return launch_kb<4>(p, maps, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -72,8 +72,8 @@ struct SplitParams {
                                 // written ran first, so pages are read without waiting for it
 };
 
-// Parameters of the persistent page-streaming kernel (attn_stream.cu): bf16
-// pages, no plan, fewer than 16 query rows per KV head.
+// Parameters of the persistent page-streaming kernel (attn_stream.cu): bf16,
+// int8 or int4 pages, no plan, fewer than 16 query rows per KV head.
 constexpr int kStreamMaxCtas = 256;   // grid cap (one CTA per SM); workspace is sized for it
 // partial slots: two per CTA (the pieces it shares with its neighbours)
 constexpr int kStreamSlots = 2 * kStreamMaxCtas;
@@ -95,11 +95,17 @@ struct StreamParams {
     float qscale;               // scale * log2(e)
     int32_t n_ctas;             // grid: one CTA per SM, at most kStreamMaxCtas
     int32_t evict_first;
+    // quantised pages (code_bits 8 or 4; 16: bf16 pages): the tensor maps view
+    // the code pools, and one fp32 scale per (page, head, token) row
+    // [num_pages, Hkv, 256]; value = code * scale
+    int32_t code_bits;
+    const float *k_scales, *v_scales;
 };
 // Tensor maps of the K and V pools, each viewed as [num_pages * Hkv * 256
-// rows][128] bf16 with 128-byte swizzle: box kind i is 64 columns x (16 << i)
-// rows.
-constexpr int kStreamBoxKinds = 3;
+// rows] of 128 bf16 values (box kind i: 64 columns x (16 << i) rows, 128-byte
+// swizzle), of 128 int8 codes (128 bytes x (16 << i) rows, 128-byte swizzle)
+// or of 64 bytes of int4 codes (64 bytes x (16 << i) rows, 64-byte swizzle).
+constexpr int kStreamBoxKinds = 5;
 struct StreamMaps {
     CUtensorMap k[kStreamBoxKinds];
     CUtensorMap v[kStreamBoxKinds];

@@ -82,9 +82,16 @@ def test_workspace_sizes(sa):
     d = sa.dims_for(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.num_pages,
                     w.max_pages_per_seq, w.total_q, 1)
     n = sa.paged_attn_workspace_size(d)
-    rows = w.total_q * w.num_q_heads
-    assert n >= 4 * rows * 130 * 4          # up to 4 splits of 130 floats per row
+    # decode (4 query rows per KV head) takes the persistent kernel: a 4 KiB
+    # counter region, then two partial slots per CTA (up to 256 CTAs) of 4
+    # rows x (128 accumulators + max and sum) fp32
+    assert n >= 4096 + 2 * 256 * 4 * 130 * 4
     assert n % 256 == 0
+    # 24 query rows per KV head (verification) take the split path: up to 8
+    # tensor-core pieces and 8 split pieces of 130 floats per row
+    dv = sa.dims_for(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.num_pages,
+                     w.max_pages_per_seq, 6 * w.num_seqs, 6)
+    assert sa.paged_attn_workspace_size(dv) >= 16 * 6 * w.num_seqs * w.num_q_heads * 130 * 4
     assert sa.spec_verify_workspace_size(16, 5, 128256) >= 16 * 6 * 8
     assert sa.spec_verify_workspace_size(16, 16, 100) == 0
 

@@ -97,7 +97,9 @@ def test_noalloc_allocates_nothing_after_the_first_call(sa):
 def test_noalloc_rejects_shapes_beyond_its_scratch(sa):
     w = wl.config(1)
     d = dims_of(w)
-    d.total_q = 1 << 20                       # a workspace far above 16 MiB
+    d.max_q_len = 6                           # 24 rows per KV head: partials per query row,
+    d.total_q = 1 << 16                       # a workspace far above 16 MiB
+    assert sa.paged_attn_workspace_size(d) > STATIC_SCRATCH_BYTES
     lib = sa.load_library()
     rc = lib.sa_paged_attn_noalloc(ctypes.byref(d), *([None] * 6), ctypes.c_float(0.1), None,
                                    None, None)
