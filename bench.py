@@ -231,10 +231,10 @@ def timed_steps(batch: GpuBatch, steps: int, warmup: int, flush, parts):
 
 
 # DRAM bytes (read + written) of one decode-batch launch of the attention
-# kernel (stream_attn_kernel<4>), from one ncu capture of this build
-# (dram__bytes_read.sum 200.362752 MB + dram__bytes_write.sum 4.123136 MB);
+# kernel (stream_attn_kernel<4, 16>), from one ncu capture of this build
+# (dram__bytes_read.sum 200.371456 MB + dram__bytes_write.sum 3.311872 MB);
 # None whenever the kernel changes until it is captured again.
-DECODE_TRAFFIC_BYTES = None
+DECODE_TRAFFIC_BYTES = 203683328
 
 
 def timed_sequence(batch: GpuBatch, steps: int, warmup: int, flush, parts):
@@ -560,9 +560,9 @@ def run_ours(args):
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": DECODE_TRAFFIC_BYTES,
-            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of stream_attn_kernel<4>, "
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of stream_attn_kernel<4, 16>, "
                               "one capture of this build",
-            "kernel": "paged_attn call (stream_attn_kernel<4>, one launch)",
+            "kernel": "paged_attn call (stream_attn_kernel<4, 16>, one launch)",
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback 6.8 TB/s",
         },
