@@ -83,6 +83,20 @@ SA_API const char *sa_status_string(int status);
 SA_API int sa_device_sm_count(void);
 
 /*
+ * sa_selftest_bounded_wait -- the failure path of the kernels' waits.
+ *
+ * Every wait of the library's kernels (on an mbarrier that copies or other
+ * warps complete) gives up after a bounded number of cycles (about a quarter
+ * of a second), sets bit 1 << SA_ERR_TIMEOUT of the caller's device flag and
+ * returns, so that the context stays usable. This call launches one CTA that
+ * makes that same wait on an mbarrier nothing completes, with no copies in
+ * flight: after the limit it sets the bit in err_flag (device int32) and
+ * returns. For tests of the failure path; asynchronous on `stream`.
+ * Returns SA_ERR_ARG when err_flag is NULL.
+ */
+SA_API int sa_selftest_bounded_wait(int32_t *err_flag, void *stream);
+
+/*
  * sa_kv_append -- write the K/V rows of the new tokens into their pages.
  *
  * ExLlamaV2 "Dynamic Generator" page, section "Continuous batching": the

@@ -27,6 +27,7 @@ from ._lib import (  # noqa: F401
     paged_attn_noalloc,
     paged_attn_workspace_size,
     plan_analyze,
+    selftest_bounded_wait,
     sm_count,
     spec_verify_greedy,
     spec_verify_greedy_advance,

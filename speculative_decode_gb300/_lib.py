@@ -54,6 +54,7 @@ def load_library() -> ctypes.CDLL:
     sig = {
         "sa_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "sa_device_sm_count": ([], ctypes.c_int),
+        "sa_selftest_bounded_wait": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
         "sa_kv_append": ([DP] + [P] * 8 + [P], ctypes.c_int),
         "sa_plan_create": ([DP, P, P, P, ctypes.POINTER(P)], ctypes.c_int),
         "sa_plan_destroy": ([P], None),
@@ -88,6 +89,13 @@ def status_string(code: int) -> str:
 
 def sm_count() -> int:
     return int(load_library().sa_device_sm_count())
+
+
+def selftest_bounded_wait(err_flag, stream=None) -> None:
+    """sa_selftest_bounded_wait: one CTA's bounded wait on an mbarrier that
+    nothing completes; sets bit 1 << SA_ERR_TIMEOUT of err_flag."""
+    _check(load_library().sa_selftest_bounded_wait(_ptr(err_flag), _stream(stream)),
+           "sa_selftest_bounded_wait")
 
 
 def _ptr(t) -> Optional[int]:

@@ -235,6 +235,24 @@ int device_sm_count() {
 
 using namespace sa;
 
+namespace sa {
+
+// One CTA waits on an mbarrier that nothing completes, with the bounded wait
+// every kernel of the library uses; when it gives up the CTA flags the
+// timeout and returns.
+__global__ void bounded_wait_selftest_kernel(int32_t *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const bool done = __all_sync(0xffffffffu, mbar_wait(&bar, 0));
+    if (!done && threadIdx.x == 0) flag_error(err, kErrBitTimeout);
+}
+
+}  // namespace sa
+
 extern "C" {
 
 const char *sa_status_string(int status) {
@@ -252,6 +270,14 @@ const char *sa_status_string(int status) {
 }
 
 int sa_device_sm_count(void) { return device_sm_count(); }
+
+int sa_selftest_bounded_wait(int32_t *err_flag, void *stream) {
+    if (err_flag == nullptr) return SA_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    sa::bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(err_flag);
+    if (cudaGetLastError() != cudaSuccess) return SA_ERR_CUDA;
+    return finish(s, err_flag);
+}
 
 int sa_kv_append(const sa_dims *dims, const uint16_t *k_new, const uint16_t *v_new,
                  uint16_t *k_pages, uint16_t *v_pages, const int32_t *block_table,

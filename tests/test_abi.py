@@ -69,6 +69,8 @@ def test_host_side_argument_checks_need_no_gpu(sa):
     assert lib.sa_spec_verify_greedy(None, None, None, -1, 3, 100, *([None] * 4), 0, None, None) == 1
     # the advancing variant needs the window and the three length buffers
     assert lib.sa_spec_verify_greedy_advance(None, None, None, 2, 3, 100, *([None] * 7), 0, None, None) == 1
+    # the bounded-wait self-test needs a flag to set
+    assert lib.sa_selftest_bounded_wait(None, None) == 1
     # quantised pages: null pools are argument errors before any GPU work
     for name in ("sa_paged_attn_q8", "sa_paged_attn_q4"):
         assert getattr(lib, name)(ctypes.byref(d), *([None] * 8), 0.1, None, None, 0, None, None) == 1
