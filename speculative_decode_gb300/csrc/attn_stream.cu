@@ -60,8 +60,7 @@ namespace {
 
 constexpr int kStageTok = 64;                    // tokens per stage of bf16 pages
 constexpr int kSub = 16;                         // tokens per sub-tile (and per smallest TMA box)
-constexpr int kConsumers = 4;                    // consumer warps (warps 4-7)
-constexpr int kThreads = 8 * 32;                 // warp 0 produces, 1 merges, 2 counts, 3 idle
+constexpr int kRoleWarps = 4;                    // warp 0 produces, 1 merges, 2 counts, 3 idle
 constexpr int kHalf = kStageTok * 128;           // bf16 pages: 64 columns x 64 rows, 8 KiB
 constexpr int kBoxBytes = kSub * 128;            // bf16 pages: one 16-row x 64-column box, 2 KiB
 // The work is cut between CTAs at whole stages of a segment (64-token
@@ -102,6 +101,10 @@ template <int KB>
 struct Fmt {
     static constexpr bool kQuant = KB != 16;
     static constexpr int kStageTok = KB == 16 ? 64 : KB == 8 ? 128 : 256;  // tokens per stage
+    // consumer warps (from warp 4 on): over codes two per scheduler, so that
+    // one's code conversions and products hide the other's latencies
+    static constexpr int kConsumers = kQuant ? 8 : 4;
+    static constexpr int kThreads = 32 * (kRoleWarps + kConsumers);
     static constexpr int kWarpTok = kStageTok / kConsumers;  // tokens of a stage per consumer warp
     static constexpr int kRowBytes = KB * kHeadDim / 8;      // one cached row: 256, 128 or 64 bytes
     static constexpr int kRegion = kStageTok * kRowBytes;    // K (or V) rows of a stage
@@ -121,17 +124,17 @@ struct Fmt {
 template <int R, int KB>
 struct Lay {
     using F = Fmt<KB>;
-    static constexpr int kStateBytes = F::kQuant ? kConsumers * R * kHeadDim * 4 : 0;
-    static constexpr int kFixed = kQSlots * 16 * kQRow * 2 + kStateBytes + kConsumers * 16 * 8 +
+    static constexpr int kStateBytes = F::kQuant ? F::kConsumers * R * kHeadDim * 4 : 0;
+    static constexpr int kFixed = kQSlots * 16 * kQRow * 2 + kStateBytes + F::kConsumers * 16 * 8 +
                                   kQSlots * kPieceInts * 4 + 2 * kMergeSlots * kMslotInts * 4 +
                                   (2 * kQSlots + 4 * kMergeSlots + 1) * 8 + 1024;
-    static constexpr int kPerStage = F::kStageBytes + 16 + 16 + (F::kQuant ? 0 : kConsumers * 16 * 8);
+    static constexpr int kPerStage = F::kStageBytes + 16 + 16 + (F::kQuant ? 0 : F::kConsumers * 16 * 8);
     static constexpr int kFit = (kSmemLimit - kFixed) / kPerStage;
     static constexpr int kStages = F::kQuant ? (kFit < 24 ? kFit : 24) : 6;  // ring depth
     static constexpr int kQ = kStages * F::kStageBytes;              // bf16 [kQSlots][16][kQRow]
     static constexpr int kState = kQ + kQSlots * 16 * kQRow * 2;     // fp32 [warp][R][128] (quantised)
     static constexpr int kMl = kState + kStateBytes;                 // float2 [stage or 1][warp][16]
-    static constexpr int kPiece = kMl + (F::kQuant ? 1 : kStages) * kConsumers * 16 * 8;  // int32 [kQSlots][16]
+    static constexpr int kPiece = kMl + (F::kQuant ? 1 : kStages) * F::kConsumers * 16 * 8;  // int32 [kQSlots][16]
     static constexpr int kDesc = kPiece + kQSlots * kPieceInts * 4;  // int32 [kStages][4]
     static constexpr int kMslot = kDesc + kStages * 16;              // int32 [4][8]
     static constexpr int kXslot = kMslot + kMergeSlots * kMslotInts * 4;  // int32 [4][8]
@@ -379,8 +382,8 @@ __device__ __forceinline__ uint32_t half2_bits(float a, float b) {
 __device__ __forceinline__ float *state_row(uint8_t *stage, int c, int r) {
     return reinterpret_cast<float *>(stage + (r >> 2) * kHalf + c * (kSub * 128) + (r & 3) * 512);
 }
-__device__ __forceinline__ float2 *state_ml(float2 *ml, int st, int c) {
-    return ml + (st * kConsumers + c) * 16;
+__device__ __forceinline__ float2 *state_ml(float2 *ml, int st, int c, int consumers) {
+    return ml + (st * consumers + c) * 16;
 }
 
 // Query row fragments (fp16) for the products with codes: the row times the
@@ -456,7 +459,7 @@ __device__ __forceinline__ int64_t part_row(int sl, int r) {
 }
 
 template <int R, int KB>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Fmt<KB>::kThreads, 1)
     stream_attn_kernel(const StreamParams P, const __grid_constant__ StreamMaps maps) {
     using L = Lay<R, KB>;
     using F = Fmt<KB>;
@@ -487,14 +490,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumers);
+            mbar_init(&empty[s], F::kConsumers);
         }
         for (int s = 0; s < kQSlots; ++s) {
             mbar_init(&qfull[s], 1);
-            mbar_init(&qempty[s], kConsumers);
+            mbar_init(&qempty[s], F::kConsumers);
         }
         for (int s = 0; s < kMergeSlots; ++s) {
-            mbar_init(&mfull[s], kConsumers);
+            mbar_init(&mfull[s], F::kConsumers);
             mbar_init(&mempty[s], 1);
             mbar_init(&xfull[s], 1);
             mbar_init(&xempty[s], 1);
@@ -774,17 +777,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 if (r < nvr) {
-                    float2 x[kConsumers];
+                    float2 x[F::kConsumers];
                     float M = -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < kConsumers; ++c) {
-                        x[c] = state_ml(mlbuf, F::kQuant ? 0 : st, c)[r];
+                    for (int c = 0; c < F::kConsumers; ++c) {
+                        x[c] = state_ml(mlbuf, F::kQuant ? 0 : st, c, F::kConsumers)[r];
                         if (x[c].y > 0.f) M = fmaxf(M, x[c].x);
                     }
                     float Ls = 0.f;
                     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int c = 0; c < kConsumers; ++c) {
+                    for (int c = 0; c < F::kConsumers; ++c) {
                         const float wt = x[c].y > 0.f ? exp2f(x[c].x - M) : 0.f;
                         Ls += x[c].y * wt;
                         const float *srow = F::kQuant ? sbuf + (c * R + r) * kHeadDim : state_row(stage, c, r);
@@ -815,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // writes to it are the TMA's)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive_n(&empty[st], kConsumers);
+                if (lane == 0) mbar_arrive_n(&empty[st], F::kConsumers);
             }
             if (!direct && !hand_over(nvr, qs, kvh, rb, pieces, f)) {
                 if (lane == 0) flag_error(P.err, kErrBitTimeout);
@@ -937,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) P.counters[f] = 0;  // ready for the next call
         }
     }
-    if (warp < kConsumers) return;  // warp 3 has no role
+    if (warp < kRoleWarps) return;  // warp 3 has no role
 
     // ==================================================================== consumers
     const int cw = warp - 4;
@@ -1275,9 +1278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             lim0 = g < pnvr ? pT - pn + (prb * R + g) / P.G : -1;  // last key of each row
             lim1 = (R == 16 && g + 8 < pnvr) ? pT - pn + (prb * R + g + 8) / P.G : -1;
         }
-        // this warp's sub-tiles of the stage: rows cw W .. cw W + W - 1, two at a
-        // time over quantised pages (16 query rows: one, no registers to spare)
-        constexpr int kNS = (F::kQuant && R < 16) ? 2 : 1;
+        // this warp's sub-tiles of the stage: rows cw W .. cw W + W - 1, one at a
+        // time (the two consumer warps of a scheduler overlap each other)
+        constexpr int kNS = 1;
         const int nvw = (flags & kSkip) ? 0 : ntok - cw * F::kWarpTok;  // its valid tokens
 #pragma unroll 1
         for (int j = 0; j < F::kWarpTok && j < nvw; j += kNS * kSub) {
@@ -1321,7 +1324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-            float2 *mlw = state_ml(mlbuf, F::kQuant ? 0 : st, cw);
+            float2 *mlw = state_ml(mlbuf, F::kQuant ? 0 : st, cw, F::kConsumers);
             if (g < pnvr && cq == 0) mlw[g] = make_float2(m0, l0);
             if (R == 16 && g + 8 < pnvr && cq == 0) mlw[g + 8] = make_float2(m1, l1);
             // the state was written by this (generic) proxy; the next writes to
@@ -1356,7 +1359,7 @@ cudaError_t launch_r(const StreamParams &p, const StreamMaps &maps, cudaStream_t
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(p.n_ctas));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Fmt<KB>::kThreads);
     cfg.dynamicSmemBytes = smem_bytes<R, KB>();
     cfg.stream = stream;
     // a programmatic dependent of the kernel before it: the work scan and the
