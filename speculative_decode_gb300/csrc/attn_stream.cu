@@ -71,7 +71,9 @@ constexpr int kCutTok = kStageTok;               // tokens per cut tile
 constexpr int kUnitsPerTile = 16;                // balancing units of a cut tile
 constexpr int kSegCost = 12;                     // units of a segment start (its queries, its
                                                  // merge)
-constexpr int kMinUnits = kUnitsPerTile;         // smallest range: one full stage
+constexpr int kMinUnits = 2 * kUnitsPerTile;     // smallest range: two full stages (a small batch
+                                                 // is cut into fewer pieces, whose merge is a
+                                                 // chain of L2 round trips)
 constexpr int kPieceInts = 16;
 constexpr int kQRow = kHeadDim + 8;              // query row stride in shared memory (bf16):
                                                  // 272 bytes, so that eight rows fall on
@@ -181,7 +183,7 @@ __device__ __forceinline__ int seq_units(const StreamParams &P, const Seq &s) {
 
 // The cut of the units [0, total) into one contiguous range per CTA: C or
 // C + 1 units each (the first `rem` get C + 1), or ranges of kMinUnits units
-// (one stage) when there is less work than that, the last CTAs then staying
+// (two stages) when there is less work than that, the last CTAs then staying
 // idle, so that a piece is never so short that its merge costs more than its
 // stream. A range of at least kUnitsPerTile units inside a segment holds a
 // tile start, so every CTA between a cut segment's first and last holds a
@@ -867,14 +869,18 @@ __global__ void __launch_bounds__(Fmt<KB>::kThreads, 1)
                     Ls[i] = 0.f;
                     o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                for (int k0 = 0; k0 < pieces; k0 += 32) {  // lane kk: piece k0 + kk
+                // lane kk holds piece k0 + kk's (max, sum) pairs; those of the
+                // first 32 pieces stay in registers for the weights below
+                float2 v0[RG];
+                for (int k0 = 0; k0 < pieces; k0 += 32) {
                     const int kk = k0 + lane;
 #pragma unroll
                     for (int i = 0; i < RG; ++i) {
-                        if (kk < pieces && r0 + i < nvr) {
-                            const float2 v = __ldcg(reinterpret_cast<const float2 *>(P.part_ml) + part_row<R>(piece_slot(kk), r0 + i));
-                            if (v.y > 0.f) M[i] = fmaxf(M[i], v.x);
-                        }
+                        float2 v = make_float2(0.f, 0.f);
+                        if (kk < pieces && r0 + i < nvr)
+                            v = __ldcg(reinterpret_cast<const float2 *>(P.part_ml) + part_row<R>(piece_slot(kk), r0 + i));
+                        if (k0 == 0) v0[i] = v;
+                        if (v.y > 0.f) M[i] = fmaxf(M[i], v.x);
                     }
                 }
 #pragma unroll
@@ -889,7 +895,9 @@ __global__ void __launch_bounds__(Fmt<KB>::kThreads, 1)
                         wt[i] = 0.f;
                         float lw = 0.f;
                         if (kk < pieces && r0 + i < nvr) {
-                            const float2 v = __ldcg(reinterpret_cast<const float2 *>(P.part_ml) + part_row<R>(piece_slot(kk), r0 + i));
+                            const float2 v = k0 == 0 ? v0[i]
+                                                     : __ldcg(reinterpret_cast<const float2 *>(P.part_ml) +
+                                                              part_row<R>(piece_slot(kk), r0 + i));
                             if (v.y > 0.f) {
                                 wt[i] = exp2f(v.x - M[i]);
                                 lw = v.y * wt[i];
@@ -900,7 +908,9 @@ __global__ void __launch_bounds__(Fmt<KB>::kThreads, 1)
                         Ls[i] += lw;
                     }
                     const int cnt = min(32, pieces - k0);
-                    constexpr int PJ = 4;  // pieces whose rows are loaded together
+                    // pieces whose rows are loaded together (over codes the
+                    // kernel runs 384 threads and has fewer registers to spare)
+                    constexpr int PJ = F::kQuant ? 4 : 8;
                     for (int j0 = 0; j0 < cnt; j0 += PJ) {
                         float4 a[PJ][RG];
                         float w[PJ][RG];
