@@ -364,11 +364,20 @@ __device__ __forceinline__ void i8x4_pairs(uint32_t w, uint32_t sel_lo, uint32_t
     lo = hsub2(prmt(w, 0x64646464u, sel_lo), 0x64806480u);  // - (1024 + 128)
     hi = hsub2(prmt(w, 0x64646464u, sel_hi), 0x64806480u);
 }
-//  * int4: nibble i of w (code + 8) and nibble i + 4 become one fp16 pair,
-//    for i = 0..3.
-__device__ __forceinline__ uint32_t i4_pair(uint32_t w, int i) {
-    const uint32_t x = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-    return hsub2(x, 0x64086408u);  // - (1024 + 8)
+//  * int4: nibble i of w (code + 8) and nibble i + 4 become one fp16 pair
+//    p[i], for i = 0..3. Nibbles 1 and 3 are masked in place (bits 4..7 of a
+//    half: 1024 + 16 u), which one fp16 FMA by 1/16 minus 72 brings to u - 8.
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+__device__ __forceinline__ void i4x8_pairs(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t w8 = w >> 8;
+    p[0] = hsub2((w & 0x000F000Fu) | 0x64006400u, 0x64086408u);                // - (1024 + 8)
+    p[1] = hfma2((w & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);   // / 16 - 72
+    p[2] = hsub2((w8 & 0x000F000Fu) | 0x64006400u, 0x64086408u);
+    p[3] = hfma2((w8 & 0x00F000F0u) | 0x64006400u, 0x2C002C00u, 0xD480D480u);
 }
 
 __device__ __forceinline__ uint32_t half2_bits(float a, float b) {
@@ -1029,8 +1038,10 @@ __global__ void __launch_bounds__(Fmt<KB>::kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int c = 2 * i + (j >> 1);
-                        mma_f16(sacc[2 * u + (j & 1)], qa[2 * c], i4_pair(r[j], 0), i4_pair(r[j], 1));
-                        mma_f16(sodd[2 * u + (j & 1)], qa[2 * c + 1], i4_pair(r[j], 2), i4_pair(r[j], 3));
+                        uint32_t x[4];
+                        i4x8_pairs(r[j], x);
+                        mma_f16(sacc[2 * u + (j & 1)], qa[2 * c], x[0], x[1]);
+                        mma_f16(sodd[2 * u + (j & 1)], qa[2 * c + 1], x[2], x[3]);
                     }
                 }
             } else {
@@ -1196,9 +1207,11 @@ __global__ void __launch_bounds__(Fmt<KB>::kThreads, 1)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int c = 2 * i + h;
-                        const uint32_t ra = r[2 * h], rb = r[2 * h + 1];
-                        const uint32_t va[4] = {i4_pair(ra, 0), i4_pair(ra, 1), i4_pair(rb, 0), i4_pair(rb, 1)};
-                        const uint32_t vb[4] = {i4_pair(ra, 2), i4_pair(ra, 3), i4_pair(rb, 2), i4_pair(rb, 3)};
+                        uint32_t xa[4], xb[4];
+                        i4x8_pairs(r[2 * h], xa);
+                        i4x8_pairs(r[2 * h + 1], xb);
+                        const uint32_t va[4] = {xa[0], xa[1], xb[0], xb[1]};
+                        const uint32_t vb[4] = {xa[2], xa[3], xb[2], xb[3]};
 #pragma unroll
                         for (int nr = 0; nr < NR; ++nr) {
                             mma_f16(ot[2 * c][nr], va, pb[u][nr][0], pb[u][nr][1]);
