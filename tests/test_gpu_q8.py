@@ -87,6 +87,19 @@ def test_q8_verify_batch_all_rows():
     assert_attention_close(out, ref, "verify q8")
 
 
+@pytest.mark.parametrize("G,q_choices", [(8, (1,)), (4, (1, 2, 3)), (2, (1, 4, 7)), (1, (1, 2, 4))])
+def test_q8_persistent_kernel_row_blocks(G, q_choices):
+    """Fewer than 16 query rows per KV head take the persistent kernel with 4,
+    8 or 16 rows per segment; long contexts over few segments, so every
+    segment is cut between many CTAs and merged across them."""
+    w = wl.random_case(380 + G, num_seqs=3, Hq=2 * G, Hkv=2, max_ctx=3000, q_len_choices=q_choices)
+    assert G * int(w.q_lens.max()) < 16
+    out, err, _ = run_q8(w)
+    assert err == 0
+    ref, _ = oracle_q8(w)
+    assert_attention_close(out, ref, f"G={G} q_lens={w.q_lens.tolist()}")
+
+
 @pytest.mark.parametrize("seed", range(4))
 def test_q8_many_rows_per_kv_head(seed):
     """Blocks of 16 query rows: G x q_len from 10 to 128 rows per KV head,
