@@ -408,7 +408,7 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
             return SA_ERR_CUDA;
         if (c.tc.min_rows > 0 &&
             launch_seq_tc(d, SeqTcConfig{c.tc.min_rows, sms}, q, pk, pv, scale, ws_acc, ws_ml, rows_total, err_flag,
-                          block_table, seq_lens, q_lens, s) != cudaSuccess)
+                          block_table, seq_lens, q_lens, out, s) != cudaSuccess)
             return SA_ERR_CUDA;
     }
 

@@ -967,11 +967,14 @@ template <int R>
 __device__ int tc_pieces(const SplitParams &P, int lane, int bt, int kvh, int mt) {
     int total = 0, max_tiles = 0, u0 = 0;
     TcSeq wb{0, 0, 0};
+    bool uniform = P.B > 0;  // as the tensor-core kernel decides its waves
+    const int T0 = P.B > 0 ? P.seq_lens[0] : 0, n0 = P.B > 0 ? P.q_lens[0] : 0;
 #pragma unroll 1
     for (int base = 0; base < P.B; base += 32) {
         const int b = base + lane;
         const int T = b < P.B ? P.seq_lens[b] : 0, n = b < P.B ? P.q_lens[b] : 0;
         const TcSeq w = tc_seq(T, n, P.G, P.Hkv, P.max_q_len, P.max_pages, P.tc_min_rows);
+        uniform = uniform && __all_sync(0xffffffffu, b >= P.B || (T == T0 && n == n0 && w.units > 0));
         int ui = w.units;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -988,9 +991,12 @@ __device__ int tc_pieces(const SplitParams &P, int lane, int bt, int kvh, int mt
         max_tiles = max(max_tiles, static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(w.tiles))));
     }
     if (wb.tiles == 0) return 0;
-    const TcRanges rg = make_tc_ranges(total, P.tc_grid, max_tiles);
+    const TcWaves waves = make_tc_waves(uniform, P.B, tc_seq(T0, n0, P.G, P.Hkv, P.max_q_len, P.max_pages, P.tc_min_rows),
+                                        P.Hkv, P.tc_grid, P.G * n0);
     const int s0 = u0 + (kvh * wb.mtiles + mt) * wb.tiles;
-    return rg.range_of(s0 + wb.tiles - 1) - rg.range_of(s0) + 1;
+    if (s0 < waves.base) return 0;  // a whole segment of a wave: written by the tensor-core kernel
+    const TcRanges rg = make_tc_ranges(total - waves.base, P.tc_grid, max_tiles);
+    return rg.range_of(s0 - waves.base + wb.tiles - 1) - rg.range_of(s0 - waves.base) + 1;
 }
 
 // ---- the combine pass: one warp per (sequence, KV head, row block, group of

@@ -58,11 +58,13 @@ struct SeqTcConfig {
     int min_rows;  // 0 disables the mode
     int grid;      // CTAs (one per SM)
 };
+// (segments a CTA attends whole, in the waves of tc_work.cuh, are written to
+// `out` directly; the combine pass skips them)
 cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t *q,
                           const CUtensorMap &tmk, const CUtensorMap &tmv, float scale,
                           float *ws_acc, float *ws_ml, int64_t rows_total, int32_t *err,
                           const int32_t *block_table, const int32_t *seq_lens,
-                          const int32_t *q_lens, cudaStream_t stream);
+                          const int32_t *q_lens, uint16_t *out, cudaStream_t stream);
 
 constexpr int kRunDescInts = 6;
 constexpr int kTileInts = 6;

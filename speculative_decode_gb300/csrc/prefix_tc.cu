@@ -197,6 +197,7 @@ struct PrefixParams {
     int32_t seq_mode, B, max_q_len, total_q, min_rows;
     float *ws_acc;
     float *ws_ml;
+    uint16_t *out;  // sequence mode: output of the segments attended whole (waves)
     int32_t *err;
     int32_t Hq, Hkv, G, max_pages, num_pages;
     int64_t n_rows_total;
@@ -213,12 +214,16 @@ struct TcPiece {
     int key_end;                      // keys at or past this position are not in the cache
     int seq_n, qstart;                // sequence mode: new tokens, packed row of the first
     int slot;                         // sequence mode: partial slot; plan mode: page chunk
+    int whole;                        // sequence mode: a whole segment of a wave (output written here)
 };
 
-// Start of this CTA's range in sequence mode, found by warp 0 and shared.
+// Start of this CTA's range in sequence mode, found by warp 0 and shared:
+// its waves of whole segments, then its range of the cut (units counted from
+// the start of the work; the cut's own units from waves.base).
 struct TcStart {
     int has_work, b, qstart, seg, tile, unit, end;
     TcRanges rg;
+    TcWaves waves;
 };
 
 // The walk over the pieces of this CTA's range (sequence mode); every role
@@ -227,6 +232,8 @@ struct TcCursor {
     int b, qstart, seg, tile, unit, end, T, n;
     TcSeq w;
     TcRanges rg;
+    TcWaves waves;
+    int wave;
 
     __device__ __forceinline__ void load(const PrefixParams &P) {
         T = P.seq_lens[b];
@@ -241,9 +248,32 @@ struct TcCursor {
         unit = s.unit;
         end = s.end;
         rg = s.rg;
+        waves = s.waves;
+        wave = 0;
         if (unit < end) load(P);
     }
     __device__ __forceinline__ bool next(const PrefixParams &P, TcPiece &pc) {
+        if (wave < waves.waves) {  // whole segment wave * grid + this CTA, its only piece
+            const int sg = wave * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+            const int bb = sg / waves.seg_per_seq, ss = sg % waves.seg_per_seq;
+            const int Tb = P.seq_lens[bb], nb = P.q_lens[bb];
+            const TcSeq wb = tc_seq(Tb, nb, P.G, P.Hkv, P.max_q_len, P.max_pages, P.min_rows);
+            pc.member = bb;
+            pc.g = ss / wb.mtiles;
+            pc.row0 = (ss % wb.mtiles) * kTcRowTile;
+            pc.row_count = P.G * nb;
+            pc.rows_begin = 0;
+            pc.pc_lo = 0;
+            pc.t_lo = 0;
+            pc.t_hi = wb.tiles;
+            pc.key_end = Tb;
+            pc.seq_n = nb;
+            pc.qstart = bb * nb;  // every sequence has nb new tokens
+            pc.slot = 0;
+            pc.whole = 1;
+            ++wave;
+            return true;
+        }
         if (unit >= end) return false;
         const int mt = seg % w.mtiles;
         pc.member = b;
@@ -257,7 +287,8 @@ struct TcCursor {
         pc.key_end = T;
         pc.seq_n = n;
         pc.qstart = qstart;
-        pc.slot = static_cast<int>(blockIdx.x) - rg.range_of(unit - tile);
+        pc.slot = static_cast<int>(blockIdx.x) - rg.range_of(unit - tile - waves.base);
+        pc.whole = 0;
         unit += pc.t_hi - tile;
         tile = pc.t_hi;
         if (tile == w.tiles && unit < end) {  // the next segment (of the next tensor-core sequence)
@@ -320,6 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 0) {
         // lane-per-sequence scan: the total work, the longest segment, the queries
         int total = 0, max_tiles = 0, q_total = 0;
+        bool uniform = P.B > 0;  // every sequence: the same length and query count, and work
+        const int T0 = P.B > 0 ? P.seq_lens[0] : 0, n0 = P.B > 0 ? P.q_lens[0] : 0;
 #pragma unroll 1
         for (int base = 0; base < P.B; base += 32) {
             const int b = base + lane;
@@ -328,12 +361,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             total += __reduce_add_sync(0xffffffffu, static_cast<unsigned>(w.units));
             max_tiles = max(max_tiles, static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(w.tiles))));
             q_total += __reduce_add_sync(0xffffffffu, static_cast<unsigned>(max(0, n)));
+            uniform = uniform && __all_sync(0xffffffffu, b >= P.B || (T == T0 && n == n0 && w.units > 0));
         }
-        const TcRanges rg = make_tc_ranges(total, gridDim.x, max_tiles);
-        const int c_begin = rg.begin(blockIdx.x), c_end = min(total, rg.begin(blockIdx.x + 1));
-        int has = q_total <= P.total_q && c_begin < c_end;  // else the split kernel flags the lengths
+        const TcWaves waves = make_tc_waves(uniform, P.B, tc_seq(T0, n0, P.G, P.Hkv, P.max_q_len, P.max_pages, P.min_rows),
+                                            P.Hkv, gridDim.x, P.G * n0);
+        const int total_cut = total - waves.base;  // the cut's units, after the waves
+        const TcRanges rg = make_tc_ranges(total_cut, gridDim.x, max_tiles);
+        const int c_begin = waves.base + rg.begin(blockIdx.x);
+        const int c_end = waves.base + min(total_cut, rg.begin(blockIdx.x + 1));
+        const bool valid_q = q_total <= P.total_q;  // else the split kernel flags the lengths
+        int has = valid_q && c_begin < c_end;
         int fb = 0, fq = 0, fu = 0;
-        if (has) {  // the sequence whose units hold c_begin
+        if (has && waves.waves > 0) {  // uniform sequences: the start by arithmetic
+            const int su = waves.seg_per_seq * tc_seq(T0, n0, P.G, P.Hkv, P.max_q_len, P.max_pages, P.min_rows).tiles;
+            fb = c_begin / su;
+            fu = fb * su;
+            fq = fb * n0;
+        } else if (has) {  // the sequence whose units hold c_begin
             int u_base = 0, q_base = 0;
             has = 0;
 #pragma unroll 1
@@ -365,8 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (lane == 0) {
-            start->has_work = has;
+            start->has_work = has || (valid_q && waves.waves > 0);
             start->rg = rg;
+            start->waves = waves;
+            start->unit = start->end = 0;  // no range of the cut unless set below
             if (has) {
                 const TcSeq w = tc_seq(P.seq_lens[fb], P.q_lens[fb], P.G, P.Hkv, P.max_q_len, P.max_pages, P.min_rows);
                 const int off = c_begin - fu;
@@ -654,7 +700,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 write_q(nx, rn);
             }
             if (rm.rf == 1) {
-                if (rm.warp_valid) {  // epilogue with one copy per row: fp32 partial (O, m, l) of this row
+                if (rm.warp_valid && pc.whole) {  // a whole segment: this row's bf16 output
+                    const int64_t orow = static_cast<int64_t>(rm.token) * P.Hq + pc.g * P.G + rm.hl;
+                    const float inv = lsum > 0.f ? __frcp_rn(lsum) : 0.f;
+#pragma unroll
+                    for (int c = 0; c < kHeadDim / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(tmem_o + lane_base + c * 32, o);
+                        if (rm.valid) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(P.out + orow * kHeadDim + c * 32);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                dst[k] = make_uint4(pack_bf16x2(o[8 * k] * inv, o[8 * k + 1] * inv),
+                                                    pack_bf16x2(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
+                                                    pack_bf16x2(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
+                                                    pack_bf16x2(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
+                        }
+                    }
+                } else if (rm.warp_valid) {  // epilogue with one copy per row: fp32 partial (O, m, l) of this row
                     const int64_t orow = static_cast<int64_t>(rm.token) * P.Hq + pc.g * P.G + rm.hl;
                     const int64_t wi = static_cast<int64_t>(rm.slot) * P.n_rows_total + orow;
 #pragma unroll
@@ -746,7 +809,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 4) {
         // ================= TMA producer
         if (lane == 0) {
-            const uint64_t policy = P.seq_mode ? l2_policy_evict_first() : l2_policy_evict_last();  // plan: row tiles re-read
+            // plan mode: the row tiles of a chunk re-read its tiles; waves: the
+            // CTAs of a wave re-read each other's tiles; otherwise a tile is read
+            // by one CTA
+            const uint64_t policy = !P.seq_mode             ? l2_policy_evict_last()
+                                    : start->waves.waves > 0 ? l2_policy_evict_normal()
+                                                             : l2_policy_evict_first();
             int i = 0;
             bool ok = true;
             TcCursor cur;
@@ -914,7 +982,7 @@ cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t
                           const CUtensorMap &tmk, const CUtensorMap &tmv, float scale,
                           float *ws_acc, float *ws_ml, int64_t rows_total, int32_t *err,
                           const int32_t *block_table, const int32_t *seq_lens,
-                          const int32_t *q_lens, cudaStream_t stream) {
+                          const int32_t *q_lens, uint16_t *out, cudaStream_t stream) {
     static cudaError_t attr = cudaFuncSetAttribute(prefix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    kSmemBytes);
     if (attr != cudaSuccess) return attr;
@@ -930,6 +998,7 @@ cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t
     p.min_rows = c.min_rows;
     p.ws_acc = ws_acc;
     p.ws_ml = ws_ml;
+    p.out = out;
     p.err = err;
     p.Hq = d.num_q_heads;
     p.Hkv = d.num_kv_heads;

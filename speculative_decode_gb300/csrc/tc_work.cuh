@@ -52,4 +52,32 @@ __device__ __forceinline__ TcRanges make_tc_ranges(int total, int W, int max_til
     return TcRanges{C_min, 0};
 }
 
+// Waves of whole segments, for batches whose sequences all have the same
+// length and query count (chunked prefill) and at least two segments per
+// CTA: CTA c takes segments c, c + W, c + 2 W, ... (W CTAs) for `waves`
+// waves, so that the CTAs running at the same time hold the row tiles of the
+// same few (sequence, KV head) pairs and walk the same K/V tiles together
+// (each tile comes from DRAM once and from L2 for the others); the segments
+// left over are cut evenly between all CTAs as above, so that every CTA ends
+// at the same time. `base` is the units of the waves (the cut's units are
+// counted from there). A CTA writes the output of a segment it attends whole
+// itself, from one copy of each row: so every row tile must hold more than
+// 32 of the `rows` query rows per KV head (fewer are held four times).
+struct TcWaves {
+    int waves, seg_per_seq, base;
+};
+
+__device__ __forceinline__ TcWaves make_tc_waves(bool uniform, int B, const TcSeq &w, int Hkv, int W, int rows) {
+    TcWaves v{0, 0, 0};
+    if (!uniform || w.units == 0) return v;
+    if (rows - (w.mtiles - 1) * kTcRowTile <= 32) return v;
+    const int seg_per_seq = Hkv * w.mtiles;
+    const long long nseg = static_cast<long long>(B) * seg_per_seq;
+    if (nseg < 2LL * W) return v;
+    v.waves = static_cast<int>(nseg / W) - 1;
+    v.seg_per_seq = seg_per_seq;
+    v.base = v.waves * W * w.tiles;
+    return v;
+}
+
 }  // namespace sa

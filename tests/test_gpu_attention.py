@@ -76,6 +76,22 @@ def test_prefill_chunk_workload_sampled_rows():
     assert_attention_close(out[tok, hd], ref, "prefill chunk")
 
 
+@pytest.mark.parametrize("chunk,waves", [(256, True), (264, False)])
+def test_uniform_prefill_batch_all_rows(chunk, waves):
+    """A batch of equal sequences with enough row tiles for whole-segment
+    waves on the tensor cores (20 sequences x 2 KV heads x 8 row tiles of 128
+    = 320 segments for 152 CTAs: one wave attended whole, written by the
+    tensor-core kernel, the rest cut evenly and merged by the combine pass);
+    with 264 new tokens the last row tile of each segment holds 32 rows and
+    the batch takes the plain cut instead. Every row against the oracle."""
+    w = wl.prefill_chunk(seed=1150 + chunk, num_seqs=20, cached=300, chunk=chunk, Hq=8, Hkv=2)
+    rows = 4 * chunk
+    assert (rows - (rows - 1) // 128 * 128 > 32) == waves
+    out, err, _, _ = run_attention(w)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w), f"chunk {chunk}")
+
+
 def test_kv_append_bit_exact():
     w = wl.random_case(31, num_seqs=5, Hq=8, Hkv=4, max_ctx=900, q_len_choices=(0, 1, 5, 16))
     _, err, kp, vp = run_attention(w)
