@@ -183,6 +183,18 @@ CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void 
               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+CUresult encode_tensor_map_3d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, const uint64_t dims[3],
+                              const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle) {
+    EncodeFn fn = encode_fn();
+    if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t gd[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t gs[2] = {strides_bytes[0], strides_bytes[1]};
+    const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, dtype, 3, base, gd, gs, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 // Tensor maps of the persistent kernel for one pair of pools: bf16 pages
 // (bits 16: rows of 128 values, boxes of 64 columns with 128-byte swizzle),
 // int8 codes (bits 8: rows of 128 bytes, 128-byte swizzle) or int4 codes

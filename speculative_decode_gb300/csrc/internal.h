@@ -164,6 +164,10 @@ cudaError_t launch_verify(const VerifyParams &p, cudaStream_t stream);
 CUresult encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base,
                               uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
                               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+// A 3-D tiled map: dims innermost first, byte strides of dims 1 and 2, box
+// extents, no interleave, zero fill outside the tensor.
+CUresult encode_tensor_map_3d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, const uint64_t dims[3],
+                              const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle);
 
 int device_sm_count();
 

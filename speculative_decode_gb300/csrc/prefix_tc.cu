@@ -13,16 +13,19 @@
 // and stores, per row, an fp32 partial (O, m, l) that the combine kernel merges
 // with the rest of the sequence's keys.
 //
-// CTA = 7 warps: warps 0-3 softmax and epilogue (thread t owns tensor-memory
-// lane t), warp 4 the TMA producer, warp 5 allocates tensor memory and issues
-// Q K^T, warp 6 issues P V (one thread each). K/V tiles of 64 keys
+// CTA = 11 warps: warps 0-7 softmax and epilogue, two per tensor-memory lane
+// quadrant (warp w reads lanes [32 (w % 4), +32), the same scheduler's lanes
+// for both), which take alternate K/V tiles of a piece, each with its own
+// running max and O buffer, merged at the piece's end; warp 8 the TMA
+// producer, warp 9 allocates tensor memory and issues Q K^T, warp 10 issues
+// P V (one thread each). K/V tiles of 64 keys
 // (32 KiB) stream through five stages, so four loads are in flight while a
-// tile is consumed; S (tensor memory, three buffers) and P (shared memory, two)
-// are multi-buffered, so Q K^T runs up to two tiles ahead and P V of the
-// previous tile runs on the tensor cores while the softmax of the current tile
-// runs on the CUDA cores. With at most 32 query rows (q_len = k+1
+// tile is consumed; S (tensor memory, three buffers) and P (shared memory, two,
+// one per half) are multi-buffered, so Q K^T runs up to two tiles ahead and
+// P V of one half's tile runs on the tensor cores while the other half's
+// softmax runs on the CUDA cores. With at most 32 query rows (q_len = k+1
 // verification of one sequence) every row is held four times and each copy's
-// softmax takes a quarter of a tile's keys. Operands sit in shared
+// softmax (warps 0-3) takes a quarter of a tile's keys. Operands sit in shared
 // memory in the 128-byte-swizzled K-major layout the TMA writes (Q, K and P)
 // or the MN-major one (V), described to the tensor core by shared-memory
 // matrix descriptors. Every wait is bounded; on timeout the CTA flags
@@ -49,18 +52,25 @@ constexpr int kKVStage = 4 * kKVBlk;          // K (2 blocks) + V (2 blocks) = 3
 constexpr int kStagesTC = 5;                  // K/V stages
 constexpr int kSBufs = 3;                     // S buffers: Q K^T runs up to two tiles ahead of the softmax
 constexpr int kTmemCols = 512;                // S buffers: columns 0 .. 3*64-1, two O buffers: the next 2*128
-constexpr int kThreads = 224;
+// softmax / epilogue warps (4 or 8), then the TMA producer, the Q K^T issuer
+// (which also holds the tensor memory) and the P V issuer
+constexpr int tc_threads(int soft_warps) { return (soft_warps + 3) * 32; }
 
 constexpr int kOffQ = 0;
 constexpr int kOffP = kOffQ + kQBytes;
 constexpr int kOffKV = kOffP + 2 * kPBytes;
 constexpr int kOffBar = kOffKV + kStagesTC * kKVStage;
-constexpr int kOffML = kOffBar + 256;             // epilogue: (max, sum) of the 128 lanes
+constexpr int kOffML = kOffBar + 320;             // epilogue of four copies: (max, sum) of the 128 lanes
 constexpr int kOffStart = kOffML + kM * 2 * 4;    // sequence mode: where this CTA's range starts
 constexpr int kSmemBytes = kOffStart + 128 + 1024;  // + alignment slack
 
 static_assert(kN == kTcKeyTile && kM == kTcRowTile, "tile shapes shared with the combine pass");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
+// barriers: K/V full and empty, Q, S full and free, P full and free, O free,
+// all MMAs done, the tensor-memory address and abort flag, four exchanges, P V
+// done, Q loaded by TMA, Q read by the piece's Q K^T
+static_assert((2 * kStagesTC + 1 + 2 * kSBufs + 2 + 2 + 2 + 1 + 2 + 4 + 1 + 2) * 8 <= kOffML - kOffBar, "barrier space");
+static_assert(kOffML + 2 * kM * 4 <= kOffStart, "the (max, sum) pairs of the copies' epilogue fit their space");
 
 // ------------------------------------------------------------ tcgen05 helpers
 // Shared-memory matrix descriptor: start address, leading / stride byte
@@ -184,6 +194,16 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float *v) {
     for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 3-D tiled TMA load (coordinates innermost first) completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t x, int32_t y,
+                                            int32_t z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 struct PrefixParams {
     const uint16_t *q;
     const int32_t *block_table;
@@ -202,6 +222,7 @@ struct PrefixParams {
     int32_t Hq, Hkv, G, max_pages, num_pages;
     int64_t n_rows_total;
     float qscale;  // scale * log2(e)
+    int32_t q_tma;  // sequence mode: pieces held once per row load Q by TMA (3-D map: d, head, token)
 };
 
 // A piece: the tiles of one segment that this CTA attends.
@@ -306,9 +327,94 @@ struct TcCursor {
     }
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Epilogue of a piece held four times (sequence mode, at most 32 rows; run
+// by the four warps of half 0, thread t on tensor-memory lane t, with o_lane
+// its lane's O address): in two halves of 64 columns staged in the P
+// buffers (idle until the next piece's softmax), every lane stages its half
+// row, then thread t merges 16 columns of row t % 32 over the copies and
+// writes the row's fp32 partial.
+__device__ __forceinline__ void merge_copies(uint8_t *smem, int t, int rpc, const TcPiece &pc, uint32_t o_lane,
+                                          float m_ref, float lsum, float *ws_acc, float *ws_ml,
+                                          int64_t n_rows_total, int Hq, int G) {
+    float *ost = reinterpret_cast<float *>(smem + kOffP);  // [128 lanes][64], 16-byte chunks xor-swizzled
+    float *mls = reinterpret_cast<float *>(smem + kOffML);
+    mls[2 * t] = m_ref;
+    mls[2 * t + 1] = lsum;
+    const int rl = t % rpc, q4 = t / rpc;
+    const int rr = pc.row0 + rl;
+    float M = -INFINITY, L = 0.f, wgt[4];
+    int64_t wi = 0;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float o[32];
+            tmem_ld32(o_lane + h * 64 + c * 32, o);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<float4 *>(ost + t * 64 + (((c * 8 + k) ^ (t & 7)) * 4)) =
+                    make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four warps of half 0 only
+        if (rr < pc.row_count) {
+            if (h == 0) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (mls[2 * (c * rpc + rl) + 1] > 0.f) M = fmaxf(M, mls[2 * (c * rpc + rl)]);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float lc = mls[2 * (c * rpc + rl) + 1];
+                    wgt[c] = lc > 0.f ? exp2f(mls[2 * (c * rpc + rl)] - M) : 0.f;
+                    L += lc * wgt[c];
+                }
+                const int64_t tk = pc.qstart + rr / G;
+                wi = static_cast<int64_t>(pc.slot) * n_rows_total + tk * Hq + pc.g * G + rr % G;
+                if (q4 == 0) *reinterpret_cast<float2 *>(ws_ml + wi * 2) = make_float2(M, L);
+            }
+            float4 o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (wgt[c] > 0.f) {
+                    const int ln = c * rpc + rl;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 v = *reinterpret_cast<const float4 *>(ost + ln * 64 + (((q4 * 4 + k) ^ (ln & 7)) * 4));
+                        o[k].x += v.x * wgt[c];
+                        o[k].y += v.y * wgt[c];
+                        o[k].z += v.z * wgt[c];
+                        o[k].w += v.w * wgt[c];
+                    }
+                }
+            }
+            float4 *dst = reinterpret_cast<float4 *>(ws_acc + wi * kHeadDim + h * 64 + q4 * 16);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) dst[k] = o[k];
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // staging read before it is rewritten
+    }
+}
+
+// The same, out of line: with eight softmax warps (168 registers a thread)
+// its registers would otherwise weigh on the softmax loop.
+__device__ __noinline__ void merge_copies_call(uint8_t *smem, int t, int rpc, const TcPiece &pc, uint32_t o_lane,
+                                               float m_ref, float lsum, float *ws_acc, float *ws_ml,
+                                               int64_t n_rows_total, int Hq, int G) {
+    merge_copies(smem, t, rpc, pc, o_lane, m_ref, lsum, ws_acc, ws_ml, n_rows_total, Hq, G);
+}
+
+template <int kSoftWarps>
+__global__ void __launch_bounds__(tc_threads(kSoftWarps), 1)
     prefix_tc_kernel(const PrefixParams P, const __grid_constant__ CUtensorMap tmk,
-                     const __grid_constant__ CUtensorMap tmv) {
+                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmq) {
+    constexpr int kSoft = kSoftWarps * 32;
+    constexpr int kWarpTMA = kSoftWarps, kWarpQK = kSoftWarps + 1;
+    // with eight softmax warps the two of a lane quadrant take alternate tiles
+    // of a piece held once per row, each into its own O buffer; with four, O is
+    // double-buffered by piece (an epilogue overlaps the next piece's P V)
+    constexpr bool kTwo = kSoftWarps == 8;
+    static_assert(kSoftWarps == 4 || kSoftWarps == 8, "one or two softmax warps per lane quadrant");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -319,11 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *s_full = q_full + 1;              // [kSBufs] S buffer holds Q K^T of a tile
     uint64_t *p_full = s_full + kSBufs;         // [2] P buffer written (and its S buffer read)
     uint64_t *p_free = p_full + 2;              // [2] P V of that buffer finished (O up to date with it)
-    uint64_t *o_free = p_free + 2;              // [2] O buffer read by its piece's epilogue
+    uint64_t *o_free = p_free + 2;              // [2] piece p's epilogue read the O buffers: o_free[p & 1]
     uint64_t *s_free = o_free + 2;              // [kSBufs] S buffer read by the softmax
     uint64_t *mma_done = s_free + kSBufs;       // every MMA of both issuers finished
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(mma_done + 1);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(mma_done + 2);
+    uint64_t *xbar = mma_done + 3;              // [4] both halves of a lane quadrant posted (max, sum)
+    uint64_t *pv_done = mma_done + 7;           // every P V of a piece finished (one phase per piece)
+    uint64_t *q_tma = mma_done + 8;             // Q rows of a piece landed by TMA (one phase per such piece)
+    uint64_t *q_free = mma_done + 9;            // every Q K^T of a piece finished (one phase per piece)
     TcStart *start = reinterpret_cast<TcStart *>(smem + kOffStart);
 
     const int tid = threadIdx.x;
@@ -438,25 +548,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         return cur.next(P, pc);
     };
     auto next_piece = [&](TcCursor &cur, TcPiece &pc) -> bool { return P.seq_mode && cur.next(P, pc); };
+    // a sequence-mode piece held once per row (more than 32 rows) takes its Q
+    // rows as one box of the 3-D map (tokens x G heads x d): the Q K^T issuer
+    // loads it; other pieces' rows are copied by the softmax warps
+    auto q_by_tma = [&](const TcPiece &pc) -> bool {
+        return P.q_tma && P.seq_mode && pc.row_count - pc.row0 > kM / 4;
+    };
 
     if (tid == 0) {
         for (int s = 0; s < kStagesTC; ++s) {
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
-        mbar_init(q_full, kM);
+        mbar_init(q_full, kSoft);
         for (int b = 0; b < kSBufs; ++b) mbar_init(&s_full[b], 1);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&p_full[b], kM);
+            mbar_init(&p_full[b], kM);  // the 128 lanes of the half attending the tile
             mbar_init(&p_free[b], 1);
-            mbar_init(&o_free[b], kM);
+            mbar_init(&o_free[b], kSoft);
         }
         for (int b = 0; b < kSBufs; ++b) mbar_init(&s_free[b], kM);
         mbar_init(mma_done, 2);
+        for (int q = 0; q < 4; ++q) mbar_init(&xbar[q], 64);
+        mbar_init(pv_done, 1);
+        mbar_init(q_tma, 1);
+        mbar_init(q_free, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {  // tensor memory for S and O
+    if (warp == kWarpQK) {  // tensor memory for S and O
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(const_cast<uint32_t *>(tmem_slot))),
                      "r"(kTmemCols)
@@ -467,21 +587,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o0 = tmem + kSBufs * kN;  // S buffers at columns 0, kN, 2 kN; two O buffers after them
+    const uint32_t tmem_o0 = tmem + kSBufs * kN;  // S buffers at columns 0, kN, 2 kN; O buffers A and B after them
 
     const uint32_t sQ = smem_u32(smem + kOffQ), sP = smem_u32(smem + kOffP), sKV = smem_u32(smem + kOffKV);
 
-    if (warp < 4) {
-        // ================= softmax / epilogue warps: thread t owns tensor-memory
-        // lane t. With at most 32 rows in a piece, every row is held by four
-        // lanes, one in each softmax warp (the Q tile holds four copies of the
-        // rows), and copy c takes keys [16c, 16c + 16) of every tile: a warp's
-        // per-tile softmax work is four times smaller. The P rows of a copy are
-        // zero outside its keys, so P V sums each copy's keys into its own lanes
-        // of O, with its own running max; the epilogue merges the four copies.
-        const int t = tid;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    if (warp < kSoftWarps) {
+        // ================= softmax / epilogue warps. Warp w reads tensor-memory
+        // lanes [32 (w % 4), +32) (lane t holds row slot t). In pieces with one
+        // copy per row the two warps of a lane quadrant (the same scheduler)
+        // take alternate tiles: half h = w / 4 attends the piece's tiles
+        // t_lo + h, t_lo + h + 2, ... with its own running max and sum, into
+        // its own O buffer, so that one warp's exponentials overlap the other's
+        // waits; the two halves merge at the end of the piece. With at most 32
+        // rows in a piece, every row is held by four lanes, one in each warp
+        // of half 0 (the Q tile holds four copies of the rows), and copy c
+        // takes keys [16c, 16c + 16) of every tile; half 1 then has no rows.
+        // The P rows of a copy are zero outside its keys, so P V sums each
+        // copy's keys into its own lanes of O, with its own running max; the
+        // epilogue merges the four copies.
+        const int t = (warp & 3) * 32 + lane;
+        const int hf = warp >> 2;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         bool ok = true;
+        uint64_t *xb = &xbar[warp & 3];  // the two halves posted their (max, sum) at a piece's end
+        uint32_t xe = 0;                  // such exchanges so far
         // P buffer b = i & 1 is free again once P V of tile i - 2 has run;
         // that P V is the ((i - 2) >> 1)-th commit on p_free[b]
         auto wait_pv = [&](int j) -> bool {
@@ -513,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m.rpc = kM / m.rf;                                               // rows per copy
             m.cp = t / m.rpc;
             m.r = pc.row0 + t % m.rpc;
-            m.valid = m.r < pc.row_count;
+            m.valid = m.r < pc.row_count && (m.rf == 1 || hf == 0);
             m.warp_valid = __any_sync(0xffffffffu, m.valid);  // warps without rows skip the softmax
             m.token = 0;
             m.hl = 0;
@@ -524,16 +653,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         // the piece's Q rows -> shared memory, 128-byte swizzled K-major (two
         // 64-column blocks), one copy per row group; every Q K^T of the
-        // previous piece has completed. The 128 threads copy the rows together
-        // with 16-byte asynchronous copies (16 threads per row: thread t takes
-        // column chunk t % 16 of rows t / 16 + 8k, for every copy of the row),
-        // all of a thread's copies in flight at once, then wait for them. Lanes
-        // past the piece's rows keep whatever they hold: their S, P and O lanes
-        // are never read for output.
+        // previous piece has completed. The softmax threads copy the rows
+        // together with 16-byte asynchronous copies (16 threads per row:
+        // thread s takes column chunk s % 16 of rows s / 16 + 16k, for every
+        // copy of the row), all of a thread's copies in flight at once, then
+        // wait for them. Lanes past the piece's rows keep whatever they hold:
+        // their S, P and O lanes are never read for output.
         auto write_q = [&](const TcPiece &pc, const RowMap &m) {
             const int nrow = min(m.rpc, pc.row_count - pc.row0);
-            const int c = t & 15;
-            for (int rr = t >> 4; rr < nrow; rr += 8) {
+            const int c = tid & 15;
+            for (int rr = tid >> 4; rr < nrow; rr += kSoft / 16) {
                 int32_t tk, hh, lim, sl;
                 row_of(pc, pc.row0 + rr, tk, hh, lim, sl);
                 const uint16_t *src = P.q + (static_cast<int64_t>(tk) * P.Hq + pc.g * P.G + hh) * kHeadDim + c * 8;
@@ -544,9 +673,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive(q_full);
         };
-        // P rows start each piece at zero in both buffers (a copy writes only
-        // its own keys); every P V of the previous piece has completed
+        // Pieces held four times need their P rows at zero outside each copy's
+        // keys: half 0 clears both buffers before such a piece, when every
+        // P V of the previous piece has completed (with one copy per row, a
+        // valid row writes all its keys and an invalid one feeds only O lanes
+        // that are never read).
         auto zero_p = [&]() {
+            if (hf != 0) return;
 #pragma unroll
             for (int c = 0; c < kN / 8; ++c) {
                 *reinterpret_cast<uint4 *>(smem + kOffP + sw128_offset(t, c)) = make_uint4(0, 0, 0, 0);
@@ -561,22 +694,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         TcPiece pc;
         bool more = first_piece(cur, pc);
         RowMap rm = map_rows(pc);
-        zero_p();
-        write_q(pc, rm);
+        if (rm.rf == 4) zero_p();
+        if (!q_by_tma(pc)) write_q(pc, rm);
         while (more && ok) {
-            const uint32_t tmem_o = tmem_o0 + (p & 1) * kHeadDim;
             float m_ref = -INFINITY, lsum = 0.f;
-            const int i_first = i;
+            bool began = false;  // this lane's O buffer holds a tile of the piece
             auto softmax_tiles = [&](auto kpc_tag) {
-                constexpr int KPC = decltype(kpc_tag)::value;  // keys of a tile this lane's copy takes
-                const int koff = rm.cp * KPC;
+                constexpr int KPC = decltype(kpc_tag)::value;  // keys of a tile this lane takes
+                constexpr bool ONE = KPC == kN;                 // one copy per row
+                constexpr bool ALT = ONE && kTwo;               // ... and the halves alternate tiles
+                const int koff = ONE ? 0 : rm.cp * KPC;
+                const uint32_t tmem_o = kTwo ? tmem_o0 + (ALT ? hf * kHeadDim : 0) : tmem_o0 + (p & 1) * kHeadDim;
+                if (!ONE && hf == 1) {  // four copies: half 0 attends every tile
+                    i += pc.t_hi - pc.t_lo;
+                    return;
+                }
                 for (int tt = pc.t_lo; tt < pc.t_hi && ok; ++tt, ++i) {
+                    if (ALT && ((tt - pc.t_lo) & 1) != hf) continue;  // the other half's tile
                     ok = __all_sync(0xffffffffu, mbar_wait(&s_full[i % kSBufs], (i / kSBufs) & 1));
                     if (!ok) break;
                     tc_fence_after();
                     const int pos0 = pc.pc_lo * kPageSize + tt * kN;
                     uint8_t *pbuf = smem + kOffP + (i & 1) * kPBytes;
                     uint8_t *vstage = smem + kOffKV + (i % kStagesTC) * kKVStage + 2 * kKVBlk;
+                    // keys past the end may hold stale data: their V rows are zeroed
+                    const bool zero_v = t < kN && pos0 + t >= pc.key_end;
                     if (!rm.warp_valid) {
                         tc_fence_before();
                         mbar_arrive(&s_free[i % kSBufs]);
@@ -587,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = wait_pv(i - 2);
                             if (!ok) break;
                         }
-                        if (t < kN && pos0 + t >= pc.key_end) {  // keys past the end may hold stale data: zero their V row
+                        if (zero_v) {
 #pragma unroll
                             for (int c = 0; c < 8; ++c) {
                                 *reinterpret_cast<uint4 *>(vstage + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
@@ -646,13 +788,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pw[k] = pack_bf16x2(ab.x, ab.y);
                     }
                     const float psum = ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
-                    if (i >= 2) {  // P V of tile i - 2 must be done before its P buffer is rewritten
+                    // P V of tile i - 2 must be done before its P buffer is rewritten;
+                    // with alternate tiles it is also the last P V into this half's O
+                    if (i >= 2) {
                         ok = wait_pv(i - 2);
                         if (!ok) break;
                     }
-                    if (i > i_first && __any_sync(0xffffffffu, grow)) {  // O must hold every earlier P V of the piece
-                        ok = wait_pv(i - 1);
-                        if (!ok) break;
+                    if (began && __any_sync(0xffffffffu, grow)) {  // O must hold every earlier P V into it
+                        if (!ALT) {
+                            ok = wait_pv(i - 1);
+                            if (!ok) break;
+                        }
                         tc_fence_after();
 #pragma unroll
                         for (int c = 0; c < kHeadDim / 32; ++c) {
@@ -663,14 +809,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tmem_st32(tmem_o + lane_base + c * 32, o);
                         }
                     }
+                    began = true;
                     lsum = lsum * alpha + psum;
                     m_ref = m_new;
-                    // this copy's keys of P row t -> shared memory (bf16, 128-byte swizzled K-major)
+                    // this lane's keys of P row t -> shared memory (bf16, 128-byte swizzled K-major)
 #pragma unroll
                     for (int c = 0; c < KPC / 8; ++c)
                         *reinterpret_cast<uint4 *>(pbuf + sw128_offset(t, koff / 8 + c)) =
                             make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-                    if (t < kN && pos0 + t >= pc.key_end) {  // keys past the end may hold stale data: zero their V row
+                    if (zero_v) {
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             *reinterpret_cast<uint4 *>(vstage + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
@@ -684,7 +831,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             if (rm.rf == 4) softmax_tiles(std::integral_constant<int, kN / 4>{});
             else softmax_tiles(std::integral_constant<int, kN>{});
-            if (ok && i > i_first) ok = wait_pv(i - 1);  // the piece's last P V (every earlier one before it)
+            // every P V of the piece: a per-piece barrier, since a half may have
+            // skipped the piece's last tiles (a parity wait on p_free is only
+            // sound one phase ahead of what this thread has seen complete)
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(pv_done, p & 1));
+            // One copy per row: the halves trade (max, sum) through the P buffers,
+            // idle now. Half h's next tile goes to buffer (i + h) & 1: each posts
+            // into the buffer its partner writes next and reads from its own, so
+            // that neither post is overwritten before it is read.
+            float m_o = -INFINITY, l_o = 0.f;  // the other half's
+            if (kTwo && ok && rm.rf == 1 && rm.warp_valid) {
+                reinterpret_cast<float2 *>(smem + kOffP + ((i + 1 + hf) & 1) * kPBytes)[t] = make_float2(m_ref, lsum);
+                mbar_arrive(xb);
+                ok = __all_sync(0xffffffffu, mbar_wait(xb, xe & 1));
+                ++xe;
+                const float2 v = reinterpret_cast<const float2 *>(smem + kOffP + ((i + hf) & 1) * kPBytes)[t];
+                m_o = v.x;
+                l_o = v.y;
+            }
             if (!ok) {
                 *abort_flag = 1;
                 if (lane == 0) flag_error(P.err, kErrBitTimeout);
@@ -697,116 +861,83 @@ __global__ void __launch_bounds__(kThreads, 1)
             RowMap rn{};
             if (has_next) {
                 rn = map_rows(nx);
-                write_q(nx, rn);
+                if (!q_by_tma(nx)) write_q(nx, rn);
             }
             if (rm.rf == 1) {
-                if (rm.warp_valid && pc.whole) {  // a whole segment: this row's bf16 output
+                if (rm.warp_valid) {
+                    // the row's two halves (max, sum, O) merged; this half writes
+                    // columns [64 hf, 64 hf + 64). A half's O holds data only once
+                    // it attended a tile (its sum may still be 0 if every key of
+                    // its tiles is masked for the row; its O is then 0).
+                    const float mA = (kTwo && hf == 1) ? m_o : m_ref, lA = (kTwo && hf == 1) ? l_o : lsum;
+                    const float mB = !kTwo ? -INFINITY : hf == 0 ? m_o : m_ref;
+                    const float lB = !kTwo ? 0.f : hf == 0 ? l_o : lsum;
+                    const float M = fmaxf(lA > 0.f ? mA : -INFINITY, lB > 0.f ? mB : -INFINITY);
+                    const float wA = lA > 0.f ? exp2f(mA - M) : 0.f;
+                    const float wB = lB > 0.f ? exp2f(mB - M) : 0.f;
+                    const float L = lA * wA + lB * wB;
                     const int64_t orow = static_cast<int64_t>(rm.token) * P.Hq + pc.g * P.G + rm.hl;
-                    const float inv = lsum > 0.f ? __frcp_rn(lsum) : 0.f;
+                    const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
+                    const int64_t wi = static_cast<int64_t>(rm.slot) * P.n_rows_total + orow;
+                    const uint32_t o_a = kTwo ? tmem_o0 : tmem_o0 + (p & 1) * kHeadDim;
 #pragma unroll
-                    for (int c = 0; c < kHeadDim / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tmem_o + lane_base + c * 32, o);
-                        if (rm.valid) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(P.out + orow * kHeadDim + c * 32);
+                    for (int c = 0; c < (kTwo ? kHeadDim / 64 : kHeadDim / 32); ++c) {
+                        const int col = (kTwo ? hf * (kHeadDim / 2) : 0) + c * 32;
+                        float oa[32];
+                        tmem_ld32(o_a + lane_base + col, oa);
+                        if constexpr (kTwo) {
+                            float ob[32];
+                            tmem_ld32(tmem_o0 + kHeadDim + lane_base + col, ob);
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) oa[k] = wB > 0.f ? fmaf(ob[k], wB, oa[k] * wA) : oa[k] * wA;
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) oa[k] *= wA;
+                        }
+                        if (rm.valid && pc.whole) {  // a whole segment: this row's bf16 output
+                            uint4 *dst = reinterpret_cast<uint4 *>(P.out + orow * kHeadDim + col);
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                dst[k] = make_uint4(pack_bf16x2(o[8 * k] * inv, o[8 * k + 1] * inv),
-                                                    pack_bf16x2(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
-                                                    pack_bf16x2(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
-                                                    pack_bf16x2(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
+                                dst[k] = make_uint4(pack_bf16x2(oa[8 * k] * inv, oa[8 * k + 1] * inv),
+                                                    pack_bf16x2(oa[8 * k + 2] * inv, oa[8 * k + 3] * inv),
+                                                    pack_bf16x2(oa[8 * k + 4] * inv, oa[8 * k + 5] * inv),
+                                                    pack_bf16x2(oa[8 * k + 6] * inv, oa[8 * k + 7] * inv));
+                        } else if (rm.valid) {  // fp32 partial (O, m, l) of this row
+                            float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + col);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) dst[k] = make_float4(oa[4 * k], oa[4 * k + 1], oa[4 * k + 2], oa[4 * k + 3]);
                         }
                     }
-                } else if (rm.warp_valid) {  // epilogue with one copy per row: fp32 partial (O, m, l) of this row
-                    const int64_t orow = static_cast<int64_t>(rm.token) * P.Hq + pc.g * P.G + rm.hl;
-                    const int64_t wi = static_cast<int64_t>(rm.slot) * P.n_rows_total + orow;
-#pragma unroll
-                    for (int c = 0; c < kHeadDim / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tmem_o + lane_base + c * 32, o);
-                        if (rm.valid) {
-                            float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + c * 32);
-#pragma unroll
-                            for (int k = 0; k < 8; ++k) dst[k] = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                        }
-                    }
-                    if (rm.valid) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(m_ref, lsum);
+                    if (rm.valid && !pc.whole && hf == 0) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(M, L);
                 }
-            } else {
-                // epilogue with four copies, in two halves of 64 columns staged
-                // in the P buffers (idle until the next piece's softmax): every
-                // lane stages its half row, then thread t merges 16 columns of
-                // row t % 32 over the copies. Every softmax warp reaches the
-                // barriers.
-                float *ost = reinterpret_cast<float *>(smem + kOffP);  // [128 lanes][64], 16-byte chunks xor-swizzled
-                float *mls = reinterpret_cast<float *>(smem + kOffML);
-                mls[2 * t] = m_ref;
-                mls[2 * t + 1] = lsum;
-                const int rl = t % rm.rpc, q4 = t / rm.rpc;
-                const int rr = pc.row0 + rl;
-                float M = -INFINITY, L = 0.f, wgt[4];
-                int64_t wi = 0;
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        float o[32];
-                        tmem_ld32(tmem_o + lane_base + h * 64 + c * 32, o);
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            *reinterpret_cast<float4 *>(ost + t * 64 + (((c * 8 + k) ^ (t & 7)) * 4)) =
-                                make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
-                    }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps only
-                    if (rr < pc.row_count) {
-                        if (h == 0) {
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                if (mls[2 * (c * rm.rpc + rl) + 1] > 0.f) M = fmaxf(M, mls[2 * (c * rm.rpc + rl)]);
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                const float lc = mls[2 * (c * rm.rpc + rl) + 1];
-                                wgt[c] = lc > 0.f ? exp2f(mls[2 * (c * rm.rpc + rl)] - M) : 0.f;
-                                L += lc * wgt[c];
-                            }
-                            int32_t tk, hh, lim, sl;
-                            row_of(pc, rr, tk, hh, lim, sl);
-                            wi = static_cast<int64_t>(sl) * P.n_rows_total + static_cast<int64_t>(tk) * P.Hq + pc.g * P.G + hh;
-                            if (q4 == 0) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(M, L);
-                        }
-                        float4 o[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            if (wgt[c] > 0.f) {
-                                const int ln = c * rm.rpc + rl;
-#pragma unroll
-                                for (int k = 0; k < 4; ++k) {
-                                    const float4 v = *reinterpret_cast<const float4 *>(ost + ln * 64 + (((q4 * 4 + k) ^ (ln & 7)) * 4));
-                                    o[k].x += v.x * wgt[c];
-                                    o[k].y += v.y * wgt[c];
-                                    o[k].z += v.z * wgt[c];
-                                    o[k].w += v.w * wgt[c];
-                                }
-                            }
-                        }
-                        float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + h * 64 + q4 * 16);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) dst[k] = o[k];
-                    }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");  // staging read before it is rewritten
-                }
+            } else if (hf == 0) {
+                if constexpr (kTwo)
+                    merge_copies_call(smem, t, rm.rpc, pc, tmem_o0 + lane_base, m_ref, lsum, P.ws_acc, P.ws_ml,
+                                      P.n_rows_total, P.Hq, P.G);
+                else
+                    merge_copies(smem, t, rm.rpc, pc, tmem_o0 + (p & 1) * kHeadDim + lane_base, m_ref, lsum, P.ws_acc,
+                                 P.ws_ml, P.n_rows_total, P.Hq, P.G);
             }
             tc_fence_before();
-            mbar_arrive(&o_free[p & 1]);  // this piece's O buffer may be overwritten
+            mbar_arrive(&o_free[p & 1]);  // this piece's O buffers may be overwritten
+            if (kTwo && ((rm.rf == 4 && hf == 1) || (has_next && rn.rf == 4 && hf == 0))) {
+                // half 1 waits for half 0's staged epilogue (it uses the P buffers
+                // and the (max, sum) space) before the next piece; half 0 clears both
+                // P buffers for a piece held four times once half 1 has read its post
+                ok = __all_sync(0xffffffffu, mbar_wait(&o_free[p & 1], (p >> 1) & 1));
+                if (!ok) {
+                    *abort_flag = 1;
+                    if (lane == 0) flag_error(P.err, kErrBitTimeout);
+                    break;
+                }
+            }
             if (!has_next) break;
-            zero_p();
+            if (rn.rf == 4) zero_p();
             pc = nx;
             rm = rn;
             ++p;
         }
-    } else if (warp == 4) {
+    } else if (warp == kWarpTMA) {
         // ================= TMA producer
         if (lane == 0) {
             // plan mode: the row tiles of a chunk re-read its tiles; waves: the
@@ -862,7 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = i - kStagesTC < 0 ? 0 : i - kStagesTC; k < i; ++k)
                 (void)mbar_wait(&kv_full[k % kStagesTC], (k / kStagesTC) & 1);
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpQK) {
         // ================= Q K^T issuer (one thread): tile qk into S buffer
         // qk % kSBufs once its K has landed and the softmax has read that
         // buffer's previous tile, so Q K^T runs up to kSBufs tiles ahead of
@@ -874,11 +1005,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdQK = idesc_bf16(false, kN);
             const uint64_t dQ = smem_desc(sQ, 16, 1024), dK = smem_desc(sKV, 16, 1024);
             bool ok = true;
-            int qk = 0, p = 0;
+            int qk = 0, p = 0, n_tma = 0, n_copy = 0;
+            const uint64_t q_policy = l2_policy_evict_first();
             TcCursor cur;
             TcPiece pc;
             for (bool more = first_piece(cur, pc); more && ok; more = next_piece(cur, pc), ++p) {
-                ok = mbar_wait(q_full, p & 1);  // this piece's Q rows
+                if (q_by_tma(pc)) {  // the rows by TMA, once every Q K^T of the previous piece has read Q
+                    if (p >= 1) ok = mbar_wait(q_free, (p - 1) & 1);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(q_tma, kQBytes);
+                    const int y = pc.g * P.G, z = pc.qstart + pc.row0 / P.G;
+                    tma_load_3d(smem + kOffQ, &tmq, q_tma, 0, y, z, q_policy);
+                    tma_load_3d(smem + kOffQ + kRowBlk, &tmq, q_tma, 64, y, z, q_policy);
+                    ok = mbar_wait(q_tma, n_tma++ & 1);
+                } else {  // the rows copied by the softmax warps
+                    ok = mbar_wait(q_full, n_copy++ & 1);
+                }
                 if (!ok) break;
                 tc_fence_after();
                 for (int tt = pc.t_lo; ok && tt < pc.t_hi; ++tt, ++qk) {
@@ -895,6 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  dKs + (((k >> 2) * kKVBlk + (k & 3) * 32) >> 4), kIdQK, k > 0);
                     mma_commit(&s_full[qk % kSBufs]);
                 }
+                if (ok) mma_commit(q_free);  // the piece's last Q K^T
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -904,8 +1047,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ================= P V issuer (one thread): tile j once the softmax has
-        // written P(j), into the O buffer of its piece (overwriting it on the
-        // piece's first tile, after the epilogue of the piece two back read it).
+        // written P(j). With one copy per row, the tiles alternate between O
+        // buffers A and B (the halves' own); with four copies all go to A. The
+        // first tile of a piece into each buffer overwrites it, after the
+        // epilogue of the previous piece has read both.
         if (lane == 0) {
             constexpr uint32_t kIdPV = idesc_bf16(true, kHeadDim);
             const uint64_t dP = smem_desc(sP, 16, 1024), dV = smem_desc(sKV + 2 * kKVBlk, kKVBlk, 1024);
@@ -914,24 +1059,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             TcCursor cur;
             TcPiece pc;
             for (bool more = first_piece(cur, pc); more && ok; more = next_piece(cur, pc), ++p) {
-                const uint32_t tmem_o = tmem_o0 + (p & 1) * kHeadDim;
+                const bool alt = kTwo && !(P.seq_mode && pc.row_count - pc.row0 <= kM / 4);
                 const int j0 = j;
                 for (int tt = pc.t_lo; ok && tt < pc.t_hi; ++tt, ++j) {
-                    if (j == j0 && p >= 2) {  // the epilogue of piece p - 2 has read this O buffer
-                        ok = mbar_wait(&o_free[p & 1], ((p - 2) >> 1) & 1);
+                    // the epilogue of the piece that last used this O buffer has read it:
+                    // piece p - 1 with the halves' buffers, p - 2 with buffers by piece
+                    constexpr int kBack = kTwo ? 1 : 2;
+                    if (j == j0 && p >= kBack) {
+                        ok = mbar_wait(&o_free[(p - kBack) & 1], ((p - kBack) >> 1) & 1);
                         if (!ok) break;
                     }
                     ok = mbar_wait(&p_full[j & 1], (j >> 1) & 1);
                     if (!ok) break;
                     tc_fence_after();
+                    const int k = j - j0;
+                    const uint32_t d_o = kTwo ? tmem_o0 + (alt ? (k & 1) * kHeadDim : 0) : tmem_o0 + (p & 1) * kHeadDim;
+                    const bool first = alt ? k < 2 : k < 1;
                     const uint64_t dVs = dV + (((j % kStagesTC) * kKVStage) >> 4);
                     const uint64_t dPj = dP + (((j & 1) * kPBytes) >> 4);
 #pragma unroll
-                    for (int k = 0; k < kN / 16; ++k)
-                        mma_bf16(tmem_o, dPj + ((k * 32) >> 4), dVs + ((k * 16 * 128) >> 4), kIdPV, j > j0 || k > 0);
+                    for (int kk = 0; kk < kN / 16; ++kk)
+                        mma_bf16(d_o, dPj + ((kk * 32) >> 4), dVs + ((kk * 16 * 128) >> 4), kIdPV, !first || kk > 0);
                     mma_commit(&kv_empty[j % kStagesTC]);
                     mma_commit(&p_free[j & 1]);
                 }
+                if (ok) mma_commit(pv_done);  // the piece's last P V
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -940,13 +1092,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(mma_done);
         }
     }
-    if (warp == 5 && lane == 0) (void)mbar_wait(mma_done, 0);
+    if (warp == kWarpQK && lane == 0) (void)mbar_wait(mma_done, 0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) {
+    if (warp == kWarpQK) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
+}
+
+// the shared-memory opt-in of both kernel instances, once
+cudaError_t tc_attributes() {
+    static const cudaError_t e = [] {
+        cudaError_t r = cudaFuncSetAttribute(prefix_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(prefix_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        return r;
+    }();
+    return e;
 }
 
 }  // namespace
@@ -955,9 +1118,7 @@ cudaError_t launch_prefix_tc(const sa_dims &d, const PlanDevice &pd, const uint1
                              const CUtensorMap &tmk, const CUtensorMap &tmv, float scale,
                              float *ws_acc, float *ws_ml, int64_t rows_total, int32_t *err,
                              const int32_t *block_table, cudaStream_t stream) {
-    static cudaError_t attr = cudaFuncSetAttribute(prefix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   kSmemBytes);
-    if (attr != cudaSuccess) return attr;
+    if (const cudaError_t e = tc_attributes(); e != cudaSuccess) return e;
     PrefixParams p{};
     p.q = q;
     p.block_table = block_table;
@@ -974,7 +1135,8 @@ cudaError_t launch_prefix_tc(const sa_dims &d, const PlanDevice &pd, const uint1
     p.num_pages = d.num_pages;
     p.n_rows_total = rows_total;
     p.qscale = scale * 1.4426950408889634f;
-    prefix_tc_kernel<<<pd.num_tiles, kThreads, kSmemBytes, stream>>>(p, tmk, tmv);
+    // a plan's rows are held once: two softmax warps per lane quadrant
+    prefix_tc_kernel<8><<<pd.num_tiles, tc_threads(8), kSmemBytes, stream>>>(p, tmk, tmv, tmk);  // no Q map
     return cudaGetLastError();
 }
 
@@ -983,9 +1145,7 @@ cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t
                           float *ws_acc, float *ws_ml, int64_t rows_total, int32_t *err,
                           const int32_t *block_table, const int32_t *seq_lens,
                           const int32_t *q_lens, uint16_t *out, cudaStream_t stream) {
-    static cudaError_t attr = cudaFuncSetAttribute(prefix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   kSmemBytes);
-    if (attr != cudaSuccess) return attr;
+    if (const cudaError_t e = tc_attributes(); e != cudaSuccess) return e;
     PrefixParams p{};
     p.q = q;
     p.block_table = block_table;
@@ -1008,8 +1168,26 @@ cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t
     p.n_rows_total = rows_total;
     p.qscale = scale * 1.4426950408889634f;
     if (d.num_seqs == 0 || c.grid <= 0) return cudaSuccess;
-    // persistent: one CTA per SM, each walks its range of the tile sequence
-    prefix_tc_kernel<<<static_cast<unsigned>(c.grid), kThreads, kSmemBytes, stream>>>(p, tmk, tmv);
+    // Q as a 3-D map (d, head, token): a piece's 128 rows of one KV head are
+    // 128 / G tokens x its G heads, one box per 64 columns
+    CUtensorMap tmq = tmk;
+    if (kM % p.G == 0 && d.total_q > 0) {
+        const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(d.num_q_heads),
+                                  static_cast<uint64_t>(d.total_q)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(kHeadDim) * 2,
+                                     static_cast<uint64_t>(d.num_q_heads) * kHeadDim * 2};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(p.G), static_cast<uint32_t>(kM / p.G)};
+        p.q_tma = encode_tensor_map_3d(&tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(q), dims, strides,
+                                       box, CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
+        if (!p.q_tma) tmq = tmk;
+    }
+    // persistent: one CTA per SM, each walks its range of the tile sequence.
+    // Pieces of at most 32 rows (every row held four times) keep half 1 idle,
+    // so such batches take four softmax warps (and their registers)
+    if (p.G * d.max_q_len > kM / 4)
+        prefix_tc_kernel<8><<<static_cast<unsigned>(c.grid), tc_threads(8), kSmemBytes, stream>>>(p, tmk, tmv, tmq);
+    else
+        prefix_tc_kernel<4><<<static_cast<unsigned>(c.grid), tc_threads(4), kSmemBytes, stream>>>(p, tmk, tmv, tmq);
     return cudaGetLastError();
 }
 
