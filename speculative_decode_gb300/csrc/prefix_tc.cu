@@ -697,6 +697,9 @@ __global__ void __launch_bounds__(tc_threads(kSoftWarps), 1)
         if (rm.rf == 4) zero_p();
         if (!q_by_tma(pc)) write_q(pc, rm);
         while (more && ok) {
+            // the next piece, found now: its lengths load while this piece's tiles run
+            TcPiece nx{};
+            const bool has_next = next_piece(cur, nx);
             float m_ref = -INFINITY, lsum = 0.f;
             bool began = false;  // this lane's O buffer holds a tile of the piece
             auto softmax_tiles = [&](auto kpc_tag) {
@@ -856,8 +859,6 @@ __global__ void __launch_bounds__(tc_threads(kSoftWarps), 1)
             }
             tc_fence_after();
             // the next piece's queries first, so that its Q K^T runs during this epilogue
-            TcPiece nx{};
-            const bool has_next = next_piece(cur, nx);
             RowMap rn{};
             if (has_next) {
                 rn = map_rows(nx);
