@@ -524,10 +524,13 @@ __global__ void __launch_bounds__(32, 1) split_attn_kernel(const SplitParams P) 
     // grid dependency wait below reads only lengths and block tables, which
     // kv_append does not write; queries and pages are read after the wait.
     // After a tensor-core kernel of this call (which started once the pages
-    // were complete and writes only partials), pages are read at once. Every
-    // warp waits before it exits, so this grid completes after its
-    // predecessor and the combine pass sees the tensor-core partials.
+    // were complete and writes only partials), pages are read at once, and
+    // CTA 0 alone waits for that kernel before it exits: this grid then
+    // completes after its predecessor (the combine pass sees the tensor-core
+    // partials), while every other CTA leaves as soon as its range is done,
+    // so that the SMs the tensor-core kernel leaves free keep taking new CTAs.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const bool exit_wait = !P.pages_ready || blockIdx.x == 0;
 
     // ---- 1. total work and this warp's range [g_begin, g_end) of tiles
     WorkScan sc;
@@ -542,7 +545,7 @@ __global__ void __launch_bounds__(32, 1) split_attn_kernel(const SplitParams P) 
     const int g_end = min(sc.total, rg.begin(blockIdx.x + 1));
     __syncwarp();
     if (g_begin >= g_end) {
-        grid_dependency_wait();
+        if (exit_wait) grid_dependency_wait();
         return;
     }
 
@@ -957,7 +960,7 @@ __global__ void __launch_bounds__(32, 1) split_attn_kernel(const SplitParams P) 
         }
         __syncwarp();
     }
-    if (P.pages_ready) grid_dependency_wait();  // every warp waits before it exits
+    if (P.pages_ready && blockIdx.x == 0) grid_dependency_wait();  // see exit_wait above
 }
 
 // Pieces the tensor-core sequence mode cut segment (bt, kvh, mt) into: a scan
