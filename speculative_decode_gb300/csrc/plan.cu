@@ -164,6 +164,17 @@ PlanHost build_plan(const sa_dims &d, const int32_t *bt, const int32_t *seq_lens
         P.run_slots[b] = next;
         P.max_run_slots = std::max(P.max_run_slots, next);
     }
+    // the first token of rows [first, first + min(n, 128)) if row k of them is
+    // token first_token + k / G with head k % G, else -1
+    auto box_token = [&](int first, int n) -> int32_t {
+        if (kPrefixTileRows % G != 0) return -1;
+        const int32_t tok0 = P.rows[first].token;
+        for (int k = 0; k < std::min(n, kPrefixTileRows); ++k) {
+            const RunRow &rw = P.rows[first + k];
+            if (rw.token != tok0 + k / G || rw.head_local != k % G) return -1;
+        }
+        return tok0;
+    };
     // rows and descriptors
     for (size_t r = 0; r < runs.size(); ++r) {
         if (!runs[r].taken) continue;
@@ -185,7 +196,7 @@ PlanHost build_plan(const sa_dims &d, const int32_t *bt, const int32_t *seq_lens
                 for (int t = 0; t < row_count; t += kPrefixTileRows) {
                     const int lo = runs[r].page_lo + c * run_chunk_pages[r];
                     const int hi = std::min(runs[r].page_hi, lo + run_chunk_pages[r]);
-                    P.tiles.insert(P.tiles.end(), {run_index[r], g, t, lo, hi, c});
+                    P.tiles.insert(P.tiles.end(), {run_index[r], g, t, lo, hi, c, box_token(row_begin + t, row_count - t)});
                 }
     }
     return P;

@@ -25,7 +25,10 @@ struct PlanHost {
     // per run: page_lo, page_hi, row_begin, row_count, chunk_pages, first member's table row
     std::vector<int32_t> run_desc;
     std::vector<RunRow> rows;
-    // per work item: run, kv head, first row of the 128-row tile, page chunk lo, page chunk hi, chunk index
+    // per work item: run, kv head, first row of the 128-row tile, page chunk lo,
+    // page chunk hi, chunk index, and the first token of the tile's rows when
+    // they are consecutive tokens each with its G heads in order (the rows are
+    // then one box of the queries), else -1
     std::vector<int32_t> tiles;
 };
 
@@ -67,7 +70,7 @@ cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t
                           const int32_t *q_lens, uint16_t *out, cudaStream_t stream);
 
 constexpr int kRunDescInts = 6;
-constexpr int kTileInts = 6;
+constexpr int kTileInts = 7;
 constexpr int kPrefixTileRows = 128;
 
 }  // namespace sa

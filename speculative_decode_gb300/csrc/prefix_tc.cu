@@ -236,6 +236,7 @@ struct TcPiece {
     int seq_n, qstart;                // sequence mode: new tokens, packed row of the first
     int slot;                         // sequence mode: partial slot; plan mode: page chunk
     int whole;                        // sequence mode: a whole segment of a wave (output written here)
+    int qbox;                         // plan mode: first token of the rows' query box, or -1
 };
 
 // Start of this CTA's range in sequence mode, found by warp 0 and shared:
@@ -292,6 +293,7 @@ struct TcCursor {
             pc.qstart = bb * nb;  // every sequence has nb new tokens
             pc.slot = 0;
             pc.whole = 1;
+            pc.qbox = -1;
             ++wave;
             return true;
         }
@@ -310,6 +312,7 @@ struct TcCursor {
         pc.qstart = qstart;
         pc.slot = static_cast<int>(blockIdx.x) - rg.range_of(unit - tile - waves.base);
         pc.whole = 0;
+        pc.qbox = -1;
         unit += pc.t_hi - tile;
         tile = pc.t_hi;
         if (tile == w.tiles && unit < end) {  // the next segment (of the next tensor-core sequence)
@@ -458,6 +461,7 @@ __global__ void __launch_bounds__(tc_threads(kSoftWarps), 1)
         plan_piece.t_hi = ((it[4] - it[3]) * kPageSize + kN - 1) / kN;
         plan_piece.key_end = 0x7fffffff;
         plan_piece.slot = it[5];
+        plan_piece.qbox = it[6];
     } else if (warp == 0) {
         // lane-per-sequence scan: the total work, the longest segment, the queries
         int total = 0, max_tiles = 0, q_total = 0;
@@ -548,11 +552,12 @@ __global__ void __launch_bounds__(tc_threads(kSoftWarps), 1)
         return cur.next(P, pc);
     };
     auto next_piece = [&](TcCursor &cur, TcPiece &pc) -> bool { return P.seq_mode && cur.next(P, pc); };
-    // a sequence-mode piece held once per row (more than 32 rows) takes its Q
+    // a sequence-mode piece held once per row (more than 32 rows), or a plan
+    // item whose rows are consecutive tokens with their G heads, takes its Q
     // rows as one box of the 3-D map (tokens x G heads x d): the Q K^T issuer
     // loads it; other pieces' rows are copied by the softmax warps
     auto q_by_tma = [&](const TcPiece &pc) -> bool {
-        return P.q_tma && P.seq_mode && pc.row_count - pc.row0 > kM / 4;
+        return P.q_tma && (P.seq_mode ? pc.row_count - pc.row0 > kM / 4 : pc.qbox >= 0);
     };
 
     if (tid == 0) {
@@ -1015,7 +1020,7 @@ __global__ void __launch_bounds__(tc_threads(kSoftWarps), 1)
                     if (p >= 1) ok = mbar_wait(q_free, (p - 1) & 1);
                     if (!ok) break;
                     mbar_arrive_expect_tx(q_tma, kQBytes);
-                    const int y = pc.g * P.G, z = pc.qstart + pc.row0 / P.G;
+                    const int y = pc.g * P.G, z = P.seq_mode ? pc.qstart + pc.row0 / P.G : pc.qbox;
                     tma_load_3d(smem + kOffQ, &tmq, q_tma, 0, y, z, q_policy);
                     tma_load_3d(smem + kOffQ + kRowBlk, &tmq, q_tma, 64, y, z, q_policy);
                     ok = mbar_wait(q_tma, n_tma++ & 1);
@@ -1102,6 +1107,26 @@ __global__ void __launch_bounds__(tc_threads(kSoftWarps), 1)
     }
 }
 
+// The queries [total_q][Hq][128] bf16 as a 3-D map (d, head, token): 128
+// rows of one KV head that are 128 / G consecutive tokens x its G heads are
+// one box per 64 columns. False (and *map untouched) when G does not divide
+// 128 or the encoding fails: the rows are then copied by the softmax warps.
+bool encode_q_map(const sa_dims &d, const uint16_t *q, CUtensorMap *map) {
+    const int G = d.num_q_heads / d.num_kv_heads;
+    if (kM % G != 0 || d.total_q <= 0) return false;
+    const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(d.num_q_heads),
+                              static_cast<uint64_t>(d.total_q)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(kHeadDim) * 2,
+                                 static_cast<uint64_t>(d.num_q_heads) * kHeadDim * 2};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(kM / G)};
+    CUtensorMap m;
+    if (encode_tensor_map_3d(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(q), dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return false;
+    *map = m;
+    return true;
+}
+
 // the shared-memory opt-in of both kernel instances, once
 cudaError_t tc_attributes() {
     static const cudaError_t e = [] {
@@ -1136,8 +1161,10 @@ cudaError_t launch_prefix_tc(const sa_dims &d, const PlanDevice &pd, const uint1
     p.num_pages = d.num_pages;
     p.n_rows_total = rows_total;
     p.qscale = scale * 1.4426950408889634f;
+    CUtensorMap tmq = tmk;
+    p.q_tma = encode_q_map(d, q, &tmq);
     // a plan's rows are held once: two softmax warps per lane quadrant
-    prefix_tc_kernel<8><<<pd.num_tiles, tc_threads(8), kSmemBytes, stream>>>(p, tmk, tmv, tmk);  // no Q map
+    prefix_tc_kernel<8><<<pd.num_tiles, tc_threads(8), kSmemBytes, stream>>>(p, tmk, tmv, tmq);
     return cudaGetLastError();
 }
 
@@ -1169,19 +1196,8 @@ cudaError_t launch_seq_tc(const sa_dims &d, const SeqTcConfig &c, const uint16_t
     p.n_rows_total = rows_total;
     p.qscale = scale * 1.4426950408889634f;
     if (d.num_seqs == 0 || c.grid <= 0) return cudaSuccess;
-    // Q as a 3-D map (d, head, token): a piece's 128 rows of one KV head are
-    // 128 / G tokens x its G heads, one box per 64 columns
     CUtensorMap tmq = tmk;
-    if (kM % p.G == 0 && d.total_q > 0) {
-        const uint64_t dims[3] = {static_cast<uint64_t>(kHeadDim), static_cast<uint64_t>(d.num_q_heads),
-                                  static_cast<uint64_t>(d.total_q)};
-        const uint64_t strides[2] = {static_cast<uint64_t>(kHeadDim) * 2,
-                                     static_cast<uint64_t>(d.num_q_heads) * kHeadDim * 2};
-        const uint32_t box[3] = {64, static_cast<uint32_t>(p.G), static_cast<uint32_t>(kM / p.G)};
-        p.q_tma = encode_tensor_map_3d(&tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<uint16_t *>(q), dims, strides,
-                                       box, CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
-        if (!p.q_tma) tmq = tmk;
-    }
+    p.q_tma = encode_q_map(d, q, &tmq);
     // persistent: one CTA per SM, each walks its range of the tile sequence.
     // Pieces of at most 32 rows (every row held four times) keep half 1 idle,
     // so such batches take four softmax warps (and their registers)

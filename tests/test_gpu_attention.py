@@ -251,6 +251,34 @@ def test_nested_shared_runs():
     assert_attention_close(out, oracle_attention(w, append=False), "nested runs")
 
 
+def test_shared_run_of_interleaved_sequences():
+    """Every other sequence shares the prefix: the run's query rows are not
+    consecutive tokens, so they are copied row by row instead of loaded as
+    one box (the other plan tests have consecutive members)."""
+    rng = np.random.default_rng(66)
+    P = wl.PAGE_SIZE
+    B, Hq, Hkv = 64, 8, 2
+    num_pages = 2 + 3 * B
+    bt = np.full((B, 3), -1, np.int32)
+    for b in range(B):
+        own = 2 + 3 * b
+        bt[b, :2] = [0, 1] if b % 2 == 0 else [own, own + 1]
+        bt[b, 2] = own + 2
+    seq = (2 * P + rng.integers(1, 200, size=B)).astype(np.int32)
+    ql = np.ones(B, np.int32)
+    w = wl.Workload(name="interleaved", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=128, page_size=P,
+                    q=wl.normal_bf16(rng, (B, Hq, 128)),
+                    k_pages=wl.normal_bf16(rng, (num_pages, Hkv, P, 128)),
+                    v_pages=wl.normal_bf16(rng, (num_pages, Hkv, P, 128)),
+                    block_table=bt, seq_lens=seq, q_lens=ql, scale=0.0883883,
+                    k_new=wl.normal_bf16(rng, (B, Hkv, 128)), v_new=wl.normal_bf16(rng, (B, Hkv, 128)))
+    st = _plan_stats(w)
+    assert st["runs"] == 1 and st["members"] == B // 2
+    out, err, _, _ = run_attention(w, use_plan=True, append=False)
+    assert err == 0
+    assert_attention_close(out, oracle_attention(w, append=False), "interleaved members")
+
+
 # ----------------------------------- multi-query rows on tensor cores (no plan)
 @pytest.mark.parametrize("seed,G,Hkv,qlens,max_ctx", [
     (71, 4, 2, (6,), 3000),          # 24 rows per KV head: the verify shape
