@@ -20,8 +20,8 @@
 // producer, warp 9 allocates tensor memory and issues Q K^T, warp 10 issues
 // P V (one thread each). K/V tiles of 64 keys
 // (32 KiB) stream through five stages, so four loads are in flight while a
-// tile is consumed; S (tensor memory, three buffers) and P (shared memory, two,
-// one per half) are multi-buffered, so Q K^T runs up to two tiles ahead and
+// tile is consumed; S (tensor memory, four buffers) and P (shared memory, two,
+// one per half) are multi-buffered, so Q K^T runs up to three tiles ahead and
 // P V of one half's tile runs on the tensor cores while the other half's
 // softmax runs on the CUDA cores. With at most 32 query rows (q_len = k+1
 // verification of one sequence) every row is held four times and each copy's
@@ -50,8 +50,9 @@ constexpr int kQBytes = 2 * kRowBlk;          // Q [128 rows][128 d]
 constexpr int kPBytes = kRowBlk;              // P [128 rows][64 keys], double-buffered
 constexpr int kKVStage = 4 * kKVBlk;          // K (2 blocks) + V (2 blocks) = 32 KiB
 constexpr int kStagesTC = 5;                  // K/V stages
-constexpr int kSBufs = 3;                     // S buffers: Q K^T runs up to two tiles ahead of the softmax
-constexpr int kTmemCols = 512;                // S buffers: columns 0 .. 3*64-1, two O buffers: the next 2*128
+constexpr int kSBufs = 4;                     // S buffers: Q K^T runs up to three tiles ahead of the softmax
+constexpr int kTmemCols = 512;                // S buffers: columns 0 .. 4*64-1, two O buffers: the next 2*128
+static_assert(kSBufs * 64 + 2 * 128 <= kTmemCols, "tensor-memory columns");
 // softmax / epilogue warps (4 or 8), then the TMA producer, the Q K^T issuer
 // (which also holds the tensor memory) and the P V issuer
 constexpr int tc_threads(int soft_warps) { return (soft_warps + 3) * 32; }
@@ -592,7 +593,7 @@ __global__ void __launch_bounds__(tc_threads(kSoftWarps), 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o0 = tmem + kSBufs * kN;  // S buffers at columns 0, kN, 2 kN; O buffers A and B after them
+    const uint32_t tmem_o0 = tmem + kSBufs * kN;  // S buffers at columns 0, kN, 2 kN, 3 kN; O buffers A and B after them
 
     const uint32_t sQ = smem_u32(smem + kOffQ), sP = smem_u32(smem + kOffP), sKV = smem_u32(smem + kOffKV);
 
@@ -887,23 +888,27 @@ __global__ void __launch_bounds__(tc_threads(kSoftWarps), 1)
                     const int64_t wi = static_cast<int64_t>(rm.slot) * P.n_rows_total + orow;
                     const uint32_t o_a = kTwo ? tmem_o0 : tmem_o0 + (p & 1) * kHeadDim;
 #pragma unroll
-                    for (int c = 0; c < (kTwo ? kHeadDim / 64 : kHeadDim / 32); ++c) {
-                        const int col = (kTwo ? hf * (kHeadDim / 2) : 0) + c * 32;
-                        float oa[32];
-                        tmem_ld32(o_a + lane_base + col, oa);
+                    // 16 columns at a time with two O buffers (fewer live registers
+                    // under the 168-register cap), 32 with one
+                    constexpr int CW = kTwo ? 16 : 32;
+#pragma unroll 1
+                    for (int c = 0; c < (kTwo ? kHeadDim / 2 : kHeadDim) / CW; ++c) {
+                        const int col = (kTwo ? hf * (kHeadDim / 2) : 0) + c * CW;
+                        float oa[CW];
+                        tmem_ld_cols<CW>(o_a + lane_base + col, oa);
                         if constexpr (kTwo) {
-                            float ob[32];
-                            tmem_ld32(tmem_o0 + kHeadDim + lane_base + col, ob);
+                            float ob[CW];
+                            tmem_ld_cols<CW>(tmem_o0 + kHeadDim + lane_base + col, ob);
 #pragma unroll
-                            for (int k = 0; k < 32; ++k) oa[k] = wB > 0.f ? fmaf(ob[k], wB, oa[k] * wA) : oa[k] * wA;
+                            for (int k = 0; k < CW; ++k) oa[k] = wB > 0.f ? fmaf(ob[k], wB, oa[k] * wA) : oa[k] * wA;
                         } else {
 #pragma unroll
-                            for (int k = 0; k < 32; ++k) oa[k] *= wA;
+                            for (int k = 0; k < CW; ++k) oa[k] *= wA;
                         }
                         if (rm.valid && pc.whole) {  // a whole segment: this row's bf16 output
                             uint4 *dst = reinterpret_cast<uint4 *>(P.out + orow * kHeadDim + col);
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
+                            for (int k = 0; k < CW / 8; ++k)
                                 dst[k] = make_uint4(pack_bf16x2(oa[8 * k] * inv, oa[8 * k + 1] * inv),
                                                     pack_bf16x2(oa[8 * k + 2] * inv, oa[8 * k + 3] * inv),
                                                     pack_bf16x2(oa[8 * k + 4] * inv, oa[8 * k + 5] * inv),
@@ -911,7 +916,7 @@ __global__ void __launch_bounds__(tc_threads(kSoftWarps), 1)
                         } else if (rm.valid) {  // fp32 partial (O, m, l) of this row
                             float4 *dst = reinterpret_cast<float4 *>(P.ws_acc + wi * kHeadDim + col);
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) dst[k] = make_float4(oa[4 * k], oa[4 * k + 1], oa[4 * k + 2], oa[4 * k + 3]);
+                            for (int k = 0; k < CW / 4; ++k) dst[k] = make_float4(oa[4 * k], oa[4 * k + 1], oa[4 * k + 2], oa[4 * k + 3]);
                         }
                     }
                     if (rm.valid && !pc.whole && hf == 0) *reinterpret_cast<float2 *>(P.ws_ml + wi * 2) = make_float2(M, L);
