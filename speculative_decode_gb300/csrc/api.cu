@@ -462,7 +462,9 @@ static int paged_attn_impl(const sa_dims *dims, const uint16_t *q, const uint16_
 
     int per_sm = 0;
     if (split_occupancy(c.R, quant ? qp.bits : 16, &per_sm) != cudaSuccess || per_sm <= 0) return SA_ERR_CUDA;
-    p.split_ctas = sms * per_sm;  // one warp per CTA, all resident
+    // one warp per CTA, all resident; after a plan's tensor-core kernel two
+    // fewer per SM, so that combine CTAs fit beside them and scan early
+    p.split_ctas = sms * ((pd && pd->num_tiles > 0 && per_sm > 2) ? per_sm - 2 : per_sm);
     p.pages_ready = ((pd && pd->num_tiles > 0) || c.tc.min_rows > 0) ? 1 : 0;
     if (launch_split_attn(p, s) != cudaSuccess)
         return SA_ERR_CUDA;
